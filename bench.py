@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark of the SiTU routed-MoE expert layer on GB300.
+
+Default workload: the Kimi-K3 TP8 decode layer, w4a16 (T=64 tokens, hidden
+3584, intermediate 384, 896 local experts, top-16 uniform routing, bf16
+activations, MXFP4 weights).  One step = one pass of the whole layer
+(permute -> gather -> FC1 + SiTU -> FC2 -> combine; for the w4a8 workload
+also the MXFP8 activation quantisation) over one batch already resident in
+HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+  python bench.py --impl reference ...     # the CPU oracle as reference arm
+
+Timing: CUDA events on the launching stream around each step, a 256 MiB
+write between steps flushes L2 (the events exclude it), max over ranks.
+Under torchrun each rank runs its own replica of the layer (its own seed);
+the layer needs no collective (each EP/TP rank produces a partial output
+the caller all-reduces), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "K3-shape MoE layer tokens/s and % of roofline (HBM or block-scaled TC), T=64/8192"
+WORKLOAD_NAMES = {
+    "decode": "Kimi-K3 TP8 decode layer, w4a16: T=64 H=3584 I=384 E=896 local, top-16 uniform, "
+              "bf16 activations x MXFP4 weights",
+    "prefill_w4a8": "Kimi-K3 TP8 prefill layer, w4a8: T=8192 H=3584 I=384 E=896, top-16 Zipf(1.0), "
+                    "MXFP8 activations x MXFP4 weights",
+    "ep_shard": "Kimi-K3 EP8 shard 3/8: T=4096 H=3584 I=3072 E_loc=112 offset 336, top-16 uniform, w4a16",
+    "nvfp4": "Kimi-K3 NVFP4 layer: T=256 H=3584 I=384 E=896, top-16 Zipf(0.8), NVFP4 x NVFP4",
+    "tiny": "tiny MoE: T=16 H=256 I=128 E=8 top-2, w4a16",
+}
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def routing_stats(wl):
+    ids = wl.host("topk_ids")
+    kept = (ids >= wl.off) & (ids < wl.off + wl.E_loc)
+    R = int(kept.sum())
+    touched = int(np.unique(ids[kept]).size)
+    return R, touched
+
+
+def algorithmic_bytes(wl, R, touched):
+    """Bytes each stage must move at minimum (weights of touched experts
+    once, activations and outputs once)."""
+    H, I, T, K = wl.H, wl.I, wl.T, wl.K
+    bs = 16 if wl.wt == 1 else 32
+    w1 = touched * (2 * I * H // 2 + 2 * I * H // bs) + (touched * 8 if wl.wt == 1 else 0)
+    w2 = touched * (H * I // 2 + H * I // bs) + (touched * 4 if wl.wt == 1 else 0)
+    act_in = {0: T * H * 2, 1: T * H + T * H // 32, 2: T * H // 2 + T * H // 16 + 4 * T}[wl.act]
+    route = T * K * 8
+    out = T * H * 2
+    return {
+        "permute": T * K * 4 + 2 * T * K * 4 + 2 * wl.E_loc * 4,
+        "gather": act_in * R / max(T, 1) + R * H * 2,
+        "fc1": w1 + R * H * 2 + R * I * 2,
+        "fc2": w2 + R * I * 2 + R * H * 2,
+        "combine": R * H * 2 + route + out,
+        "quant": T * H * 2 + T * H + T * H // 32,
+        "layer": w1 + w2 + act_in + route + out,
+    }
+
+
+def layer_flops(wl, R):
+    return 2.0 * R * (wl.H * 2 * wl.I + wl.I * wl.H)
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_tokens_per_s(wl, budget_s: float, host_kw=None, max_tokens=None):
+    """Time the oracle on a bounded token sample; returns (tok/s, n_tok, seconds, threads)."""
+    import oracle
+    from block_scaled_fp4_permute_gb300 import workloads as W
+    if host_kw is None:
+        host_kw = host_oracle_kwargs(wl)
+    T = wl.T
+    n0 = min(T, 2)
+    t0 = time.perf_counter()
+    _oracle_run(oracle, W, wl, host_kw, n0)
+    dt0 = time.perf_counter() - t0
+    n = int(max(1, min(max_tokens or T, T, round(budget_s / max(dt0 / n0, 1e-6)))))
+    t0 = time.perf_counter()
+    _oracle_run(oracle, W, wl, host_kw, n)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt, oracle.get_threads()
+
+
+def host_oracle_kwargs(wl):
+    import oracle
+    from block_scaled_fp4_permute_gb300 import workloads as W
+    if wl.act == W.ACT_MXFP8:
+        return W.oracle_kwargs(wl), wl.host("x_bf16")
+    return W.oracle_kwargs(wl), None
+
+
+def _oracle_run(oracle, W, wl, host_kw, n):
+    kw, xbits = host_kw
+    toks = np.arange(n, dtype=np.int32)
+    if xbits is not None:   # w4a8: the oracle's own MXFP8 quantisation is part of the step
+        q, s = oracle.quant_mxfp8(xbits[:n])
+        kw = dict(kw)
+        qf = np.zeros((wl.T, wl.H), np.uint8)
+        sf = np.zeros((wl.T, wl.H // 32), np.uint8)
+        qf[:n], sf[:n] = q, s
+        kw["hidden_states_q"], kw["hidden_states_scale"] = qf, sf
+    return oracle.moe_forward(**kw, tokens=toks)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_workload(name, device, seed):
+    from block_scaled_fp4_permute_gb300 import workloads as W
+    return W.make(name, device=device, seed=seed)
+
+
+def run_reference(args):
+    """The oracle (CPU, as it stands) as the reference arm."""
+    import torch
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    wl = make_workload(args.workload, dev, args.seed)
+    host_kw = host_oracle_kwargs(wl)
+    per_step = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    _, n, _, threads = oracle_tokens_per_s(wl, per_step, host_kw)
+    from block_scaled_fp4_permute_gb300 import workloads as W
+    for _ in range(args.warmup):
+        _oracle_run(oracle, W, wl, host_kw, n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_run(oracle, W, wl, host_kw, n)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = n / dt
+    sample = f"{n} of {wl.T} tokens per step ({wl.name} workload), all local experts"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAMES[args.workload], "T": wl.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from block_scaled_fp4_permute_gb300 import binding, build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    build.build()
+    wl = make_workload(args.workload, dev, args.seed + rank)
+    layer = binding.Layer(wl)
+    R, touched = routing_stats(wl)
+    nbytes = algorithmic_bytes(wl, R, touched)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    nst = len(binding.PROFILE_STAGES)
+    is_w4a8 = wl.act == binding.SITU_ACT_MXFP8
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)     # creates the underlying cudaEvent_t
+        return evs
+
+    steps = [new_events(nst + 1) for _ in range(args.steps)]
+    qevs = [new_events(2) for _ in range(args.steps)] if is_w4a8 else None
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer()
+    torch.cuda.synchronize()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local].strip() if vis else local)
+    sampler.start()
+    time.sleep(0.25)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        layer.profiled(steps[i], qevs[i] if is_w4a8 else None)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    stage_ms = np.zeros(nst)
+    step_ms = np.zeros(args.steps)
+    quant_ms = 0.0
+    for i, evs in enumerate(steps):
+        for s in range(nst):
+            stage_ms[s] += evs[s].elapsed_time(evs[s + 1])
+        step_ms[i] = evs[0].elapsed_time(evs[nst])
+        if is_w4a8:
+            q = qevs[i][0].elapsed_time(qevs[i][1])
+            quant_ms += q
+            step_ms[i] = qevs[i][0].elapsed_time(evs[nst])
+    stage_ms /= args.steps
+    quant_ms /= args.steps
+    ms = float(step_ms.mean())
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end: pinned host inputs -> device, layer, output -> pinned host
+    if wl.act == binding.SITU_ACT_NVFP4:
+        dev_in = [wl.x_q, wl.x_scale, wl.x_gscale, wl.topk_ids, wl.topk_weights]
+    else:
+        dev_in = [wl.x_bf16, wl.topk_ids, wl.topk_weights]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = torch.empty(layer.out.shape, dtype=layer.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e_ms = []
+    for i in range(max(args.warmup, 1) + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        layer()
+        host_out.copy_(layer.out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= max(args.warmup, 1):
+            e_ms.append(e0.elapsed_time(e1))
+    e2e_ms = float(np.mean(e_ms))
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    hbm, peak_kind = peaks()
+    stages = {}
+    for s, name in enumerate(binding.PROFILE_STAGES):
+        gbs = nbytes[name] / (stage_ms[s] * 1e-3) / 1e9 if stage_ms[s] > 0 else None
+        stages[name] = {"ms": float(stage_ms[s]), "alg_bytes": int(nbytes[name]),
+                        "gbs": gbs, "frac_hbm": gbs / hbm if gbs else None}
+    if is_w4a8:
+        gbs = nbytes["quant"] / (quant_ms * 1e-3) / 1e9
+        stages["quant_mxfp8"] = {"ms": quant_ms, "alg_bytes": int(nbytes["quant"]), "gbs": gbs,
+                                 "frac_hbm": gbs / hbm}
+    dom = max(stages, key=lambda k: stages[k]["ms"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(dom)
+    roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["gbs"], "peak": hbm,
+            "unit": "GB/s", "frac": stages[dom]["frac_hbm"], "traffic": traffic,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+    layer_gbs = nbytes["layer"] / (ms * 1e-3) / 1e9
+    flops = layer_flops(wl, R)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        tps, n, dt, threads = oracle_tokens_per_s(wl, args.cpu_budget)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} of {wl.T} tokens of the same workload, {dt:.1f} s"}
+
+    launches_per_step = 7 + (1 if is_w4a8 else 0)
+    line = {
+        "metric": METRIC, "value": ws * wl.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; weights N(0,0.02) packed to the block-scaled format)",
+        "config": {"workload": WORKLOAD_NAMES[args.workload], "T": wl.T, "H": wl.H, "I": wl.I,
+                   "E_total": wl.E_total, "E_loc": wl.E_loc, "offset": wl.off, "top_k": wl.K,
+                   "kept_pairs": R, "touched_experts": touched,
+                   "l2": "flushed between steps (256 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{ws}, no collective"},
+        "roofline": roof,
+        "layer_roofline": {"bound": "hbm", "alg_bytes": int(nbytes["layer"]), "achieved": layer_gbs,
+                           "peak": hbm, "unit": "GB/s", "frac": layer_gbs / hbm,
+                           "tflops": flops / (ms * 1e-3) / 1e12},
+        "stages": stages,
+        "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=tuple(WORKLOAD_NAMES), default="decode")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,228 @@
+"""ctypes binding of ``libsitu_moe.so`` (C ABI in ``include/situ_moe.h``).
+
+Argument marshalling only: PyTorch provides device memory and the stream,
+every step of the layer runs in the library's CUDA kernels.  There is no
+fallback: if the library is not built, or a call returns an error status,
+the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+SITU_OK = 0
+SITU_ACT_BF16, SITU_ACT_MXFP8, SITU_ACT_NVFP4 = 0, 1, 2
+SITU_W_MXFP4, SITU_W_NVFP4 = 0, 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+class SituError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class SituMoeArgs(ctypes.Structure):
+    """Mirror of ``situ_moe_args``."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "T", "H", "I", "num_experts_total", "num_local_experts", "local_expert_offset", "top_k",
+        "act_dtype", "weight_dtype")] + [(n, ctypes.c_void_p) for n in (
+            "hidden_states", "hidden_states_q", "hidden_states_scale", "hidden_states_gscale",
+            "topk_ids", "topk_weights", "w1", "w1_scale", "w1_gscale", "w2", "w2_scale",
+            "w2_gscale", "gemm1_alpha", "gemm1_beta", "g1_alphas", "g1_alphas_up", "g2_alphas",
+            "out")]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise ImportError(f"{path} is missing: build it with "
+                                  "`python -m block_scaled_fp4_permute_gb300.build` "
+                                  "(the layer has no CPU fallback)")
+            l = ctypes.CDLL(path)
+            vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            l.situ_status_string.restype = ctypes.c_char_p
+            l.situ_status_string.argtypes = [ctypes.c_int]
+            l.situ_moe_permute_workspace_size.restype = sz
+            l.situ_moe_permute_workspace_size.argtypes = [i32, i32, i32]
+            l.situ_moe_permute.restype = ctypes.c_int
+            l.situ_moe_permute.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+            l.situ_moe_quant_mxfp8.restype = ctypes.c_int
+            l.situ_moe_quant_mxfp8.argtypes = [vp, i32, i32, vp, vp, vp]
+            l.situ_moe_workspace_size.restype = sz
+            l.situ_moe_workspace_size.argtypes = [ctypes.POINTER(SituMoeArgs)]
+            l.situ_moe_forward.restype = ctypes.c_int
+            l.situ_moe_forward.argtypes = [ctypes.POINTER(SituMoeArgs), vp, sz, vp]
+            l.situ_moe_forward_profiled.restype = ctypes.c_int
+            l.situ_moe_forward_profiled.argtypes = [ctypes.POINTER(SituMoeArgs), vp, sz, vp,
+                                                    ctypes.POINTER(ctypes.c_void_p)]
+            _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().situ_status_string(status).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != SITU_OK:
+        raise SituError(fn, status)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+
+def situ_moe_permute_workspace_size(T: int, top_k: int, num_local_experts: int) -> int:
+    return lib().situ_moe_permute_workspace_size(T, top_k, num_local_experts)
+
+
+def situ_moe_permute(topk_ids: torch.Tensor, num_experts_total: int, num_local_experts: int,
+                     local_expert_offset: int, stream=None):
+    """Returns (expert_counts, expert_offsets, permuted_src, slot_to_row)."""
+    T, K = topk_ids.shape
+    dev = topk_ids.device
+    counts = torch.empty(num_local_experts, dtype=torch.int32, device=dev)
+    offsets = torch.empty(num_local_experts + 1, dtype=torch.int32, device=dev)
+    psrc = torch.empty(max(T * K, 1), dtype=torch.int32, device=dev)
+    s2r = torch.empty(max(T * K, 1), dtype=torch.int32, device=dev)
+    nbytes = situ_moe_permute_workspace_size(T, K, num_local_experts)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _check("situ_moe_permute", lib().situ_moe_permute(
+        _p(topk_ids.contiguous()), T, K, num_experts_total, num_local_experts, local_expert_offset,
+        _p(counts), _p(offsets), _p(psrc), _p(s2r), _p(ws), ws.numel(), _stream(stream)))
+    return counts, offsets, psrc[:T * K], s2r[:T * K]
+
+
+def situ_moe_quant_mxfp8(x_bf16: torch.Tensor, stream=None, out=None):
+    """bf16 [T,H] -> (E4M3 uint8 [T,H], UE8M0 uint8 [T,H/32])."""
+    T, H = x_bf16.shape
+    if out is None:
+        q = torch.empty((T, H), dtype=torch.uint8, device=x_bf16.device)
+        s = torch.empty((T, H // 32), dtype=torch.uint8, device=x_bf16.device)
+    else:
+        q, s = out
+    _check("situ_moe_quant_mxfp8", lib().situ_moe_quant_mxfp8(
+        _p(x_bf16), T, H, _p(q), _p(s), _stream(stream)))
+    return q, s
+
+
+def make_args(*, T, H, I, num_experts_total, num_local_experts, local_expert_offset, top_k,
+              act_dtype, weight_dtype, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale,
+              gemm1_alpha, gemm1_beta, out, hidden_states=None, hidden_states_q=None,
+              hidden_states_scale=None, hidden_states_gscale=None, w1_gscale=None, w2_gscale=None,
+              g1_alphas=None, g1_alphas_up=None, g2_alphas=None) -> SituMoeArgs:
+    a = SituMoeArgs(T=T, H=H, I=I, num_experts_total=num_experts_total,
+                    num_local_experts=num_local_experts, local_expert_offset=local_expert_offset,
+                    top_k=top_k, act_dtype=act_dtype, weight_dtype=weight_dtype)
+    for name, t in dict(hidden_states=hidden_states, hidden_states_q=hidden_states_q,
+                        hidden_states_scale=hidden_states_scale,
+                        hidden_states_gscale=hidden_states_gscale, topk_ids=topk_ids,
+                        topk_weights=topk_weights, w1=w1, w1_scale=w1_scale, w1_gscale=w1_gscale,
+                        w2=w2, w2_scale=w2_scale, w2_gscale=w2_gscale, gemm1_alpha=gemm1_alpha,
+                        gemm1_beta=gemm1_beta, g1_alphas=g1_alphas, g1_alphas_up=g1_alphas_up,
+                        g2_alphas=g2_alphas, out=out).items():
+        setattr(a, name, None if t is None else t.data_ptr())
+    return a
+
+
+def situ_moe_workspace_size(args: SituMoeArgs) -> int:
+    return lib().situ_moe_workspace_size(ctypes.byref(args))
+
+
+def situ_moe_forward(args: SituMoeArgs, workspace: torch.Tensor, stream=None) -> None:
+    _check("situ_moe_forward", lib().situ_moe_forward(
+        ctypes.byref(args), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+PROFILE_STAGES = ("permute", "gather", "fc1", "fc2", "combine")
+
+
+def situ_moe_forward_profiled(args: SituMoeArgs, workspace: torch.Tensor, events, stream=None):
+    """situ_moe_forward recording ``events`` (len(PROFILE_STAGES) + 1
+    torch.cuda.Event objects with timing enabled) around each stage."""
+    assert len(events) == len(PROFILE_STAGES) + 1
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check("situ_moe_forward_profiled", lib().situ_moe_forward_profiled(
+        ctypes.byref(args), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream), arr))
+
+
+class Layer:
+    """Keeps the argument struct and a workspace for one workload, so that a
+    forward call is a single C-ABI call (the bench times exactly this)."""
+
+    def __init__(self, wl, out: Optional[torch.Tensor] = None, x_q=None, x_scale=None):
+        self.wl = wl
+        dev = wl.x_bf16.device
+        self.out = out if out is not None else torch.empty((wl.T, wl.H), dtype=torch.bfloat16,
+                                                           device=dev)
+        kw = dict(T=wl.T, H=wl.H, I=wl.I, num_experts_total=wl.E_total,
+                  num_local_experts=wl.E_loc, local_expert_offset=wl.off, top_k=wl.K,
+                  act_dtype=wl.act, weight_dtype=wl.wt, topk_ids=wl.topk_ids,
+                  topk_weights=wl.topk_weights, w1=wl.w1, w1_scale=wl.w1_scale, w2=wl.w2,
+                  w2_scale=wl.w2_scale, gemm1_alpha=wl.gemm1_alpha, gemm1_beta=wl.gemm1_beta,
+                  g1_alphas=wl.g1_alphas, g1_alphas_up=wl.g1_alphas_up, g2_alphas=wl.g2_alphas,
+                  w1_gscale=wl.w1_gscale, w2_gscale=wl.w2_gscale, out=self.out)
+        if wl.act == SITU_ACT_BF16:
+            kw["hidden_states"] = wl.x_bf16
+        elif wl.act == SITU_ACT_MXFP8:
+            if x_q is None:
+                x_q = torch.empty((wl.T, wl.H), dtype=torch.uint8, device=dev)
+                x_scale = torch.empty((wl.T, wl.H // 32), dtype=torch.uint8, device=dev)
+            self.x_q, self.x_scale = x_q, x_scale
+            kw["hidden_states_q"], kw["hidden_states_scale"] = x_q, x_scale
+        else:
+            kw["hidden_states_q"], kw["hidden_states_scale"] = wl.x_q, wl.x_scale
+            kw["hidden_states_gscale"] = wl.x_gscale
+        self._keep = kw
+        self.args = make_args(**kw)
+        n = situ_moe_workspace_size(self.args)
+        self.workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+
+    def profiled(self, events, quant_events=None, stream=None) -> torch.Tensor:
+        """Like __call__, recording per-stage events (see situ_moe_forward_profiled);
+        ``quant_events`` (start, end) bracket the MXFP8 quantisation of w4a8."""
+        if self.wl.act == SITU_ACT_MXFP8:
+            if quant_events:
+                quant_events[0].record(stream)
+            situ_moe_quant_mxfp8(self.wl.x_bf16, stream, out=(self.x_q, self.x_scale))
+            if quant_events:
+                quant_events[1].record(stream)
+        situ_moe_forward_profiled(self.args, self.workspace, events, stream)
+        return self.out
+
+    def __call__(self, stream=None) -> torch.Tensor:
+        """One pass of the layer; for w4a8 this includes the MXFP8 activation
+        quantisation of the bf16 hidden states."""
+        if self.wl.act == SITU_ACT_MXFP8:
+            situ_moe_quant_mxfp8(self.wl.x_bf16, stream, out=(self.x_q, self.x_scale))
+        situ_moe_forward(self.args, self.workspace, stream)
+        return self.out

@@ -1,0 +1,106 @@
+// common.cuh -- device helpers shared by the SiTU MoE kernels (sm_103a).
+//
+// Number formats (OCP Microscaling): E2M1 codes (sign in bit 3, two
+// exponent bits with bias 1, one mantissa bit), E4M3 "fn" (bias 7, max 448),
+// UE8M0 (2^(b-127)).  bf16 values are handled as raw 16-bit patterns packed
+// in pairs (low half = even element).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace situ {
+
+constexpr int kWarp = 32;
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Eight E2M1 codes (one 32-bit word, element 0 in bits 0..3) to eight bf16
+// values, exactly: out[q] holds elements (2q, 2q+1).  The bf16 bit patterns
+// of the eight magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} are split into a
+// high-byte table {00 3F 3F 3F 40 40 40 40} and a low-byte table
+// {00 00 80 C0 00 40 80 C0}; PRMT looks four magnitudes up at a time, a
+// second PRMT interleaves the bytes into bf16 pairs and the sign bits are
+// moved to bit 15 / 31.
+__device__ __forceinline__ void e2m1x8_to_bf16x8(uint32_t w, uint32_t out[4]) {
+  const uint32_t kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;
+  const uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u;
+  uint32_t sel_lo = w & 0x7777u;
+  uint32_t sel_hi = (w >> 16) & 0x7777u;
+  uint32_t h0 = prmt(kHiA, kHiB, sel_lo), l0 = prmt(kLoA, kLoB, sel_lo);
+  uint32_t h1 = prmt(kHiA, kHiB, sel_hi), l1 = prmt(kLoA, kLoB, sel_hi);
+  out[0] = prmt(l0, h0, 0x5140u) | ((w << 12) & 0x00008000u) | ((w << 24) & 0x80000000u);
+  out[1] = prmt(l0, h0, 0x7362u) | ((w << 4) & 0x00008000u) | ((w << 16) & 0x80000000u);
+  out[2] = prmt(l1, h1, 0x5140u) | ((w >> 4) & 0x00008000u) | ((w << 8) & 0x80000000u);
+  out[3] = prmt(l1, h1, 0x7362u) | ((w >> 12) & 0x00008000u) | (w & 0x80000000u);
+}
+
+// bf16x2 multiply (round to nearest even; exact when the product is a bf16).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// E4M3 code to fp32, exactly (finite codes).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float v = (e == 0) ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (b & 0x80u) ? -v : v;
+}
+
+// 2^k as fp32 for k in [-149, 127] (exact, including the subnormal range).
+__device__ __forceinline__ float exp2i(int k) {
+  if (k >= -126) return __uint_as_float((uint32_t)(k + 127) << 23);
+  return __uint_as_float(1u << (k + 149));
+}
+
+// UE8M0 scale byte in [1, 254] as a bf16 pair (both halves 2^(b-127)).
+__device__ __forceinline__ uint32_t ue8m0_to_bf16x2(uint32_t b) {
+  return (b << 7) | (b << 23);
+}
+
+// fp32 pair -> bf16 pair, round to nearest even; lo in the low half.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
+
+// E4M3 codes of two fp32 values, nearest even with saturation to +-448;
+// returns lo in bits 0..7 and hi in bits 8..15.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return (uint32_t)d;
+}
+
+// The MXFP8 block exponent: the smallest e in [-127, 127] with
+// amax * 2^-e <= 448, from the fp32 bits of amax (amax = m * 2^k with
+// m in [1, 2); 448 = 1.75 * 2^8, so e = k - 8 + (m > 1.75)).
+__device__ __forceinline__ int mxfp8_exponent(float amax) {
+  uint32_t bits = __float_as_uint(amax);
+  int k = (int)((bits >> 23) & 0xFFu) - 127;
+  if (((bits >> 23) & 0xFFu) == 0) return -127;   // zero or fp32 subnormal
+  int e = k - 8 + (((bits & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// SiTU: [b*tanh(g/b)*sigmoid(g)] * [bl*tanh(u/bl)], a cap <= 0 meaning the
+// factor's limit (g*sigmoid(g), u).
+__device__ __forceinline__ float situ_f(float g, float u, float b, float bl) {
+  float gate = (b > 0.f) ? b * tanhf(g / b) * sigmoid_f(g) : g * sigmoid_f(g);
+  float up = (bl > 0.f) ? bl * tanhf(u / bl) : u;
+  return gate * up;
+}
+
+}  // namespace situ

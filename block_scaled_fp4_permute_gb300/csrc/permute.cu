@@ -1,0 +1,206 @@
+// permute.cu -- expert histogram, prefix scan and stable scatter.
+//
+// Groups the (token, slot) pairs of a global top-k routing by local expert,
+// dropping IDs outside the rank's contiguous shard (TokenSpeed SiTU,
+// "Supported contract": top-k IDs stay global and the routing filters the
+// experts outside the current shard).  The row order inside an expert is the
+// ascending slot order, so the result is deterministic and bit-exact.
+//
+// Three launches over chunks of kPermChunk slots:
+//   count   -- per-chunk histogram in shared memory (block-local atomics);
+//   scan    -- one block: per-expert prefix over chunks, then an exclusive
+//              scan over experts of the counts and of the GEMM token tiles
+//              (ceil(count / tile_n)); clears the unused permuted_src tail;
+//   scatter -- per chunk: per-warp counts, a prefix over warps, then each
+//              warp walks its slots 32 at a time; __match_any_sync groups the
+//              lanes that hit the same expert and a popcount of the lower
+//              peers gives each lane its rank, so equal experts keep slot
+//              order without any global atomics.
+// Scratch: blk_counts [n_chunks, E_loc] int32.
+#include "situ_internal.h"
+
+namespace situ {
+
+constexpr int kPermThreads = 256;
+constexpr int kPermWarps = kPermThreads / kWarp;
+constexpr int kPermSlotsPerWarp = kPermChunk / kPermWarps;   // 512
+
+__device__ __forceinline__ int local_expert(int id, int off, int E_loc) {
+  int e = id - off;
+  return (id >= off && e < E_loc) ? e : -1;
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+permute_count_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int off,
+                     int32_t* __restrict__ blk_counts) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E_loc; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  long base = (long)blockIdx.x * kPermChunk;
+  for (int i = threadIdx.x; i < kPermChunk; i += blockDim.x) {
+    long s = base + i;
+    if (s < S) {
+      int e = local_expert(__ldg(ids + s), off, E_loc);
+      if (e >= 0) atomicAdd(&hist[e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E_loc; e += blockDim.x)
+    blk_counts[(size_t)blockIdx.x * E_loc + e] = hist[e];
+}
+
+// Exclusive scan of one int per thread across the block; returns the
+// thread's prefix and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_sums[32];
+  int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += y;
+    }
+    warp_sums[lane] = w;   // inclusive prefix over warps
+  }
+  __syncthreads();
+  int warp_prefix = warp ? warp_sums[warp - 1] : 0;
+  *total = warp_sums[nwarps - 1];
+  __syncthreads();
+  return warp_prefix + x - v;
+}
+
+__global__ void __launch_bounds__(1024)
+permute_scan_kernel(int32_t* __restrict__ blk_counts, int nblk, int E_loc, long S, int tile_n,
+                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ tile_offsets, int32_t* __restrict__ permuted_src,
+                    int32_t* __restrict__ meta) {
+  // 1. per expert: prefix over chunks (becomes each chunk's base), total count
+  for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblk; ++b) {
+      int v = blk_counts[(size_t)b * E_loc + e];
+      blk_counts[(size_t)b * E_loc + e] = run;
+      run += v;
+    }
+    counts[e] = run;
+  }
+  __syncthreads();
+  // 2. exclusive scans over experts: each thread owns a contiguous segment
+  int per = (E_loc + blockDim.x - 1) / blockDim.x;
+  int e0 = min(E_loc, (int)threadIdx.x * per), e1 = min(E_loc, e0 + per);
+  int sc = 0, st = 0;
+  for (int e = e0; e < e1; ++e) {
+    int c = counts[e];
+    sc += c;
+    st += (c + tile_n - 1) / tile_n;
+  }
+  int R, tiles;
+  int pc = block_exclusive_scan(sc, &R);
+  int pt = block_exclusive_scan(st, &tiles);
+  for (int e = e0; e < e1; ++e) {
+    int c = counts[e];
+    offsets[e] = pc;
+    pc += c;
+    if (tile_offsets) {
+      tile_offsets[e] = pt;
+      pt += (c + tile_n - 1) / tile_n;
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[E_loc] = R;
+    if (tile_offsets) tile_offsets[E_loc] = tiles;
+    if (meta) { meta[0] = R; meta[1] = tiles; }
+  }
+  // 3. rows >= R of permuted_src hold -1
+  for (long r = R + threadIdx.x; r < S; r += blockDim.x) permuted_src[r] = -1;
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+permute_scatter_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int off,
+                       const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ permuted_src, int32_t* __restrict__ slot_to_row) {
+  extern __shared__ int32_t wcnt[];   // [kPermWarps][E_loc]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kPermWarps * E_loc; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const long wbase = (long)blockIdx.x * kPermChunk + (long)warp * kPermSlotsPerWarp;
+  for (int r = 0; r < kPermSlotsPerWarp; r += kWarp) {
+    long s = wbase + r + lane;
+    if (s < S) {
+      int e = local_expert(__ldg(ids + s), off, E_loc);
+      if (e >= 0) atomicAdd(&wcnt[warp * E_loc + e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
+    int run = offsets[e] + blk_base[(size_t)blockIdx.x * E_loc + e];
+    for (int w = 0; w < kPermWarps; ++w) {
+      int v = wcnt[w * E_loc + e];
+      wcnt[w * E_loc + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  int32_t* my = wcnt + warp * E_loc;
+  for (int r = 0; r < kPermSlotsPerWarp; r += kWarp) {
+    long s = wbase + r + lane;
+    int e = -1;
+    if (s < S) e = local_expert(__ldg(ids + s), off, E_loc);
+    unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      int row = my[e] + __popc(peers & lt);
+      permuted_src[row] = (int32_t)s;
+      slot_to_row[s] = row;
+    } else if (s < S) {
+      slot_to_row[s] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && (peers & lt) == 0) my[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+static int g_scatter_smem_set[64];
+
+cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off, int tile_n,
+                           int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
+                           int32_t* permuted_src, int32_t* slot_to_row, int32_t* meta,
+                           int32_t* blk_counts, cudaStream_t st) {
+  long S = (long)T * K;
+  int nblk = (int)((S + kPermChunk - 1) / kPermChunk);
+  size_t hist_smem = sizeof(int32_t) * (size_t)E_loc;
+  size_t wcnt_smem = sizeof(int32_t) * (size_t)kPermWarps * E_loc;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && g_scatter_smem_set[dev] < (int)wcnt_smem) {
+    cudaError_t err = cudaFuncSetAttribute(permute_scatter_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)wcnt_smem);
+    if (err != cudaSuccess) return err;
+    g_scatter_smem_set[dev] = (int)wcnt_smem;
+  }
+  permute_count_kernel<<<nblk, kPermThreads, hist_smem, st>>>(ids, S, E_loc, off, blk_counts);
+  permute_scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, E_loc, S, tile_n, counts, offsets,
+                                          tile_offsets, permuted_src, meta);
+  permute_scatter_kernel<<<nblk, kPermThreads, wcnt_smem, st>>>(ids, S, E_loc, off, blk_counts,
+                                                                offsets, permuted_src, slot_to_row);
+  return cudaGetLastError();
+}
+
+size_t permute_scratch_bytes(int T, int K, int E_loc) {
+  long S = (long)T * K;
+  long nblk = (S + kPermChunk - 1) / kPermChunk;
+  return sizeof(int32_t) * (size_t)(nblk > 0 ? nblk : 1) * (size_t)(E_loc > 0 ? E_loc : 1);
+}
+
+}  // namespace situ

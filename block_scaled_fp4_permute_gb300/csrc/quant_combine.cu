@@ -1,0 +1,85 @@
+// quant_combine.cu -- the two HBM-bound elementwise steps of the layer.
+//
+// quant_mxfp8: bf16 activations -> MXFP8 (E4M3 + one UE8M0 scale per token
+// per 32 hidden elements; TokenSpeed SiTU, "Supported contract").  Four
+// lanes share one 32-element block: each lane loads 8 bf16 with one 128-bit
+// load (a warp reads 512 contiguous bytes), the block amax is reduced with
+// two shuffles, and each lane stores its 8 E4M3 codes with one 64-bit store.
+//
+// combine: the top-k-weighted un-permute sum out[t] = sum_j w[t,j] * Y[row]
+// over the kept slots in ascending j, accumulated in fp32 and rounded to
+// bf16 once (the golden loop of TensorRT-LLM PR #17865 adds
+// weight * expert output per slot); a token with no kept slot gets 0.  Each
+// thread owns 8 consecutive hidden elements and reads them with 128-bit
+// loads, so each row of Y is read fully coalesced.
+#include "situ_internal.h"
+
+namespace situ {
+
+__global__ void __launch_bounds__(256)
+quant_mxfp8_kernel(const uint4* __restrict__ x, long n_lanes, uint2* __restrict__ q,
+                   uint8_t* __restrict__ s) {
+  long gid = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  bool valid = gid < n_lanes;
+  uint4 v = valid ? __ldg(x + gid) : make_uint4(0, 0, 0, 0);
+  float f[8];
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { f[2 * i] = bf16_lo(w[i]); f[2 * i + 1] = bf16_hi(w[i]); }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  int e = mxfp8_exponent(amax);
+  float sc = exp2i(-e);
+  uint32_t c01 = f32x2_to_e4m3x2(f[0] * sc, f[1] * sc);
+  uint32_t c23 = f32x2_to_e4m3x2(f[2] * sc, f[3] * sc);
+  uint32_t c45 = f32x2_to_e4m3x2(f[4] * sc, f[5] * sc);
+  uint32_t c67 = f32x2_to_e4m3x2(f[6] * sc, f[7] * sc);
+  if (valid) {
+    q[gid] = make_uint2(c01 | (c23 << 16), c45 | (c67 << 16));
+    if ((gid & 3) == 0) s[gid >> 2] = (uint8_t)(e + 127);
+  }
+}
+
+cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t* s,
+                               cudaStream_t st) {
+  long n_lanes = (long)T * H / 8;
+  long blocks = (n_lanes + 255) / 256;
+  quant_mxfp8_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint4*)x, n_lanes, (uint2*)q, s);
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
+               const float* __restrict__ w, int K, int H8, uint4* __restrict__ out) {
+  int t = blockIdx.x;
+  int h8 = blockIdx.y * blockDim.x + threadIdx.x;
+  if (h8 >= H8) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < K; ++j) {
+    int r = __ldg(slot_to_row + (size_t)t * K + j);
+    if (r < 0) continue;
+    float wt = __ldg(w + (size_t)t * K + j);
+    uint4 v = __ldg(y + (size_t)r * H8 + h8);
+    uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wt, bf16_lo(p[i]), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wt, bf16_hi(p[i]), acc[2 * i + 1]);
+    }
+  }
+  out[(size_t)t * H8 + h8] = make_uint4(f32x2_to_bf16x2(acc[0], acc[1]), f32x2_to_bf16x2(acc[2], acc[3]),
+                                        f32x2_to_bf16x2(acc[4], acc[5]), f32x2_to_bf16x2(acc[6], acc[7]));
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,
+                           int H, void* out, cudaStream_t st) {
+  int H8 = H / 8;
+  dim3 grid(T, (H8 + 255) / 256);
+  combine_kernel<<<grid, 256, 0, st>>>((const uint4*)y, slot_to_row, w, K, H8, (uint4*)out);
+  return cudaGetLastError();
+}
+
+}  // namespace situ

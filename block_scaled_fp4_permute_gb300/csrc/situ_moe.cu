@@ -1,0 +1,261 @@
+// situ_moe.cu -- the C ABI (include/situ_moe.h): host-side validation,
+// workspace layout and the launch sequence of the layer.
+//
+// situ_moe_forward enqueues, on the caller's stream:
+//   permute (3 launches) -> gather -> FC1 (+SiTU) -> FC2 -> combine.
+// No host synchronisation: the number of kept rows and the GEMM token tiles
+// live on the device (written by the permute) and every later kernel reads
+// them there; grids are sized for the worst case and surplus CTAs exit.
+#include <cstring>
+
+#include "../../include/situ_moe.h"
+#include "situ_internal.h"
+
+using namespace situ;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t counts, offsets, tile_offsets, meta, psrc, s2r, blk, xperm, xg, h1, y, total;
+};
+
+Layout make_layout(const situ_moe_args* a) {
+  Layout L;
+  size_t o = 0;
+  const size_t S = (size_t)a->T * (size_t)a->top_k;
+  const size_t E = (size_t)a->num_local_experts;
+  auto take = [&](size_t bytes) { size_t at = o; o += align_up(bytes > 0 ? bytes : 1); return at; };
+  L.counts = take(4 * E);
+  L.offsets = take(4 * (E + 1));
+  L.tile_offsets = take(4 * (E + 1));
+  L.meta = take(16);
+  L.psrc = take(4 * S);
+  L.s2r = take(4 * S);
+  L.blk = take(permute_scratch_bytes(a->T, a->top_k, a->num_local_experts));
+  L.xperm = take(2 * S * (size_t)a->H);
+  L.xg = take(4 * S);
+  L.h1 = take(2 * S * (size_t)a->I);
+  L.y = take(2 * S * (size_t)a->H);
+  L.total = o;
+  return L;
+}
+
+situ_status check_routing(int32_t T, int32_t top_k, int32_t E_total, int32_t E_loc, int32_t off) {
+  if (T < 0 || top_k < 1 || top_k > SITU_MAX_TOP_K) return SITU_ERR_BAD_SHAPE;
+  if (E_loc < 1 || E_loc > SITU_MAX_LOCAL_EXPERTS || off < 0 || E_total < 1 ||
+      (int64_t)off + E_loc > (int64_t)E_total)
+    return SITU_ERR_BAD_SHAPE;
+  if ((int64_t)T * top_k > (int64_t)0x7FFFFFFF) return SITU_ERR_BAD_SHAPE;
+  return SITU_OK;
+}
+
+situ_status validate(const situ_moe_args* a) {
+  if (!a) return SITU_ERR_NULL_ARG;
+  situ_status s = check_routing(a->T, a->top_k, a->num_experts_total, a->num_local_experts,
+                                a->local_expert_offset);
+  if (s != SITU_OK) return s;
+  if (a->H <= 0 || a->I <= 0 || a->H % 32 || a->I % 32) return SITU_ERR_BAD_SHAPE;
+  const bool w4a16 = a->act_dtype == SITU_ACT_BF16 && a->weight_dtype == SITU_W_MXFP4;
+  const bool w4a8 = a->act_dtype == SITU_ACT_MXFP8 && a->weight_dtype == SITU_W_MXFP4;
+  const bool nv = a->act_dtype == SITU_ACT_NVFP4 && a->weight_dtype == SITU_W_NVFP4;
+  if (!(w4a16 || w4a8 || nv)) return SITU_ERR_UNSUPPORTED;
+  if (!a->topk_ids || !a->topk_weights || !a->w1 || !a->w1_scale || !a->w2 || !a->w2_scale ||
+      !a->gemm1_alpha || !a->gemm1_beta || !a->out)
+    return SITU_ERR_NULL_ARG;
+  if (w4a16 && !a->hidden_states) return SITU_ERR_NULL_ARG;
+  if ((w4a8 || nv) && (!a->hidden_states_q || !a->hidden_states_scale)) return SITU_ERR_NULL_ARG;
+  if (nv && (!a->hidden_states_gscale || !a->w1_gscale || !a->w2_gscale)) return SITU_ERR_NULL_ARG;
+  const void* ptrs[] = {a->hidden_states, a->hidden_states_q, a->hidden_states_scale,
+                        a->hidden_states_gscale, a->topk_ids, a->topk_weights, a->w1, a->w1_scale,
+                        a->w1_gscale, a->w2, a->w2_scale, a->w2_gscale, a->gemm1_alpha,
+                        a->gemm1_beta, a->g1_alphas, a->g1_alphas_up, a->g2_alphas, a->out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SITU_ERR_MISALIGNED;
+  return SITU_OK;
+}
+
+// Token-tile width of the grouped GEMMs: 8 * ns tokens, chosen from the
+// expected rows per expert (decode: 1-2 rows, prefill: hundreds).
+int choose_ns(const situ_moe_args* a) {
+  double avg = (double)a->T * a->top_k / (double)a->num_experts_total;
+  if (avg <= 6.0) return 1;
+  if (avg <= 12.0) return 2;
+  if (avg <= 24.0) return 4;
+  return 8;
+}
+
+situ_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SITU_OK : SITU_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* situ_status_string(situ_status s) {
+  switch (s) {
+    case SITU_OK: return "SITU_OK";
+    case SITU_ERR_NULL_ARG: return "SITU_ERR_NULL_ARG: a required pointer is NULL";
+    case SITU_ERR_BAD_SHAPE: return "SITU_ERR_BAD_SHAPE: unsupported or inconsistent sizes";
+    case SITU_ERR_UNSUPPORTED: return "SITU_ERR_UNSUPPORTED: unsupported format pair";
+    case SITU_ERR_WORKSPACE_TOO_SMALL: return "SITU_ERR_WORKSPACE_TOO_SMALL";
+    case SITU_ERR_CUDA: return "SITU_ERR_CUDA: a CUDA launch or call failed";
+    case SITU_ERR_MISALIGNED: return "SITU_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+  }
+  return "unknown situ_status";
+}
+
+size_t situ_moe_permute_workspace_size(int32_t T, int32_t top_k, int32_t num_local_experts) {
+  if (T < 0 || top_k < 1 || num_local_experts < 1) return 0;
+  return permute_scratch_bytes(T, top_k, num_local_experts);
+}
+
+situ_status situ_moe_permute(const int32_t* topk_ids, int32_t T, int32_t top_k,
+                             int32_t num_experts_total, int32_t num_local_experts,
+                             int32_t local_expert_offset, int32_t* expert_counts,
+                             int32_t* expert_offsets, int32_t* permuted_src,
+                             int32_t* slot_to_row, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  situ_status s = check_routing(T, top_k, num_experts_total, num_local_experts, local_expert_offset);
+  if (s != SITU_OK) return s;
+  if (T == 0) return SITU_OK;
+  if (!topk_ids || !expert_counts || !expert_offsets || !permuted_src || !slot_to_row || !workspace)
+    return SITU_ERR_NULL_ARG;
+  const void* ptrs[] = {topk_ids, expert_counts, expert_offsets, permuted_src, slot_to_row, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return SITU_ERR_MISALIGNED;
+  if (workspace_bytes < permute_scratch_bytes(T, top_k, num_local_experts))
+    return SITU_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_permute(topk_ids, T, top_k, num_local_experts, local_expert_offset, 1,
+                                    expert_counts, expert_offsets, nullptr, permuted_src,
+                                    slot_to_row, nullptr, (int32_t*)workspace,
+                                    (cudaStream_t)stream));
+}
+
+situ_status situ_moe_quant_mxfp8(const void* x_bf16, int32_t T, int32_t H, uint8_t* x_e4m3,
+                                 uint8_t* x_scale_ue8m0, void* stream) {
+  if (T < 0 || H <= 0 || H % 32) return SITU_ERR_BAD_SHAPE;
+  if (T == 0) return SITU_OK;
+  if (!x_bf16 || !x_e4m3 || !x_scale_ue8m0) return SITU_ERR_NULL_ARG;
+  if (!aligned16(x_bf16) || !aligned16(x_e4m3) || !aligned16(x_scale_ue8m0)) return SITU_ERR_MISALIGNED;
+  return cuda_status(launch_quant_mxfp8(x_bf16, T, H, x_e4m3, x_scale_ue8m0, (cudaStream_t)stream));
+}
+
+size_t situ_moe_workspace_size(const situ_moe_args* args) {
+  if (!args) return 0;
+  if (check_routing(args->T, args->top_k, args->num_experts_total, args->num_local_experts,
+                    args->local_expert_offset) != SITU_OK || args->H <= 0 || args->I <= 0)
+    return 0;
+  return make_layout(args).total;
+}
+
+static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t workspace_bytes,
+                                void* stream, void* const* events) {
+  situ_status s = validate(a);
+  if (s != SITU_OK) return s;
+  if (a->T == 0) return SITU_OK;
+  if (!workspace) return SITU_ERR_NULL_ARG;
+  if (!aligned16(workspace)) return SITU_ERR_MISALIGNED;
+  const Layout L = make_layout(a);
+  if (workspace_bytes < L.total) return SITU_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  int32_t* counts = (int32_t*)(ws + L.counts);
+  int32_t* offsets = (int32_t*)(ws + L.offsets);
+  int32_t* tile_offsets = (int32_t*)(ws + L.tile_offsets);
+  int32_t* meta = (int32_t*)(ws + L.meta);
+  int32_t* psrc = (int32_t*)(ws + L.psrc);
+  int32_t* s2r = (int32_t*)(ws + L.s2r);
+  uint16_t* xperm = (uint16_t*)(ws + L.xperm);
+  float* xg = (float*)(ws + L.xg);
+  uint16_t* h1 = (uint16_t*)(ws + L.h1);
+  uint16_t* y = (uint16_t*)(ws + L.y);
+  const bool nv = a->weight_dtype == SITU_W_NVFP4;
+  const int ns = choose_ns(a);
+  const int tile_n = 8 * ns;
+  const long S = (long)a->T * a->top_k;
+  const long max_tiles = S / tile_n + a->num_local_experts + 1;
+  auto mark = [&](int i) {
+    if (events) cudaEventRecord((cudaEvent_t)events[i], st);
+  };
+
+  mark(0);
+  cudaError_t err = launch_permute(a->topk_ids, a->T, a->top_k, a->num_local_experts,
+                                   a->local_expert_offset, tile_n, counts, offsets, tile_offsets,
+                                   psrc, s2r, meta, (int32_t*)(ws + L.blk), st);
+  if (err != cudaSuccess) return SITU_ERR_CUDA;
+  mark(1);
+
+  GatherParams gp;
+  gp.act = a->act_dtype;
+  gp.x_bf16 = a->hidden_states;
+  gp.x_q = a->hidden_states_q;
+  gp.x_s = a->hidden_states_scale;
+  gp.x_gs = a->hidden_states_gscale;
+  gp.permuted_src = psrc;
+  gp.meta = meta;
+  gp.top_k = a->top_k;
+  gp.H = a->H;
+  gp.S = S;
+  gp.x_perm = xperm;
+  gp.xg_perm = a->act_dtype == SITU_ACT_NVFP4 ? xg : nullptr;
+  if ((err = launch_gather(gp, st)) != cudaSuccess) return SITU_ERR_CUDA;
+  mark(2);
+
+  FcParams f;
+  std::memset(&f, 0, sizeof(f));
+  f.offsets = offsets;
+  f.tile_offsets = tile_offsets;
+  f.E_loc = a->num_local_experts;
+  f.I = a->I;
+  // FC1: W1 [E_loc, 2I, H], gate rows 0..I-1, up rows I..2I-1
+  f.w = a->w1;
+  f.ws = a->w1_scale;
+  f.Mtot = 2 * a->I;
+  f.K = a->H;
+  f.x = xperm;
+  f.n_mtiles = (a->I + 63) / 64;
+  f.beta = a->gemm1_alpha;
+  f.beta_lin = a->gemm1_beta;
+  f.alpha_g = a->g1_alphas;
+  f.alpha_u = a->g1_alphas_up;
+  f.w1_gs = a->w1_gscale;
+  f.xg = gp.xg_perm;
+  f.mxfp8_h = a->act_dtype == SITU_ACT_MXFP8;
+  f.h_out = h1;
+  if ((err = launch_fc(f, true, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+  mark(3);
+  // FC2: W2 [E_loc, H, I]
+  f.w = a->w2;
+  f.ws = a->w2_scale;
+  f.Mtot = a->H;
+  f.K = a->I;
+  f.x = h1;
+  f.n_mtiles = (a->H + 127) / 128;
+  f.alpha2 = a->g2_alphas;
+  f.w2_gs = a->w2_gscale;
+  f.y_out = y;
+  if ((err = launch_fc(f, false, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+  mark(4);
+
+  if ((err = launch_combine(y, s2r, a->topk_weights, a->T, a->top_k, a->H, a->out, st)) != cudaSuccess)
+    return SITU_ERR_CUDA;
+  mark(5);
+  return cuda_status(cudaGetLastError());
+}
+
+situ_status situ_moe_forward(const situ_moe_args* a, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  return forward_impl(a, workspace, workspace_bytes, stream, nullptr);
+}
+
+situ_status situ_moe_forward_profiled(const situ_moe_args* a, void* workspace,
+                                      size_t workspace_bytes, void* stream, void* const* events) {
+  if (!events) return SITU_ERR_NULL_ARG;
+  return forward_impl(a, workspace, workspace_bytes, stream, events);
+}
+
+}  // extern "C"

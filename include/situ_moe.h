@@ -1,0 +1,219 @@
+/*
+ * situ_moe.h -- C ABI of the GB300 (sm_103a) SiTU routed-MoE expert layer.
+ *
+ * The layer is the Kimi-K3 routed-expert MoE of the TokenSpeed SiTU page
+ * (pypi.org/project/tokenspeed-situ, "Supported contract" and "Activation
+ * precision (w4a16 vs w4a8)"): precomputed global top-k routing; a permute
+ * of the (token, slot) pairs by local expert that drops experts outside the
+ * rank's contiguous shard; FC1 gate/up with the SiTU gated activation; FC2;
+ * and a top-k-weighted un-permute sum that is a partial output the caller
+ * all-reduces across its MoE TP/EP group (this library performs no
+ * collective).
+ *
+ * Conventions, for every entry point:
+ *   - Pointers are DEVICE pointers unless stated otherwise, row-major and
+ *     contiguous, each 16-byte aligned.  The caller owns every buffer,
+ *     including the workspace; the library allocates no device memory and
+ *     keeps no state between calls.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     non-SITU_OK return means nothing was enqueued, except SITU_ERR_CUDA,
+ *     which reports a launch failure (cudaGetLastError) after enqueueing.
+ *   - Element formats: E2M1 (FP4) codes are packed two per byte, element 2i
+ *     in the low nibble of byte i; UE8M0 scales are one byte 2^(b-127);
+ *     E4M3 is the OCP "fn" variant (max 448, no infinities); bf16 is
+ *     IEEE binary32 truncated to its upper 16 bits.
+ *   - MXFP4 = E2M1 elements with one UE8M0 scale per 32 consecutive
+ *     elements along the contraction dimension; NVFP4 = E2M1 with one E4M3
+ *     scale per 16 plus an fp32 per-tensor global scale; MXFP8 = E4M3 with
+ *     one UE8M0 scale per 32.
+ */
+#ifndef SITU_MOE_H
+#define SITU_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum situ_status {
+  SITU_OK = 0,
+  SITU_ERR_NULL_ARG = 1,           /* a required pointer is NULL */
+  SITU_ERR_BAD_SHAPE = 2,          /* a size is negative, inconsistent or not a supported multiple */
+  SITU_ERR_UNSUPPORTED = 3,        /* unsupported (activation, weight) format pair or limit */
+  SITU_ERR_WORKSPACE_TOO_SMALL = 4,
+  SITU_ERR_CUDA = 5,               /* a CUDA launch or runtime call failed */
+  SITU_ERR_MISALIGNED = 6          /* a pointer is not 16-byte aligned */
+} situ_status;
+
+typedef enum situ_act_dtype {
+  SITU_ACT_BF16 = 0,   /* w4a16: bf16 activations */
+  SITU_ACT_MXFP8 = 1,  /* w4a8: MXFP8 activations + per-token hidden_states_scale */
+  SITU_ACT_NVFP4 = 2   /* NVFP4 activations with a per-token fp32 global scale */
+} situ_act_dtype;
+
+typedef enum situ_weight_dtype {
+  SITU_W_MXFP4 = 0,
+  SITU_W_NVFP4 = 1
+} situ_weight_dtype;
+
+/* Largest supported top-k and local expert count. */
+#define SITU_MAX_TOP_K 16
+#define SITU_MAX_LOCAL_EXPERTS 4096
+
+/* Human-readable name of a status code (static storage). */
+const char* situ_status_string(situ_status s);
+
+/* ------------------------------------------------------------------------
+ * situ_moe_permute -- group the (token, slot) pairs by local expert.
+ *
+ * Defined by TokenSpeed SiTU, "Supported contract": top-k expert IDs stay
+ * global (0..num_experts_total-1); experts outside the contiguous shard
+ * [local_expert_offset, local_expert_offset + num_local_experts) are
+ * filtered out.  Slot s = t*top_k + j of token t is kept when its ID lies in
+ * the shard (IDs outside it, including negative ones, are dropped).
+ *
+ *   topk_ids        int32 [T, top_k]               (input)
+ *   expert_counts   int32 [num_local_experts]      kept slots per local expert
+ *   expert_offsets  int32 [num_local_experts + 1]  exclusive prefix sum; the last
+ *                                                  entry is R, the kept-slot count
+ *   permuted_src    int32 [T*top_k]                row r < R holds the slot it came
+ *                                                  from; rows are grouped by local
+ *                                                  expert and ascending in slot
+ *                                                  index within an expert (a stable
+ *                                                  order); rows >= R hold -1
+ *   slot_to_row     int32 [T*top_k]                row of each slot, -1 if dropped
+ *   workspace       device scratch of at least situ_moe_permute_workspace_size()
+ *                   bytes; contents on entry are ignored
+ *
+ * All outputs are bit-exact and deterministic.  T == 0 launches nothing.
+ * Errors: NULL_ARG, BAD_SHAPE (T < 0, top_k not in 1..16, local shard not
+ * inside [0, num_experts_total), num_local_experts > 4096), MISALIGNED,
+ * WORKSPACE_TOO_SMALL, CUDA.
+ * --------------------------------------------------------------------- */
+size_t situ_moe_permute_workspace_size(int32_t T, int32_t top_k, int32_t num_local_experts);
+
+situ_status situ_moe_permute(const int32_t* topk_ids, int32_t T, int32_t top_k,
+                             int32_t num_experts_total, int32_t num_local_experts,
+                             int32_t local_expert_offset, int32_t* expert_counts,
+                             int32_t* expert_offsets, int32_t* permuted_src,
+                             int32_t* slot_to_row, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
+ * situ_moe_quant_mxfp8 -- quantise bf16 activations to MXFP8 (w4a8 chain).
+ *
+ * TokenSpeed SiTU, "Activation precision (w4a16 vs w4a8)" and "Supported
+ * contract": MXFP8 activations with a per-token hidden_states_scale
+ * block-scale tensor.  The pages do not fix the scale rule; this library
+ * uses, per token and per 32 consecutive hidden elements, the smallest
+ * power of two 2^e (e in [-127, 127]) with amax * 2^-e <= 448, stored as
+ * the UE8M0 byte e + 127 (an all-zero block gets byte 0), and rounds each
+ * element x * 2^-e to the nearest E4M3 value, ties to even, saturating.
+ *
+ *   x_bf16          bf16  [T, H]      (input; finite values)
+ *   x_e4m3          uint8 [T, H]      E4M3 codes
+ *   x_scale_ue8m0   uint8 [T, H/32]   hidden_states_scale
+ *
+ * Bit-exact.  H must be a positive multiple of 32; T == 0 launches nothing.
+ * Errors: NULL_ARG, BAD_SHAPE, MISALIGNED, CUDA.
+ * --------------------------------------------------------------------- */
+situ_status situ_moe_quant_mxfp8(const void* x_bf16, int32_t T, int32_t H, uint8_t* x_e4m3,
+                                 uint8_t* x_scale_ue8m0, void* stream);
+
+/* ------------------------------------------------------------------------
+ * situ_moe_forward -- the whole routed-expert layer.
+ *
+ * For each kept pair (t, j) with local expert e = topk_ids[t,j] - offset:
+ *   gate_i = g1_alphas[e]    * gs_gate * xs_t * <x_t, W1[e, i, :]>       i <  I
+ *   up_i   = g1_alphas_up[e] * gs_up   * xs_t * <x_t, W1[e, I+i, :]>
+ *   h_i    = [b*tanh(gate_i/b)*sigmoid(gate_i)] * [bl*tanh(up_i/bl)]
+ *            with b = gemm1_alpha[e], bl = gemm1_beta[e]
+ *   y      = g2_alphas[e] * gs_2 * H1 W2[e]^T,  H1 = h rounded to bf16
+ *            (w4a16, NVFP4) or MXFP8-quantised per 32 along I and
+ *            dequantised (w4a8)
+ *   out[t] = sum over kept j, ascending, of topk_weights[t,j] * y
+ * Sources: the SiTU formula is the golden `_situ_act` in TensorRT-LLM PR
+ * #17865 ("bring up Kimi K3 NVFP4 with CUTLASS and cuteDSL MegaMoE SiTU");
+ * the per-expert beta / linear beta from gemm1_alpha / gemm1_beta and the
+ * up half rescaled by g1_alphas_up / g1_alphas before the tanh are from the
+ * FlashInfer 0.6.18 SM100a+SM103a MoE-LoRA AOT release notes ("Changes since
+ * 875b7d7"); the FC1-w4a8 + FC2-w4a16 chain with the FC1 fp8 output
+ * dequantised before FC2 is TokenSpeed SiTU, "Activation precision".
+ * g1_alphas scales both FC1 halves and the up half is further rescaled by
+ * g1_alphas_up / g1_alphas, so the net up scale is g1_alphas_up.  A cap
+ * b or bl <= 0 switches that factor to its limit (gate*sigmoid(gate), up).
+ * gs_* are the NVFP4 per-tensor global scales (1 for MXFP4) and xs_t the
+ * NVFP4 per-token activation scale (1 otherwise).  Tokens with no kept
+ * slot get out = 0.  W1 rows 0..I-1 are the gate half, I..2I-1 the up half.
+ *
+ * Supported (act, weight) pairs: (BF16, MXFP4) w4a16, (MXFP8, MXFP4) w4a8,
+ * (NVFP4, NVFP4).  Shapes: H and I positive multiples of 32, top_k 1..16,
+ * the local shard inside [0, num_experts_total).  MXFP4 weight scale bytes
+ * must lie in [2, 252] so that every dequantised weight is a bf16 normal or
+ * zero (the layer's synthetic and real checkpoints are far inside this).
+ * --------------------------------------------------------------------- */
+typedef struct situ_moe_args {
+  int32_t T;                      /* tokens */
+  int32_t H;                      /* hidden size (FC1 K, FC2 N) */
+  int32_t I;                      /* intermediate size (FC1 has 2*I rows) */
+  int32_t num_experts_total;      /* global expert count (896 for Kimi-K3) */
+  int32_t num_local_experts;      /* E_loc */
+  int32_t local_expert_offset;    /* first global ID of the shard */
+  int32_t top_k;
+  int32_t act_dtype;              /* situ_act_dtype */
+  int32_t weight_dtype;           /* situ_weight_dtype */
+  const void* hidden_states;      /* bf16 [T, H] (SITU_ACT_BF16) */
+  const uint8_t* hidden_states_q; /* E4M3 [T, H] (MXFP8) or packed E2M1 [T, H/2] (NVFP4) */
+  const uint8_t* hidden_states_scale;  /* UE8M0 [T, H/32] (MXFP8) or E4M3 [T, H/16] (NVFP4) */
+  const float* hidden_states_gscale;   /* fp32 [T] per-token global scale (NVFP4) */
+  const int32_t* topk_ids;        /* int32 [T, top_k] global expert IDs */
+  const float* topk_weights;      /* fp32 [T, top_k] */
+  const uint8_t* w1;              /* packed E2M1 [E_loc, 2I, H/2] */
+  const uint8_t* w1_scale;        /* UE8M0 [E_loc, 2I, H/32] or E4M3 [E_loc, 2I, H/16] */
+  const float* w1_gscale;         /* fp32 [E_loc, 2] gate / up global scale (NVFP4) */
+  const uint8_t* w2;              /* packed E2M1 [E_loc, H, I/2] */
+  const uint8_t* w2_scale;        /* UE8M0 [E_loc, H, I/32] or E4M3 [E_loc, H, I/16] */
+  const float* w2_gscale;         /* fp32 [E_loc] (NVFP4) */
+  const float* gemm1_alpha;       /* fp32 [E_loc] SiTU beta, required */
+  const float* gemm1_beta;        /* fp32 [E_loc] SiTU linear beta, required */
+  const float* g1_alphas;         /* fp32 [E_loc] or NULL (1) */
+  const float* g1_alphas_up;      /* fp32 [E_loc] or NULL (1) */
+  const float* g2_alphas;         /* fp32 [E_loc] or NULL (1) */
+  void* out;                      /* bf16 [T, H] partial output of this shard */
+} situ_moe_args;
+
+/* Workspace bytes situ_moe_forward needs for these shapes (0 on bad args).
+ * It grows with T*top_k: permute arrays, the permuted activations
+ * [T*top_k, H] bf16, the FC1 output [T*top_k, I] bf16 and the FC2 output
+ * [T*top_k, H] bf16. */
+size_t situ_moe_workspace_size(const situ_moe_args* args);
+
+/* Errors: NULL_ARG (args, required pointers, gemm1_alpha / gemm1_beta --
+ * the SiTU caps have no default), BAD_SHAPE, UNSUPPORTED, MISALIGNED,
+ * WORKSPACE_TOO_SMALL, CUDA.  T == 0 launches nothing. */
+situ_status situ_moe_forward(const situ_moe_args* args, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* ------------------------------------------------------------------------
+ * situ_moe_forward_profiled -- situ_moe_forward plus stage timing events.
+ *
+ * Enqueues exactly the launches of situ_moe_forward and records, on the same
+ * stream, events[0] before the first launch and events[i] after stage i:
+ * 1 permute (3 launches), 2 gather, 3 FC1 + SiTU, 4 FC2, 5 combine.  `events`
+ * holds SITU_PROFILE_EVENTS cudaEvent_t handles (passed as void*) created by
+ * the caller with timing enabled.  Measurement aid only; the pages define no
+ * counterpart.  Errors: those of situ_moe_forward, NULL_ARG for a NULL
+ * events array.
+ * --------------------------------------------------------------------- */
+#define SITU_PROFILE_EVENTS 6
+situ_status situ_moe_forward_profiled(const situ_moe_args* args, void* workspace,
+                                      size_t workspace_bytes, void* stream, void* const* events);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SITU_MOE_H */

@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every function include/situ_moe.h declares, and rejects bad
+arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from block_scaled_fp4_permute_gb300 import binding, build
+
+HEADER = os.path.join(ROOT, "include", "situ_moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+([a-z_][a-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def test_header_declares_the_page_contract_calls():
+    names = declared_functions()
+    for n in ("situ_moe_permute", "situ_moe_quant_mxfp8", "situ_moe_forward",
+              "situ_moe_workspace_size", "situ_moe_permute_workspace_size", "situ_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    raw = ctypes.CDLL(binding.library_path())
+    for n in declared_functions():
+        assert hasattr(raw, n), n
+
+
+def _args(**over):
+    a = dict(T=4, H=64, I=32, num_experts_total=8, num_local_experts=8, local_expert_offset=0,
+             top_k=2, act_dtype=0, weight_dtype=0)
+    a.update(over)
+    s = binding.SituMoeArgs(**a)
+    for f in ("hidden_states", "topk_ids", "topk_weights", "w1", "w1_scale", "w2", "w2_scale",
+              "gemm1_alpha", "gemm1_beta", "out"):
+        setattr(s, f, 0x1000)     # never dereferenced: validation fails first or T == 0
+    return s
+
+
+def _fwd(lib, args, ws=0x2000, nbytes=1 << 40):
+    return lib.situ_moe_forward(ctypes.byref(args), ctypes.c_void_p(ws), nbytes, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(H=48), 2), (dict(I=40), 2), (dict(top_k=17), 2), (dict(top_k=0), 2), (dict(T=-1), 2),
+    (dict(local_expert_offset=4), 2), (dict(num_local_experts=0), 2),
+    (dict(num_local_experts=5000, num_experts_total=6000), 2),
+    (dict(act_dtype=1, weight_dtype=1), 3), (dict(act_dtype=0, weight_dtype=1), 3),
+])
+def test_forward_rejects_bad_shapes(lib, over, status):
+    assert _fwd(lib, _args(**over)) == status
+
+
+def test_forward_requires_situ_caps(lib):
+    # the SiTU caps have no default (TensorRT-LLM PR #17865 requires non-null
+    # swiglu_alpha / swiglu_beta for SiTU instead of a silent zero)
+    a = _args()
+    a.gemm1_beta = None
+    assert _fwd(lib, a) == 1
+    a = _args()
+    a.gemm1_alpha = None
+    assert _fwd(lib, a) == 1
+
+
+def test_forward_other_errors(lib):
+    a = _args()
+    a.w1 = 0x1001
+    assert _fwd(lib, a) == 6                         # misaligned
+    assert _fwd(lib, _args(), nbytes=16) == 4        # workspace too small
+    assert _fwd(lib, _args(), ws=0) == 1
+    a = _args(act_dtype=1)                           # MXFP8 needs hidden_states_q / scale
+    assert _fwd(lib, a) == 1
+    assert _fwd(lib, _args(T=0)) == 0                # nothing to do, nothing launched
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    small = lib.situ_moe_workspace_size(ctypes.byref(_args(T=4)))
+    big = lib.situ_moe_workspace_size(ctypes.byref(_args(T=400)))
+    assert 0 < small < big
+    assert lib.situ_moe_workspace_size(ctypes.byref(_args(top_k=0))) == 0
+
+
+def test_permute_and_quant_validation(lib):
+    vp = ctypes.c_void_p
+    ok_ptr = vp(0x1000)
+    assert lib.situ_moe_permute(ok_ptr, 4, 0, 8, 8, 0, ok_ptr, ok_ptr, ok_ptr, ok_ptr, ok_ptr,
+                                1 << 20, None) == 2
+    assert lib.situ_moe_permute(ok_ptr, 4, 2, 8, 8, 1, ok_ptr, ok_ptr, ok_ptr, ok_ptr, ok_ptr,
+                                1 << 20, None) == 2
+    assert lib.situ_moe_permute(ok_ptr, 4, 2, 8, 8, 0, ok_ptr, ok_ptr, ok_ptr, ok_ptr, ok_ptr,
+                                0, None) == 4
+    assert lib.situ_moe_permute(None, 4, 2, 8, 8, 0, ok_ptr, ok_ptr, ok_ptr, ok_ptr, ok_ptr,
+                                1 << 20, None) == 1
+    assert lib.situ_moe_permute(None, 0, 2, 8, 8, 0, None, None, None, None, None, 0, None) == 0
+    assert lib.situ_moe_quant_mxfp8(ok_ptr, 4, 48, ok_ptr, ok_ptr, None) == 2
+    assert lib.situ_moe_quant_mxfp8(None, 4, 64, ok_ptr, ok_ptr, None) == 1
+    assert lib.situ_moe_quant_mxfp8(vp(0x1008), 4, 64, ok_ptr, ok_ptr, None) == 6
+    assert lib.situ_moe_quant_mxfp8(None, 0, 64, None, None, None) == 0
+    assert lib.situ_moe_permute_workspace_size(100, 16, 896) >= 4 * 896
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert binding.status_string(s).startswith("SITU_")

@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_kernel(const FcParams p) {
                             f32x2_to_bf16x2(v[8 * q + 4], v[8 * q + 5]), f32x2_to_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     }
   } else {
-    uint16_t* sY = reinterpret_cast<uint16_t*>(smem);   // [NT][128]
+    float* sY = reinterpret_cast<float*>(smem);   // [NT][128] fp32
     const float scale = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * (NV ? __ldg(p.w2_gs + e) : 1.f);
     const int nl = warp * 16 + g;
 #pragma unroll
@@ -270,18 +270,17 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_kernel(const FcParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int tok = 8 * j + 2 * c + h;
-        uint32_t pr = f32x2_to_bf16x2(acc[j][h] * scale, acc[j][2 + h] * scale);
-        sY[tok * 128 + nl] = (uint16_t)(pr & 0xFFFFu);
-        sY[tok * 128 + nl + 8] = (uint16_t)(pr >> 16);
+        sY[tok * 128 + nl] = acc[j][h] * scale;
+        sY[tok * 128 + nl + 8] = acc[j][2 + h] * scale;
       }
     }
     __syncthreads();
-    for (int idx = tid; idx < NT * 16; idx += kFcThreads) {
-      const int tok = idx >> 4, ch = idx & 15;
-      const int n0 = mt * 128 + ch * 8;
+    for (int idx = tid; idx < NT * 32; idx += kFcThreads) {
+      const int tok = idx >> 5, ch = idx & 31;
+      const int n0 = mt * 128 + ch * 4;
       if (tok >= nrows || n0 >= p.Mtot) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(sY + tok * 128 + ch * 8);
-      *reinterpret_cast<uint4*>(p.y_out + (size_t)(row0 + tok) * p.Mtot + n0) = v;
+      const float4 v = *reinterpret_cast<const float4*>(sY + tok * 128 + ch * 4);
+      *reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + tok) * p.Mtot + n0) = v;
     }
   }
 }

@@ -7,8 +7,8 @@
 // two shuffles, and each lane stores its 8 E4M3 codes with one 64-bit store.
 //
 // combine: the top-k-weighted un-permute sum out[t] = sum_j w[t,j] * Y[row]
-// over the kept slots in ascending j, accumulated in fp32 and rounded to
-// bf16 once (the golden loop of TensorRT-LLM PR #17865 adds
+// over the kept slots in ascending j, from the fp32 FC2 output, accumulated
+// in fp32 and rounded to bf16 once (the golden loop of TensorRT-LLM PR #17865 adds
 // weight * expert output per slot); a token with no kept slot gets 0.  Each
 // thread owns 8 consecutive hidden elements and reads them with 128-bit
 // loads, so each row of Y is read fully coalesced.
@@ -52,7 +52,7 @@ cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t*
 }
 
 __global__ void __launch_bounds__(256)
-combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
+combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
                const float* __restrict__ w, int K, int H8, uint4* __restrict__ out) {
   int t = blockIdx.x;
   int h8 = blockIdx.y * blockDim.x + threadIdx.x;
@@ -62,13 +62,12 @@ combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ slot_to_
     int r = __ldg(slot_to_row + (size_t)t * K + j);
     if (r < 0) continue;
     float wt = __ldg(w + (size_t)t * K + j);
-    uint4 v = __ldg(y + (size_t)r * H8 + h8);
-    uint32_t p[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = fmaf(wt, bf16_lo(p[i]), acc[2 * i]);
-      acc[2 * i + 1] = fmaf(wt, bf16_hi(p[i]), acc[2 * i + 1]);
-    }
+    const float4 v0 = __ldg(y + ((size_t)r * H8 + h8) * 2);
+    const float4 v1 = __ldg(y + ((size_t)r * H8 + h8) * 2 + 1);
+    acc[0] = fmaf(wt, v0.x, acc[0]); acc[1] = fmaf(wt, v0.y, acc[1]);
+    acc[2] = fmaf(wt, v0.z, acc[2]); acc[3] = fmaf(wt, v0.w, acc[3]);
+    acc[4] = fmaf(wt, v1.x, acc[4]); acc[5] = fmaf(wt, v1.y, acc[5]);
+    acc[6] = fmaf(wt, v1.z, acc[6]); acc[7] = fmaf(wt, v1.w, acc[7]);
   }
   out[(size_t)t * H8 + h8] = make_uint4(f32x2_to_bf16x2(acc[0], acc[1]), f32x2_to_bf16x2(acc[2], acc[3]),
                                         f32x2_to_bf16x2(acc[4], acc[5]), f32x2_to_bf16x2(acc[6], acc[7]));
@@ -78,7 +77,7 @@ cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const floa
                            int H, void* out, cudaStream_t st) {
   int H8 = H / 8;
   dim3 grid(T, (H8 + 255) / 256);
-  combine_kernel<<<grid, 256, 0, st>>>((const uint4*)y, slot_to_row, w, K, H8, (uint4*)out);
+  combine_kernel<<<grid, 256, 0, st>>>((const float4*)y, slot_to_row, w, K, H8, (uint4*)out);
   return cudaGetLastError();
 }
 

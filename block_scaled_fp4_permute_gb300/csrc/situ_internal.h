@@ -43,7 +43,7 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t st);
 // One grouped GEMM over the token tiles built by the permute:
 // rows of W (block-scaled FP4, one matrix per local expert) times the
 // expert's permuted bf16 activation rows, with the FC1 (SiTU) or FC2
-// (scale + bf16) epilogue.
+// (scale, fp32 output) epilogue.
 struct FcParams {
   const uint8_t* w;              // packed E2M1 [E_loc, Mtot, K/2]
   const uint8_t* ws;             // block scales [E_loc, Mtot, K/bs]
@@ -59,7 +59,7 @@ struct FcParams {
   uint16_t* h_out;               // bf16 [S, I]
   // FC2
   const float *alpha2, *w2_gs;
-  uint16_t* y_out;               // bf16 [S, H]
+  float* y_out;                  // fp32 [S, H]
 };
 cudaError_t launch_fc(const FcParams& p, bool fc1, bool nvfp4, int ns, long max_tiles,
                       cudaStream_t st);

@@ -18,7 +18,8 @@ namespace {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, uintptr_t a) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, meta, psrc, s2r, blk, xperm, xg, h1, y, total;
@@ -40,7 +41,7 @@ Layout make_layout(const situ_moe_args* a) {
   L.xperm = take(2 * S * (size_t)a->H);
   L.xg = take(4 * S);
   L.h1 = take(2 * S * (size_t)a->I);
-  L.y = take(2 * S * (size_t)a->H);
+  L.y = take(4 * S * (size_t)a->H);
   L.total = o;
   return L;
 }
@@ -64,18 +65,24 @@ situ_status validate(const situ_moe_args* a) {
   const bool w4a8 = a->act_dtype == SITU_ACT_MXFP8 && a->weight_dtype == SITU_W_MXFP4;
   const bool nv = a->act_dtype == SITU_ACT_NVFP4 && a->weight_dtype == SITU_W_NVFP4;
   if (!(w4a16 || w4a8 || nv)) return SITU_ERR_UNSUPPORTED;
+  if (a->T == 0) return SITU_OK;
   if (!a->topk_ids || !a->topk_weights || !a->w1 || !a->w1_scale || !a->w2 || !a->w2_scale ||
       !a->gemm1_alpha || !a->gemm1_beta || !a->out)
     return SITU_ERR_NULL_ARG;
   if (w4a16 && !a->hidden_states) return SITU_ERR_NULL_ARG;
   if ((w4a8 || nv) && (!a->hidden_states_q || !a->hidden_states_scale)) return SITU_ERR_NULL_ARG;
   if (nv && (!a->hidden_states_gscale || !a->w1_gscale || !a->w2_gscale)) return SITU_ERR_NULL_ARG;
-  const void* ptrs[] = {a->hidden_states, a->hidden_states_q, a->hidden_states_scale,
-                        a->hidden_states_gscale, a->topk_ids, a->topk_weights, a->w1, a->w1_scale,
-                        a->w1_gscale, a->w2, a->w2_scale, a->w2_gscale, a->gemm1_alpha,
-                        a->gemm1_beta, a->g1_alphas, a->g1_alphas_up, a->g2_alphas, a->out};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return SITU_ERR_MISALIGNED;
+  // vector-loaded tensors need 16 bytes, scale rows 2 (NVFP4 reads scale
+  // pairs), fp32 / int32 vectors 4
+  const void* p16[] = {a->hidden_states, a->hidden_states_q, a->w1, a->w2, a->out};
+  const void* p4[] = {a->hidden_states_gscale, a->topk_ids, a->topk_weights, a->w1_gscale,
+                      a->w2_gscale, a->gemm1_alpha, a->gemm1_beta, a->g1_alphas,
+                      a->g1_alphas_up, a->g2_alphas};
+  for (const void* p : p16)
+    if (!aligned_to(p, 16)) return SITU_ERR_MISALIGNED;
+  for (const void* p : p4)
+    if (!aligned_to(p, 4)) return SITU_ERR_MISALIGNED;
+  if (!aligned_to(a->w1_scale, 2) || !aligned_to(a->w2_scale, 2)) return SITU_ERR_MISALIGNED;
   return SITU_OK;
 }
 
@@ -172,7 +179,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   uint16_t* xperm = (uint16_t*)(ws + L.xperm);
   float* xg = (float*)(ws + L.xg);
   uint16_t* h1 = (uint16_t*)(ws + L.h1);
-  uint16_t* y = (uint16_t*)(ws + L.y);
+  float* y = (float*)(ws + L.y);
   const bool nv = a->weight_dtype == SITU_W_NVFP4;
   const int ns = choose_ns(a);
   const int tile_n = 8 * ns;

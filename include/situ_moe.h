@@ -12,7 +12,11 @@
  *
  * Conventions, for every entry point:
  *   - Pointers are DEVICE pointers unless stated otherwise, row-major and
- *     contiguous, each 16-byte aligned.  The caller owns every buffer,
+ *     contiguous.  Activation, packed-weight, output and workspace pointers
+ *     must be 16-byte aligned, block-scale arrays 2-byte aligned, fp32 and
+ *     int32 vectors 4-byte aligned (SITU_ERR_MISALIGNED otherwise).  For
+ *     situ_moe_permute and situ_moe_quant_mxfp8 every pointer must be
+ *     16-byte aligned.  The caller owns every buffer,
  *     including the workspace; the library allocates no device memory and
  *     keeps no state between calls.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as

@@ -1,12 +1,15 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle.
 
-Bars: permute outputs and MXFP8 bytes bit-exact; layer outputs within
-max|gpu - oracle| <= 2e-2 * rms(oracle) and cosine >= 0.999 (the float
-parity bar of this layer; the pages' own op-level check reports cosine 0.986
-against a dequantised bf16 reference at H=3584, I=384, FlashInfer 0.6.18
-MoE-LoRA AOT release notes, "Validation").  Large shapes run the full layer
-on the GPU and compare a seeded subset of tokens with the oracle (rows are
-independent given the routing).
+Bars: permute outputs and MXFP8 bytes bit-exact.  Layer outputs: per
+element |gpu - oracle| <= 2e-2 * rms(oracle) + ulp_bf16(oracle) / 2, and
+cosine >= 0.999.  The second term is the rounding of the layer's bf16
+output itself, which the fp64 oracle does not perform; at tokens whose
+output is ten or more times the rms (routing with few kept slots) half an
+ulp alone exceeds 2% of the rms.  For context, the pages' own op-level check
+reports cosine 0.986 against a dequantised bf16 reference at H=3584, I=384
+(FlashInfer 0.6.18 MoE-LoRA AOT release notes, "Validation").  Large shapes
+run the full layer on the GPU and compare a seeded subset of tokens with
+the oracle (rows are independent given the routing).
 """
 import functools
 
@@ -36,17 +39,25 @@ def wl_(name, **kw):
     return _wl(name, **kw)
 
 
-def assert_parity(got, ref, what=""):
+def half_ulp_bf16(x):
+    """Half a unit in the last place of bf16 at |x| (8 significant bits)."""
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
+
+
+def assert_parity(got, ref, what="", bf16_out=True):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape
     assert np.all(np.isfinite(got)), what
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    err = float(np.max(np.abs(got - ref)))
+    excess = np.abs(got - ref) - (half_ulp_bf16(ref) if bf16_out else 0.0)
+    err = float(np.max(excess))
     den = float(np.sqrt((got ** 2).sum() * (ref ** 2).sum()))
-    cos = float((got * ref).sum() / den) if den > 0 else (1.0 if err == 0 else 0.0)
+    cos = float((got * ref).sum() / den) if den > 0 else (1.0 if err <= 0 else 0.0)
     assert rms > 0, what
-    assert err <= TOL_REL * rms, f"{what}: max err {err:.3e} > {TOL_REL} * rms {rms:.3e}"
+    assert err <= TOL_REL * rms, f"{what}: max err beyond bf16 rounding {err:.3e} > {TOL_REL} * rms {rms:.3e}"
     assert cos >= TOL_COS, f"{what}: cosine {cos:.6f}"
     return err / rms, cos
 
@@ -246,6 +257,7 @@ def test_eight_shards_sum_to_unsharded():
         _, part = run_layer(sh)
         acc += part
     assert_parity(acc, oracle_out(wl), "sum of 8 shards vs oracle")
+    # both sides are sums of bf16-rounded outputs: allow their rounding too
     assert_parity(acc, full, "sum of 8 shards vs unsharded GPU")
 
 

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             l.situ_moe_permute_workspace_size.argtypes = [i32, i32, i32]
             l.situ_moe_permute.restype = ctypes.c_int
             l.situ_moe_permute.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+            l.situ_moe_permute_noalloc.restype = ctypes.c_int
+            l.situ_moe_permute_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
             l.situ_moe_quant_mxfp8.restype = ctypes.c_int
             l.situ_moe_quant_mxfp8.argtypes = [vp, i32, i32, vp, vp, vp]
             l.situ_moe_workspace_size.restype = sz
@@ -117,6 +119,27 @@ def situ_moe_permute(topk_ids: torch.Tensor, num_experts_total: int, num_local_e
     _check("situ_moe_permute", lib().situ_moe_permute(
         _p(topk_ids.contiguous()), T, K, num_experts_total, num_local_experts, local_expert_offset,
         _p(counts), _p(offsets), _p(psrc), _p(s2r), _p(ws), ws.numel(), _stream(stream)))
+    return counts, offsets, psrc[:T * K], s2r[:T * K]
+
+
+def situ_moe_permute_noalloc(topk_ids: torch.Tensor, num_experts_total: int,
+                             num_local_experts: int, local_expert_offset: int, out=None,
+                             stream=None):
+    """situ_moe_permute with the library's fixed scratch instead of a
+    workspace.  ``out`` = (counts, offsets, permuted_src, slot_to_row)
+    preallocated by the caller; without it they are allocated here with torch
+    (the C entry point itself never allocates)."""
+    T, K = topk_ids.shape
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(num_local_experts, dtype=torch.int32, device=dev),
+               torch.empty(num_local_experts + 1, dtype=torch.int32, device=dev),
+               torch.empty(max(T * K, 1), dtype=torch.int32, device=dev),
+               torch.empty(max(T * K, 1), dtype=torch.int32, device=dev))
+    counts, offsets, psrc, s2r = out
+    _check("situ_moe_permute_noalloc", lib().situ_moe_permute_noalloc(
+        _p(topk_ids), T, K, num_experts_total, num_local_experts, local_expert_offset,
+        _p(counts), _p(offsets), _p(psrc), _p(s2r), _stream(stream)))
     return counts, offsets, psrc[:T * K], s2r[:T * K]
 
 

@@ -108,6 +108,42 @@ situ_status situ_moe_permute(const int32_t* topk_ids, int32_t T, int32_t top_k,
                              void* stream);
 
 /* ------------------------------------------------------------------------
+ * situ_moe_permute_noalloc -- situ_moe_permute without a caller workspace.
+ *
+ * The paper has no counterpart to this call; it is a convenience of this
+ * library for callers that cannot allocate device memory where they route
+ * tokens.  Examples: a serving engine that hands all device memory to its own
+ * pool at start-up, or code in a region where a cudaMalloc would synchronise
+ * the device or is not permitted at all.  Such a caller has nowhere to get
+ * the permute's scratch from.
+ *
+ * Inputs, outputs, ordering and errors are those of situ_moe_permute.  The
+ * scratch (the per-chunk expert counts) lives in a fixed array inside the
+ * library: SITU_NOALLOC_SCRATCH_INTS int32 (4 MiB), which every GPU that
+ * loads the library holds until the process exits.  The call never calls
+ * cudaMalloc, cudaFree or any other allocating routine.
+ *
+ * Limit: ceil(T*top_k / 4096) * num_local_experts must not exceed
+ * SITU_NOALLOC_SCRATCH_INTS (for 896 local experts: T*top_k up to 4,792,320
+ * slots); a larger request returns SITU_ERR_WORKSPACE_TOO_SMALL and launches
+ * nothing.
+ *
+ * The first call on each device looks up the array's device address with
+ * that device current (cudaGetSymbolAddress), so make that first call before
+ * any stream capture.  All calls share the one array, which keeps whatever
+ * the last call left in it; nothing in it has to start at zero, because
+ * each call writes every entry it later reads.  Calls whose kernels can
+ * overlap on the GPU (different streams, or unordered host threads) race on
+ * the array and must be serialised by the caller.
+ * --------------------------------------------------------------------- */
+#define SITU_NOALLOC_SCRATCH_INTS (1 << 20)
+situ_status situ_moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t top_k,
+                                     int32_t num_experts_total, int32_t num_local_experts,
+                                     int32_t local_expert_offset, int32_t* expert_counts,
+                                     int32_t* expert_offsets, int32_t* permuted_src,
+                                     int32_t* slot_to_row, void* stream);
+
+/* ------------------------------------------------------------------------
  * situ_moe_quant_mxfp8 -- quantise bf16 activations to MXFP8 (w4a8 chain).
  *
  * TokenSpeed SiTU, "Activation precision (w4a16 vs w4a8)" and "Supported

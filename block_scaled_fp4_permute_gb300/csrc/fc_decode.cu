@@ -1,0 +1,550 @@
+// fc_decode.cu -- FC1 (gate/up + SiTU) and FC2 for decode-sized token tiles.
+//
+// Decode streams every touched expert's FP4 weights once and has one or two
+// tokens per expert, so the bound is HBM bandwidth plus the ALU work of
+// turning FP4 into MMA operands.  This kernel keeps the latter small:
+//   * E2M1 codes become f16 pairs with the hardware conversion
+//     (cvt.rn.f16x2.e2m1x2, exact), one instruction per two weights;
+//   * weight block scales are applied in fp32 after each block's MMAs
+//     (acc += scale * partial), the way a block-scaled MMA applies them,
+//     instead of rescaling every weight;
+//   * activations are converted once per CTA to f16 mantissas.  bf16 rows
+//     take one power-of-two scale per token that puts the row maximum in
+//     [2^14, 2^15) (exact for every element within 2^-28 of the row
+//     maximum); NVFP4 rows convert exactly with their E4M3 block scales
+//     folded in and the fp32 global scale per token; MXFP8 rows convert
+//     exactly and keep their UE8M0 scale per (token, 32-block), applied with
+//     the weight scale.  Per-token scales are applied once in the epilogue.
+// The token tile (8 rows) is staged for the whole K at CTA start (FC1
+// gathers its rows straight from the token-major input through
+// permuted_src; bf16 rows arrive by cp.async and are converted in place),
+// after the CTA has started its weight stream.  Each warp streams its own
+// 16 weight rows through a kST-stage shared ring with 16-byte cp.async
+// copies (full sectors, asynchronous); the stream runs on across the
+// m-tiles a CTA owns, so the next m-tile's loads overlap an epilogue.
+//
+// Fragment mapping (m16n8k16, A = weights, B = tokens): within a 32-element
+// MXFP4 block lane (g, c) owns elements 8c..8c+7 of rows g and g+8, so one
+// 4-byte read per row feeds both k16 steps of the block; for NVFP4 the lane
+// owns elements 16s + 4c..+3 of step s, which keeps each step inside one
+// 16-element scale block.  The K order is permuted identically in A and B,
+// so the contraction is unchanged.
+#include "situ_internal.h"
+
+namespace situ {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kNT = 8;                  // tokens per CTA
+constexpr int kST = 6;                  // weight-ring stages per warp (128-element chunks)
+constexpr int kStageBytes = 16 * 64;    // one chunk of the warp's 16 rows
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// four E2M1 pairs (one 32-bit word, byte j = elements 2j, 2j+1) -> f16 pairs
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* d) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(w));
+}
+
+// two E2M1 pairs in the low 16 bits -> f16 pairs
+__device__ __forceinline__ void e2m1x4_to_f16x4(uint32_t w, uint32_t* d) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %2;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n}"
+      : "=r"(d[0]), "=r"(d[1])
+      : "r"(w));
+}
+
+// two E4M3 codes (low byte -> low half) -> f16 pair, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t ldg32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg8(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0));
+}
+
+// UE8M0 byte in [1, 254] as an fp32 power of two (byte 0, reserved for
+// all-zero blocks, gives 0)
+__device__ __forceinline__ float ue8m0_f32(uint32_t b) { return __uint_as_float(b << 23); }
+
+// Row stride of the staged activation tile, in bytes: 2K padded so that the
+// fragment loads of a quarter warp (LDS.128, MXFP4 mapping) or half warp
+// (LDS.64, NVFP4 mapping) hit distinct banks.
+__host__ __device__ __forceinline__ int x_stride(int K, bool nv) {
+  int s = 2 * K;
+  int want = nv ? 32 : 64;
+  return s + ((want - (s % 128)) % 128 + 128) % 128;
+}
+
+}  // namespace
+
+// ABLK: activation scales per (token, 32-block) (MXFP8 rows); otherwise one
+// scale per token.
+template <bool FC1, bool WNV, bool ABLK>
+__global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_src[kNT];
+  __shared__ float s_tok[kNT];       // per-token activation scale
+  __shared__ unsigned s_amax[kNT];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  const int K = p.K;
+  const int nkb = K / 32;
+  const int stride = x_stride(K, WNV);
+  uint8_t* sX = smem;                                               // [kNT][stride]
+  float* sS = reinterpret_cast<float*>(smem + kNT * stride);        // [nkb][kNT] (ABLK)
+  float* sE = sS + nkb * kNT;                                       // epilogue [kNT][128]
+  uint8_t* sWw = reinterpret_cast<uint8_t*>(sE + kNT * 128) + warp * kST * kStageBytes;
+
+  const int ngroups = (p.n_mtiles + p.mg - 1) / p.mg;
+  const int grp = blockIdx.x % ngroups;
+  const int tile = blockIdx.x / ngroups;
+  const int total = __ldg(p.tile_offsets + p.E_loc);
+  if (tile >= total) return;
+  const int2 ti = __ldg(p.tile_info + tile);
+  const int e = ti.x;
+  const int row0 = ti.y;
+  const int nrows = min(kNT, __ldg(p.offsets + e + 1) - row0);
+  const int mt0 = grp * p.mg;
+  const int mcount = min(p.mg, p.n_mtiles - mt0);
+  const int nch = (nkb + 3) / 4;
+  const int steps = mcount * nch;
+  const int bsz = WNV ? 16 : 32;
+  const size_t wrow = (size_t)(K / 2), srow = (size_t)(K / bsz);
+  const uint8_t* wexp = p.w + (size_t)e * p.Mtot * wrow;
+  const uint8_t* sexp = p.ws + (size_t)e * p.Mtot * srow;
+  const bool scale_words = !WNV && ((nkb & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.ws) & 3) == 0);
+
+  // weight row r16 (0..15 of the warp's 16) of m-tile mt
+  auto row_of = [&](int mt, int r16, bool& v) -> int {
+    if (FC1) {
+      const int i = mt * 64 + warp * 8 + (r16 & 7);
+      v = i < p.I;
+      return r16 < 8 ? i : p.I + i;
+    }
+    const int r = mt * 128 + warp * 16 + r16;
+    v = r < p.Mtot;
+    return r;
+  };
+
+  // ---- weight ring: piece p of row r at r*64 + 16*(p ^ ((r>>1)&3)) ----
+  const uint32_t sw_u = smem_addr(sWw);
+  uint32_t SA[kST], SB[kST], NA[kST][2], NB[kST][2];
+  int ld_mi = -1, ld_cc = nch - 1;        // position of the last issued chunk
+  const uint8_t *cpA = wexp, *cpB = wexp, *scA = sexp, *scB = sexp;
+  bool cvA = false, cvB = false, fvA = false, fvB = false;
+  auto issue = [&](int u, uint32_t& sA, uint32_t& sB, uint32_t* nA, uint32_t* nB) {
+    if (++ld_cc == nch) {   // next m-tile: recompute the row pointers once
+      ld_cc = 0;
+      ++ld_mi;
+      const int mt = mt0 + ld_mi;
+      const int rc = lane >> 2;
+      int r;
+      r = row_of(mt, rc, cvA);
+      cpA = wexp + (size_t)(cvA ? r : 0) * wrow;
+      r = row_of(mt, rc + 8, cvB);
+      cpB = wexp + (size_t)(cvB ? r : 0) * wrow;
+      r = row_of(mt, g, fvA);
+      scA = sexp + (size_t)(fvA ? r : 0) * srow;
+      r = row_of(mt, g + 8, fvB);
+      scB = sexp + (size_t)(fvB ? r : 0) * srow;
+    }
+    const bool live = u < steps;
+    const int cc = ld_cc;
+    const int slot = u % kST;
+    const int piece = lane & 3, rc = lane >> 2;
+    const int b = cc * 4 + piece;
+    const bool kb = live && b < nkb;
+    const uint32_t st = sw_u + slot * kStageBytes;
+    cp_async16(st + rc * 64 + 16 * (piece ^ ((rc >> 1) & 3)), cpA + (kb && cvA ? b * 16 : 0), kb && cvA);
+    cp_async16(st + (rc + 8) * 64 + 16 * (piece ^ (((rc + 8) >> 1) & 3)), cpB + (kb && cvB ? b * 16 : 0),
+               kb && cvB);
+    asm volatile("cp.async.commit_group;");
+    const bool va = live && fvA, vb = live && fvB;
+    if (WNV) {   // two E4M3 scales per block: blocks 2h, 2h+1 of the chunk in nA[h]
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t xa = 0u, xb = 0u;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int bq = cc * 4 + 2 * h + q;
+          if (bq < nkb) {
+            xa |= (va ? ldg16(scA + 2 * bq) : 0u) << (16 * q);
+            xb |= (vb ? ldg16(scB + 2 * bq) : 0u) << (16 * q);
+          }
+        }
+        nA[h] = xa;
+        nB[h] = xb;
+      }
+    } else if (scale_words) {
+      const bool kv = cc * 4 < nkb;
+      sA = (va && kv) ? ldg32(scA + cc * 4) : 0u;
+      sB = (vb && kv) ? ldg32(scB + cc * 4) : 0u;
+    } else {
+      sA = sB = 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int bq = cc * 4 + q;
+        if (bq < nkb) {
+          sA |= (va ? ldg8(scA + bq) : 0u) << (8 * q);
+          sB |= (vb ? ldg8(scB + bq) : 0u) << (8 * q);
+        }
+      }
+    }
+  };
+
+  // start the weight stream (kST - 1 chunks) before staging the activations
+#pragma unroll
+  for (int i = 0; i < kST - 1; ++i) issue(i, SA[i], SB[i], NA[i], NB[i]);
+
+  // ---- stage the token tile as f16 mantissas ----
+  if (tid < kNT) {
+    s_src[tid] = tid < nrows ? (p.row_src ? __ldg(p.row_src + row0 + tid) / p.top_k : row0 + tid) : -1;
+    s_amax[tid] = 0u;
+  }
+  __syncthreads();
+  {
+    const int k8n = K / 8;
+    const int items = kNT * k8n;
+    if (p.act == 0) {
+      // raw bf16 rows land in place with cp.async; one scale per token row
+      const uint32_t sx_u = smem_addr(sX);
+      for (int it = tid; it < items; it += kThreads) {
+        const int tok = it / k8n, k8 = it - tok * k8n;
+        const int t = s_src[tok];
+        cp_async16(sx_u + tok * stride + k8 * 16,
+                   reinterpret_cast<const uint4*>(p.xa) + (size_t)(t >= 0 ? t : 0) * k8n + k8, t >= 0);
+      }
+      asm volatile("cp.async.commit_group;");
+      asm volatile("cp.async.wait_group 0;");
+      __syncthreads();
+      for (int it = tid; it < items; it += kThreads) {
+        const int tok = it / k8n, k8 = it - tok * k8n;
+        const uint4 v = *reinterpret_cast<const uint4*>(sX + tok * stride + k8 * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        if (amax > 0.f) atomicMax(&s_amax[tok], __float_as_uint(amax));
+      }
+      __syncthreads();
+      if (tid < kNT) {
+        const float amax = __uint_as_float(s_amax[tid]);
+        // token exponent: amax * 2^-ex in [2^14, 2^15)
+        int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
+        ex = ex < -126 ? -126 : ex;
+        s_amax[tid] = (unsigned)(ex + 256);
+        s_tok[tid] = s_src[tid] >= 0 ? exp2i(ex) : 0.f;
+      }
+      __syncthreads();
+      for (int it = tid; it < items; it += kThreads) {
+        const int tok = it / k8n, k8 = it - tok * k8n;
+        uint4* q = reinterpret_cast<uint4*>(sX + tok * stride + k8 * 16);
+        const uint4 v = *q;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const float inv = exp2i(-((int)s_amax[tok] - 256));
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = f32x2_to_f16x2(bf16_lo(w[i]) * inv, bf16_hi(w[i]) * inv);
+        *q = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    } else {
+      // MXFP8 / NVFP4 rows: four loads in flight per thread, then convert
+      for (int base = 0; base < items; base += 4 * kThreads) {
+        uint32_t qa[4], qb[4], sb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int it = base + j * kThreads + tid;
+          const int tok = it / k8n, k8 = it - tok * k8n;
+          const int t = it < items ? s_src[tok] : -1;
+          qa[j] = qb[j] = sb[j] = 0u;
+          if (t >= 0) {
+            if (p.act == 1) {
+              const uint2 q = __ldg(reinterpret_cast<const uint2*>(
+                                        reinterpret_cast<const uint8_t*>(p.xa) + (size_t)t * K) + k8);
+              qa[j] = q.x;
+              qb[j] = q.y;
+              sb[j] = __ldg(p.xs + (size_t)t * nkb + k8 / 4);
+            } else {
+              qa[j] = __ldg(reinterpret_cast<const uint32_t*>(
+                                reinterpret_cast<const uint8_t*>(p.xa) + (size_t)t * (K / 2)) + k8);
+              sb[j] = __ldg(p.xs + (size_t)t * (K / 16) + k8 / 2);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int it = base + j * kThreads + tid;
+          if (it >= items) continue;
+          const int tok = it / k8n, k8 = it - tok * k8n;
+          const bool valid = s_src[tok] >= 0;
+          uint32_t o[4];
+          if (p.act == 1) {
+            o[0] = e4m3x2_to_f16x2(qa[j] & 0xFFFFu);
+            o[1] = e4m3x2_to_f16x2(qa[j] >> 16);
+            o[2] = e4m3x2_to_f16x2(qb[j] & 0xFFFFu);
+            o[3] = e4m3x2_to_f16x2(qb[j] >> 16);
+            if ((k8 & 3) == 0) sS[(k8 >> 2) * kNT + tok] = valid ? exp2i((int)sb[j] - 127) : 0.f;
+          } else {
+            e2m1x8_to_f16x8(qa[j], o);
+            const uint32_t s2 = e4m3x2_to_f16x2(sb[j] | (sb[j] << 8));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = hmul2_f16(o[i], s2);
+          }
+          *reinterpret_cast<uint4*>(sX + tok * stride + k8 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      if (tid < kNT) {
+        const int t = s_src[tid];
+        s_tok[tid] = t < 0 ? 0.f : (p.act == 2 ? __ldg(p.xg + t) : 1.f);
+      }
+    }
+  }
+  __syncthreads();
+
+  const uint32_t sx_base = smem_addr(sX);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+
+  // ---- epilogue of m-tile mt ----
+  auto epilogue = [&](int mt) {
+    const float t0 = s_tok[2 * c], t1 = s_tok[2 * c + 1];
+    if (FC1) {
+      float* sH = sE;   // [kNT][64]
+      const int il = warp * 8 + g;
+      if (mt * 64 + il < p.I) {
+        const float ag = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
+        const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
+        const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+        const float gg = WNV ? __ldg(p.w1_gs + 2 * e) : 1.f, gu = WNV ? __ldg(p.w1_gs + 2 * e + 1) : 1.f;
+        sH[(2 * c) * 64 + il] = situ_f(acc[0] * (ag * gg * t0), acc[2] * (au * gu * t0), bt, btl);
+        sH[(2 * c + 1) * 64 + il] = situ_f(acc[1] * (ag * gg * t1), acc[3] * (au * gu * t1), bt, btl);
+      }
+      __syncthreads();
+      if (tid < kNT * 2) {
+        const int tok = tid >> 1, blk = tid & 1;
+        const int i0 = mt * 64 + blk * 32;
+        if (tok < nrows && i0 < p.I) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = sH[tok * 64 + blk * 32 + i];
+          const size_t r = (size_t)(row0 + tok);
+          if (p.h_mxfp8) {
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            const int ex = mxfp8_exponent(amax);
+            const float sc = exp2i(-ex);
+            uint32_t wds[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              wds[i] = f32x2_to_e4m3x2(v[4 * i] * sc, v[4 * i + 1] * sc) |
+                       (f32x2_to_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc) << 16);
+            uint4* dq = reinterpret_cast<uint4*>(p.h_q + r * p.I + i0);
+            dq[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            dq[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+            p.h_s[r * (p.I / 32) + i0 / 32] = (uint8_t)(ex + 127);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(p.h_bf16 + r * p.I + i0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(f32x2_to_bf16x2(v[8 * q + 0], v[8 * q + 1]), f32x2_to_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                  f32x2_to_bf16x2(v[8 * q + 4], v[8 * q + 5]), f32x2_to_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+          }
+        }
+      }
+      __syncthreads();
+    } else {
+      const float scale = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * (WNV ? __ldg(p.w2_gs + e) : 1.f);
+      const int nl = warp * 16 + g;
+      sE[(2 * c) * 128 + nl] = acc[0] * (scale * t0);
+      sE[(2 * c + 1) * 128 + nl] = acc[1] * (scale * t1);
+      sE[(2 * c) * 128 + nl + 8] = acc[2] * (scale * t0);
+      sE[(2 * c + 1) * 128 + nl + 8] = acc[3] * (scale * t1);
+      __syncthreads();
+      {
+        const int tok = tid >> 5, ch = tid & 31;   // 8 tokens x 32 float4
+        const int n0 = mt * 128 + ch * 4;
+        if (tok < nrows && n0 < p.Mtot)
+          *reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + tok) * p.Mtot + n0) =
+              *reinterpret_cast<const float4*>(sE + tok * 128 + ch * 4);
+      }
+      __syncthreads();
+    }
+  };
+
+  // ---- the (m-tile, chunk) stream: kST - 1 chunks in flight, across
+  // m-tile boundaries, so the next m-tile's loads overlap an epilogue ----
+  const int f = (g >> 1) & 3;
+  int mi = 0, cc = 0;   // position of the chunk being consumed
+  for (int u0 = 0; u0 < steps; u0 += kST) {
+#pragma unroll
+    for (int i = 0; i < kST; ++i) {
+      const int u = u0 + i;
+      if (u < steps) {
+        // refill the stage freed last step, then wait for chunk u
+        const int prev = (i + kST - 1) % kST;
+        issue(u + kST - 1, SA[prev], SB[prev], NA[prev], NB[prev]);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kST - 1));
+        __syncwarp();
+        const uint32_t stg = sw_u + (u % kST) * kStageBytes;
+        const uint32_t rowA = stg + g * 64, rowB = stg + (g + 8) * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int b = cc * 4 + q;
+          if (b < nkb) {
+            const uint32_t off = 16 * (q ^ f);
+            float2 as = make_float2(1.f, 1.f);
+            if (ABLK) as = *reinterpret_cast<const float2*>(sS + b * kNT + 2 * c);
+            if (WNV) {
+#pragma unroll
+              for (int s2 = 0; s2 < 2; ++s2) {
+                uint16_t ha, hb;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ha) : "r"(rowA + off + 8 * s2 + 2 * c));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hb) : "r"(rowB + off + 8 * s2 + 2 * c));
+                uint32_t fa[2], fb[2];
+                e2m1x4_to_f16x4((uint32_t)ha, fa);
+                e2m1x4_to_f16x4((uint32_t)hb, fb);
+                uint32_t b0, b1;
+                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(b0), "=r"(b1)
+                             : "r"(sx_base + g * stride + b * 64 + s2 * 32 + c * 8));
+                float t4[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16(t4, fa[0], fb[0], fa[1], fb[1], b0, b1);
+                const int sh = 16 * (q & 1) + 8 * s2;
+                const float swa = e4m3_to_f32((NA[i][q >> 1] >> sh) & 0xFFu);
+                const float swb = e4m3_to_f32((NB[i][q >> 1] >> sh) & 0xFFu);
+                if (ABLK) {
+                  acc[0] = fmaf(t4[0], swa * as.x, acc[0]);
+                  acc[1] = fmaf(t4[1], swa * as.y, acc[1]);
+                  acc[2] = fmaf(t4[2], swb * as.x, acc[2]);
+                  acc[3] = fmaf(t4[3], swb * as.y, acc[3]);
+                } else {
+                  acc[0] = fmaf(t4[0], swa, acc[0]);
+                  acc[1] = fmaf(t4[1], swa, acc[1]);
+                  acc[2] = fmaf(t4[2], swb, acc[2]);
+                  acc[3] = fmaf(t4[3], swb, acc[3]);
+                }
+              }
+            } else {
+              uint32_t wa, wb;
+              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(rowA + off + 4 * c));
+              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(rowB + off + 4 * c));
+              uint32_t fa[4], fb[4];
+              e2m1x8_to_f16x8(wa, fa);
+              e2m1x8_to_f16x8(wb, fb);
+              uint32_t bx[4];
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(bx[0]), "=r"(bx[1]), "=r"(bx[2]), "=r"(bx[3])
+                           : "r"(sx_base + g * stride + b * 64 + c * 16));
+              float t4[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_f16(t4, fa[0], fb[0], fa[1], fb[1], bx[0], bx[1]);
+              mma_f16(t4, fa[2], fb[2], fa[3], fb[3], bx[2], bx[3]);
+              const float swa = ue8m0_f32((SA[i] >> (8 * q)) & 0xFFu);
+              const float swb = ue8m0_f32((SB[i] >> (8 * q)) & 0xFFu);
+              if (ABLK) {
+                acc[0] = fmaf(t4[0], swa * as.x, acc[0]);
+                acc[1] = fmaf(t4[1], swa * as.y, acc[1]);
+                acc[2] = fmaf(t4[2], swb * as.x, acc[2]);
+                acc[3] = fmaf(t4[3], swb * as.y, acc[3]);
+              } else {
+                acc[0] = fmaf(t4[0], swa, acc[0]);
+                acc[1] = fmaf(t4[1], swa, acc[1]);
+                acc[2] = fmaf(t4[2], swb, acc[2]);
+                acc[3] = fmaf(t4[3], swb, acc[3]);
+              }
+            }
+          }
+        }
+        __syncwarp();   // every lane is done with this stage before it is refilled
+        if (++cc == nch) {
+          epilogue(mt0 + mi);
+          acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+          cc = 0;
+          ++mi;
+        }
+      }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;");
+}
+
+size_t fcd_smem_bytes(int K, bool nvfp4) {
+  return (size_t)kNT * x_stride(K, nvfp4) + (size_t)(K / 32) * kNT * 4 + (size_t)kNT * 128 * 4 +
+         (size_t)kWarps * kST * kStageBytes;
+}
+
+template <bool FC1, bool WNV, bool ABLK>
+static cudaError_t launch_fcd_t(const FcdParams& p, long max_tiles, cudaStream_t st) {
+  const size_t smem = fcd_smem_bytes(p.K, WNV);
+  static int set_for[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && (dev >= 64 || set_for[dev] < (int)smem)) {
+    cudaError_t err = cudaFuncSetAttribute(fcd_kernel<FC1, WNV, ABLK>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) set_for[dev] = (int)smem;
+  }
+  const long ngroups = (p.n_mtiles + p.mg - 1) / p.mg;
+  const long grid = max_tiles * ngroups;
+  if (grid <= 0) return cudaSuccess;
+  fcd_kernel<FC1, WNV, ABLK><<<(unsigned)grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st) {
+  const bool ablk = p.act == 1;
+  if (fc1) {
+    if (nvfp4) return ablk ? launch_fcd_t<true, true, true>(p, max_tiles, st) : launch_fcd_t<true, true, false>(p, max_tiles, st);
+    return ablk ? launch_fcd_t<true, false, true>(p, max_tiles, st) : launch_fcd_t<true, false, false>(p, max_tiles, st);
+  }
+  if (nvfp4) return ablk ? launch_fcd_t<false, true, true>(p, max_tiles, st) : launch_fcd_t<false, true, false>(p, max_tiles, st);
+  return ablk ? launch_fcd_t<false, false, true>(p, max_tiles, st) : launch_fcd_t<false, false, false>(p, max_tiles, st);
+}
+
+}  // namespace situ

@@ -113,14 +113,9 @@ __global__ void __launch_bounds__(kFcThreads, 2) fc_kernel(const FcParams p) {
   const int tile = blockIdx.x / p.n_mtiles;
   const int total = __ldg(p.tile_offsets + p.E_loc);
   if (tile >= total) return;
-  // local expert owning this tile: largest e with tile_offsets[e] <= tile
-  int lo = 0, hi = p.E_loc;
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(p.tile_offsets + mid) <= tile) lo = mid; else hi = mid;
-  }
-  const int e = lo;
-  const int row0 = __ldg(p.offsets + e) + (tile - __ldg(p.tile_offsets + e)) * NT;
+  const int2 ti = __ldg(p.tile_info + tile);   // (local expert, first row)
+  const int e = ti.x;
+  const int row0 = ti.y;
   const int nrows = min(NT, __ldg(p.offsets + e + 1) - row0);
 
   // the two weight rows this thread feeds (MMA rows g and g+8)

@@ -6,11 +6,14 @@
 // experts outside the current shard).  The row order inside an expert is the
 // ascending slot order, so the result is deterministic and bit-exact.
 //
-// Three launches over chunks of kPermChunk slots:
+// Up to kPermChunk slots (decode) one CTA does everything in one launch
+// (permute_small_kernel).  Beyond that, three launches over chunks of
+// kPermChunk slots:
 //   count   -- per-chunk histogram in shared memory (block-local atomics);
 //   scan    -- one block: per-expert prefix over chunks, then an exclusive
 //              scan over experts of the counts and of the GEMM token tiles
-//              (ceil(count / tile_n)); clears the unused permuted_src tail;
+//              (ceil(count / tile_n)), with a table tile -> (expert, first
+//              row) for the GEMMs; clears the unused permuted_src tail;
 //   scatter -- per chunk: per-warp counts, a prefix over warps, then each
 //              warp walks its slots 32 at a time; __match_any_sync groups the
 //              lanes that hit the same expert and a popcount of the lower
@@ -81,8 +84,8 @@ __device__ int block_exclusive_scan(int v, int* total) {
 __global__ void __launch_bounds__(1024)
 permute_scan_kernel(int32_t* __restrict__ blk_counts, int nblk, int E_loc, long S, int tile_n,
                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                    int32_t* __restrict__ tile_offsets, int32_t* __restrict__ permuted_src,
-                    int32_t* __restrict__ meta) {
+                    int32_t* __restrict__ tile_offsets, int2* __restrict__ tile_info,
+                    int32_t* __restrict__ permuted_src, int32_t* __restrict__ meta) {
   // 1. per expert: prefix over chunks (becomes each chunk's base), total count
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
     int run = 0;
@@ -109,11 +112,14 @@ permute_scan_kernel(int32_t* __restrict__ blk_counts, int nblk, int E_loc, long 
   for (int e = e0; e < e1; ++e) {
     int c = counts[e];
     offsets[e] = pc;
-    pc += c;
     if (tile_offsets) {
       tile_offsets[e] = pt;
-      pt += (c + tile_n - 1) / tile_n;
+      const int nt = (c + tile_n - 1) / tile_n;
+      if (tile_info)
+        for (int k = 0; k < nt; ++k) tile_info[pt + k] = make_int2(e, pc + k * tile_n);
+      pt += nt;
     }
+    pc += c;
   }
   if (threadIdx.x == 0) {
     offsets[E_loc] = R;
@@ -170,18 +176,122 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int o
   }
 }
 
+// One CTA for routings of at most kPermChunk slots: histogram, scans and
+// scatter in shared memory with no global scratch and a single launch.
+// Warp w owns slots [128w, 128w + 128), so the per-warp prefix keeps slot
+// order exactly as the three-launch path does.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / kWarp;
+constexpr int kSmallMaxExperts = 1024;
+
+__global__ void __launch_bounds__(kSmallThreads)
+permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off, int tile_n,
+                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                     int32_t* __restrict__ tile_offsets, int2* __restrict__ tile_info,
+                     int32_t* __restrict__ permuted_src, int32_t* __restrict__ slot_to_row,
+                     int32_t* __restrict__ meta) {
+  extern __shared__ int32_t sm[];
+  int32_t* wcnt = sm;                        // [kSmallWarps][E_loc]
+  int32_t* cnt = sm + kSmallWarps * E_loc;   // [E_loc]
+  int32_t* offs = cnt + E_loc;               // [E_loc]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kPerWarp = kPermChunk / kSmallWarps;   // 128
+  for (int i = threadIdx.x; i < kSmallWarps * E_loc; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  for (int r = 0; r < kPerWarp; r += kWarp) {
+    const int s = warp * kPerWarp + r + lane;
+    if (s < S) {
+      const int e = local_expert(__ldg(ids + s), off, E_loc);
+      if (e >= 0) atomicAdd(&wcnt[warp * E_loc + e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int v = wcnt[w * E_loc + e];
+      wcnt[w * E_loc + e] = run;
+      run += v;
+    }
+    cnt[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  const int per = (E_loc + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(E_loc, (int)threadIdx.x * per), e1 = min(E_loc, e0 + per);
+  int sc = 0, st = 0;
+  for (int e = e0; e < e1; ++e) {
+    sc += cnt[e];
+    st += (cnt[e] + tile_n - 1) / tile_n;
+  }
+  int R, tiles;
+  int pc = block_exclusive_scan(sc, &R);
+  int pt = block_exclusive_scan(st, &tiles);
+  for (int e = e0; e < e1; ++e) {
+    offs[e] = pc;
+    offsets[e] = pc;
+    if (tile_offsets) {
+      tile_offsets[e] = pt;
+      const int nt = (cnt[e] + tile_n - 1) / tile_n;
+      if (tile_info)
+        for (int k = 0; k < nt; ++k) tile_info[pt + k] = make_int2(e, pc + k * tile_n);
+      pt += nt;
+    }
+    pc += cnt[e];
+  }
+  if (threadIdx.x == 0) {
+    offsets[E_loc] = R;
+    if (tile_offsets) tile_offsets[E_loc] = tiles;
+    if (meta) { meta[0] = R; meta[1] = tiles; }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  int32_t* my = wcnt + warp * E_loc;
+  for (int r = 0; r < kPerWarp; r += kWarp) {
+    const int s = warp * kPerWarp + r + lane;
+    int e = -1;
+    if (s < S) e = local_expert(__ldg(ids + s), off, E_loc);
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int row = offs[e] + my[e] + __popc(peers & lt);
+      permuted_src[row] = s;
+      slot_to_row[s] = row;
+    } else if (s < S) {
+      slot_to_row[s] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && (peers & lt) == 0) my[e] += __popc(peers);
+    __syncwarp();
+  }
+  for (int r = R + threadIdx.x; r < S; r += blockDim.x) permuted_src[r] = -1;
+}
+
 static int g_scatter_smem_set[64];
+static int g_small_smem_set[64];
 
 cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off, int tile_n,
                            int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
-                           int32_t* permuted_src, int32_t* slot_to_row, int32_t* meta,
-                           int32_t* blk_counts, cudaStream_t st) {
+                           int2* tile_info, int32_t* permuted_src, int32_t* slot_to_row,
+                           int32_t* meta, int32_t* blk_counts, cudaStream_t st) {
   long S = (long)T * K;
   int nblk = (int)((S + kPermChunk - 1) / kPermChunk);
   size_t hist_smem = sizeof(int32_t) * (size_t)E_loc;
   size_t wcnt_smem = sizeof(int32_t) * (size_t)kPermWarps * E_loc;
   int dev = 0;
   cudaGetDevice(&dev);
+  if (nblk == 1 && E_loc <= kSmallMaxExperts) {
+    const size_t smem = sizeof(int32_t) * (size_t)(kSmallWarps + 2) * E_loc;
+    if (dev < 0 || dev >= 64 || g_small_smem_set[dev] < (int)smem) {
+      cudaError_t err = cudaFuncSetAttribute(permute_small_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      if (dev >= 0 && dev < 64) g_small_smem_set[dev] = (int)smem;
+    }
+    permute_small_kernel<<<1, kSmallThreads, smem, st>>>(ids, (int)S, E_loc, off, tile_n, counts,
+                                                         offsets, tile_offsets, tile_info,
+                                                         permuted_src, slot_to_row, meta);
+    return cudaGetLastError();
+  }
   if (dev >= 0 && dev < 64 && g_scatter_smem_set[dev] < (int)wcnt_smem) {
     cudaError_t err = cudaFuncSetAttribute(permute_scatter_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -191,7 +301,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
   }
   permute_count_kernel<<<nblk, kPermThreads, hist_smem, st>>>(ids, S, E_loc, off, blk_counts);
   permute_scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, E_loc, S, tile_n, counts, offsets,
-                                          tile_offsets, permuted_src, meta);
+                                          tile_offsets, tile_info, permuted_src, meta);
   permute_scatter_kernel<<<nblk, kPermThreads, wcnt_smem, st>>>(ids, S, E_loc, off, blk_counts,
                                                                 offsets, permuted_src, slot_to_row);
   return cudaGetLastError();

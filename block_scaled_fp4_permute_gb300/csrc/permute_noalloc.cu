@@ -73,7 +73,8 @@ extern "C" situ_status situ_moe_permute_noalloc(const int32_t* topk_ids, int32_t
   // so no part of the scratch has to be cleared first.
   cudaError_t err = situ::launch_permute(topk_ids, T, top_k, num_local_experts,
                                          local_expert_offset, 1, expert_counts, expert_offsets,
-                                         nullptr, permuted_src, slot_to_row, nullptr, scratch,
+                                         nullptr, nullptr, permuted_src, slot_to_row, nullptr,
+                                         scratch,
                                          (cudaStream_t)stream);
   return err == cudaSuccess ? SITU_OK : SITU_ERR_CUDA;
 }

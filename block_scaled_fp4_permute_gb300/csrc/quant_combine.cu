@@ -10,8 +10,8 @@
 // over the kept slots in ascending j, from the fp32 FC2 output, accumulated
 // in fp32 and rounded to bf16 once (the golden loop of TensorRT-LLM PR #17865 adds
 // weight * expert output per slot); a token with no kept slot gets 0.  Each
-// thread owns 8 consecutive hidden elements and reads them with 128-bit
-// loads, so each row of Y is read fully coalesced.
+// thread owns 4 consecutive hidden elements (one 128-bit load per kept
+// slot, four slots in flight), so each row of Y is read fully coalesced.
 #include "situ_internal.h"
 
 namespace situ {
@@ -53,31 +53,43 @@ cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t*
 
 __global__ void __launch_bounds__(256)
 combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
-               const float* __restrict__ w, int K, int H8, uint4* __restrict__ out) {
-  int t = blockIdx.x;
-  int h8 = blockIdx.y * blockDim.x + threadIdx.x;
-  if (h8 >= H8) return;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < K; ++j) {
-    int r = __ldg(slot_to_row + (size_t)t * K + j);
-    if (r < 0) continue;
-    float wt = __ldg(w + (size_t)t * K + j);
-    const float4 v0 = __ldg(y + ((size_t)r * H8 + h8) * 2);
-    const float4 v1 = __ldg(y + ((size_t)r * H8 + h8) * 2 + 1);
-    acc[0] = fmaf(wt, v0.x, acc[0]); acc[1] = fmaf(wt, v0.y, acc[1]);
-    acc[2] = fmaf(wt, v0.z, acc[2]); acc[3] = fmaf(wt, v0.w, acc[3]);
-    acc[4] = fmaf(wt, v1.x, acc[4]); acc[5] = fmaf(wt, v1.y, acc[5]);
-    acc[6] = fmaf(wt, v1.z, acc[6]); acc[7] = fmaf(wt, v1.w, acc[7]);
+               const float* __restrict__ w, int K, int H4, uint2* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int h4 = blockIdx.y * blockDim.x + threadIdx.x;
+  if (h4 >= H4) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // slots in ascending j; four row loads in flight at a time
+  for (int j0 = 0; j0 < K; j0 += 4) {
+    int r[4];
+    float wt[4];
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      r[u] = j < K ? __ldg(slot_to_row + (size_t)t * K + j) : -1;
+      wt[u] = r[u] >= 0 ? __ldg(w + (size_t)t * K + j) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      v[u] = r[u] >= 0 ? __ldg(y + (size_t)r[u] * H4 + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (r[u] >= 0) {
+        acc.x = fmaf(wt[u], v[u].x, acc.x);
+        acc.y = fmaf(wt[u], v[u].y, acc.y);
+        acc.z = fmaf(wt[u], v[u].z, acc.z);
+        acc.w = fmaf(wt[u], v[u].w, acc.w);
+      }
+    }
   }
-  out[(size_t)t * H8 + h8] = make_uint4(f32x2_to_bf16x2(acc[0], acc[1]), f32x2_to_bf16x2(acc[2], acc[3]),
-                                        f32x2_to_bf16x2(acc[4], acc[5]), f32x2_to_bf16x2(acc[6], acc[7]));
+  out[(size_t)t * H4 + h4] = make_uint2(f32x2_to_bf16x2(acc.x, acc.y), f32x2_to_bf16x2(acc.z, acc.w));
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,
                            int H, void* out, cudaStream_t st) {
-  int H8 = H / 8;
-  dim3 grid(T, (H8 + 255) / 256);
-  combine_kernel<<<grid, 256, 0, st>>>((const float4*)y, slot_to_row, w, K, H8, (uint4*)out);
+  const int H4 = H / 4;
+  dim3 grid(T, (H4 + 255) / 256);
+  combine_kernel<<<grid, 256, 0, st>>>((const float4*)y, slot_to_row, w, K, H4, (uint2*)out);
   return cudaGetLastError();
 }
 

@@ -11,10 +11,12 @@ namespace situ {
 
 constexpr int kPermChunk = 4096;   // routing slots per permute block
 
+// tile_offsets / tile_info / meta may be null (the standalone permute).
+// tile_info[t] = (local expert, first expert-ordered row) of GEMM token tile t.
 cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off, int tile_n,
                            int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
-                           int32_t* permuted_src, int32_t* slot_to_row, int32_t* meta,
-                           int32_t* blk_counts, cudaStream_t st);
+                           int2* tile_info, int32_t* permuted_src, int32_t* slot_to_row,
+                           int32_t* meta, int32_t* blk_counts, cudaStream_t st);
 size_t permute_scratch_bytes(int T, int K, int E_loc);
 
 cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t* s,
@@ -51,6 +53,7 @@ struct FcParams {
   const uint16_t* x;             // bf16 [S, K], rows in expert order
   const int32_t* offsets;        // [E_loc+1]
   const int32_t* tile_offsets;   // [E_loc+1]
+  const int2* tile_info;         // [tiles] (expert, first row)
   int E_loc, n_mtiles;
   // FC1
   int I;
@@ -63,5 +66,40 @@ struct FcParams {
 };
 cudaError_t launch_fc(const FcParams& p, bool fc1, bool nvfp4, int ns, long max_tiles,
                       cudaStream_t st);
+
+// Decode-tile grouped GEMM (8 tokens per CTA, whole K staged once).  The
+// activation rows come from `xa` in one of three formats (act): 0 bf16
+// [rows, K]; 1 MXFP8 E4M3 [rows, K] + UE8M0 xs [rows, K/32]; 2 NVFP4 packed
+// [rows, K/2] + E4M3 xs [rows, K/16] + fp32 xg [rows].  With row_src set,
+// expert-ordered row r reads source row row_src[r] / top_k (FC1 gathers
+// from the token-major input); without it, row r itself.
+struct FcdParams {
+  const uint8_t* w;
+  const uint8_t* ws;
+  int Mtot, K;
+  int act;
+  const void* xa;
+  const uint8_t* xs;
+  const float* xg;
+  const int32_t* row_src;
+  int top_k;
+  const int32_t* offsets;
+  const int32_t* tile_offsets;
+  const int2* tile_info;
+  int E_loc, n_mtiles, mg;
+  // FC1
+  int I;
+  const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs;
+  int h_mxfp8;
+  uint16_t* h_bf16;              // bf16 [S, I]
+  uint8_t* h_q;                  // MXFP8 [S, I] (w4a8)
+  uint8_t* h_s;                  // UE8M0 [S, I/32]
+  // FC2
+  const float *alpha2, *w2_gs;
+  float* y_out;                  // fp32 [S, H]
+};
+constexpr int kDecodeTileTokens = 8;
+size_t fcd_smem_bytes(int K, bool nvfp4);
+cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 
 }  // namespace situ

@@ -22,7 +22,7 @@ bool aligned_to(const void* p, uintptr_t a) { return p == nullptr || (reinterpre
 bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
-  size_t counts, offsets, tile_offsets, meta, psrc, s2r, blk, xperm, xg, h1, y, total;
+  size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, xperm, xg, h1, y, total;
 };
 
 Layout make_layout(const situ_moe_args* a) {
@@ -34,6 +34,7 @@ Layout make_layout(const situ_moe_args* a) {
   L.counts = take(4 * E);
   L.offsets = take(4 * (E + 1));
   L.tile_offsets = take(4 * (E + 1));
+  L.tile_info = take(8 * (S / kDecodeTileTokens + E + 2));   // any tile width >= 8
   L.meta = take(16);
   L.psrc = take(4 * S);
   L.s2r = take(4 * S);
@@ -137,7 +138,7 @@ situ_status situ_moe_permute(const int32_t* topk_ids, int32_t T, int32_t top_k,
   if (workspace_bytes < permute_scratch_bytes(T, top_k, num_local_experts))
     return SITU_ERR_WORKSPACE_TOO_SMALL;
   return cuda_status(launch_permute(topk_ids, T, top_k, num_local_experts, local_expert_offset, 1,
-                                    expert_counts, expert_offsets, nullptr, permuted_src,
+                                    expert_counts, expert_offsets, nullptr, nullptr, permuted_src,
                                     slot_to_row, nullptr, (int32_t*)workspace,
                                     (cudaStream_t)stream));
 }
@@ -173,6 +174,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   int32_t* counts = (int32_t*)(ws + L.counts);
   int32_t* offsets = (int32_t*)(ws + L.offsets);
   int32_t* tile_offsets = (int32_t*)(ws + L.tile_offsets);
+  int2* tile_info = (int2*)(ws + L.tile_info);
   int32_t* meta = (int32_t*)(ws + L.meta);
   int32_t* psrc = (int32_t*)(ws + L.psrc);
   int32_t* s2r = (int32_t*)(ws + L.s2r);
@@ -192,61 +194,129 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   mark(0);
   cudaError_t err = launch_permute(a->topk_ids, a->T, a->top_k, a->num_local_experts,
                                    a->local_expert_offset, tile_n, counts, offsets, tile_offsets,
-                                   psrc, s2r, meta, (int32_t*)(ws + L.blk), st);
+                                   tile_info, psrc, s2r, meta, (int32_t*)(ws + L.blk), st);
   if (err != cudaSuccess) return SITU_ERR_CUDA;
   mark(1);
 
-  GatherParams gp;
-  gp.act = a->act_dtype;
-  gp.x_bf16 = a->hidden_states;
-  gp.x_q = a->hidden_states_q;
-  gp.x_s = a->hidden_states_scale;
-  gp.x_gs = a->hidden_states_gscale;
-  gp.permuted_src = psrc;
-  gp.meta = meta;
-  gp.top_k = a->top_k;
-  gp.H = a->H;
-  gp.S = S;
-  gp.x_perm = xperm;
-  gp.xg_perm = a->act_dtype == SITU_ACT_NVFP4 ? xg : nullptr;
-  if ((err = launch_gather(gp, st)) != cudaSuccess) return SITU_ERR_CUDA;
-  mark(2);
+  // the decode kernel stages the whole K of its token tile in shared memory
+  const size_t kMaxSmem = 220 * 1024;
+  const bool decode_path = ns == 1 && fcd_smem_bytes(a->H, nv) <= kMaxSmem &&
+                           fcd_smem_bytes(a->I, nv) <= kMaxSmem;
+  if (decode_path) {
+    // 8-token tiles: FC1 gathers its rows straight from the input, so there
+    // is no separate gather stage.
+    mark(2);
+    FcdParams d;
+    std::memset(&d, 0, sizeof(d));
+    d.offsets = offsets;
+    d.tile_offsets = tile_offsets;
+    d.tile_info = tile_info;
+    d.E_loc = a->num_local_experts;
+    d.I = a->I;
+    d.w = a->w1;
+    d.ws = a->w1_scale;
+    d.Mtot = 2 * a->I;
+    d.K = a->H;
+    if (a->act_dtype == SITU_ACT_BF16) {
+      d.act = 0;
+      d.xa = a->hidden_states;
+    } else if (a->act_dtype == SITU_ACT_MXFP8) {
+      d.act = 1;
+      d.xa = a->hidden_states_q;
+      d.xs = a->hidden_states_scale;
+    } else {
+      d.act = 2;
+      d.xa = a->hidden_states_q;
+      d.xs = a->hidden_states_scale;
+      d.xg = a->hidden_states_gscale;
+    }
+    d.row_src = psrc;
+    d.top_k = a->top_k;
+    d.n_mtiles = (a->I + 63) / 64;
+    d.mg = 1;
+    d.beta = a->gemm1_alpha;
+    d.beta_lin = a->gemm1_beta;
+    d.alpha_g = a->g1_alphas;
+    d.alpha_u = a->g1_alphas_up;
+    d.w1_gs = a->w1_gscale;
+    const bool h_mx = a->act_dtype == SITU_ACT_MXFP8;
+    d.h_mxfp8 = h_mx;
+    d.h_bf16 = h1;
+    d.h_q = (uint8_t*)h1;                         // MXFP8 H1 shares the bf16 H1 region:
+    d.h_s = (uint8_t*)h1 + (size_t)S * a->I;      // S*I codes, then S*I/32 scales
+    if ((err = launch_fcd(d, true, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(3);
+    // FC2 reads H1 in expert order
+    d.w = a->w2;
+    d.ws = a->w2_scale;
+    d.Mtot = a->H;
+    d.K = a->I;
+    d.act = h_mx ? 1 : 0;
+    d.xa = h_mx ? (const void*)d.h_q : (const void*)h1;
+    d.xs = h_mx ? d.h_s : nullptr;
+    d.xg = nullptr;
+    d.row_src = nullptr;
+    d.n_mtiles = (a->H + 127) / 128;
+    d.mg = 4;
+    d.alpha2 = a->g2_alphas;
+    d.w2_gs = a->w2_gscale;
+    d.y_out = y;
+    if ((err = launch_fcd(d, false, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(4);
+  } else {
+    GatherParams gp;
+    gp.act = a->act_dtype;
+    gp.x_bf16 = a->hidden_states;
+    gp.x_q = a->hidden_states_q;
+    gp.x_s = a->hidden_states_scale;
+    gp.x_gs = a->hidden_states_gscale;
+    gp.permuted_src = psrc;
+    gp.meta = meta;
+    gp.top_k = a->top_k;
+    gp.H = a->H;
+    gp.S = S;
+    gp.x_perm = xperm;
+    gp.xg_perm = a->act_dtype == SITU_ACT_NVFP4 ? xg : nullptr;
+    if ((err = launch_gather(gp, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(2);
 
-  FcParams f;
-  std::memset(&f, 0, sizeof(f));
-  f.offsets = offsets;
-  f.tile_offsets = tile_offsets;
-  f.E_loc = a->num_local_experts;
-  f.I = a->I;
-  // FC1: W1 [E_loc, 2I, H], gate rows 0..I-1, up rows I..2I-1
-  f.w = a->w1;
-  f.ws = a->w1_scale;
-  f.Mtot = 2 * a->I;
-  f.K = a->H;
-  f.x = xperm;
-  f.n_mtiles = (a->I + 63) / 64;
-  f.beta = a->gemm1_alpha;
-  f.beta_lin = a->gemm1_beta;
-  f.alpha_g = a->g1_alphas;
-  f.alpha_u = a->g1_alphas_up;
-  f.w1_gs = a->w1_gscale;
-  f.xg = gp.xg_perm;
-  f.mxfp8_h = a->act_dtype == SITU_ACT_MXFP8;
-  f.h_out = h1;
-  if ((err = launch_fc(f, true, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
-  mark(3);
-  // FC2: W2 [E_loc, H, I]
-  f.w = a->w2;
-  f.ws = a->w2_scale;
-  f.Mtot = a->H;
-  f.K = a->I;
-  f.x = h1;
-  f.n_mtiles = (a->H + 127) / 128;
-  f.alpha2 = a->g2_alphas;
-  f.w2_gs = a->w2_gscale;
-  f.y_out = y;
-  if ((err = launch_fc(f, false, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
-  mark(4);
+    FcParams f;
+    std::memset(&f, 0, sizeof(f));
+    f.offsets = offsets;
+    f.tile_offsets = tile_offsets;
+    f.tile_info = tile_info;
+    f.E_loc = a->num_local_experts;
+    f.I = a->I;
+    // FC1: W1 [E_loc, 2I, H], gate rows 0..I-1, up rows I..2I-1
+    f.w = a->w1;
+    f.ws = a->w1_scale;
+    f.Mtot = 2 * a->I;
+    f.K = a->H;
+    f.x = xperm;
+    f.n_mtiles = (a->I + 63) / 64;
+    f.beta = a->gemm1_alpha;
+    f.beta_lin = a->gemm1_beta;
+    f.alpha_g = a->g1_alphas;
+    f.alpha_u = a->g1_alphas_up;
+    f.w1_gs = a->w1_gscale;
+    f.xg = gp.xg_perm;
+    f.mxfp8_h = a->act_dtype == SITU_ACT_MXFP8;
+    f.h_out = h1;
+    if ((err = launch_fc(f, true, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(3);
+    // FC2: W2 [E_loc, H, I]
+    f.w = a->w2;
+    f.ws = a->w2_scale;
+    f.Mtot = a->H;
+    f.K = a->I;
+    f.x = h1;
+    f.n_mtiles = (a->H + 127) / 128;
+    f.alpha2 = a->g2_alphas;
+    f.w2_gs = a->w2_gscale;
+    f.y_out = y;
+    if ((err = launch_fc(f, false, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(4);
+  }
 
   if ((err = launch_combine(y, s2r, a->topk_weights, a->T, a->top_k, a->H, a->out, st)) != cudaSuccess)
     return SITU_ERR_CUDA;

@@ -175,6 +175,14 @@ def test_decode_k3_constants():
     assert_parity(out, oracle_out(wl), "decode w4a16, beta=4, beta_lin=25")
 
 
+def test_decode_w4a8():
+    """w4a8 at decode size: MXFP8 activations and MXFP8 FC1 output on the
+    8-token-tile path."""
+    wl = W.make("prefill_w4a8", device="cuda", T=64)
+    _, out = run_layer(wl)
+    assert_parity(out, oracle_out(wl), "decode w4a8")
+
+
 def test_prefill_w4a8_subset():
     wl = wl_("prefill_w4a8")
     _, out = run_layer(wl)
@@ -208,6 +216,9 @@ def test_nvfp4_sweep(T):
     dict(T=33, H=512, I=192, E_total=16, E_loc=16, off=0, K=4, act=W.ACT_MXFP8, params="k3_random"),
     dict(T=29, H=320, I=160, E_total=16, E_loc=8, off=8, K=4, act=W.ACT_NVFP4, wt=W.W_NVFP4,
          params="k3_random"),
+    dict(T=5, H=160, I=96, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+         params="k3_random"),                                                          # 8-token tiles, NVFP4
+    dict(T=7, H=224, I=96, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_MXFP8, params="k3_random"),
 ])
 def test_small_shapes(over):
     wl = W.make("tiny", device="cuda", **over)

@@ -38,8 +38,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kNT = 8;                  // tokens per CTA
-constexpr int kST = 6;                  // weight-ring stages per warp (128-element chunks)
-constexpr int kStageBytes = 16 * 64;    // one chunk of the warp's 16 rows
+constexpr int kST = 5;                  // weight-ring stages per warp (128-element chunks)
+constexpr int kStageW = 16 * 64;        // one chunk of the warp's 16 rows
+constexpr int kStageBytes = kStageW + 16 * 8;   // + their block scales (8 bytes per row)
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -83,23 +84,23 @@ __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ void mma_f16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t ldg32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
+// first MMA of a block: C = 0
+__device__ __forceinline__ void mma_f16_z(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
-__device__ __forceinline__ uint32_t ldg16(const void* p) {
-  uint16_t v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
+
 __device__ __forceinline__ uint32_t ldg8(const void* p) {
   uint16_t v;
   asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
@@ -108,6 +109,12 @@ __device__ __forceinline__ uint32_t ldg8(const void* p) {
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool ok) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(ok ? 8 : 0));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0));
 }
 
 // UE8M0 byte in [1, 254] as an fp32 power of two (byte 0, reserved for
@@ -118,7 +125,7 @@ __device__ __forceinline__ float ue8m0_f32(uint32_t b) { return __uint_as_float(
 // fragment loads of a quarter warp (LDS.128, MXFP4 mapping) or half warp
 // (LDS.64, NVFP4 mapping) hit distinct banks.
 __host__ __device__ __forceinline__ int x_stride(int K, bool nv) {
-  int s = 2 * K;
+  int s = 2 * ((K + 127) / 128 * 128);   // rows zero-padded to whole 128-element chunks
   int want = nv ? 32 : 64;
   return s + ((want - (s % 128)) % 128 + 128) % 128;
 }
@@ -138,8 +145,9 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
   const int nkb = K / 32;
   const int stride = x_stride(K, WNV);
   uint8_t* sX = smem;                                               // [kNT][stride]
-  float* sS = reinterpret_cast<float*>(smem + kNT * stride);        // [nkb][kNT] (ABLK)
-  float* sE = sS + nkb * kNT;                                       // epilogue [kNT][128]
+  float* sS = reinterpret_cast<float*>(smem + kNT * stride);        // [nkb4][kNT] (ABLK)
+  const int nkb4 = (nkb + 3) / 4 * 4;                               // blocks incl. zero padding
+  float* sE = sS + nkb4 * kNT;                                      // epilogue [kNT][128]
   uint8_t* sWw = reinterpret_cast<uint8_t*>(sE + kNT * 128) + warp * kST * kStageBytes;
 
   const int ngroups = (p.n_mtiles + p.mg - 1) / p.mg;
@@ -159,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
   const size_t wrow = (size_t)(K / 2), srow = (size_t)(K / bsz);
   const uint8_t* wexp = p.w + (size_t)e * p.Mtot * wrow;
   const uint8_t* sexp = p.ws + (size_t)e * p.Mtot * srow;
-  const bool scale_words = !WNV && ((nkb & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.ws) & 3) == 0);
 
   // weight row r16 (0..15 of the warp's 16) of m-tile mt
   auto row_of = [&](int mt, int r16, bool& v) -> int {
@@ -173,31 +180,32 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
     return r;
   };
 
-  // ---- weight ring: piece p of row r at r*64 + 16*(p ^ ((r>>1)&3)) ----
+  // ---- weight ring: per stage, piece p of row r at r*64 + 16*(p ^ ((r>>1)&3)),
+  // then the 16 rows' scale bytes for the chunk, 8 bytes per row ----
   const uint32_t sw_u = smem_addr(sWw);
-  uint32_t SA[kST], SB[kST], NA[kST][2], NB[kST][2];
+  // scale bytes per row per chunk: 4 (MXFP4) or 8 (NVFP4); cp.async needs
+  // them aligned, which whole-128 rows give; otherwise plain loads
+  const int sc_bytes = WNV ? 8 : 4;
+  const bool sc_async = ((srow % sc_bytes) == 0) && ((reinterpret_cast<uintptr_t>(p.ws) % sc_bytes) == 0) &&
+                        (nkb % 4 == 0);
   int ld_mi = -1, ld_cc = nch - 1;        // position of the last issued chunk
-  const uint8_t *cpA = wexp, *cpB = wexp, *scA = sexp, *scB = sexp;
-  bool cvA = false, cvB = false, fvA = false, fvB = false;
-  auto issue = [&](int u, uint32_t& sA, uint32_t& sB, uint32_t* nA, uint32_t* nB) {
+  const uint8_t *cpA = wexp, *cpB = wexp, *cpS = sexp;
+  bool cvA = false, cvB = false, cvS = false;
+  auto issue = [&](int u, int slot) {
     if (++ld_cc == nch) {   // next m-tile: recompute the row pointers once
       ld_cc = 0;
       ++ld_mi;
       const int mt = mt0 + ld_mi;
-      const int rc = lane >> 2;
       int r;
-      r = row_of(mt, rc, cvA);
+      r = row_of(mt, lane >> 2, cvA);
       cpA = wexp + (size_t)(cvA ? r : 0) * wrow;
-      r = row_of(mt, rc + 8, cvB);
+      r = row_of(mt, (lane >> 2) + 8, cvB);
       cpB = wexp + (size_t)(cvB ? r : 0) * wrow;
-      r = row_of(mt, g, fvA);
-      scA = sexp + (size_t)(fvA ? r : 0) * srow;
-      r = row_of(mt, g + 8, fvB);
-      scB = sexp + (size_t)(fvB ? r : 0) * srow;
+      r = row_of(mt, lane & 15, cvS);
+      cpS = sexp + (size_t)(cvS ? r : 0) * srow;
     }
     const bool live = u < steps;
     const int cc = ld_cc;
-    const int slot = u % kST;
     const int piece = lane & 3, rc = lane >> 2;
     const int b = cc * 4 + piece;
     const bool kb = live && b < nkb;
@@ -205,43 +213,29 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
     cp_async16(st + rc * 64 + 16 * (piece ^ ((rc >> 1) & 3)), cpA + (kb && cvA ? b * 16 : 0), kb && cvA);
     cp_async16(st + (rc + 8) * 64 + 16 * (piece ^ (((rc + 8) >> 1) & 3)), cpB + (kb && cvB ? b * 16 : 0),
                kb && cvB);
-    asm volatile("cp.async.commit_group;");
-    const bool va = live && fvA, vb = live && fvB;
-    if (WNV) {   // two E4M3 scales per block: blocks 2h, 2h+1 of the chunk in nA[h]
+    if (lane < 16) {
+      const uint32_t sdst = st + kStageW + lane * 8;
+      const bool sv = live && cvS;
+      if (sc_async) {
+        if (WNV) cp_async8(sdst, cpS + (sv ? cc * 8 : 0), sv);
+        else cp_async4(sdst, cpS + (sv ? cc * 4 : 0), sv);
+      } else {
+        // rows whose scales are not 4/8-byte aligned, or a partial last chunk
+        uint32_t lo = 0u, hi = 0u;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t xa = 0u, xb = 0u;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int bq = cc * 4 + 2 * h + q;
-          if (bq < nkb) {
-            xa |= (va ? ldg16(scA + 2 * bq) : 0u) << (16 * q);
-            xb |= (vb ? ldg16(scB + 2 * bq) : 0u) << (16 * q);
-          }
+        for (int q = 0; q < (WNV ? 8 : 4); ++q) {
+          const int idx = cc * (WNV ? 8 : 4) + q;
+          const uint32_t v = (sv && idx < (int)srow) ? ldg8(cpS + idx) : 0u;
+          if (q < 4) lo |= v << (8 * q); else hi |= v << (8 * (q - 4));
         }
-        nA[h] = xa;
-        nB[h] = xb;
-      }
-    } else if (scale_words) {
-      const bool kv = cc * 4 < nkb;
-      sA = (va && kv) ? ldg32(scA + cc * 4) : 0u;
-      sB = (vb && kv) ? ldg32(scB + cc * 4) : 0u;
-    } else {
-      sA = sB = 0u;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int bq = cc * 4 + q;
-        if (bq < nkb) {
-          sA |= (va ? ldg8(scA + bq) : 0u) << (8 * q);
-          sB |= (vb ? ldg8(scB + bq) : 0u) << (8 * q);
-        }
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sdst), "r"(lo), "r"(hi));
       }
     }
+    asm volatile("cp.async.commit_group;");
   };
 
   // start the weight stream (kST - 1 chunks) before staging the activations
-#pragma unroll
-  for (int i = 0; i < kST - 1; ++i) issue(i, SA[i], SB[i], NA[i], NB[i]);
+  for (int i = 0; i < kST - 1; ++i) issue(i, i);
 
   // ---- stage the token tile as f16 mantissas ----
   if (tid < kNT) {
@@ -262,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
                    reinterpret_cast<const uint4*>(p.xa) + (size_t)(t >= 0 ? t : 0) * k8n + k8, t >= 0);
       }
       asm volatile("cp.async.commit_group;");
-      asm volatile("cp.async.wait_group 0;");
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
       __syncthreads();
       for (int it = tid; it < items; it += kThreads) {
         const int tok = it / k8n, k8 = it - tok * k8n;
@@ -346,6 +340,16 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
       }
     }
   }
+  // zero padding to a whole number of 128-element chunks
+  {
+    const int padk8 = nkb4 * 4 - K / 8;   // 16-byte pieces of padding per token row
+    for (int it = tid; it < kNT * padk8; it += kThreads) {
+      const int tok = it / padk8, k8 = K / 8 + it % padk8;
+      *reinterpret_cast<uint4*>(sX + tok * stride + k8 * 16) = make_uint4(0, 0, 0, 0);
+    }
+    if (ABLK)
+      for (int it = tid; it < (nkb4 - nkb) * kNT; it += kThreads) sS[nkb * kNT + it] = 0.f;
+  }
   __syncthreads();
 
   const uint32_t sx_base = smem_addr(sX);
@@ -421,101 +425,97 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
   // ---- the (m-tile, chunk) stream: kST - 1 chunks in flight, across
   // m-tile boundaries, so the next m-tile's loads overlap an epilogue ----
   const int f = (g >> 1) & 3;
-  int mi = 0, cc = 0;   // position of the chunk being consumed
-  for (int u0 = 0; u0 < steps; u0 += kST) {
+  const uint32_t off0 = 16 * (0 ^ f), off1 = 16 * (1 ^ f), off2 = 16 * (2 ^ f), off3 = 16 * (3 ^ f);
+  const uint8_t* xrowp = sX + g * stride;
+  int mi = 0, cc = 0, slot = 0;
+  for (int u = 0; u < steps; ++u) {
+    // refill the stage freed last step, then wait for chunk u
+    issue(u + kST - 1, slot == 0 ? kST - 1 : slot - 1);
+    asm volatile("cp.async.wait_group %0;" ::"n"(kST - 1) : "memory");
+    __syncwarp();
+    const uint8_t* stg = sWw + slot * kStageBytes;
+    const uint8_t* rowA = stg + g * 64;
+    const uint8_t* rowB = stg + (g + 8) * 64;
+    // this lane's rows' scale bytes for the chunk
+    const uint2 scA = *reinterpret_cast<const uint2*>(stg + kStageW + g * 8);
+    const uint2 scB = *reinterpret_cast<const uint2*>(stg + kStageW + (g + 8) * 8);
+    const uint32_t scA0 = scA.x, scA1 = scA.y, scB0 = scB.x, scB1 = scB.y;
+    const uint8_t* xb = xrowp + cc * 256;
 #pragma unroll
-    for (int i = 0; i < kST; ++i) {
-      const int u = u0 + i;
-      if (u < steps) {
-        // refill the stage freed last step, then wait for chunk u
-        const int prev = (i + kST - 1) % kST;
-        issue(u + kST - 1, SA[prev], SB[prev], NA[prev], NB[prev]);
-        asm volatile("cp.async.wait_group %0;" ::"n"(kST - 1));
-        __syncwarp();
-        const uint32_t stg = sw_u + (u % kST) * kStageBytes;
-        const uint32_t rowA = stg + g * 64, rowB = stg + (g + 8) * 64;
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t off = q == 0 ? off0 : q == 1 ? off1 : q == 2 ? off2 : off3;
+      float2 as = make_float2(1.f, 1.f);
+      if (ABLK) as = *reinterpret_cast<const float2*>(sS + (cc * 4 + q) * kNT + 2 * c);
+      if (WNV) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int b = cc * 4 + q;
-          if (b < nkb) {
-            const uint32_t off = 16 * (q ^ f);
-            float2 as = make_float2(1.f, 1.f);
-            if (ABLK) as = *reinterpret_cast<const float2*>(sS + b * kNT + 2 * c);
-            if (WNV) {
-#pragma unroll
-              for (int s2 = 0; s2 < 2; ++s2) {
-                uint16_t ha, hb;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ha) : "r"(rowA + off + 8 * s2 + 2 * c));
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hb) : "r"(rowB + off + 8 * s2 + 2 * c));
-                uint32_t fa[2], fb[2];
-                e2m1x4_to_f16x4((uint32_t)ha, fa);
-                e2m1x4_to_f16x4((uint32_t)hb, fb);
-                uint32_t b0, b1;
-                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(b0), "=r"(b1)
-                             : "r"(sx_base + g * stride + b * 64 + s2 * 32 + c * 8));
-                float t4[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16(t4, fa[0], fb[0], fa[1], fb[1], b0, b1);
-                const int sh = 16 * (q & 1) + 8 * s2;
-                const float swa = e4m3_to_f32((NA[i][q >> 1] >> sh) & 0xFFu);
-                const float swb = e4m3_to_f32((NB[i][q >> 1] >> sh) & 0xFFu);
-                if (ABLK) {
-                  acc[0] = fmaf(t4[0], swa * as.x, acc[0]);
-                  acc[1] = fmaf(t4[1], swa * as.y, acc[1]);
-                  acc[2] = fmaf(t4[2], swb * as.x, acc[2]);
-                  acc[3] = fmaf(t4[3], swb * as.y, acc[3]);
-                } else {
-                  acc[0] = fmaf(t4[0], swa, acc[0]);
-                  acc[1] = fmaf(t4[1], swa, acc[1]);
-                  acc[2] = fmaf(t4[2], swb, acc[2]);
-                  acc[3] = fmaf(t4[3], swb, acc[3]);
-                }
-              }
-            } else {
-              uint32_t wa, wb;
-              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(rowA + off + 4 * c));
-              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(rowB + off + 4 * c));
-              uint32_t fa[4], fb[4];
-              e2m1x8_to_f16x8(wa, fa);
-              e2m1x8_to_f16x8(wb, fb);
-              uint32_t bx[4];
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(bx[0]), "=r"(bx[1]), "=r"(bx[2]), "=r"(bx[3])
-                           : "r"(sx_base + g * stride + b * 64 + c * 16));
-              float t4[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_f16(t4, fa[0], fb[0], fa[1], fb[1], bx[0], bx[1]);
-              mma_f16(t4, fa[2], fb[2], fa[3], fb[3], bx[2], bx[3]);
-              const float swa = ue8m0_f32((SA[i] >> (8 * q)) & 0xFFu);
-              const float swb = ue8m0_f32((SB[i] >> (8 * q)) & 0xFFu);
-              if (ABLK) {
-                acc[0] = fmaf(t4[0], swa * as.x, acc[0]);
-                acc[1] = fmaf(t4[1], swa * as.y, acc[1]);
-                acc[2] = fmaf(t4[2], swb * as.x, acc[2]);
-                acc[3] = fmaf(t4[3], swb * as.y, acc[3]);
-              } else {
-                acc[0] = fmaf(t4[0], swa, acc[0]);
-                acc[1] = fmaf(t4[1], swa, acc[1]);
-                acc[2] = fmaf(t4[2], swb, acc[2]);
-                acc[3] = fmaf(t4[3], swb, acc[3]);
-              }
-            }
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const uint16_t ha = *reinterpret_cast<const uint16_t*>(rowA + off + 8 * s2 + 2 * c);
+          const uint16_t hb = *reinterpret_cast<const uint16_t*>(rowB + off + 8 * s2 + 2 * c);
+          uint32_t fa[2], fb[2];
+          e2m1x4_to_f16x4((uint32_t)ha, fa);
+          e2m1x4_to_f16x4((uint32_t)hb, fb);
+          const uint2 bb = *reinterpret_cast<const uint2*>(xb + q * 64 + s2 * 32 + c * 8);
+          const uint32_t b0 = bb.x, b1 = bb.y;
+          float t4[4];
+          mma_f16_z(t4, fa[0], fb[0], fa[1], fb[1], b0, b1);
+          // scale of 16-block 2q+s2: byte (2q+s2) of the row's 8 scale bytes
+          const int sb = 2 * q + s2;
+          const uint32_t wa = sb < 4 ? scA0 : scA1, wb = sb < 4 ? scB0 : scB1;
+          const float swa = e4m3_to_f32((wa >> (8 * (sb & 3))) & 0xFFu);
+          const float swb = e4m3_to_f32((wb >> (8 * (sb & 3))) & 0xFFu);
+          if (ABLK) {
+            acc[0] = fmaf(t4[0], swa * as.x, acc[0]);
+            acc[1] = fmaf(t4[1], swa * as.y, acc[1]);
+            acc[2] = fmaf(t4[2], swb * as.x, acc[2]);
+            acc[3] = fmaf(t4[3], swb * as.y, acc[3]);
+          } else {
+            acc[0] = fmaf(t4[0], swa, acc[0]);
+            acc[1] = fmaf(t4[1], swa, acc[1]);
+            acc[2] = fmaf(t4[2], swb, acc[2]);
+            acc[3] = fmaf(t4[3], swb, acc[3]);
           }
         }
-        __syncwarp();   // every lane is done with this stage before it is refilled
-        if (++cc == nch) {
-          epilogue(mt0 + mi);
-          acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-          cc = 0;
-          ++mi;
+      } else {
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(rowA + off + 4 * c);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(rowB + off + 4 * c);
+        uint32_t fa[4], fb[4];
+        e2m1x8_to_f16x8(wa, fa);
+        e2m1x8_to_f16x8(wb, fb);
+        const uint4 bv = *reinterpret_cast<const uint4*>(xb + q * 64 + c * 16);
+        const uint32_t bx[4] = {bv.x, bv.y, bv.z, bv.w};
+        float t4[4];
+        mma_f16_z(t4, fa[0], fb[0], fa[1], fb[1], bx[0], bx[1]);
+        mma_f16(t4, fa[2], fb[2], fa[3], fb[3], bx[2], bx[3]);
+        const float swa = ue8m0_f32((scA0 >> (8 * q)) & 0xFFu);
+        const float swb = ue8m0_f32((scB0 >> (8 * q)) & 0xFFu);
+        if (ABLK) {
+          acc[0] = fmaf(t4[0], swa * as.x, acc[0]);
+          acc[1] = fmaf(t4[1], swa * as.y, acc[1]);
+          acc[2] = fmaf(t4[2], swb * as.x, acc[2]);
+          acc[3] = fmaf(t4[3], swb * as.y, acc[3]);
+        } else {
+          acc[0] = fmaf(t4[0], swa, acc[0]);
+          acc[1] = fmaf(t4[1], swa, acc[1]);
+          acc[2] = fmaf(t4[2], swb, acc[2]);
+          acc[3] = fmaf(t4[3], swb, acc[3]);
         }
       }
     }
+    __syncwarp();   // every lane is done with this stage before it is refilled
+    slot = slot == kST - 1 ? 0 : slot + 1;
+    if (++cc == nch) {
+      epilogue(mt0 + mi);
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      cc = 0;
+      ++mi;
+    }
   }
-  asm volatile("cp.async.wait_group 0;");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 size_t fcd_smem_bytes(int K, bool nvfp4) {
-  return (size_t)kNT * x_stride(K, nvfp4) + (size_t)(K / 32) * kNT * 4 + (size_t)kNT * 128 * 4 +
-         (size_t)kWarps * kST * kStageBytes;
+  return (size_t)kNT * x_stride(K, nvfp4) + (size_t)((K / 32 + 3) / 4 * 4) * kNT * 4 +
+         (size_t)kNT * 128 * 4 + (size_t)kWarps * kST * kStageBytes;
 }
 
 template <bool FC1, bool WNV, bool ABLK>

@@ -2,26 +2,25 @@
 //
 // Decode streams every touched expert's FP4 weights once and has one or two
 // tokens per expert, so the bound is HBM bandwidth plus the ALU work of
-// turning FP4 into MMA operands.  This kernel keeps the latter small:
+// turning FP4 into MMA operands.  This path keeps the latter small:
 //   * E2M1 codes become f16 pairs with the hardware conversion
 //     (cvt.rn.f16x2.e2m1x2, exact), one instruction per two weights;
 //   * weight block scales are applied in fp32 after each block's MMAs
 //     (acc += scale * partial), the way a block-scaled MMA applies them,
 //     instead of rescaling every weight;
-//   * activations are converted once per CTA to f16 mantissas.  bf16 rows
-//     take one power-of-two scale per token that puts the row maximum in
-//     [2^14, 2^15) (exact for every element within 2^-28 of the row
-//     maximum); NVFP4 rows convert exactly with their E4M3 block scales
-//     folded in and the fp32 global scale per token; MXFP8 rows convert
-//     exactly and keep their UE8M0 scale per (token, 32-block), applied with
-//     the weight scale.  Per-token scales are applied once in the epilogue.
-// The token tile (8 rows) is staged for the whole K at CTA start (FC1
-// gathers its rows straight from the token-major input through
-// permuted_src; bf16 rows arrive by cp.async and are converted in place),
-// after the CTA has started its weight stream.  Each warp streams its own
-// 16 weight rows through a kST-stage shared ring with 16-byte cp.async
-// copies (full sectors, asynchronous); the stream runs on across the
-// m-tiles a CTA owns, so the next m-tile's loads overlap an epilogue.
+//   * activations arrive as "f16 block rows" (mantissa * per-32-block fp32
+//     scale), built once per row: gather16 converts the token-major input
+//     in expert order (bf16 rows take one power-of-two scale per row that
+//     puts the row maximum in [2^14, 2^15), exact for every element within
+//     2^-28 of it; MXFP8 rows convert exactly and keep their block scales;
+//     NVFP4 rows convert exactly with the E4M3 block scales folded in and
+//     the per-token fp32 scale as the row scale), and FC1's epilogue writes
+//     H1 the same way for FC2.
+// A CTA stages its 8-row token tile for the whole K with one cp.async pass,
+// after it has started its weight stream.  Each warp streams its own 16
+// weight rows, and their block scales, through a kST-stage shared ring with
+// cp.async copies (full sectors, asynchronous); the stream runs on across
+// the m-tiles a CTA owns, so the next m-tile's loads overlap an epilogue.
 //
 // Fragment mapping (m16n8k16, A = weights, B = tokens): within a 32-element
 // MXFP4 block lane (g, c) owns elements 8c..8c+7 of rows g and g+8, so one
@@ -137,15 +136,13 @@ __host__ __device__ __forceinline__ int x_stride(int K, bool nv) {
 template <bool FC1, bool WNV, bool ABLK>
 __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ int s_src[kNT];
-  __shared__ float s_tok[kNT];       // per-token activation scale
-  __shared__ unsigned s_amax[kNT];
+  __shared__ float s_tok[kNT];       // per-token activation scale (rows without block scales)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int K = p.K;
   const int nkb = K / 32;
   const int stride = x_stride(K, WNV);
   uint8_t* sX = smem;                                               // [kNT][stride]
-  float* sS = reinterpret_cast<float*>(smem + kNT * stride);        // [nkb4][kNT] (ABLK)
+  float* sS = reinterpret_cast<float*>(smem + kNT * stride);        // [kNT][nkb4]
   const int nkb4 = (nkb + 3) / 4 * 4;                               // blocks incl. zero padding
   float* sE = sS + nkb4 * kNT;                                      // epilogue [kNT][128]
   uint8_t* sWw = reinterpret_cast<uint8_t*>(sE + kNT * 128) + warp * kST * kStageBytes;
@@ -237,118 +234,36 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
   // start the weight stream (kST - 1 chunks) before staging the activations
   for (int i = 0; i < kST - 1; ++i) issue(i, i);
 
-  // ---- stage the token tile as f16 mantissas ----
-  if (tid < kNT) {
-    s_src[tid] = tid < nrows ? (p.row_src ? __ldg(p.row_src + row0 + tid) / p.top_k : row0 + tid) : -1;
-    s_amax[tid] = 0u;
-  }
-  __syncthreads();
+  // ---- stage the token tile: f16 block rows in expert order ----
   {
-    const int k8n = K / 8;
-    const int items = kNT * k8n;
-    if (p.act == 0) {
-      // raw bf16 rows land in place with cp.async; one scale per token row
-      const uint32_t sx_u = smem_addr(sX);
-      for (int it = tid; it < items; it += kThreads) {
+    const int kpad = nkb4 * 32;
+    const int k8n = kpad / 8;            // 16-byte mantissa pieces per row
+    const int s4n = nkb4 / 4;            // 16-byte scale pieces per row
+    const uint32_t sx_u = smem_addr(sX), ss_u = smem_addr(sS);
+    for (int it = tid; it < kNT * (k8n + s4n); it += kThreads) {
+      if (it < kNT * k8n) {
         const int tok = it / k8n, k8 = it - tok * k8n;
-        const int t = s_src[tok];
+        const bool v = tok < nrows && k8 < K / 8;   // columns past K are zero-filled
         cp_async16(sx_u + tok * stride + k8 * 16,
-                   reinterpret_cast<const uint4*>(p.xa) + (size_t)(t >= 0 ? t : 0) * k8n + k8, t >= 0);
-      }
-      asm volatile("cp.async.commit_group;");
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      __syncthreads();
-      for (int it = tid; it < items; it += kThreads) {
-        const int tok = it / k8n, k8 = it - tok * k8n;
-        const uint4 v = *reinterpret_cast<const uint4*>(sX + tok * stride + k8 * 16);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-        if (amax > 0.f) atomicMax(&s_amax[tok], __float_as_uint(amax));
-      }
-      __syncthreads();
-      if (tid < kNT) {
-        const float amax = __uint_as_float(s_amax[tid]);
-        // token exponent: amax * 2^-ex in [2^14, 2^15)
-        int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
-        ex = ex < -126 ? -126 : ex;
-        s_amax[tid] = (unsigned)(ex + 256);
-        s_tok[tid] = s_src[tid] >= 0 ? exp2i(ex) : 0.f;
-      }
-      __syncthreads();
-      for (int it = tid; it < items; it += kThreads) {
-        const int tok = it / k8n, k8 = it - tok * k8n;
-        uint4* q = reinterpret_cast<uint4*>(sX + tok * stride + k8 * 16);
-        const uint4 v = *q;
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        const float inv = exp2i(-((int)s_amax[tok] - 256));
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = f32x2_to_f16x2(bf16_lo(w[i]) * inv, bf16_hi(w[i]) * inv);
-        *q = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    } else {
-      // MXFP8 / NVFP4 rows: four loads in flight per thread, then convert
-      for (int base = 0; base < items; base += 4 * kThreads) {
-        uint32_t qa[4], qb[4], sb[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int it = base + j * kThreads + tid;
-          const int tok = it / k8n, k8 = it - tok * k8n;
-          const int t = it < items ? s_src[tok] : -1;
-          qa[j] = qb[j] = sb[j] = 0u;
-          if (t >= 0) {
-            if (p.act == 1) {
-              const uint2 q = __ldg(reinterpret_cast<const uint2*>(
-                                        reinterpret_cast<const uint8_t*>(p.xa) + (size_t)t * K) + k8);
-              qa[j] = q.x;
-              qb[j] = q.y;
-              sb[j] = __ldg(p.xs + (size_t)t * nkb + k8 / 4);
-            } else {
-              qa[j] = __ldg(reinterpret_cast<const uint32_t*>(
-                                reinterpret_cast<const uint8_t*>(p.xa) + (size_t)t * (K / 2)) + k8);
-              sb[j] = __ldg(p.xs + (size_t)t * (K / 16) + k8 / 2);
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int it = base + j * kThreads + tid;
-          if (it >= items) continue;
-          const int tok = it / k8n, k8 = it - tok * k8n;
-          const bool valid = s_src[tok] >= 0;
-          uint32_t o[4];
-          if (p.act == 1) {
-            o[0] = e4m3x2_to_f16x2(qa[j] & 0xFFFFu);
-            o[1] = e4m3x2_to_f16x2(qa[j] >> 16);
-            o[2] = e4m3x2_to_f16x2(qb[j] & 0xFFFFu);
-            o[3] = e4m3x2_to_f16x2(qb[j] >> 16);
-            if ((k8 & 3) == 0) sS[(k8 >> 2) * kNT + tok] = valid ? exp2i((int)sb[j] - 127) : 0.f;
-          } else {
-            e2m1x8_to_f16x8(qa[j], o);
-            const uint32_t s2 = e4m3x2_to_f16x2(sb[j] | (sb[j] << 8));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = hmul2_f16(o[i], s2);
-          }
-          *reinterpret_cast<uint4*>(sX + tok * stride + k8 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      if (tid < kNT) {
-        const int t = s_src[tid];
-        s_tok[tid] = t < 0 ? 0.f : (p.act == 2 ? __ldg(p.xg + t) : 1.f);
+                   p.x16 + (size_t)(v ? row0 + tok : 0) * kpad + k8 * 8, v);
+      } else {
+        const int j2 = it - kNT * k8n;
+        const int tok = j2 / s4n, s4 = j2 - tok * s4n;
+        const bool v = tok < nrows;
+        cp_async16(ss_u + (tok * nkb4 + s4 * 4) * 4, p.xs + (size_t)(v ? row0 + tok : 0) * nkb4 + s4 * 4, v);
       }
     }
-  }
-  // zero padding to a whole number of 128-element chunks
-  {
-    const int padk8 = nkb4 * 4 - K / 8;   // 16-byte pieces of padding per token row
-    for (int it = tid; it < kNT * padk8; it += kThreads) {
-      const int tok = it / padk8, k8 = K / 8 + it % padk8;
-      *reinterpret_cast<uint4*>(sX + tok * stride + k8 * 16) = make_uint4(0, 0, 0, 0);
+    asm volatile("cp.async.commit_group;");
+    // this group was committed after the weight prologue's groups, so
+    // waiting for all but none of them is the simple, correct choice
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // the scales of blocks past K are zero whatever the source row holds there
+    for (int it = tid; it < kNT * (nkb4 - nkb); it += kThreads) {
+      const int tok = it / (nkb4 - nkb), b = nkb + it % (nkb4 - nkb);
+      sS[tok * nkb4 + b] = 0.f;
     }
-    if (ABLK)
-      for (int it = tid; it < (nkb4 - nkb) * kNT; it += kThreads) sS[nkb * kNT + it] = 0.f;
+    __syncthreads();
+    if (tid < kNT) s_tok[tid] = (tid < nrows && !ABLK) ? sS[tid * nkb4] : (tid < nrows ? 1.f : 0.f);
   }
   __syncthreads();
 
@@ -378,28 +293,38 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = sH[tok * 64 + blk * 32 + i];
           const size_t r = (size_t)(row0 + tok);
+          // H1 as FC2 consumes it: the MXFP8 round trip of h (w4a8) or h
+          // rounded to bf16, held exactly as f16 mantissas x 2^ex
+          uint32_t o[16];
+          float scale;
           if (p.h_mxfp8) {
             float amax = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
             const int ex = mxfp8_exponent(amax);
             const float sc = exp2i(-ex);
-            uint32_t wds[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              wds[i] = f32x2_to_e4m3x2(v[4 * i] * sc, v[4 * i + 1] * sc) |
-                       (f32x2_to_e4m3x2(v[4 * i + 2] * sc, v[4 * i + 3] * sc) << 16);
-            uint4* dq = reinterpret_cast<uint4*>(p.h_q + r * p.I + i0);
-            dq[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-            dq[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
-            p.h_s[r * (p.I / 32) + i0 / 32] = (uint8_t)(ex + 127);
+            for (int i = 0; i < 16; ++i) o[i] = e4m3x2_to_f16x2(f32x2_to_e4m3x2(v[2 * i] * sc, v[2 * i + 1] * sc));
+            scale = exp2i(ex);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(p.h_bf16 + r * p.I + i0);
+            float amax = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(f32x2_to_bf16x2(v[8 * q + 0], v[8 * q + 1]), f32x2_to_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                  f32x2_to_bf16x2(v[8 * q + 4], v[8 * q + 5]), f32x2_to_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            for (int i = 0; i < 32; ++i) {
+              v[i] = bf16_lo(f32x2_to_bf16x2(v[i], 0.f));
+              amax = fmaxf(amax, fabsf(v[i]));
+            }
+            int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
+            ex = ex < -126 ? -126 : ex;
+            const float inv = exp2i(-ex);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = f32x2_to_f16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+            scale = exp2i(ex);
           }
+          const int ipad = pad128(p.I);
+          uint4* dst = reinterpret_cast<uint4*>(p.h16 + r * ipad + i0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          p.hs[r * (ipad / 32) + i0 / 32] = scale;
         }
       }
       __syncthreads();
@@ -445,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
     for (int q = 0; q < 4; ++q) {
       const uint32_t off = q == 0 ? off0 : q == 1 ? off1 : q == 2 ? off2 : off3;
       float2 as = make_float2(1.f, 1.f);
-      if (ABLK) as = *reinterpret_cast<const float2*>(sS + (cc * 4 + q) * kNT + 2 * c);
+      if (ABLK) as = make_float2(sS[(2 * c) * nkb4 + cc * 4 + q], sS[(2 * c + 1) * nkb4 + cc * 4 + q]);
       if (WNV) {
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
@@ -513,6 +438,81 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// gather16: expert-ordered f16 block rows from the token-major input
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(128) gather16_kernel(const Gather16Params p) {
+  __shared__ float red[4];
+  const long r = blockIdx.x;
+  if (r >= __ldg(p.meta)) return;
+  const int tid = threadIdx.x;
+  const int K = p.K, kpad = pad128(K), nkb4 = kpad / 32, nkb = K / 32, k8n = K / 8;
+  const int t = __ldg(p.permuted_src + r) / p.top_k;
+  uint4* orow = reinterpret_cast<uint4*>(p.x16 + (size_t)r * kpad);
+  float* srow = p.xs + (size_t)r * nkb4;
+  float row_scale = 0.f;
+  if (p.act == 0) {
+    const uint4* xrow = reinterpret_cast<const uint4*>(p.x_bf16) + (size_t)t * k8n;
+    float amax = 0.f;
+    for (int k8 = tid; k8 < k8n; k8 += 128) {
+      const uint4 v = __ldg(xrow + k8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    // row exponent: amax * 2^-ex in [2^14, 2^15)
+    int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
+    ex = ex < -126 ? -126 : ex;
+    const float inv = exp2i(-ex);
+    row_scale = exp2i(ex);
+    for (int k8 = tid; k8 < k8n; k8 += 128) {
+      const uint4 v = __ldg(xrow + k8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = f32x2_to_f16x2(bf16_lo(w[i]) * inv, bf16_hi(w[i]) * inv);
+      orow[k8] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  } else if (p.act == 1) {
+    const uint2* xrow = reinterpret_cast<const uint2*>(p.x_q + (size_t)t * K);
+    for (int k8 = tid; k8 < k8n; k8 += 128) {
+      const uint2 q = __ldg(xrow + k8);
+      orow[k8] = make_uint4(e4m3x2_to_f16x2(q.x & 0xFFFFu), e4m3x2_to_f16x2(q.x >> 16),
+                            e4m3x2_to_f16x2(q.y & 0xFFFFu), e4m3x2_to_f16x2(q.y >> 16));
+    }
+  } else {
+    const uint32_t* xrow = reinterpret_cast<const uint32_t*>(p.x_q + (size_t)t * (K / 2));
+    for (int k8 = tid; k8 < k8n; k8 += 128) {
+      uint32_t o[4];
+      e2m1x8_to_f16x8(__ldg(xrow + k8), o);
+      const uint32_t sb = __ldg(p.x_s + (size_t)t * (K / 16) + k8 / 2);
+      const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = hmul2_f16(o[i], s2);
+      orow[k8] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    row_scale = __ldg(p.x_gs + t);
+  }
+  for (int k8 = k8n + tid; k8 < kpad / 8; k8 += 128) orow[k8] = make_uint4(0, 0, 0, 0);
+  for (int b = tid; b < nkb4; b += 128) {
+    float v = 0.f;
+    if (b < nkb) v = p.act == 1 ? exp2i((int)__ldg(p.x_s + (size_t)t * nkb + b) - 127) : row_scale;
+    srow[b] = v;
+  }
+}
+
+cudaError_t launch_gather16(const Gather16Params& p, cudaStream_t st) {
+  if (p.S <= 0) return cudaSuccess;
+  gather16_kernel<<<(unsigned)p.S, 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
 size_t fcd_smem_bytes(int K, bool nvfp4) {
   return (size_t)kNT * x_stride(K, nvfp4) + (size_t)((K / 32 + 3) / 4 * 4) * kNT * 4 +
          (size_t)kNT * 128 * 4 + (size_t)kWarps * kST * kStageBytes;
@@ -538,7 +538,7 @@ static cudaError_t launch_fcd_t(const FcdParams& p, long max_tiles, cudaStream_t
 }
 
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st) {
-  const bool ablk = p.act == 1;
+  const bool ablk = p.ablk != 0;
   if (fc1) {
     if (nvfp4) return ablk ? launch_fcd_t<true, true, true>(p, max_tiles, st) : launch_fcd_t<true, true, false>(p, max_tiles, st);
     return ablk ? launch_fcd_t<true, false, true>(p, max_tiles, st) : launch_fcd_t<true, false, false>(p, max_tiles, st);

@@ -67,22 +67,36 @@ struct FcParams {
 cudaError_t launch_fc(const FcParams& p, bool fc1, bool nvfp4, int ns, long max_tiles,
                       cudaStream_t st);
 
-// Decode-tile grouped GEMM (8 tokens per CTA, whole K staged once).  The
-// activation rows come from `xa` in one of three formats (act): 0 bf16
-// [rows, K]; 1 MXFP8 E4M3 [rows, K] + UE8M0 xs [rows, K/32]; 2 NVFP4 packed
-// [rows, K/2] + E4M3 xs [rows, K/16] + fp32 xg [rows].  With row_src set,
-// expert-ordered row r reads source row row_src[r] / top_k (FC1 gathers
-// from the token-major input); without it, row r itself.
+// Decode path.  Activation rows for the decode-tile GEMMs are "f16 block
+// rows": f16 mantissas [rows, kpad] (kpad = K rounded up to 128, zero
+// padded) and one fp32 scale per (row, 32-block) [rows, kpad/32]; a row's
+// value is mantissa * scale.  gather16 builds them from the token-major
+// input in expert order; FC1 writes H1 in the same form for FC2.
+__host__ __device__ inline int pad128(int k) { return (k + 127) / 128 * 128; }
+
+struct Gather16Params {
+  int act;                       // situ_act_dtype of the input
+  const void* x_bf16;
+  const uint8_t* x_q;
+  const uint8_t* x_s;
+  const float* x_gs;
+  const int32_t* permuted_src;
+  const int32_t* meta;           // meta[0] = R
+  int top_k, K;
+  long S;                        // upper bound on R
+  uint16_t* x16;                 // f16 [S, pad128(K)]
+  float* xs;                     // fp32 [S, pad128(K)/32]
+};
+cudaError_t launch_gather16(const Gather16Params& p, cudaStream_t st);
+
+// Decode-tile grouped GEMM (8 tokens per CTA, whole K staged once).
 struct FcdParams {
-  const uint8_t* w;
-  const uint8_t* ws;
+  const uint8_t* w;              // packed E2M1 [E_loc, Mtot, K/2]
+  const uint8_t* ws;             // block scales [E_loc, Mtot, K/bs]
   int Mtot, K;
-  int act;
-  const void* xa;
-  const uint8_t* xs;
-  const float* xg;
-  const int32_t* row_src;
-  int top_k;
+  const uint16_t* x16;           // f16 block rows [S, pad128(K)] in expert order
+  const float* xs;               // [S, pad128(K)/32]
+  int ablk;                      // scales differ per block (else one per row)
   const int32_t* offsets;
   const int32_t* tile_offsets;
   const int2* tile_info;
@@ -90,10 +104,9 @@ struct FcdParams {
   // FC1
   int I;
   const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs;
-  int h_mxfp8;
-  uint16_t* h_bf16;              // bf16 [S, I]
-  uint8_t* h_q;                  // MXFP8 [S, I] (w4a8)
-  uint8_t* h_s;                  // UE8M0 [S, I/32]
+  int h_mxfp8;                   // H1 is the MXFP8 round trip of h (else bf16 of h)
+  uint16_t* h16;                 // f16 block rows [S, pad128(I)]
+  float* hs;                     // [S, pad128(I)/32]
   // FC2
   const float *alpha2, *w2_gs;
   float* y_out;                  // fp32 [S, H]

@@ -22,7 +22,8 @@ bool aligned_to(const void* p, uintptr_t a) { return p == nullptr || (reinterpre
 bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
-  size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, xperm, xg, h1, y, total;
+  size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, xperm, xg, h1, y;
+  size_t x16, x16s, h16, h16s, total;
 };
 
 Layout make_layout(const situ_moe_args* a) {
@@ -43,6 +44,11 @@ Layout make_layout(const situ_moe_args* a) {
   L.xg = take(4 * S);
   L.h1 = take(2 * S * (size_t)a->I);
   L.y = take(4 * S * (size_t)a->H);
+  // decode path: f16 block rows of the input and of H1
+  L.x16 = take(2 * S * (size_t)pad128(a->H));
+  L.x16s = take(4 * S * (size_t)(pad128(a->H) / 32));
+  L.h16 = take(2 * S * (size_t)pad128(a->I));
+  L.h16s = take(4 * S * (size_t)(pad128(a->I) / 32));
   L.total = o;
   return L;
 }
@@ -203,8 +209,22 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   const bool decode_path = ns == 1 && fcd_smem_bytes(a->H, nv) <= kMaxSmem &&
                            fcd_smem_bytes(a->I, nv) <= kMaxSmem;
   if (decode_path) {
-    // 8-token tiles: FC1 gathers its rows straight from the input, so there
-    // is no separate gather stage.
+    // 8-token tiles: rows are converted once to f16 block rows, then FC1
+    // (+SiTU, writing H1 as f16 block rows) and FC2
+    Gather16Params g16;
+    g16.act = a->act_dtype;
+    g16.x_bf16 = a->hidden_states;
+    g16.x_q = a->hidden_states_q;
+    g16.x_s = a->hidden_states_scale;
+    g16.x_gs = a->hidden_states_gscale;
+    g16.permuted_src = psrc;
+    g16.meta = meta;
+    g16.top_k = a->top_k;
+    g16.K = a->H;
+    g16.S = S;
+    g16.x16 = (uint16_t*)(ws + L.x16);
+    g16.xs = (float*)(ws + L.x16s);
+    if ((err = launch_gather16(g16, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(2);
     FcdParams d;
     std::memset(&d, 0, sizeof(d));
@@ -217,21 +237,9 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.ws = a->w1_scale;
     d.Mtot = 2 * a->I;
     d.K = a->H;
-    if (a->act_dtype == SITU_ACT_BF16) {
-      d.act = 0;
-      d.xa = a->hidden_states;
-    } else if (a->act_dtype == SITU_ACT_MXFP8) {
-      d.act = 1;
-      d.xa = a->hidden_states_q;
-      d.xs = a->hidden_states_scale;
-    } else {
-      d.act = 2;
-      d.xa = a->hidden_states_q;
-      d.xs = a->hidden_states_scale;
-      d.xg = a->hidden_states_gscale;
-    }
-    d.row_src = psrc;
-    d.top_k = a->top_k;
+    d.x16 = g16.x16;
+    d.xs = g16.xs;
+    d.ablk = a->act_dtype == SITU_ACT_MXFP8;
     d.n_mtiles = (a->I + 63) / 64;
     d.mg = 1;
     d.beta = a->gemm1_alpha;
@@ -239,23 +247,19 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.alpha_g = a->g1_alphas;
     d.alpha_u = a->g1_alphas_up;
     d.w1_gs = a->w1_gscale;
-    const bool h_mx = a->act_dtype == SITU_ACT_MXFP8;
-    d.h_mxfp8 = h_mx;
-    d.h_bf16 = h1;
-    d.h_q = (uint8_t*)h1;                         // MXFP8 H1 shares the bf16 H1 region:
-    d.h_s = (uint8_t*)h1 + (size_t)S * a->I;      // S*I codes, then S*I/32 scales
+    d.h_mxfp8 = a->act_dtype == SITU_ACT_MXFP8;
+    d.h16 = (uint16_t*)(ws + L.h16);
+    d.hs = (float*)(ws + L.h16s);
     if ((err = launch_fcd(d, true, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(3);
-    // FC2 reads H1 in expert order
+    // FC2 reads H1 (f16 block rows, one scale per 32-block) in expert order
     d.w = a->w2;
     d.ws = a->w2_scale;
     d.Mtot = a->H;
     d.K = a->I;
-    d.act = h_mx ? 1 : 0;
-    d.xa = h_mx ? (const void*)d.h_q : (const void*)h1;
-    d.xs = h_mx ? d.h_s : nullptr;
-    d.xg = nullptr;
-    d.row_src = nullptr;
+    d.x16 = d.h16;
+    d.xs = d.hs;
+    d.ablk = 1;
     d.n_mtiles = (a->H + 127) / 128;
     d.mg = 4;
     d.alpha2 = a->g2_alphas;

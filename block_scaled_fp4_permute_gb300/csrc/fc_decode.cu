@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(128) gather16_kernel(const Gather16Params p) {
   if (r >= __ldg(p.meta)) return;
   const int tid = threadIdx.x;
   const int K = p.K, kpad = pad128(K), nkb4 = kpad / 32, nkb = K / 32, k8n = K / 8;
-  const int t = __ldg(p.permuted_src + r) / p.top_k;
+  const int t = p.permuted_src ? __ldg(p.permuted_src + r) / p.top_k : (int)r;
   uint4* orow = reinterpret_cast<uint4*>(p.x16 + (size_t)r * kpad);
   float* srow = p.xs + (size_t)r * nkb4;
   float row_scale = 0.f;
@@ -481,10 +481,29 @@ __global__ void __launch_bounds__(128) gather16_kernel(const Gather16Params p) {
     }
   } else if (p.act == 1) {
     const uint2* xrow = reinterpret_cast<const uint2*>(p.x_q + (size_t)t * K);
+    int smax = 0;
+    if (p.row_scale) {   // fold the block scales into the mantissas, relative to the row's largest
+      for (int b = tid; b < nkb; b += 128) smax = max(smax, (int)__ldg(p.x_s + (size_t)t * nkb + b));
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) smax = max(smax, __shfl_xor_sync(0xffffffffu, smax, d));
+      if ((tid & 31) == 0) red[tid >> 5] = (float)smax;
+      __syncthreads();
+      smax = (int)fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+      row_scale = exp2i(smax - 127);
+    }
     for (int k8 = tid; k8 < k8n; k8 += 128) {
       const uint2 q = __ldg(xrow + k8);
-      orow[k8] = make_uint4(e4m3x2_to_f16x2(q.x & 0xFFFFu), e4m3x2_to_f16x2(q.x >> 16),
-                            e4m3x2_to_f16x2(q.y & 0xFFFFu), e4m3x2_to_f16x2(q.y >> 16));
+      uint4 o = make_uint4(e4m3x2_to_f16x2(q.x & 0xFFFFu), e4m3x2_to_f16x2(q.x >> 16),
+                           e4m3x2_to_f16x2(q.y & 0xFFFFu), e4m3x2_to_f16x2(q.y >> 16));
+      if (p.row_scale) {
+        // 2^(s_b - s_max) as an f16 pair: exact while the block is within
+        // 2^15 of the row's largest block scale
+        const int k = (int)__ldg(p.x_s + (size_t)t * nkb + k8 / 4) - smax;
+        const uint32_t hk = k >= -14 ? (uint32_t)(k + 15) << 10 : (k >= -24 ? 1u << (k + 24) : 0u);
+        const uint32_t f2 = hk | (hk << 16);
+        o = make_uint4(hmul2_f16(o.x, f2), hmul2_f16(o.y, f2), hmul2_f16(o.z, f2), hmul2_f16(o.w, f2));
+      }
+      orow[k8] = o;
     }
   } else {
     const uint32_t* xrow = reinterpret_cast<const uint32_t*>(p.x_q + (size_t)t * (K / 2));
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(128) gather16_kernel(const Gather16Params p) {
   for (int k8 = k8n + tid; k8 < kpad / 8; k8 += 128) orow[k8] = make_uint4(0, 0, 0, 0);
   for (int b = tid; b < nkb4; b += 128) {
     float v = 0.f;
-    if (b < nkb) v = p.act == 1 ? exp2i((int)__ldg(p.x_s + (size_t)t * nkb + b) - 127) : row_scale;
+    if (b < nkb) v = (p.act == 1 && !p.row_scale) ? exp2i((int)__ldg(p.x_s + (size_t)t * nkb + b) - 127) : row_scale;
     srow[b] = v;
   }
 }

@@ -1,0 +1,477 @@
+// fc_tc.cu -- FC1 (gate/up + SiTU) and FC2 on the 5th-generation tensor
+// cores (tcgen05) for prefill-sized token tiles.
+//
+// One CTA computes a [128 tokens x 256 weight rows] tile of one local
+// expert, K in stages of 64:
+//   * warp 0 (one lane) is the TMA producer: per stage it loads the token
+//     tile's f16 activation rows (128 x 64, 128-byte swizzle, the layout the
+//     MMA descriptors expect) and the weight rows' packed E2M1 bytes
+//     (256 x 32 B) into a 3-stage shared ring, completion tracked by
+//     mbarrier transaction counts;
+//   * warps 4..7 (128 threads, two weight rows each) dequantise the packed
+//     weights to f16 in shared memory, in the 128-byte-swizzled K-major
+//     layout: E2M1 -> f16 with the hardware conversion, times the block scale
+//     relative to the row's largest block scale (2^(s_b - s_max), exact for
+//     blocks within 2^23 of the row maximum; NVFP4's E4M3 block scales are
+//     folded in directly, always exact); the row's 2^(s_max - 127) and any
+//     NVFP4 global scale go to the epilogue;
+//   * warp 1 allocates 256 TMEM columns and one lane issues
+//     tcgen05.mma.kind::f16 (M = 128 tokens, N = 256, K = 16 per
+//     instruction, fp32 accumulation in TMEM), committing each stage back to
+//     the producer and the final accumulator to the epilogue;
+//   * warps 4..7 then read the accumulator (each thread one token row) with
+//     tcgen05.ld and apply the per-token and per-row scales and, for FC1,
+//     SiTU on the gate/up column pair (the tile's 256 columns are 128 gate
+//     rows and the 128 matching up rows), writing H1 as bf16 (or its MXFP8
+//     round trip for w4a8); FC2 writes fp32.
+// Activations are "f16 rows with one scale per row" (gather16 in row-scale
+// mode).  Every mbarrier wait is bounded by a wall-clock limit; on expiry
+// the CTA records an error code in the device status word and unwinds, and
+// TMEM is always released.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "situ_internal.h"
+
+namespace situ {
+
+namespace {
+
+constexpr int kBM = 128;        // tokens per tile (MMA M, TMEM lanes)
+constexpr int kBN = 256;        // weight rows per tile (MMA N)
+constexpr int kBK = 64;         // K elements per stage
+constexpr int kStages = 3;
+constexpr int kThreads = 256;
+constexpr int kTmemCols = 256;
+constexpr int kABytes = kBM * kBK * 2;     // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;     // 32 KB
+constexpr int kPBytes = kBN * kBK / 2;     // 8 KB packed E2M1
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kABytes;
+constexpr int kOffP = kOffB + kStages * kBBytes;
+constexpr int kOffW = kOffP + kStages * kPBytes;          // float[kBN] epilogue row scales
+constexpr int kOffBar = kOffW + kBN * 4;                   // mbarriers
+constexpr int kNumBars = 4 * kStages + 1;
+constexpr int kOffTm = kOffBar + kNumBars * 8;             // TMEM base address
+constexpr int kSmemBytes = kOffTm + 16 + 1024;             // + alignment slack
+constexpr unsigned long long kWaitNs = 200000000ull;      // 200 ms
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false (and an error
+// code in *err) if it does not complete within kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int* err, int code) {
+  if (mbar_try(a, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(a, parity)) return true;
+    if ((i & 1023u) == 0) {
+      // give up past the limit, or as soon as another CTA has given up
+      if (globaltimer() - t0 > kWaitNs) {
+        atomicCAS(err, 0, code);
+        return false;
+      }
+      if (*reinterpret_cast<volatile int*>(err) != 0) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle,
+// 8-row groups 1024 bytes apart (SBO), start address >> 4.
+__device__ __forceinline__ uint64_t sdesc(uint32_t a) {
+  uint64_t d = 0;
+  d |= (uint64_t)((a >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024u >> 4) << 32;   // stride byte offset
+  d |= (uint64_t)1u << 46;             // descriptor version
+  d |= (uint64_t)2u << 61;             // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: f16 x f16 -> f32, both K-major,
+// N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                            ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* d) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// 2^k as an f16 pair, k in [-24, 15] (0 below)
+__device__ __forceinline__ uint32_t f16x2_pow2(int k) {
+  uint32_t h;
+  if (k >= -14) h = (uint32_t)(k + 15) << 10;
+  else if (k >= -24) h = 1u << (k + 24);
+  else h = 0u;
+  return h | (h << 16);
+}
+
+}  // namespace
+
+template <bool FC1, bool WNV>
+__global__ void __launch_bounds__(kThreads, 1)
+fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const FcpParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int ntile = blockIdx.x % p.n_ntiles;
+  const int tile = blockIdx.x / p.n_ntiles;
+  if (tile >= __ldg(p.tile_offsets + p.E_loc)) return;
+  if (*reinterpret_cast<volatile int*>(p.err) != 0) return;   // an earlier CTA timed out
+  const int2 ti = __ldg(p.tile_info + tile);
+  const int e = ti.x, row0 = ti.y;
+  const int nrows = min(kBM, __ldg(p.offsets + e + 1) - row0);
+  const int K = p.K;
+  const int nk = (K + kBK - 1) / kBK;
+  const int bsz = WNV ? 16 : 32;
+  const int nsb = K / bsz;                        // block scales per weight row
+  const int nbase = FC1 ? ntile * (kBN / 2) : ntile * kBN;
+
+  const uint32_t sbase = saddr(smem);
+  float* wsc = reinterpret_cast<float*>(smem + kOffW);
+  const uint32_t bar0 = sbase + kOffBar;
+  auto full_a = [&](int s) { return bar0 + 8 * s; };
+  auto full_p = [&](int s) { return bar0 + 8 * (kStages + s); };
+  auto full_b = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
+  auto empty = [&](int s) { return bar0 + 8 * (3 * kStages + s); };
+  const uint32_t acc_full = bar0 + 8 * (4 * kStages);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + kOffTm);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(full_p(s), 1);
+      mbar_init(full_b(s), 128);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tm_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tm_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const int yw = e * p.Mtot + nbase;
+      for (int kk = 0; kk < nk; ++kk) {
+        const int s = kk % kStages, r = kk / kStages;
+        if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1, p.err, 11)) break;
+        mbar_expect_tx(full_a(s), kABytes);
+        tma_load_2d(sbase + kOffA + s * kABytes, &tmA, kk * kBK, row0, full_a(s));
+        mbar_expect_tx(full_p(s), kPBytes);
+        if (FC1) {
+          tma_load_2d(sbase + kOffP + s * kPBytes, &tmB, kk * (kBK / 2), yw, full_p(s));
+          tma_load_2d(sbase + kOffP + s * kPBytes + kPBytes / 2, &tmB, kk * (kBK / 2), yw + p.I, full_p(s));
+        } else {
+          tma_load_2d(sbase + kOffP + s * kPBytes, &tmB, kk * (kBK / 2), yw, full_p(s));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int kk = 0; kk < nk && ok; ++kk) {
+        const int s = kk % kStages, par = (kk / kStages) & 1;
+        ok = mbar_wait(full_a(s), par, p.err, 12) && mbar_wait(full_b(s), par, p.err, 13);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint64_t ad = sdesc(sbase + kOffA + s * kABytes);
+        const uint64_t bd = sdesc(sbase + kOffB + s * kBBytes);
+#pragma unroll
+        for (int k4 = 0; k4 < kBK / 16; ++k4)   // +32 bytes along K per instruction
+          mma_f16_ss(tmem, ad + 2 * k4, bd + 2 * k4, (kk | k4) != 0);
+        mma_commit(empty(s));
+      }
+      mma_commit(acc_full);
+    }
+  } else if (warp >= 4) {
+    // ---------------- converters, then epilogue ----------------
+    const int t = tid - 128;
+    int grow[2];
+    bool gv[2];
+    for (int h = 0; h < 2; ++h) {
+      const int n = t + 128 * h;
+      if (FC1) {
+        const int i = nbase + t;
+        gv[h] = i < p.I;
+        grow[h] = h ? p.I + i : i;
+      } else {
+        grow[h] = nbase + n;
+        gv[h] = grow[h] < p.Mtot;
+      }
+    }
+    const uint8_t* srow[2];
+    int smax[2];
+    for (int h = 0; h < 2; ++h) {
+      srow[h] = p.ws + ((size_t)e * p.Mtot + (gv[h] ? grow[h] : 0)) * (size_t)nsb;
+      int m = 0;
+      if (!WNV && gv[h])
+        for (int b = 0; b < nsb; ++b) m = max(m, (int)__ldg(srow[h] + b));
+      smax[h] = m;
+      float ws = 0.f;
+      if (gv[h]) {
+        if (WNV) ws = FC1 ? __ldg(p.w1_gs + 2 * e + h) : __ldg(p.w2_gs + e);
+        else ws = exp2i(m - 127);
+      }
+      wsc[t + 128 * h] = ws;
+    }
+    for (int kk = 0; kk < nk; ++kk) {
+      const int s = kk % kStages, par = (kk / kStages) & 1;
+      if (!mbar_wait(full_p(s), par, p.err, 14)) break;
+      const uint8_t* pk = smem + kOffP + s * kPBytes;
+      uint8_t* bt = smem + kOffB + s * kBBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int n = t + 128 * h;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(pk + n * 32);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(pk + n * 32 + 16);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // dequant factors: word j covers elements 8j..8j+7 of the stage
+        uint32_t f[8];
+        if (WNV) {
+#pragma unroll
+          for (int j2 = 0; j2 < 4; ++j2) {   // 16-element blocks of the stage
+            const int b = kk * 4 + j2;
+            uint32_t sb = 0u;
+            if (gv[h] && b < nsb) sb = __ldg(srow[h] + b);
+            f[2 * j2] = f[2 * j2 + 1] = e4m3x2_to_f16x2(sb | (sb << 8));
+          }
+        } else {
+#pragma unroll
+          for (int j2 = 0; j2 < 2; ++j2) {   // 32-element blocks
+            const int b = kk * 2 + j2;
+            uint32_t fb = 0u;
+            if (gv[h] && b < nsb) fb = f16x2_pow2((int)__ldg(srow[h] + b) - smax[h]);
+            f[4 * j2] = f[4 * j2 + 1] = f[4 * j2 + 2] = f[4 * j2 + 3] = fb;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {   // 16-byte chunk j = elements 8j..8j+7
+          uint32_t d[4];
+          e2m1x8_to_f16x8(w[j], d);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d[i] = hmul2(d[i], f[j]);
+          *reinterpret_cast<uint4*>(bt + n * 128 + ((j ^ (n & 7)) << 4)) = make_uint4(d[0], d[1], d[2], d[3]);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(full_b(s));
+    }
+    // ---- epilogue: thread = token row (TMEM lane) ----
+    const int m = (warp - 4) * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // converters' wsc writes visible
+    // warp-uniform outcome: the tcgen05.ld below are .sync.aligned
+    const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.err, 15));
+    if (acc_ok) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const bool vrow = m < nrows;
+      const size_t row = (size_t)(row0 + (vrow ? m : 0));
+      const float xs = vrow ? __ldg(p.xs + row * p.xs_stride) : 0.f;
+      if (FC1) {
+        const float ag = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
+        const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
+        const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+        for (int c0 = 0; c0 < kBN / 2; c0 += 32) {
+          float gt[32], up[32];
+          tmem_ld16(trow + c0, gt);
+          tmem_ld16(trow + c0 + 16, gt + 16);
+          tmem_ld16(trow + 128 + c0, up);
+          tmem_ld16(trow + 128 + c0 + 16, up + 16);
+          const int i0 = nbase + c0;
+          if (!vrow || i0 >= p.I) continue;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = situ_f(gt[j] * (xs * wsc[c0 + j] * ag), up[j] * (xs * wsc[128 + c0 + j] * au), bt, btl);
+          if (p.h_mxfp8) {   // the MXFP8 round trip FC2 consumes (w4a8)
+            float amax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+            const int ex = mxfp8_exponent(amax);
+            const float sc = exp2i(-ex), back = exp2i(ex);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const uint32_t cc = f32x2_to_e4m3x2(v[j] * sc, v[j + 1] * sc);
+              v[j] = e4m3_to_f32(cc & 0xFFu) * back;
+              v[j + 1] = e4m3_to_f32(cc >> 8) * back;
+            }
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.h_out + row * p.I + i0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(f32x2_to_bf16x2(v[8 * q], v[8 * q + 1]), f32x2_to_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                f32x2_to_bf16x2(v[8 * q + 4], v[8 * q + 5]), f32x2_to_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        }
+      } else {
+        const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
+        for (int c0 = 0; c0 < kBN; c0 += 16) {
+          float acc[16];
+          tmem_ld16(trow + c0, acc);
+          const int n0 = nbase + c0;
+          if (!vrow || n0 >= p.Mtot) continue;
+          float4* dst = reinterpret_cast<float4*>(p.y_out + row * p.Mtot + n0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_float4(acc[4 * q] * (xs * wsc[c0 + 4 * q] * a2), acc[4 * q + 1] * (xs * wsc[c0 + 4 * q + 1] * a2),
+                                 acc[4 * q + 2] * (xs * wsc[c0 + 4 * q + 2] * a2),
+                                 acc[4 * q + 3] * (xs * wsc[c0 + 4 * q + 3] * a2));
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FC1, bool WNV>
+cudaError_t launch_fcp_t(const FcpParams& p, const CUtensorMap& a, const CUtensorMap& b, long max_tiles,
+                         cudaStream_t st) {
+  static int set_for[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || set_for[dev] == 0) {
+    cudaError_t err = cudaFuncSetAttribute(fcp_kernel<FC1, WNV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) set_for[dev] = 1;
+  }
+  const long grid = max_tiles * p.n_ntiles;
+  if (grid <= 0) return cudaSuccess;
+  fcp_kernel<FC1, WNV><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int fcp_token_tile() { return kBM; }
+
+cudaError_t launch_fcp(const FcpParams& p, const uint16_t* x16, long S, int kpad, const uint8_t* w, int E_loc,
+                       bool fc1, bool nvfp4, long max_tiles, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  // activations: f16 [S, kpad], boxes of 64 columns (128 B) x 128 rows, 128-byte swizzle
+  if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)kpad, (uint64_t)S, (uint64_t)kpad * 2, kBK, kBM,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // packed weights: u8 [E_loc * Mtot, K/2], boxes of 32 bytes x (128 | 256) rows
+  if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)(p.K / 2), (uint64_t)E_loc * p.Mtot,
+                (uint64_t)(p.K / 2), kBK / 2, fc1 ? kBN / 2 : kBN, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (fc1) return nvfp4 ? launch_fcp_t<true, true>(p, ma, mb, max_tiles, st) : launch_fcp_t<true, false>(p, ma, mb, max_tiles, st);
+  return nvfp4 ? launch_fcp_t<false, true>(p, ma, mb, max_tiles, st) : launch_fcp_t<false, false>(p, ma, mb, max_tiles, st);
+}
+
+}  // namespace situ

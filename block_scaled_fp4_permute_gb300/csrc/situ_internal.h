@@ -25,48 +25,6 @@ cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t*
 cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,
                            int H, void* out, cudaStream_t st);
 
-// Gather the kept rows into expert order as bf16 (exact dequantisation of
-// MXFP8 / NVFP4 activations) and, for NVFP4, the per-row activation scale.
-struct GatherParams {
-  int act;                       // situ_act_dtype
-  const void* x_bf16;
-  const uint8_t* x_q;
-  const uint8_t* x_s;
-  const float* x_gs;
-  const int32_t* permuted_src;
-  const int32_t* meta;           // meta[0] = R
-  int top_k, H;
-  long S;                        // T * top_k, an upper bound on R
-  uint16_t* x_perm;              // bf16 [S, H]
-  float* xg_perm;                // fp32 [S] (NVFP4) or nullptr
-};
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t st);
-
-// One grouped GEMM over the token tiles built by the permute:
-// rows of W (block-scaled FP4, one matrix per local expert) times the
-// expert's permuted bf16 activation rows, with the FC1 (SiTU) or FC2
-// (scale, fp32 output) epilogue.
-struct FcParams {
-  const uint8_t* w;              // packed E2M1 [E_loc, Mtot, K/2]
-  const uint8_t* ws;             // block scales [E_loc, Mtot, K/bs]
-  int Mtot, K;
-  const uint16_t* x;             // bf16 [S, K], rows in expert order
-  const int32_t* offsets;        // [E_loc+1]
-  const int32_t* tile_offsets;   // [E_loc+1]
-  const int2* tile_info;         // [tiles] (expert, first row)
-  int E_loc, n_mtiles;
-  // FC1
-  int I;
-  const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs, *xg;
-  int mxfp8_h;
-  uint16_t* h_out;               // bf16 [S, I]
-  // FC2
-  const float *alpha2, *w2_gs;
-  float* y_out;                  // fp32 [S, H]
-};
-cudaError_t launch_fc(const FcParams& p, bool fc1, bool nvfp4, int ns, long max_tiles,
-                      cudaStream_t st);
-
 // Decode path.  Activation rows for the decode-tile GEMMs are "f16 block
 // rows": f16 mantissas [rows, kpad] (kpad = K rounded up to 128, zero
 // padded) and one fp32 scale per (row, 32-block) [rows, kpad/32]; a row's
@@ -76,11 +34,12 @@ __host__ __device__ inline int pad128(int k) { return (k + 127) / 128 * 128; }
 
 struct Gather16Params {
   int act;                       // situ_act_dtype of the input
+  int row_scale;                 // 1: one scale per row (MXFP8 block scales folded into the mantissas)
   const void* x_bf16;
   const uint8_t* x_q;
   const uint8_t* x_s;
   const float* x_gs;
-  const int32_t* permuted_src;
+  const int32_t* permuted_src;   // row r reads source row permuted_src[r] / top_k; null: row r
   const int32_t* meta;           // meta[0] = R
   int top_k, K;
   long S;                        // upper bound on R
@@ -112,6 +71,31 @@ struct FcdParams {
   float* y_out;                  // fp32 [S, H]
 };
 constexpr int kDecodeTileTokens = 8;
+
+// Prefill-tile grouped GEMM on tcgen05 (fc_tc.cu): 128 token rows x 256
+// weight rows per CTA.  Activations: f16 rows [S, pad128(K)] with one fp32
+// scale per row (xs[row * xs_stride]).
+struct FcpParams {
+  int Mtot, K, I;
+  const uint8_t* ws;             // block scales [E_loc, Mtot, K/bs]
+  const int32_t* offsets;
+  const int32_t* tile_offsets;
+  const int2* tile_info;
+  int E_loc, n_ntiles;
+  const float* xs;
+  int xs_stride;
+  // FC1
+  const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs;
+  int h_mxfp8;
+  uint16_t* h_out;               // bf16 [S, I]
+  // FC2
+  const float *alpha2, *w2_gs;
+  float* y_out;                  // fp32 [S, H]
+  int* err;                      // device status word (0 = ok)
+};
+int fcp_token_tile();
+cudaError_t launch_fcp(const FcpParams& p, const uint16_t* x16, long S, int kpad, const uint8_t* w, int E_loc,
+                       bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 size_t fcd_smem_bytes(int K, bool nvfp4);
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 

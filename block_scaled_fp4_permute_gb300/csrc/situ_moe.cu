@@ -22,7 +22,7 @@ bool aligned_to(const void* p, uintptr_t a) { return p == nullptr || (reinterpre
 bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
-  size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, xperm, xg, h1, y;
+  size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
   size_t x16, x16s, h16, h16s, total;
 };
 
@@ -40,8 +40,6 @@ Layout make_layout(const situ_moe_args* a) {
   L.psrc = take(4 * S);
   L.s2r = take(4 * S);
   L.blk = take(permute_scratch_bytes(a->T, a->top_k, a->num_local_experts));
-  L.xperm = take(2 * S * (size_t)a->H);
-  L.xg = take(4 * S);
   L.h1 = take(2 * S * (size_t)a->I);
   L.y = take(4 * S * (size_t)a->H);
   // decode path: f16 block rows of the input and of H1
@@ -95,12 +93,10 @@ situ_status validate(const situ_moe_args* a) {
 
 // Token-tile width of the grouped GEMMs: 8 * ns tokens, chosen from the
 // expected rows per expert (decode: 1-2 rows, prefill: hundreds).
-int choose_ns(const situ_moe_args* a) {
-  double avg = (double)a->T * a->top_k / (double)a->num_experts_total;
-  if (avg <= 6.0) return 1;
-  if (avg <= 12.0) return 2;
-  if (avg <= 24.0) return 4;
-  return 8;
+// Decode-like routings (about six or fewer rows per expert) take the
+// 8-token-tile path; everything else the tcgen05 prefill path.
+bool decode_like(const situ_moe_args* a) {
+  return (double)a->T * a->top_k / (double)a->num_experts_total <= 6.0;
 }
 
 situ_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SITU_OK : SITU_ERR_CUDA; }
@@ -184,13 +180,11 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   int32_t* meta = (int32_t*)(ws + L.meta);
   int32_t* psrc = (int32_t*)(ws + L.psrc);
   int32_t* s2r = (int32_t*)(ws + L.s2r);
-  uint16_t* xperm = (uint16_t*)(ws + L.xperm);
-  float* xg = (float*)(ws + L.xg);
   uint16_t* h1 = (uint16_t*)(ws + L.h1);
   float* y = (float*)(ws + L.y);
   const bool nv = a->weight_dtype == SITU_W_NVFP4;
-  const int ns = choose_ns(a);
-  const int tile_n = 8 * ns;
+  const bool small_tiles = decode_like(a);
+  const int tile_n = small_tiles ? kDecodeTileTokens : fcp_token_tile();
   const long S = (long)a->T * a->top_k;
   const long max_tiles = S / tile_n + a->num_local_experts + 1;
   auto mark = [&](int i) {
@@ -206,13 +200,14 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
 
   // the decode kernel stages the whole K of its token tile in shared memory
   const size_t kMaxSmem = 220 * 1024;
-  const bool decode_path = ns == 1 && fcd_smem_bytes(a->H, nv) <= kMaxSmem &&
+  const bool decode_path = small_tiles && fcd_smem_bytes(a->H, nv) <= kMaxSmem &&
                            fcd_smem_bytes(a->I, nv) <= kMaxSmem;
   if (decode_path) {
     // 8-token tiles: rows are converted once to f16 block rows, then FC1
     // (+SiTU, writing H1 as f16 block rows) and FC2
     Gather16Params g16;
     g16.act = a->act_dtype;
+    g16.row_scale = 0;
     g16.x_bf16 = a->hidden_states;
     g16.x_q = a->hidden_states_q;
     g16.x_s = a->hidden_states_scale;
@@ -268,57 +263,75 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if ((err = launch_fcd(d, false, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(4);
   } else {
-    GatherParams gp;
-    gp.act = a->act_dtype;
-    gp.x_bf16 = a->hidden_states;
-    gp.x_q = a->hidden_states_q;
-    gp.x_s = a->hidden_states_scale;
-    gp.x_gs = a->hidden_states_gscale;
-    gp.permuted_src = psrc;
-    gp.meta = meta;
-    gp.top_k = a->top_k;
-    gp.H = a->H;
-    gp.S = S;
-    gp.x_perm = xperm;
-    gp.xg_perm = a->act_dtype == SITU_ACT_NVFP4 ? xg : nullptr;
-    if ((err = launch_gather(gp, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    // 128-token tiles on tcgen05: f16 rows with one scale per row, FC1 (+SiTU)
+    // writing bf16 H1, H1 to f16 rows, FC2
+    int* err_word = meta + 2;
+    Gather16Params g16;
+    g16.act = a->act_dtype;
+    g16.row_scale = 1;
+    g16.x_bf16 = a->hidden_states;
+    g16.x_q = a->hidden_states_q;
+    g16.x_s = a->hidden_states_scale;
+    g16.x_gs = a->hidden_states_gscale;
+    g16.permuted_src = psrc;
+    g16.meta = meta;
+    g16.top_k = a->top_k;
+    g16.K = a->H;
+    g16.S = S;
+    g16.x16 = (uint16_t*)(ws + L.x16);
+    g16.xs = (float*)(ws + L.x16s);
+    if ((err = launch_gather16(g16, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(2);
-
-    FcParams f;
+    FcpParams f;
     std::memset(&f, 0, sizeof(f));
     f.offsets = offsets;
     f.tile_offsets = tile_offsets;
     f.tile_info = tile_info;
     f.E_loc = a->num_local_experts;
     f.I = a->I;
-    // FC1: W1 [E_loc, 2I, H], gate rows 0..I-1, up rows I..2I-1
-    f.w = a->w1;
+    f.err = err_word;
     f.ws = a->w1_scale;
     f.Mtot = 2 * a->I;
     f.K = a->H;
-    f.x = xperm;
-    f.n_mtiles = (a->I + 63) / 64;
+    f.n_ntiles = (a->I + 127) / 128;
+    f.xs = g16.xs;
+    f.xs_stride = pad128(a->H) / 32;
     f.beta = a->gemm1_alpha;
     f.beta_lin = a->gemm1_beta;
     f.alpha_g = a->g1_alphas;
     f.alpha_u = a->g1_alphas_up;
     f.w1_gs = a->w1_gscale;
-    f.xg = gp.xg_perm;
-    f.mxfp8_h = a->act_dtype == SITU_ACT_MXFP8;
+    f.h_mxfp8 = a->act_dtype == SITU_ACT_MXFP8;
     f.h_out = h1;
-    if ((err = launch_fc(f, true, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    if ((err = launch_fcp(f, g16.x16, S, pad128(a->H), a->w1, a->num_local_experts, true, nv, max_tiles, st)) !=
+        cudaSuccess)
+      return SITU_ERR_CUDA;
+    // H1 (bf16, expert order) to f16 rows with one scale per row
+    Gather16Params h16;
+    std::memset(&h16, 0, sizeof(h16));
+    h16.act = SITU_ACT_BF16;
+    h16.row_scale = 1;
+    h16.x_bf16 = h1;
+    h16.permuted_src = nullptr;
+    h16.meta = meta;
+    h16.K = a->I;
+    h16.S = S;
+    h16.x16 = (uint16_t*)(ws + L.h16);
+    h16.xs = (float*)(ws + L.h16s);
+    if ((err = launch_gather16(h16, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(3);
-    // FC2: W2 [E_loc, H, I]
-    f.w = a->w2;
     f.ws = a->w2_scale;
     f.Mtot = a->H;
     f.K = a->I;
-    f.x = h1;
-    f.n_mtiles = (a->H + 127) / 128;
+    f.n_ntiles = (a->H + 255) / 256;
+    f.xs = h16.xs;
+    f.xs_stride = pad128(a->I) / 32;
     f.alpha2 = a->g2_alphas;
     f.w2_gs = a->w2_gscale;
     f.y_out = y;
-    if ((err = launch_fc(f, false, nv, ns, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    if ((err = launch_fcp(f, h16.x16, S, pad128(a->I), a->w2, a->num_local_experts, false, nv, max_tiles, st)) !=
+        cudaSuccess)
+      return SITU_ERR_CUDA;
     mark(4);
   }
 

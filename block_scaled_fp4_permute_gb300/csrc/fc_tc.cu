@@ -282,8 +282,20 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     for (int h = 0; h < 2; ++h) {
       srow[h] = p.ws + ((size_t)e * p.Mtot + (gv[h] ? grow[h] : 0)) * (size_t)nsb;
       int m = 0;
-      if (!WNV && gv[h])
-        for (int b = 0; b < nsb; ++b) m = max(m, (int)__ldg(srow[h] + b));
+      if (!WNV && gv[h]) {
+        if ((nsb & 15) == 0 && (reinterpret_cast<uintptr_t>(srow[h]) & 15) == 0) {
+          // the row's largest block scale, 16 bytes per load
+          uint32_t acc = 0u;
+          for (int b = 0; b < nsb; b += 16) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(srow[h] + b));
+            acc = __vmaxu4(acc, __vmaxu4(__vmaxu4(v.x, v.y), __vmaxu4(v.z, v.w)));
+          }
+          m = max(max((int)(acc & 0xFFu), (int)((acc >> 8) & 0xFFu)),
+                  max((int)((acc >> 16) & 0xFFu), (int)(acc >> 24)));
+        } else {
+          for (int b = 0; b < nsb; ++b) m = max(m, (int)__ldg(srow[h] + b));
+        }
+      }
       smax[h] = m;
       float ws = 0.f;
       if (gv[h]) {
@@ -292,7 +304,23 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       }
       wsc[t + 128 * h] = ws;
     }
+    // the stage's block-scale bytes of both rows, packed per row (4 x E4M3
+    // or 2 x UE8M0), prefetched two stages ahead so their load latency
+    // hides behind the conversion
+    constexpr int kSB = WNV ? 4 : 2;
+    auto load_sc = [&](int kk, int h) -> uint32_t {
+      uint32_t v = 0u;
+#pragma unroll
+      for (int j = 0; j < kSB; ++j) {
+        const int b = kk * kSB + j;
+        if (gv[h] && kk < nk && b < nsb) v |= (uint32_t)__ldg(srow[h] + b) << (8 * j);
+      }
+      return v;
+    };
+    uint32_t sc0[2] = {load_sc(0, 0), load_sc(0, 1)};
+    uint32_t sc1[2] = {load_sc(1, 0), load_sc(1, 1)};
     for (int kk = 0; kk < nk; ++kk) {
+      const uint32_t sc2[2] = {load_sc(kk + 2, 0), load_sc(kk + 2, 1)};
       const int s = kk % kStages, par = (kk / kStages) & 1;
       if (!mbar_wait(full_p(s), par, p.err, 14)) break;
       const uint8_t* pk = smem + kOffP + s * kPBytes;
@@ -308,17 +336,15 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         if (WNV) {
 #pragma unroll
           for (int j2 = 0; j2 < 4; ++j2) {   // 16-element blocks of the stage
-            const int b = kk * 4 + j2;
-            uint32_t sb = 0u;
-            if (gv[h] && b < nsb) sb = __ldg(srow[h] + b);
+            const uint32_t sb = (sc0[h] >> (8 * j2)) & 0xFFu;
             f[2 * j2] = f[2 * j2 + 1] = e4m3x2_to_f16x2(sb | (sb << 8));
           }
         } else {
 #pragma unroll
           for (int j2 = 0; j2 < 2; ++j2) {   // 32-element blocks
             const int b = kk * 2 + j2;
-            uint32_t fb = 0u;
-            if (gv[h] && b < nsb) fb = f16x2_pow2((int)__ldg(srow[h] + b) - smax[h]);
+            const uint32_t fb =
+                (gv[h] && b < nsb) ? f16x2_pow2((int)((sc0[h] >> (8 * j2)) & 0xFFu) - smax[h]) : 0u;
             f[4 * j2] = f[4 * j2 + 1] = f[4 * j2 + 2] = f[4 * j2 + 3] = fb;
           }
         }
@@ -333,6 +359,10 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(full_b(s));
+      sc0[0] = sc1[0];
+      sc0[1] = sc1[1];
+      sc1[0] = sc2[0];
+      sc1[1] = sc2[1];
     }
     // ---- epilogue: thread = token row (TMEM lane) ----
     const int m = (warp - 4) * 32 + lane;

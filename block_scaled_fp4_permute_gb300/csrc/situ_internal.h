@@ -77,6 +77,7 @@ constexpr int kDecodeTileTokens = 8;
 // scale per row (xs[row * xs_stride]).
 struct FcpParams {
   int Mtot, K, I;
+  const uint8_t* w;              // packed E2M1 [E_loc, Mtot, K/2]
   const uint8_t* ws;             // block scales [E_loc, Mtot, K/bs]
   const int32_t* offsets;
   const int32_t* tile_offsets;

@@ -290,6 +290,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     f.E_loc = a->num_local_experts;
     f.I = a->I;
     f.err = err_word;
+    f.w = a->w1;
     f.ws = a->w1_scale;
     f.Mtot = 2 * a->I;
     f.K = a->H;
@@ -320,6 +321,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     h16.xs = (float*)(ws + L.h16s);
     if ((err = launch_gather16(h16, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(3);
+    f.w = a->w2;
     f.ws = a->w2_scale;
     f.Mtot = a->H;
     f.K = a->I;

@@ -17,6 +17,7 @@ import torch
 from . import build as _build
 
 SITU_OK = 0
+SITU_ERR_DEVICE_TIMEOUT = 7
 SITU_ACT_BF16, SITU_ACT_MXFP8, SITU_ACT_NVFP4 = 0, 1, 2
 SITU_W_MXFP4, SITU_W_NVFP4 = 0, 1
 
@@ -74,6 +75,9 @@ def lib() -> ctypes.CDLL:
             l.situ_moe_forward_profiled.restype = ctypes.c_int
             l.situ_moe_forward_profiled.argtypes = [ctypes.POINTER(SituMoeArgs), vp, sz, vp,
                                                     ctypes.POINTER(ctypes.c_void_p)]
+            l.situ_moe_device_status.restype = ctypes.c_int
+            l.situ_moe_device_status.argtypes = [ctypes.POINTER(SituMoeArgs), vp, vp,
+                                                 ctypes.POINTER(ctypes.c_int32)]
             _lib = l
     return _lib
 
@@ -185,6 +189,19 @@ def situ_moe_forward(args: SituMoeArgs, workspace: torch.Tensor, stream=None) ->
         _stream(stream)))
 
 
+def situ_moe_device_status(args: SituMoeArgs, workspace: torch.Tensor, stream=None) -> int:
+    """Waits for ``stream`` and returns the device status word of the last
+    forward run with this workspace: 0, or the code of the first bounded
+    wait a kernel gave up (the C call's SITU_ERR_DEVICE_TIMEOUT is not
+    raised, it is reported through the code)."""
+    code = ctypes.c_int32(0)
+    st = lib().situ_moe_device_status(ctypes.byref(args), _p(workspace), _stream(stream),
+                                      ctypes.byref(code))
+    if st not in (0, SITU_ERR_DEVICE_TIMEOUT):
+        _check("situ_moe_device_status", st)
+    return int(code.value)
+
+
 PROFILE_STAGES = ("permute", "gather", "fc1", "fc2", "combine")
 
 
@@ -229,6 +246,10 @@ class Layer:
         self.args = make_args(**kw)
         n = situ_moe_workspace_size(self.args)
         self.workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+
+    def device_status(self, stream=None) -> int:
+        """0 when every bounded device wait of the last call completed."""
+        return situ_moe_device_status(self.args, self.workspace, stream)
 
     def profiled(self, events, quant_events=None, stream=None) -> torch.Tensor:
         """Like __call__, recording per-stage events (see situ_moe_forward_profiled);

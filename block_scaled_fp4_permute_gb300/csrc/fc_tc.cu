@@ -28,12 +28,12 @@
 // mode).  Every mbarrier wait is bounded by a wall-clock limit; on expiry
 // the CTA records an error code in the device status word and unwinds, and
 // TMEM is always released.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "situ_internal.h"
+#include "tc_common.cuh"
 
 namespace situ {
+
+using namespace tc;
 
 namespace {
 
@@ -54,70 +54,6 @@ constexpr int kOffBar = kOffW + kBN * 4;                   // mbarriers
 constexpr int kNumBars = 4 * kStages + 1;
 constexpr int kOffTm = kOffBar + kNumBars * 8;             // TMEM base address
 constexpr int kSmemBytes = kOffTm + 16 + 1024;             // + alignment slack
-constexpr unsigned long long kWaitNs = 200000000ull;      // 200 ms
-
-__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase with the given parity; false (and an error
-// code in *err) if it does not complete within kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int* err, int code) {
-  if (mbar_try(a, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try(a, parity)) return true;
-    if ((i & 1023u) == 0) {
-      // give up past the limit, or as soon as another CTA has given up
-      if (globaltimer() - t0 > kWaitNs) {
-        atomicCAS(err, 0, code);
-        return false;
-      }
-      if (*reinterpret_cast<volatile int*>(err) != 0) return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle,
-// 8-row groups 1024 bytes apart (SBO), start address >> 4.
-__device__ __forceinline__ uint64_t sdesc(uint32_t a) {
-  uint64_t d = 0;
-  d |= (uint64_t)((a >> 4) & 0x3FFFu);
-  d |= (uint64_t)1u << 16;             // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024u >> 4) << 32;   // stride byte offset
-  d |= (uint64_t)1u << 46;             // descriptor version
-  d |= (uint64_t)2u << 61;             // 128-byte swizzle
-  return d;
-}
 
 // kind::f16 instruction descriptor: f16 x f16 -> f32, both K-major,
 // N = 256, M = 128.
@@ -131,21 +67,6 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t
       "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* d) {
   asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
       " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
@@ -441,31 +362,6 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 // ---------------------------------------------------------------------------
 
 namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <bool FC1, bool WNV>
 cudaError_t launch_fcp_t(const FcpParams& p, const CUtensorMap& a, const CUtensorMap& b, long max_tiles,

@@ -97,6 +97,51 @@ struct FcpParams {
 int fcp_token_tile();
 cudaError_t launch_fcp(const FcpParams& p, const uint16_t* x16, long S, int kpad, const uint8_t* w, int E_loc,
                        bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
+
+// Block-scaled tcgen05 path for MXFP8 activations x MXFP4 weights (w4a8):
+// A operand E4M3 rows in expert order [S, K] with UE8M0 scales [S, K/32];
+// K a multiple of 128.  FC1 writes H1 as MXFP8 rows (hq [S, hq_stride],
+// hs [S, hq_stride/32]), FC2 writes fp32 Y [S, Mtot].
+struct FcqParams {
+  int Mtot, K, I;
+  const uint8_t* ws;             // weight block scales [E_loc, Mtot, K/32]
+  int ws_vec;                    // 1: ws is 4-byte aligned (rows are, K/32 being a multiple of 4)
+  const int32_t* offsets;
+  const int32_t* tile_offsets;
+  const int2* tile_info;
+  int E_loc;
+  int n_ntiles;
+  const uint8_t* xs;             // activation scales, xs_stride bytes per row (4-byte aligned)
+  int xs_stride;
+  const float* beta;
+  const float* beta_lin;
+  const float* alpha_g;
+  const float* alpha_u;
+  uint8_t* hq;
+  uint8_t* hs;
+  int hq_stride;
+  const float* alpha2;
+  float* y_out;
+  int* err;                      // device status word
+};
+bool fcq_supported(int H, int I, const void* w1, const void* w2);
+cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint8_t* w, int E_loc, bool fc1,
+                       long max_tiles, cudaStream_t st);
+
+// MXFP8 rows (x_q [T, K], x_s [T, K/32]) copied into expert order
+// (x8 [S, K], x8s [S, K/32]); K a multiple of 16, s_vec = 1 when the scale
+// rows may be copied as 32-bit words.
+struct Gather8Params {
+  const uint8_t* x_q;
+  const uint8_t* x_s;
+  const int32_t* permuted_src;
+  const int32_t* meta;
+  int top_k, K, s_vec;
+  long S;
+  uint8_t* x8;
+  uint8_t* x8s;
+};
+cudaError_t launch_gather8(const Gather8Params& p, cudaStream_t st);
 size_t fcd_smem_bytes(int K, bool nvfp4);
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 

@@ -114,6 +114,7 @@ const char* situ_status_string(situ_status s) {
     case SITU_ERR_WORKSPACE_TOO_SMALL: return "SITU_ERR_WORKSPACE_TOO_SMALL";
     case SITU_ERR_CUDA: return "SITU_ERR_CUDA: a CUDA launch or call failed";
     case SITU_ERR_MISALIGNED: return "SITU_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+    case SITU_ERR_DEVICE_TIMEOUT: return "SITU_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait";
   }
   return "unknown situ_status";
 }
@@ -262,6 +263,59 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.y_out = y;
     if ((err = launch_fcd(d, false, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(4);
+  } else if (a->act_dtype == SITU_ACT_MXFP8 && !nv && fcq_supported(a->H, a->I, a->w1, a->w2)) {
+    // w4a8 on the block-scaled tensor cores: MXFP8 rows copied into expert
+    // order, FC1 (+SiTU) writing H1 as MXFP8, FC2 reading it as it stands
+    Gather8Params g8;
+    g8.x_q = (const uint8_t*)a->hidden_states_q;
+    g8.x_s = (const uint8_t*)a->hidden_states_scale;
+    g8.permuted_src = psrc;
+    g8.meta = meta;
+    g8.top_k = a->top_k;
+    g8.K = a->H;
+    g8.s_vec = (reinterpret_cast<uintptr_t>(a->hidden_states_scale) & 3) == 0;
+    g8.S = S;
+    g8.x8 = ws + L.x16;
+    g8.x8s = ws + L.x16s;
+    if ((err = launch_gather8(g8, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(2);
+    FcqParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.offsets = offsets;
+    q.tile_offsets = tile_offsets;
+    q.tile_info = tile_info;
+    q.E_loc = a->num_local_experts;
+    q.I = a->I;
+    q.err = meta + 2;
+    q.ws = a->w1_scale;
+    q.ws_vec = (reinterpret_cast<uintptr_t>(a->w1_scale) & 3) == 0;
+    q.Mtot = 2 * a->I;
+    q.K = a->H;
+    q.n_ntiles = (a->I + 127) / 128;
+    q.xs = g8.x8s;
+    q.xs_stride = a->H / 32;
+    q.beta = a->gemm1_alpha;
+    q.beta_lin = a->gemm1_beta;
+    q.alpha_g = a->g1_alphas;
+    q.alpha_u = a->g1_alphas_up;
+    q.hq = ws + L.h16;
+    q.hs = ws + L.h16s;
+    q.hq_stride = a->I;
+    if ((err = launch_fcq(q, g8.x8, S, a->w1, a->num_local_experts, true, max_tiles, st)) != cudaSuccess)
+      return SITU_ERR_CUDA;
+    mark(3);
+    q.ws = a->w2_scale;
+    q.ws_vec = (reinterpret_cast<uintptr_t>(a->w2_scale) & 3) == 0;
+    q.Mtot = a->H;
+    q.K = a->I;
+    q.n_ntiles = (a->H + 255) / 256;
+    q.xs = q.hs;
+    q.xs_stride = a->I / 32;
+    q.alpha2 = a->g2_alphas;
+    q.y_out = y;
+    if ((err = launch_fcq(q, q.hq, S, a->w2, a->num_local_experts, false, max_tiles, st)) != cudaSuccess)
+      return SITU_ERR_CUDA;
+    mark(4);
   } else {
     // 128-token tiles on tcgen05: f16 rows with one scale per row, FC1 (+SiTU)
     // writing bf16 H1, H1 to f16 rows, FC2
@@ -352,6 +406,26 @@ situ_status situ_moe_forward_profiled(const situ_moe_args* a, void* workspace,
                                       size_t workspace_bytes, void* stream, void* const* events) {
   if (!events) return SITU_ERR_NULL_ARG;
   return forward_impl(a, workspace, workspace_bytes, stream, events);
+}
+
+situ_status situ_moe_device_status(const situ_moe_args* a, const void* workspace, void* stream,
+                                   int32_t* code) {
+  if (code) *code = 0;
+  if (!a || !workspace) return SITU_ERR_NULL_ARG;
+  if (check_routing(a->T, a->top_k, a->num_experts_total, a->num_local_experts, a->local_expert_offset) !=
+          SITU_OK ||
+      a->H <= 0 || a->I <= 0)
+    return SITU_ERR_BAD_SHAPE;
+  if (a->T == 0) return SITU_OK;
+  const Layout L = make_layout(a);
+  int32_t word = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, (const uint8_t*)workspace + L.meta + 2 * sizeof(int32_t), sizeof(word),
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return SITU_ERR_CUDA;
+  if (code) *code = word;
+  return word == 0 ? SITU_OK : SITU_ERR_DEVICE_TIMEOUT;
 }
 
 }  // extern "C"

@@ -50,7 +50,8 @@ typedef enum situ_status {
   SITU_ERR_UNSUPPORTED = 3,        /* unsupported (activation, weight) format pair or limit */
   SITU_ERR_WORKSPACE_TOO_SMALL = 4,
   SITU_ERR_CUDA = 5,               /* a CUDA launch or runtime call failed */
-  SITU_ERR_MISALIGNED = 6          /* a pointer is not 16-byte aligned */
+  SITU_ERR_MISALIGNED = 6,         /* a pointer is not 16-byte aligned */
+  SITU_ERR_DEVICE_TIMEOUT = 7      /* a kernel gave up a bounded wait (see situ_moe_device_status) */
 } situ_status;
 
 typedef enum situ_act_dtype {
@@ -228,8 +229,8 @@ typedef struct situ_moe_args {
 
 /* Workspace bytes situ_moe_forward needs for these shapes (0 on bad args).
  * It grows with T*top_k: permute arrays, the permuted activations
- * [T*top_k, H] bf16, the FC1 output [T*top_k, I] bf16 and the FC2 output
- * [T*top_k, H] bf16. */
+ * [T*top_k, H] (f16 or E4M3 rows plus scales), the FC1 output [T*top_k, I]
+ * and the FC2 output [T*top_k, H] fp32. */
 size_t situ_moe_workspace_size(const situ_moe_args* args);
 
 /* Errors: NULL_ARG (args, required pointers, gemm1_alpha / gemm1_beta --
@@ -252,6 +253,23 @@ situ_status situ_moe_forward(const situ_moe_args* args, void* workspace, size_t 
 #define SITU_PROFILE_EVENTS 6
 situ_status situ_moe_forward_profiled(const situ_moe_args* args, void* workspace,
                                       size_t workspace_bytes, void* stream, void* const* events);
+
+/* ------------------------------------------------------------------------
+ * situ_moe_device_status -- outcome of the device-side waits of the last
+ * situ_moe_forward enqueued on `stream` with this workspace.
+ *
+ * The tensor-core GEMM kernels bound every wait on their asynchronous
+ * copies and MMAs (200 ms); a CTA that runs out records a nonzero code in
+ * a status word inside the workspace and returns, and the kernels after it
+ * stop early, so the CUDA context stays usable.  This call waits for
+ * `stream`, reads the word (4 bytes, device to host) and returns SITU_OK
+ * when it is 0, SITU_ERR_DEVICE_TIMEOUT otherwise; the raw code (which
+ * wait gave up first) goes to *code when `code` is not NULL.  `args` must
+ * be the shapes the workspace was used with.  Synchronous; the pages
+ * define no counterpart.  Errors: NULL_ARG, BAD_SHAPE, CUDA.
+ * --------------------------------------------------------------------- */
+situ_status situ_moe_device_status(const situ_moe_args* args, const void* workspace, void* stream,
+                                   int32_t* code);
 
 #ifdef __cplusplus
 }

@@ -87,6 +87,16 @@ def test_forward_other_errors(lib):
     assert _fwd(lib, _args(T=0)) == 0                # nothing to do, nothing launched
 
 
+def test_device_status_argument_errors(lib):
+    code = ctypes.c_int32(-1)
+    assert lib.situ_moe_device_status(None, ctypes.c_void_p(16), None, ctypes.byref(code)) == 1
+    assert code.value == 0
+    assert lib.situ_moe_device_status(ctypes.byref(_args()), None, None, None) == 1
+    assert lib.situ_moe_device_status(ctypes.byref(_args(top_k=0)), ctypes.c_void_p(16), None, None) == 2
+    # T == 0: nothing ran, nothing to read
+    assert lib.situ_moe_device_status(ctypes.byref(_args(T=0)), ctypes.c_void_p(16), None, None) == 0
+
+
 def test_workspace_size_grows_with_tokens(lib):
     small = lib.situ_moe_workspace_size(ctypes.byref(_args(T=4)))
     big = lib.situ_moe_workspace_size(ctypes.byref(_args(T=400)))

@@ -185,9 +185,26 @@ def test_decode_w4a8():
 
 def test_prefill_w4a8_subset():
     wl = wl_("prefill_w4a8")
-    _, out = run_layer(wl)
+    layer, out = run_layer(wl)
+    assert layer.device_status() == 0
     toks = token_subset(wl.T, 192, seed=1)
     assert_parity(out[toks], oracle_out(wl, toks), "prefill w4a8")
+
+
+@pytest.mark.parametrize("over", [
+    # two ragged 128-token tiles per expert, one N tile in FC1 and FC2
+    dict(T=300, H=256, I=128, E_total=4, E_loc=4, off=0, K=2, act=W.ACT_MXFP8, params="k3_random"),
+    # a filtered shard, two FC1 N tiles, FC2's last N tile half full (640 = 2 x 256 + 128)
+    dict(T=257, H=640, I=256, E_total=6, E_loc=3, off=2, K=3, act=W.ACT_MXFP8, params="k3_random"),
+    # K = 3 stages in both GEMMs, one hot expert
+    dict(T=200, H=384, I=384, E_total=3, E_loc=3, off=0, K=2, act=W.ACT_MXFP8, params="k3_random"),
+])
+def test_w4a8_block_scaled_shapes(over):
+    """w4a8 shapes on the block-scaled tensor-core path (H, I multiples of 128)."""
+    wl = W.make("tiny", device="cuda", **over)
+    layer, out = run_layer(wl)
+    assert layer.device_status() == 0
+    assert_parity(out, oracle_out(wl), str(over))
 
 
 def test_ep_shard_subset_and_filtered_rows():

@@ -188,9 +188,9 @@ def dist_env():
     return ws, rank, local
 
 
-def make_workload(name, device, seed):
+def make_workload(name, device, seed, tokens=None):
     from block_scaled_fp4_permute_gb300 import workloads as W
-    return W.make(name, device=device, seed=seed)
+    return W.make(name, device=device, seed=seed, T=tokens)
 
 
 def run_reference(args):
@@ -202,7 +202,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     dev = "cuda:0" if torch.cuda.is_available() else "cpu"
-    wl = make_workload(args.workload, dev, args.seed)
+    wl = make_workload(args.workload, dev, args.seed, args.tokens)
     host_kw = host_oracle_kwargs(wl)
     per_step = max(0.5, 120.0 / max(1, args.steps + args.warmup))
     _, n, _, threads = oracle_tokens_per_s(wl, per_step, host_kw)
@@ -239,7 +239,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device(f"cuda:{local}")
     build.build()
-    wl = make_workload(args.workload, dev, args.seed + rank)
+    wl = make_workload(args.workload, dev, args.seed + rank, args.tokens)
     layer = binding.Layer(wl)
     R, touched = routing_stats(wl)
     nbytes = algorithmic_bytes(wl, R, touched)
@@ -396,6 +396,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=tuple(WORKLOAD_NAMES), default="decode")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count T (smaller profiling captures); "
+                         "the JSON line's config then carries that T")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

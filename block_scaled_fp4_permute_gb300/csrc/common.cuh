@@ -93,14 +93,33 @@ __device__ __forceinline__ int mxfp8_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
-
 // SiTU: [b*tanh(g/b)*sigmoid(g)] * [bl*tanh(u/bl)], a cap <= 0 meaning the
-// factor's limit (g*sigmoid(g), u).
+// factor's limit (g*sigmoid(g), u).  With E(y) = exp(-y):
+//   sigmoid(g) = 1 / (1 + E(g)),  tanh(y) = (1 - E(2y)) / (1 + E(2y)),
+// so the whole product is one fraction and takes three fast exponentials and
+// one division.  The exponent arguments are clamped to [-25, 25], where
+// tanh is +-1 and sigmoid 0 or 1 to within 1.4e-11 absolute, which keeps
+// the product of the three denominators below 4e32.  The error is a few
+// fp32 ulps of the factors' magnitudes (absolute, not relative, near 0).
+__device__ __forceinline__ float exp_neg_clamped(float y) { return __expf(-fminf(fmaxf(y, -25.f), 25.f)); }
 __device__ __forceinline__ float situ_f(float g, float u, float b, float bl) {
-  float gate = (b > 0.f) ? b * tanhf(g / b) * sigmoid_f(g) : g * sigmoid_f(g);
-  float up = (bl > 0.f) ? bl * tanhf(u / bl) : u;
-  return gate * up;
+  const float e0 = exp_neg_clamped(g);
+  float num = 1.f, den = 1.f + e0;               // sigmoid(g)
+  if (b > 0.f) {
+    const float e1 = exp_neg_clamped((2.f / b) * g);
+    num = b * (1.f - e1);
+    den *= 1.f + e1;
+  } else {
+    num = g;
+  }
+  if (bl > 0.f) {
+    const float e2 = exp_neg_clamped((2.f / bl) * u);
+    num *= bl * (1.f - e2);
+    den *= 1.f + e2;
+  } else {
+    num *= u;
+  }
+  return __fdividef(num, den);
 }
 
 }  // namespace situ

@@ -3,33 +3,37 @@
 // tcgen05.mma.kind::mxf8f6f4.block_scale, E4M3 x E2M1 with one UE8M0 scale
 // per 32 elements of K on both operands, fp32 accumulation in TMEM.
 //
-// One CTA computes a [128 tokens x 256 weight rows] tile of one local
-// expert, K in stages of 128:
-//   * warp 0 (one lane) is the TMA producer: per stage the token tile's
-//     E4M3 rows (128 x 128 B, 128-byte swizzle) and the weight rows' E2M1
-//     codes (256 x 128 elements).  The weights are read with the tensor-map
-//     type that expands each 8-byte group of 16 packed codes into a 16-byte
-//     slot in shared memory, the operand layout the MMA takes for 4-bit
-//     types next to 8-bit ones, so the packed weights go from HBM to the
-//     tensor core untouched;
-//   * warps 4..7 stage the block scales: per stage each row's four UE8M0
-//     bytes (the four 32-element blocks of the stage) as one 32-bit word,
-//     written to shared memory as 32 x 16-byte rows in which row i holds the
+// A persistent kernel: one CTA per SM walks the work items (a 128-token
+// tile of one local expert x an N tile of weight rows; FC1 N = 96 gate rows
+// + the 96 matching up rows, FC2 N = 224 rows of H), K in stages of 128.
+// Warp roles:
+//   * warp 0 (one lane), TMA producer: per stage the token tile's E4M3 rows
+//     (128 x 128 B, 128-byte swizzle) and the weight rows' E2M1 codes.  The
+//     weights are read with the tensor-map type that expands each 8-byte
+//     group of 16 packed codes into a 16-byte slot in shared memory, the
+//     operand layout the MMA takes for 4-bit types next to 8-bit ones, so the
+//     packed weights go from HBM to the tensor core untouched;
+//   * warps 2..3, scale stream: per stage each row's four UE8M0 bytes (the
+//     four 32-element blocks of the stage) as one 32-bit cp.async, placed so
+//     that each 512-byte block is 32 x 16-byte rows with row i holding the
 //     words of tile rows i, i+32, i+64, i+96 -- the source layout of
 //     tcgen05.cp.32x128b.warpx4, which copies it into four TMEM columns of
-//     every 32-lane quarter;
-//   * warp 1 allocates 512 TMEM columns (256 for the accumulator, 12 per
-//     stage for scales); one lane copies each stage's scales into TMEM and
-//     issues four MMAs (M = 128, N = 256, K = 32), the k-th taking byte k of
-//     the scale words, then commits the stage back to the producer;
-//   * warps 4..7 then read the accumulator (each thread one token row):
-//     FC1 applies the per-expert alphas and SiTU to each gate/up column pair
-//     (the tile's columns are 128 gate rows then the 128 matching up rows)
-//     and writes H1 as MXFP8 (E4M3 + one UE8M0 per 32 along I), which is
-//     FC2's A operand as it stands; FC2 writes alpha2 * acc as fp32.
+//     every 32-lane quarter.  The scales run several stages ahead of the
+//     MMAs through their own 12-slot ring;
+//   * warp 1 allocates all 512 TMEM columns (two accumulators plus 12
+//     scale columns per stage); one lane copies each stage's scales into
+//     TMEM and issues four MMAs (M = 128, K = 32), the k-th taking byte k of
+//     the scale words, committing the stage back to the producer and the
+//     scale stream, and each finished accumulator to the epilogue;
+//   * warps 4..7 and 8..11, epilogue (each thread one token row), one
+//     warpgroup per accumulator, so that two items drain while the MMAs run
+//     on: FC1 applies the per-expert alphas and SiTU to each gate/up column
+//     pair and writes H1 as MXFP8 (E4M3 + one UE8M0 per 32 along I), FC2's
+//     A operand as it stands; FC2 writes alpha2 * acc as fp32.
 // K (H for FC1, I for FC2) must be a multiple of 128.  Every mbarrier wait
 // is bounded; on expiry the CTA records an error code in the device status
-// word and unwinds, and TMEM is always released.
+// word, waits (bounded) for its copies and MMAs in flight, releases TMEM
+// and returns.
 #include "situ_internal.h"
 #include "tc_common.cuh"
 
@@ -40,36 +44,45 @@ using namespace tc;
 namespace {
 
 constexpr int kBM = 128;         // tokens per tile (MMA M, TMEM lanes)
-constexpr int kBN = 256;         // weight rows per tile (MMA N)
 constexpr int kBK = 128;         // K elements per stage
-constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr int kABytes = kBM * kBK;           // 16 KB of E4M3
-constexpr int kBBytes = kBN * kBK;           // 32 KB: E2M1 in 16-byte slots of 16 codes
-constexpr int kBTxBytes = kBN * kBK / 2;     // what the loads transfer: the packed 16 KB
-constexpr int kSfaBytes = kBM * 4;           // four UE8M0 bytes per row
-constexpr int kSfbBytes = kBN * 4;
-constexpr int kSfStage = kSfaBytes + kSfbBytes;
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffSF = kOffB + kStages * kBBytes;
-constexpr int kOffBar = kOffSF + kStages * kSfStage;
-constexpr int kNumBars = 3 * kStages + 1;    // full, sf_full, empty per stage; acc_full
-constexpr int kOffTm = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffTm + 16 + 1024;   // + alignment slack
-// TMEM columns: accumulator [0, 256); stage s's A scales at 256 + 12 s
-// (4 columns), its B scales at 256 + 12 s + 4 (4 columns per 128 rows)
-constexpr int kSfCol0 = 256;
+constexpr int kSfRing = 12;      // scale slots in shared memory
+constexpr int kSfAhead = 8;      // stages the scale copies run ahead of their MMAs
+constexpr int kSfStage = 3 * 512;   // A block, B rows 0..127, B rows 128..255
 constexpr int kSfColsPerStage = 12;
-static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
-// Instruction descriptor, block-scaled kinds: A = E4M3 (0), B = E2M1 (5),
-// both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24;
-// the B and A scale byte selectors sit at bits 4..5 and 29..30.
-constexpr uint32_t kIdesc = (0u << 7) | (5u << 10) | ((uint32_t)(kBN >> 3) << 17) | (1u << 23) |
-                            ((uint32_t)(kBM >> 4) << 24);
-__device__ __forceinline__ uint32_t idesc_sf(uint32_t k) { return kIdesc | (k << 4) | (k << 29); }
+template <bool FC1>
+struct Cfg {
+  static constexpr int BN = FC1 ? 192 : 224;        // MMA N
+  static constexpr int NH = FC1 ? BN / 2 : BN;      // rows per weight box
+  static constexpr int kStages = FC1 ? 5 : 3;
+  static constexpr int kABytes = kBM * kBK;         // 16 KB of E4M3
+  static constexpr int kBBytes = BN * kBK;          // E2M1 in 16-byte slots of 16 codes
+  static constexpr int kBTx = BN * kBK / 2;         // bytes the weight loads transfer (packed)
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSF = kOffB + kStages * kBBytes;
+  // FC2: per epilogue warp a 32 x 32 fp32 staging block (rows padded to
+  // 144 bytes), so that Y leaves in whole 128-byte row segments
+  static constexpr int kYRow = 144;
+  static constexpr int kOffY = kOffSF + kSfRing * kSfStage;
+  static constexpr int kYBytes = FC1 ? 0 : 8 * 32 * kYRow;
+  static constexpr int kOffBar = kOffY + kYBytes;
+  // full, empty per stage; sf_full, sf_empty per scale slot; acc_full[2],
+  // acc_empty[2]; drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kSfRing + 5;
+  static constexpr int kOffTm = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffTm + 16 + 1024;  // + alignment slack
+  static constexpr int kSfCol0 = 2 * BN;            // TMEM: accumulators [0, 2 BN), then scales
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  // Instruction descriptor, block-scaled kinds: A = E4M3 (0), B = E2M1 (5),
+  // both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit
+  // 24; the B and A scale byte selectors sit at bits 4..5 and 29..30.
+  static constexpr uint32_t kIdesc = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                                     ((uint32_t)(kBM >> 4) << 24);
+};
 
 __device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t accumulate) {
@@ -93,12 +106,18 @@ __device__ __forceinline__ uint64_t sf_desc(uint32_t a) {
 __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t desc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
+// 4-byte asynchronous copy, zero-filled when !ok (src is then not read)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0) : "memory");
+}
+// the word of row 32 j + i of a 128-row block goes to byte 16 i + 4 j
+__device__ __forceinline__ uint32_t sf_pos(int r) { return (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4); }
 
-// one 32-bit word of four scale bytes; 4-byte aligned when vec
-__device__ __forceinline__ uint32_t ld_sf4(const uint8_t* p, bool vec) {
-  if (vec) return __ldg(reinterpret_cast<const uint32_t*>(p));
-  return (uint32_t)__ldg(p) | ((uint32_t)__ldg(p + 1) << 8) | ((uint32_t)__ldg(p + 2) << 16) |
-         ((uint32_t)__ldg(p + 3) << 24);
+// Short bounded wait used only while unwinding (no error code recorded).
+__device__ __forceinline__ void drain_wait(uint32_t a, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try(a, parity))
+    if (globaltimer() - t0 > kWaitNs) return;
 }
 
 }  // namespace
@@ -106,36 +125,43 @@ __device__ __forceinline__ uint32_t ld_sf4(const uint8_t* p, bool vec) {
 template <bool FC1>
 __global__ void __launch_bounds__(kThreads, 1)
 fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const FcqParams p) {
+  using C = Cfg<FC1>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int ntile = blockIdx.x % p.n_ntiles;
-  const int tile = blockIdx.x / p.n_ntiles;
-  if (tile >= __ldg(p.tile_offsets + p.E_loc)) return;
+  const long total = (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
+  if ((long)blockIdx.x >= total) return;
   if (*reinterpret_cast<volatile int*>(p.err) != 0) return;   // an earlier CTA timed out
-  const int2 ti = __ldg(p.tile_info + tile);
-  const int e = ti.x, row0 = ti.y;
-  const int nrows = min(kBM, __ldg(p.offsets + e + 1) - row0);
   const int nk = p.K / kBK;
-  const int nsb = p.K / 32;                       // block scales per row
-  const int nbase = FC1 ? ntile * (kBN / 2) : ntile * kBN;
+  const int nsb = p.K / 32;                                    // block scales per row
 
   const uint32_t sbase = saddr(smem);
-  const uint32_t bar0 = sbase + kOffBar;
+  const uint32_t bar0 = sbase + C::kOffBar;
   auto full = [&](int s) { return bar0 + 8 * s; };
-  auto sf_full = [&](int s) { return bar0 + 8 * (kStages + s); };
-  auto empty = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
-  const uint32_t acc_full = bar0 + 8 * (3 * kStages);
-  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + kOffTm);
+  auto empty = [&](int s) { return bar0 + 8 * (kStages + s); };
+  auto sf_full = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
+  auto sf_empty = [&](int s) { return bar0 + 8 * (2 * kStages + kSfRing + s); };
+  auto acc_full = [&](int b) { return bar0 + 8 * (2 * kStages + 2 * kSfRing + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8 * (2 * kStages + 2 * kSfRing + 2 + b); };
+  const uint32_t drain = bar0 + 8 * (2 * kStages + 2 * kSfRing + 4);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::kOffTm);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(sf_full(s), 128);
       mbar_init(empty(s), 1);
     }
-    mbar_init(acc_full, 1);
+    for (int s = 0; s < kSfRing; ++s) {
+      mbar_init(sf_full(s), 64);
+      mbar_init(sf_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);
+    }
+    mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -149,110 +175,174 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tm_holder;
 
+  // item -> (expert, first row, rows, first weight row of the N tile)
+  auto item_info = [&](long item, int& e, int& row0, int& nrows, int& nbase) {
+    const int tile = (int)(item / p.n_ntiles);
+    const int ntile = (int)(item % p.n_ntiles);
+    const int2 ti = __ldg(p.tile_info + tile);
+    e = ti.x;
+    row0 = ti.y;
+    nrows = min(kBM, __ldg(p.offsets + e + 1) - row0);
+    nbase = ntile * C::NH;
+  };
+
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const int wrow = e * p.Mtot + nbase;
-      const int wrow2 = FC1 ? wrow + p.I : wrow + kBN / 2;   // second 128 rows: up rows / next rows
-      for (int kk = 0; kk < nk; ++kk) {
-        const int s = kk % kStages, r = kk / kStages;
-        if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1, p.err, 21)) break;
-        mbar_expect_tx(full(s), kABytes + kBTxBytes);
-        tma_load_2d(sbase + kOffA + s * kABytes, &tmA, kk * kBK, row0, full(s));
-        tma_load_2d(sbase + kOffB + s * kBBytes, &tmB, kk * kBK, wrow, full(s));
-        tma_load_2d(sbase + kOffB + s * kBBytes + kBBytes / 2, &tmB, kk * kBK, wrow2, full(s));
+      long it = 0;
+      bool ok = true;
+      for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        int e, row0, nrows, nbase;
+        item_info(item, e, row0, nrows, nbase);
+        const int wrow = e * p.Mtot + nbase;
+        for (int kk = 0; kk < nk; ++kk, ++it) {
+          const int s = (int)(it % kStages);
+          const long r = it / kStages;
+          if (r > 0 && !mbar_wait(empty(s), (uint32_t)((r - 1) & 1), p.err, 21)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full(s), C::kABytes + C::kBTx);
+          const uint32_t b_smem = sbase + C::kOffB + s * C::kBBytes;
+          tma_load_2d(sbase + C::kOffA + s * C::kABytes, &tmA, kk * kBK, row0, full(s));
+          tma_load_2d(b_smem, &tmB, kk * kBK, wrow, full(s));
+          if (FC1) tma_load_2d(b_smem + C::NH * kBK, &tmB, kk * kBK, wrow + p.I, full(s));
+        }
       }
+      // unwind: the loads of the last stages may still be landing
+      for (long j = it - 1; j >= 0 && j >= it - kStages; --j)
+        drain_wait(full((int)(j % kStages)), (uint32_t)((j / kStages) & 1));
     }
   } else if (warp == 1) {
     // ---------------- scale copies + MMA issuer ----------------
     if (lane == 0) {
+      long it = 0;
+      int li = 0;
       bool ok = true;
-      for (int kk = 0; kk < nk && ok; ++kk) {
-        const int s = kk % kStages, par = (kk / kStages) & 1;
-        ok = mbar_wait(full(s), par, p.err, 22) && mbar_wait(sf_full(s), par, p.err, 23);
-        if (!ok) break;
+      for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+        const int buf = li & 1, use = li >> 1;
+        if (use > 0 && !mbar_wait(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 22)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t sf_smem = sbase + kOffSF + s * kSfStage;
-        const uint32_t sfa = tmem + kSfCol0 + s * kSfColsPerStage;
-        const uint32_t sfb = sfa + 4;
-        tmem_cp_sf(sfa, sf_desc(sf_smem));
-        tmem_cp_sf(sfb, sf_desc(sf_smem + kSfaBytes));
-        tmem_cp_sf(sfb + 4, sf_desc(sf_smem + kSfaBytes + 512));
-        const uint64_t ad = sdesc(sbase + kOffA + s * kABytes);
-        const uint64_t bd = sdesc(sbase + kOffB + s * kBBytes);
+        const uint32_t d = tmem + (uint32_t)(buf * C::BN);
+        for (int kk = 0; kk < nk; ++kk, ++it) {
+          const int s = (int)(it % kStages);
+          const int q = (int)(it % kSfRing);
+          if (!mbar_wait(full(s), (uint32_t)((it / kStages) & 1), p.err, 23) ||
+              !mbar_wait(sf_full(q), (uint32_t)((it / kSfRing) & 1), p.err, 24)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t sf_smem = sbase + C::kOffSF + q * kSfStage;
+          const uint32_t sfa = tmem + (uint32_t)(C::kSfCol0 + s * kSfColsPerStage);
+          const uint32_t sfb = sfa + 4;
+          tmem_cp_sf(sfa, sf_desc(sf_smem));
+          tmem_cp_sf(sfb, sf_desc(sf_smem + 512));
+          tmem_cp_sf(sfb + 4, sf_desc(sf_smem + 1024));
+          const uint64_t ad = sdesc(sbase + C::kOffA + s * C::kABytes);
+          const uint64_t bd = sdesc(sbase + C::kOffB + s * C::kBBytes);
 #pragma unroll
-        for (int k4 = 0; k4 < kBK / 32; ++k4)   // +32 bytes along K per instruction
-          mma_bs(tmem, ad + 2 * k4, bd + 2 * k4, idesc_sf((uint32_t)k4), sfa, sfb, (kk | k4) != 0);
-        mma_commit(empty(s));
+          for (uint32_t k4 = 0; k4 < kBK / 32; ++k4)   // +32 bytes along K per instruction
+            mma_bs(d, ad + 2 * k4, bd + 2 * k4, C::kIdesc | (k4 << 4) | (k4 << 29), sfa, sfb,
+                   (kk | (int)k4) != 0);
+          mma_commit(empty(s));
+          mma_commit(sf_empty(q));
+        }
+        if (!ok) break;
+        mma_commit(acc_full(buf));
       }
-      mma_commit(acc_full);
+      // unwind: every MMA and scale copy issued so far has completed
+      mma_commit(drain);
+      drain_wait(drain, 0);
     }
-  } else if (warp >= 4) {
-    // ---------------- scale staging, then epilogue ----------------
-    const int t = tid - 128;
-    const bool a_ok = t < nrows;
-    const uint8_t* a_src = p.xs + (size_t)(row0 + (a_ok ? t : 0)) * p.xs_stride;
-    const uint8_t* b_src[2];
-    bool b_ok[2];
-    for (int h = 0; h < 2; ++h) {
-      int brow;
-      if (FC1) {
-        b_ok[h] = nbase + t < p.I;
-        brow = (h ? p.I : 0) + nbase + t;
-      } else {
-        brow = nbase + t + 128 * h;
-        b_ok[h] = brow < p.Mtot;
-      }
-      b_src[h] = p.ws + ((size_t)e * p.Mtot + (b_ok[h] ? brow : 0)) * (size_t)nsb;
-    }
-    const bool vec = p.ws_vec != 0;
-    auto load = [&](int kk, uint32_t* w) {
-      const bool in = kk < nk;
-      w[0] = (a_ok && in) ? __ldg(reinterpret_cast<const uint32_t*>(a_src + 4 * kk)) : 0u;
-      w[1] = (b_ok[0] && in) ? ld_sf4(b_src[0] + 4 * kk, vec) : 0u;
-      w[2] = (b_ok[1] && in) ? ld_sf4(b_src[1] + 4 * kk, vec) : 0u;
-    };
-    // the word of tile row 32 j + i goes to byte (16 i + 4 j) of its 512-byte block
-    const int so = (t & 31) * 16 + (t >> 5) * 4;
-    uint32_t w0[3], w1[3], w2[3];
-    load(0, w0);
-    load(1, w1);
-    for (int kk = 0; kk < nk; ++kk) {
-      load(kk + 2, w2);
-      const int s = kk % kStages, r = kk / kStages;
-      // the stage's scale block is free once the MMAs of its previous round are done
-      if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1, p.err, 24)) break;
-      uint8_t* sf = smem + kOffSF + s * kSfStage;
-      *reinterpret_cast<uint32_t*>(sf + so) = w0[0];
-      *reinterpret_cast<uint32_t*>(sf + kSfaBytes + so) = w0[1];
-      *reinterpret_cast<uint32_t*>(sf + kSfaBytes + 512 + so) = w0[2];
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(sf_full(s));
+  } else if (warp < 4) {
+    // ---------------- scale stream (64 threads) ----------------
+    const int t = tid - 64;
+    long it = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      int e, row0, nrows, nbase;
+      item_info(item, e, row0, nrows, nbase);
+      // this thread's rows: A rows t, t + 64; B rows t, t + 64, t + 128, t + 192
+      const uint8_t* src[6];
+      bool val[6];
+      uint32_t pos[6];
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        w0[i] = w1[i];
-        w1[i] = w2[i];
+      for (int h = 0; h < 2; ++h) {
+        const int m = t + 64 * h;
+        val[h] = m < nrows;
+        src[h] = p.xs + (size_t)(row0 + (val[h] ? m : 0)) * p.xs_stride;
+        pos[h] = sf_pos(m);
+      }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int n = t + 64 * h;
+        int wr;
+        bool v;
+        if (FC1) {
+          const int i = nbase + (n < C::NH ? n : n - C::NH);
+          v = n < C::BN && i < p.I;
+          wr = (n < C::NH ? 0 : p.I) + i;
+        } else {
+          wr = nbase + n;
+          v = n < C::BN && wr < p.Mtot;
+        }
+        val[2 + h] = v;
+        src[2 + h] = p.ws + ((size_t)e * p.Mtot + (v ? wr : 0)) * (size_t)nsb;
+        pos[2 + h] = 512u + (uint32_t)((n >> 7) & 1) * 512u + sf_pos(n);
+      }
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int q = (int)(it % kSfRing);
+        const long r = it / kSfRing;
+        if (r > 0 && !mbar_wait(sf_empty(q), (uint32_t)((r - 1) & 1), p.err, 25)) {
+          ok = false;
+          break;
+        }
+        const uint32_t slot = sbase + C::kOffSF + q * kSfStage;
+#pragma unroll
+        for (int h = 0; h < 6; ++h)
+          if (h < 2 || t + 64 * (h - 2) < C::BN) cp_async4(slot + pos[h], src[h] + 4 * kk, val[h]);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (it >= kSfAhead) {
+          // the copies of stage it - kSfAhead have landed: hand them to the MMA
+          asm volatile("cp.async.wait_group %0;" ::"n"(kSfAhead) : "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(sf_full((int)((it - kSfAhead) % kSfRing)));
+        }
       }
     }
-    // ---- epilogue: thread = token row (TMEM lane) ----
-    const int m = (warp - 4) * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-    // warp-uniform outcome: the tcgen05.ld below are .sync.aligned
-    const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.err, 25));
-    if (acc_ok) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (ok)
+      for (long j = (it > kSfAhead ? it - kSfAhead : 0); j < it; ++j) mbar_arrive(sf_full((int)(j % kSfRing)));
+  } else {
+    // ---------------- epilogue: thread = token row (TMEM lane) ----------------
+    // warpgroup buf drains accumulator buf, i.e. this CTA's items buf, buf + 2, ...
+    const int buf = (warp - 4) >> 2;
+    const int quarter = warp & 3;        // the TMEM lanes a warp may read: 32 * (warp % 4) ..
+    const int m = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    for (int li = buf;; li += 2) {
+      const long item = blockIdx.x + (long)li * gridDim.x;
+      if (item >= total) break;
+      int e, row0, nrows, nbase;
+      item_info(item, e, row0, nrows, nbase);
+      // warp-uniform outcome: the tcgen05.ld below are .sync.aligned
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 26))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t trow = tmem + lane_off + (uint32_t)(buf * C::BN);
       const bool vrow = m < nrows;
       const size_t row = (size_t)(row0 + (vrow ? m : 0));
       if (FC1) {
         const float ag = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
         const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
         const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
-        for (int c0 = 0; c0 < kBN / 2; c0 += 32) {
+        for (int c0 = 0; c0 < C::NH; c0 += 32) {
           float gt[32], up[32];
           tmem_ld16(trow + c0, gt);
           tmem_ld16(trow + c0 + 16, gt + 16);
-          tmem_ld16(trow + 128 + c0, up);
-          tmem_ld16(trow + 128 + c0 + 16, up + 16);
+          tmem_ld16(trow + C::NH + c0, up);
+          tmem_ld16(trow + C::NH + c0 + 16, up + 16);
           const int i0 = nbase + c0;
           if (!vrow || i0 >= p.I) continue;
           float v[32];
@@ -265,29 +355,46 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           // MXFP8 of the 32-element block: the smallest e with amax * 2^-e <= 448
           const int ex = mxfp8_exponent(amax);
           const float sc = exp2i(-ex);
-          uint32_t q[8];
+          uint32_t qv[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            q[j] = f32x2_to_e4m3x2(v[4 * j] * sc, v[4 * j + 1] * sc) |
-                   (f32x2_to_e4m3x2(v[4 * j + 2] * sc, v[4 * j + 3] * sc) << 16);
+            qv[j] = f32x2_to_e4m3x2(v[4 * j] * sc, v[4 * j + 1] * sc) |
+                    (f32x2_to_e4m3x2(v[4 * j + 2] * sc, v[4 * j + 3] * sc) << 16);
           uint4* dst = reinterpret_cast<uint4*>(p.hq + row * p.hq_stride + i0);
-          dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-          dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+          dst[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+          dst[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
           p.hs[row * (p.hq_stride / 32) + i0 / 32] = (uint8_t)(ex + 127);
         }
       } else {
         const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
-        for (int c0 = 0; c0 < kBN; c0 += 16) {
-          float acc[16];
+        // this warp's staging block; the warp owns tile rows 32 quarter .. + 31
+        uint8_t* yst = smem + C::kOffY + (warp - 4) * 32 * C::kYRow;
+        const int wrow0 = quarter * 32;
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          float acc[32];
           tmem_ld16(trow + c0, acc);
-          const int n0 = nbase + c0;
-          if (!vrow || n0 >= p.Mtot) continue;
-          float4* dst = reinterpret_cast<float4*>(p.y_out + row * p.Mtot + n0);
+          tmem_ld16(trow + c0 + 16, acc + 16);
+          // own row into the staging block ...
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_float4(acc[4 * q] * a2, acc[4 * q + 1] * a2, acc[4 * q + 2] * a2, acc[4 * q + 3] * a2);
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(yst + lane * C::kYRow + 16 * q) =
+                make_float4(acc[4 * q] * a2, acc[4 * q + 1] * a2, acc[4 * q + 2] * a2, acc[4 * q + 3] * a2);
+          __syncwarp();
+          // ... and out as 4 rows x 128 bytes per instruction
+          const int n = nbase + c0 + 4 * (lane & 7);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + (lane >> 3);
+            const float4 v = *reinterpret_cast<const float4*>(yst + r * C::kYRow + 16 * (lane & 7));
+            if (wrow0 + r < nrows && n < p.Mtot)
+              *reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + wrow0 + r) * p.Mtot + n) = v;
+          }
+          __syncwarp();
         }
       }
+      // this accumulator may be overwritten by the item after next
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(acc_empty(buf));
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -330,31 +437,46 @@ __global__ void __launch_bounds__(256) gather8_kernel(const Gather8Params p) {
 
 namespace {
 
+int sm_count() {
+  static int n[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && n[dev] > 0) return n[dev];
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+  if (dev < 64) n[dev] = v;
+  return v;
+}
+
 template <bool FC1>
 cudaError_t launch_fcq_t(const FcqParams& p, const CUtensorMap& a, const CUtensorMap& b, long max_tiles,
                          cudaStream_t st) {
+  using C = Cfg<FC1>;
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || set_for[dev] == 0) {
     cudaError_t err =
-        cudaFuncSetAttribute(fcq_kernel<FC1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(fcq_kernel<FC1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (err != cudaSuccess) return err;
     if (dev < 64) set_for[dev] = 1;
   }
-  const long grid = max_tiles * p.n_ntiles;
+  const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
+  const long grid = items < sm_count() ? items : sm_count();
   if (grid <= 0) return cudaSuccess;
-  fcq_kernel<FC1><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(a, b, p);
+  fcq_kernel<FC1><<<(unsigned)grid, kThreads, C::kSmem, st>>>(a, b, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-bool fcq_supported(int H, int I, const void* w1, const void* w2) {
+int fcq_n_rows(bool fc1) { return fc1 ? Cfg<true>::NH : Cfg<false>::NH; }
+
+bool fcq_supported(int H, int I, const void* w1, const void* w2, const void* w1s, const void* w2s) {
   // the 4-bit tensor-map type wants rows of a multiple of 128 codes and a
-  // 32-byte aligned base
-  return H % kBK == 0 && I % kBK == 0 && (reinterpret_cast<uintptr_t>(w1) & 31) == 0 &&
-         (reinterpret_cast<uintptr_t>(w2) & 31) == 0;
+  // 32-byte aligned base; the scale stream copies 4-byte words
+  auto al = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
+  return H % kBK == 0 && I % kBK == 0 && al(w1, 32) && al(w2, 32) && al(w1s, 4) && al(w2s, 4);
 }
 
 cudaError_t launch_gather8(const Gather8Params& p, cudaStream_t st) {
@@ -371,9 +493,10 @@ cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // weights: E2M1 [E_loc * Mtot, K] (K/2 bytes per row), boxes of 128 codes x
-  // 128 rows, each 16 codes landing in a 16-byte slot, 128-byte swizzle
+  // NH rows, each 16 codes landing in a 16-byte slot, 128-byte swizzle
+  const uint32_t nh = (uint32_t)fcq_n_rows(fc1);
   if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, (uint64_t)p.K, (uint64_t)E_loc * p.Mtot,
-                (uint64_t)(p.K / 2), kBK, kBN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+                (uint64_t)(p.K / 2), kBK, nh, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   return fc1 ? launch_fcq_t<true>(p, ma, mb, max_tiles, st) : launch_fcq_t<false>(p, ma, mb, max_tiles, st);
 }

@@ -124,7 +124,10 @@ struct FcqParams {
   float* y_out;
   int* err;                      // device status word
 };
-bool fcq_supported(int H, int I, const void* w1, const void* w2);
+bool fcq_supported(int H, int I, const void* w1, const void* w2, const void* w1_scale, const void* w2_scale);
+// weight rows per N tile: FC1 gate rows (the tile also holds the matching
+// up rows), FC2 rows of H
+int fcq_n_rows(bool fc1);
 cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint8_t* w, int E_loc, bool fc1,
                        long max_tiles, cudaStream_t st);
 

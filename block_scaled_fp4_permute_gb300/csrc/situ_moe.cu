@@ -263,7 +263,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.y_out = y;
     if ((err = launch_fcd(d, false, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(4);
-  } else if (a->act_dtype == SITU_ACT_MXFP8 && !nv && fcq_supported(a->H, a->I, a->w1, a->w2)) {
+  } else if (a->act_dtype == SITU_ACT_MXFP8 && !nv &&
+             fcq_supported(a->H, a->I, a->w1, a->w2, a->w1_scale, a->w2_scale)) {
     // w4a8 on the block-scaled tensor cores: MXFP8 rows copied into expert
     // order, FC1 (+SiTU) writing H1 as MXFP8, FC2 reading it as it stands
     Gather8Params g8;
@@ -291,7 +292,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.ws_vec = (reinterpret_cast<uintptr_t>(a->w1_scale) & 3) == 0;
     q.Mtot = 2 * a->I;
     q.K = a->H;
-    q.n_ntiles = (a->I + 127) / 128;
+    q.n_ntiles = (a->I + fcq_n_rows(true) - 1) / fcq_n_rows(true);
     q.xs = g8.x8s;
     q.xs_stride = a->H / 32;
     q.beta = a->gemm1_alpha;
@@ -308,7 +309,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.ws_vec = (reinterpret_cast<uintptr_t>(a->w2_scale) & 3) == 0;
     q.Mtot = a->H;
     q.K = a->I;
-    q.n_ntiles = (a->H + 255) / 256;
+    q.n_ntiles = (a->H + fcq_n_rows(false) - 1) / fcq_n_rows(false);
     q.xs = q.hs;
     q.xs_stride = a->I / 32;
     q.alpha2 = a->g2_alphas;

@@ -39,7 +39,7 @@ class SituMoeArgs(ctypes.Structure):
             "hidden_states", "hidden_states_q", "hidden_states_scale", "hidden_states_gscale",
             "topk_ids", "topk_weights", "w1", "w1_scale", "w1_gscale", "w2", "w2_scale",
             "w2_gscale", "gemm1_alpha", "gemm1_beta", "g1_alphas", "g1_alphas_up", "g2_alphas",
-            "out")]
+            "out", "scales_packed")]
 
 
 def library_path() -> str:
@@ -75,6 +75,10 @@ def lib() -> ctypes.CDLL:
             l.situ_moe_forward_profiled.restype = ctypes.c_int
             l.situ_moe_forward_profiled.argtypes = [ctypes.POINTER(SituMoeArgs), vp, sz, vp,
                                                     ctypes.POINTER(ctypes.c_void_p)]
+            l.situ_moe_packed_scales_size.restype = sz
+            l.situ_moe_packed_scales_size.argtypes = [ctypes.POINTER(SituMoeArgs)]
+            l.situ_moe_pack_scales.restype = ctypes.c_int
+            l.situ_moe_pack_scales.argtypes = [ctypes.POINTER(SituMoeArgs), vp, sz, vp]
             l.situ_moe_device_status.restype = ctypes.c_int
             l.situ_moe_device_status.argtypes = [ctypes.POINTER(SituMoeArgs), vp, vp,
                                                  ctypes.POINTER(ctypes.c_int32)]
@@ -183,6 +187,17 @@ def situ_moe_workspace_size(args: SituMoeArgs) -> int:
     return lib().situ_moe_workspace_size(ctypes.byref(args))
 
 
+def situ_moe_packed_scales_size(args: SituMoeArgs) -> int:
+    return lib().situ_moe_packed_scales_size(ctypes.byref(args))
+
+
+def situ_moe_pack_scales(args: SituMoeArgs, packed: torch.Tensor, stream=None) -> None:
+    """Packs the weight scales of ``args`` into ``packed`` (uint8 device
+    tensor of at least situ_moe_packed_scales_size bytes)."""
+    _check("situ_moe_pack_scales", lib().situ_moe_pack_scales(
+        ctypes.byref(args), _p(packed), packed.numel() * packed.element_size(), _stream(stream)))
+
+
 def situ_moe_forward(args: SituMoeArgs, workspace: torch.Tensor, stream=None) -> None:
     _check("situ_moe_forward", lib().situ_moe_forward(
         ctypes.byref(args), _p(workspace), workspace.numel() * workspace.element_size(),
@@ -219,7 +234,8 @@ class Layer:
     """Keeps the argument struct and a workspace for one workload, so that a
     forward call is a single C-ABI call (the bench times exactly this)."""
 
-    def __init__(self, wl, out: Optional[torch.Tensor] = None, x_q=None, x_scale=None):
+    def __init__(self, wl, out: Optional[torch.Tensor] = None, x_q=None, x_scale=None,
+                 pack_scales: bool = True):
         self.wl = wl
         dev = wl.x_bf16.device
         self.out = out if out is not None else torch.empty((wl.T, wl.H), dtype=torch.bfloat16,
@@ -244,6 +260,14 @@ class Layer:
             kw["hidden_states_gscale"] = wl.x_gscale
         self._keep = kw
         self.args = make_args(**kw)
+        # weight scales in the block-scaled GEMMs' layout, packed once per
+        # weight set (as at weight-load time) when the shapes use it
+        self.scales_packed = None
+        np_ = situ_moe_packed_scales_size(self.args) if pack_scales else 0
+        if np_ > 0:
+            self.scales_packed = torch.empty(np_, dtype=torch.uint8, device=dev)
+            situ_moe_pack_scales(self.args, self.scales_packed)
+            self.args.scales_packed = self.scales_packed.data_ptr()
         n = situ_moe_workspace_size(self.args)
         self.workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
 

@@ -6,30 +6,36 @@
 // A persistent kernel: one CTA per SM walks the work items (a 128-token
 // tile of one local expert x an N tile of weight rows; FC1 N = 96 gate rows
 // + the 96 matching up rows, FC2 N = 224 rows of H), K in stages of 128.
+//
+// Block scales travel in "scale blocks": 512 bytes holding the four UE8M0
+// bytes (the four 32-element K blocks of one stage) of 128 rows, as 32
+// 16-byte rows in which row i holds the words of rows i, i+32, i+64, i+96 --
+// the source layout of tcgen05.cp.32x128b.warpx4, which copies a block
+// into four TMEM columns of every 32-lane quarter, where the MMA reads it.
+// The activation scales are written in that layout per token tile by the
+// gather (FC1) and by FC1's epilogue (FC2); the weight scales are packed
+// into it once per weight set (pack_scales), so every stage's scales are two
+// contiguous bulk copies.
+//
 // Warp roles:
 //   * warp 0 (one lane), TMA producer: per stage the token tile's E4M3 rows
-//     (128 x 128 B, 128-byte swizzle) and the weight rows' E2M1 codes.  The
-//     weights are read with the tensor-map type that expands each 8-byte
-//     group of 16 packed codes into a 16-byte slot in shared memory, the
-//     operand layout the MMA takes for 4-bit types next to 8-bit ones, so the
-//     packed weights go from HBM to the tensor core untouched;
-//   * warps 2..3, scale stream: per stage each row's four UE8M0 bytes (the
-//     four 32-element blocks of the stage) as one 32-bit cp.async, placed so
-//     that each 512-byte block is 32 x 16-byte rows with row i holding the
-//     words of tile rows i, i+32, i+64, i+96 -- the source layout of
-//     tcgen05.cp.32x128b.warpx4, which copies it into four TMEM columns of
-//     every 32-lane quarter.  The scales run several stages ahead of the
-//     MMAs through their own 12-slot ring;
-//   * warp 1 allocates all 512 TMEM columns (two accumulators plus 12
-//     scale columns per stage); one lane copies each stage's scales into
-//     TMEM and issues four MMAs (M = 128, K = 32), the k-th taking byte k of
-//     the scale words, committing the stage back to the producer and the
-//     scale stream, and each finished accumulator to the epilogue;
+//     (128 x 128 B, 128-byte swizzle), the weight rows' E2M1 codes and the
+//     stage's scale blocks (1 for A, 2 for B).  The weights are read with the
+//     tensor-map type that expands each 8-byte group of 16 packed codes into a
+//     16-byte slot in shared memory, the operand layout the MMA takes for
+//     4-bit types next to 8-bit ones, so the packed weights go from HBM to the
+//     tensor core untouched;
+//   * warp 1 allocates all 512 TMEM columns (two accumulators plus 12 scale
+//     columns per stage); one lane copies each stage's scale blocks into TMEM
+//     and issues four MMAs (M = 128, K = 32), the k-th taking byte k of the
+//     scale words, committing the stage back to the producer and each
+//     finished accumulator to the epilogue;
 //   * warps 4..7 and 8..11, epilogue (each thread one token row), one
 //     warpgroup per accumulator, so that two items drain while the MMAs run
 //     on: FC1 applies the per-expert alphas and SiTU to each gate/up column
-//     pair and writes H1 as MXFP8 (E4M3 + one UE8M0 per 32 along I), FC2's
-//     A operand as it stands; FC2 writes alpha2 * acc as fp32.
+//     pair and writes H1 as MXFP8 (E4M3 rows + scale blocks), FC2's A
+//     operand as it stands; FC2 writes alpha2 * acc as fp32 through a small
+//     shared staging block, so that Y leaves in whole 128-byte row segments.
 // K (H for FC1, I for FC2) must be a multiple of 128.  Every mbarrier wait
 // is bounded; on expiry the CTA records an error code in the device status
 // word, waits (bounded) for its copies and MMAs in flight, releases TMEM
@@ -47,31 +53,30 @@ constexpr int kBM = 128;         // tokens per tile (MMA M, TMEM lanes)
 constexpr int kBK = 128;         // K elements per stage
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
-constexpr int kSfRing = 12;      // scale slots in shared memory
-constexpr int kSfAhead = 8;      // stages the scale copies run ahead of their MMAs
-constexpr int kSfStage = 3 * 512;   // A block, B rows 0..127, B rows 128..255
+constexpr int kSfBlock = 512;    // one scale block: 128 rows x 4 K blocks
 constexpr int kSfColsPerStage = 12;
 
 template <bool FC1>
 struct Cfg {
   static constexpr int BN = FC1 ? 192 : 224;        // MMA N
   static constexpr int NH = FC1 ? BN / 2 : BN;      // rows per weight box
-  static constexpr int kStages = FC1 ? 5 : 3;
+  static constexpr int kStages = FC1 ? 5 : 4;
   static constexpr int kABytes = kBM * kBK;         // 16 KB of E4M3
   static constexpr int kBBytes = BN * kBK;          // E2M1 in 16-byte slots of 16 codes
   static constexpr int kBTx = BN * kBK / 2;         // bytes the weight loads transfer (packed)
+  static constexpr int kSfBytes = 3 * kSfBlock;     // A block, B rows 0..127, B rows 128..255
+  static constexpr int kTx = kABytes + kBTx + kSfBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffSF = kOffB + kStages * kBBytes;
   // FC2: per epilogue warp a 32 x 32 fp32 staging block (rows padded to
-  // 144 bytes), so that Y leaves in whole 128-byte row segments
+  // 144 bytes)
   static constexpr int kYRow = 144;
-  static constexpr int kOffY = kOffSF + kSfRing * kSfStage;
+  static constexpr int kOffY = kOffSF + kStages * kSfBytes;
   static constexpr int kYBytes = FC1 ? 0 : 8 * 32 * kYRow;
   static constexpr int kOffBar = kOffY + kYBytes;
-  // full, empty per stage; sf_full, sf_empty per scale slot; acc_full[2],
-  // acc_empty[2]; drain
-  static constexpr int kNumBars = 2 * kStages + 2 * kSfRing + 5;
+  // full, empty per stage; acc_full[2], acc_empty[2]; drain
+  static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kOffTm = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffTm + 16 + 1024;  // + alignment slack
   static constexpr int kSfCol0 = 2 * BN;            // TMEM: accumulators [0, 2 BN), then scales
@@ -94,8 +99,8 @@ __device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a, uint64_t b, 
       : "memory");
 }
 
-// Descriptor of a 32 x 16-byte scale block: no swizzle, 8-row groups of
-// 128 contiguous bytes.
+// Descriptor of a scale block: no swizzle, 8-row groups of 128 contiguous
+// bytes.
 __device__ __forceinline__ uint64_t sf_desc(uint32_t a) {
   uint64_t d = 0;
   d |= (uint64_t)((a >> 4) & 0x3FFFu);
@@ -106,18 +111,23 @@ __device__ __forceinline__ uint64_t sf_desc(uint32_t a) {
 __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t desc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
-// 4-byte asynchronous copy, zero-filled when !ok (src is then not read)
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool ok) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0) : "memory");
+// contiguous global -> shared copy on the TMA engine, completing on an mbarrier
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
-// the word of row 32 j + i of a 128-row block goes to byte 16 i + 4 j
-__device__ __forceinline__ uint32_t sf_pos(int r) { return (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4); }
 
 // Short bounded wait used only while unwinding (no error code recorded).
 __device__ __forceinline__ void drain_wait(uint32_t a, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try(a, parity))
     if (globaltimer() - t0 > kWaitNs) return;
+}
+
+// byte offset of (row r, K block kb of the stage) inside a scale block
+__device__ __forceinline__ uint32_t sf_offset(int r, int kb) {
+  return (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4 + kb);
 }
 
 }  // namespace
@@ -135,27 +145,20 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   if ((long)blockIdx.x >= total) return;
   if (*reinterpret_cast<volatile int*>(p.err) != 0) return;   // an earlier CTA timed out
   const int nk = p.K / kBK;
-  const int nsb = p.K / 32;                                    // block scales per row
 
   const uint32_t sbase = saddr(smem);
   const uint32_t bar0 = sbase + C::kOffBar;
   auto full = [&](int s) { return bar0 + 8 * s; };
   auto empty = [&](int s) { return bar0 + 8 * (kStages + s); };
-  auto sf_full = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
-  auto sf_empty = [&](int s) { return bar0 + 8 * (2 * kStages + kSfRing + s); };
-  auto acc_full = [&](int b) { return bar0 + 8 * (2 * kStages + 2 * kSfRing + b); };
-  auto acc_empty = [&](int b) { return bar0 + 8 * (2 * kStages + 2 * kSfRing + 2 + b); };
-  const uint32_t drain = bar0 + 8 * (2 * kStages + 2 * kSfRing + 4);
+  auto acc_full = [&](int b) { return bar0 + 8 * (2 * kStages + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8 * (2 * kStages + 2 + b); };
+  const uint32_t drain = bar0 + 8 * (2 * kStages + 4);
   uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::kOffTm);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
-    }
-    for (int s = 0; s < kSfRing; ++s) {
-      mbar_init(sf_full(s), 64);
-      mbar_init(sf_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
@@ -175,26 +178,18 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tm_holder;
 
-  // item -> (expert, first row, rows, first weight row of the N tile)
-  auto item_info = [&](long item, int& e, int& row0, int& nrows, int& nbase) {
-    const int tile = (int)(item / p.n_ntiles);
-    const int ntile = (int)(item % p.n_ntiles);
-    const int2 ti = __ldg(p.tile_info + tile);
-    e = ti.x;
-    row0 = ti.y;
-    nrows = min(kBM, __ldg(p.offsets + e + 1) - row0);
-    nbase = ntile * C::NH;
-  };
-
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       long it = 0;
       bool ok = true;
       for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        int e, row0, nrows, nbase;
-        item_info(item, e, row0, nrows, nbase);
-        const int wrow = e * p.Mtot + nbase;
+        const int tile = (int)(item / p.n_ntiles), ntile = (int)(item % p.n_ntiles);
+        const int2 ti = __ldg(p.tile_info + tile);
+        const int e = ti.x, row0 = ti.y;
+        const int wrow = e * p.Mtot + ntile * C::NH;
+        const uint8_t* xsb = p.xsp + (size_t)tile * nk * kSfBlock;
+        const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + ntile) * nk * (2 * kSfBlock);
         for (int kk = 0; kk < nk; ++kk, ++it) {
           const int s = (int)(it % kStages);
           const long r = it / kStages;
@@ -202,11 +197,14 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             ok = false;
             break;
           }
-          mbar_expect_tx(full(s), C::kABytes + C::kBTx);
+          mbar_expect_tx(full(s), C::kTx);
           const uint32_t b_smem = sbase + C::kOffB + s * C::kBBytes;
+          const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
           tma_load_2d(sbase + C::kOffA + s * C::kABytes, &tmA, kk * kBK, row0, full(s));
           tma_load_2d(b_smem, &tmB, kk * kBK, wrow, full(s));
           if (FC1) tma_load_2d(b_smem + C::NH * kBK, &tmB, kk * kBK, wrow + p.I, full(s));
+          bulk_load(sf_smem, xsb + (size_t)kk * kSfBlock, kSfBlock, full(s));
+          bulk_load(sf_smem + kSfBlock, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
         }
       }
       // unwind: the loads of the last stages may still be landing
@@ -226,19 +224,17 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const uint32_t d = tmem + (uint32_t)(buf * C::BN);
         for (int kk = 0; kk < nk; ++kk, ++it) {
           const int s = (int)(it % kStages);
-          const int q = (int)(it % kSfRing);
-          if (!mbar_wait(full(s), (uint32_t)((it / kStages) & 1), p.err, 23) ||
-              !mbar_wait(sf_full(q), (uint32_t)((it / kSfRing) & 1), p.err, 24)) {
+          if (!mbar_wait(full(s), (uint32_t)((it / kStages) & 1), p.err, 23)) {
             ok = false;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t sf_smem = sbase + C::kOffSF + q * kSfStage;
+          const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
           const uint32_t sfa = tmem + (uint32_t)(C::kSfCol0 + s * kSfColsPerStage);
           const uint32_t sfb = sfa + 4;
           tmem_cp_sf(sfa, sf_desc(sf_smem));
-          tmem_cp_sf(sfb, sf_desc(sf_smem + 512));
-          tmem_cp_sf(sfb + 4, sf_desc(sf_smem + 1024));
+          tmem_cp_sf(sfb, sf_desc(sf_smem + kSfBlock));
+          tmem_cp_sf(sfb + 4, sf_desc(sf_smem + 2 * kSfBlock));
           const uint64_t ad = sdesc(sbase + C::kOffA + s * C::kABytes);
           const uint64_t bd = sdesc(sbase + C::kOffB + s * C::kBBytes);
 #pragma unroll
@@ -246,7 +242,6 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             mma_bs(d, ad + 2 * k4, bd + 2 * k4, C::kIdesc | (k4 << 4) | (k4 << 29), sfa, sfb,
                    (kk | (int)k4) != 0);
           mma_commit(empty(s));
-          mma_commit(sf_empty(q));
         }
         if (!ok) break;
         mma_commit(acc_full(buf));
@@ -255,67 +250,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       mma_commit(drain);
       drain_wait(drain, 0);
     }
-  } else if (warp < 4) {
-    // ---------------- scale stream (64 threads) ----------------
-    const int t = tid - 64;
-    long it = 0;
-    bool ok = true;
-    for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      int e, row0, nrows, nbase;
-      item_info(item, e, row0, nrows, nbase);
-      // this thread's rows: A rows t, t + 64; B rows t, t + 64, t + 128, t + 192
-      const uint8_t* src[6];
-      bool val[6];
-      uint32_t pos[6];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int m = t + 64 * h;
-        val[h] = m < nrows;
-        src[h] = p.xs + (size_t)(row0 + (val[h] ? m : 0)) * p.xs_stride;
-        pos[h] = sf_pos(m);
-      }
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int n = t + 64 * h;
-        int wr;
-        bool v;
-        if (FC1) {
-          const int i = nbase + (n < C::NH ? n : n - C::NH);
-          v = n < C::BN && i < p.I;
-          wr = (n < C::NH ? 0 : p.I) + i;
-        } else {
-          wr = nbase + n;
-          v = n < C::BN && wr < p.Mtot;
-        }
-        val[2 + h] = v;
-        src[2 + h] = p.ws + ((size_t)e * p.Mtot + (v ? wr : 0)) * (size_t)nsb;
-        pos[2 + h] = 512u + (uint32_t)((n >> 7) & 1) * 512u + sf_pos(n);
-      }
-      for (int kk = 0; kk < nk; ++kk, ++it) {
-        const int q = (int)(it % kSfRing);
-        const long r = it / kSfRing;
-        if (r > 0 && !mbar_wait(sf_empty(q), (uint32_t)((r - 1) & 1), p.err, 25)) {
-          ok = false;
-          break;
-        }
-        const uint32_t slot = sbase + C::kOffSF + q * kSfStage;
-#pragma unroll
-        for (int h = 0; h < 6; ++h)
-          if (h < 2 || t + 64 * (h - 2) < C::BN) cp_async4(slot + pos[h], src[h] + 4 * kk, val[h]);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        if (it >= kSfAhead) {
-          // the copies of stage it - kSfAhead have landed: hand them to the MMA
-          asm volatile("cp.async.wait_group %0;" ::"n"(kSfAhead) : "memory");
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(sf_full((int)((it - kSfAhead) % kSfRing)));
-        }
-      }
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (ok)
-      for (long j = (it > kSfAhead ? it - kSfAhead : 0); j < it; ++j) mbar_arrive(sf_full((int)(j % kSfRing)));
-  } else {
+  } else if (warp >= 4) {
     // ---------------- epilogue: thread = token row (TMEM lane) ----------------
     // warpgroup buf drains accumulator buf, i.e. this CTA's items buf, buf + 2, ...
     const int buf = (warp - 4) >> 2;
@@ -325,8 +260,11 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     for (int li = buf;; li += 2) {
       const long item = blockIdx.x + (long)li * gridDim.x;
       if (item >= total) break;
-      int e, row0, nrows, nbase;
-      item_info(item, e, row0, nrows, nbase);
+      const int tile = (int)(item / p.n_ntiles), ntile = (int)(item % p.n_ntiles);
+      const int2 ti = __ldg(p.tile_info + tile);
+      const int e = ti.x, row0 = ti.y;
+      const int nrows = min(kBM, __ldg(p.offsets + e + 1) - row0);
+      const int nbase = ntile * C::NH;
       // warp-uniform outcome: the tcgen05.ld below are .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 26))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -337,6 +275,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const float ag = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
         const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
         const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+        const int nkh = p.I / kBK;   // FC2's stages: H1's scale blocks per tile
         for (int c0 = 0; c0 < C::NH; c0 += 32) {
           float gt[32], up[32];
           tmem_ld16(trow + c0, gt);
@@ -363,7 +302,8 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           uint4* dst = reinterpret_cast<uint4*>(p.hq + row * p.hq_stride + i0);
           dst[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
           dst[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
-          p.hs[row * (p.hq_stride / 32) + i0 / 32] = (uint8_t)(ex + 127);
+          const int b = i0 / 32;   // K block of FC2
+          p.hsp[((size_t)tile * nkh + b / 4) * kSfBlock + sf_offset(m, b & 3)] = (uint8_t)(ex + 127);
         }
       } else {
         const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
@@ -407,27 +347,78 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 }
 
 // ---------------------------------------------------------------------------
-// gather8: MXFP8 activation rows (E4M3 bytes and UE8M0 scale bytes) copied
-// into expert order; one warp per row, 16-byte copies.
+// gather8: per token tile, the MXFP8 activation rows copied into expert
+// order (16-byte copies, one warp per row) and their UE8M0 scales written
+// as the tile's scale blocks.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(256) gather8_kernel(const Gather8Params p) {
-  const long r = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= __ldg(p.meta)) return;
-  const long t = __ldg(p.permuted_src + r) / p.top_k;
-  const int K = p.K, n16 = K / 16;
-  const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * K);
-  uint4* dst = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
-  for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
-  const int nsb = K / 32;
-  const uint8_t* ss = p.x_s + (size_t)t * nsb;
-  uint8_t* sd = p.x8s + (size_t)r * nsb;
-  if (p.s_vec) {
-    for (int i = lane; i < nsb / 4; i += 32)
-      reinterpret_cast<uint32_t*>(sd)[i] = __ldg(reinterpret_cast<const uint32_t*>(ss) + i);
-  } else {
-    for (int i = lane; i < nsb; i += 32) sd[i] = __ldg(ss + i);
+  const int tile = blockIdx.x;
+  if (tile >= __ldg(p.tile_offsets + p.E_loc)) return;
+  const int2 ti = __ldg(p.tile_info + tile);
+  const int row0 = ti.y;
+  const int nrows = min(kBM, __ldg(p.offsets + ti.x + 1) - row0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.K, n16 = K / 16, nsb = K / 32, nk = K / kBK;
+  uint8_t* blocks = p.xsp + (size_t)tile * nk * kSfBlock;
+  for (int m = warp; m < kBM; m += 8) {
+    if (m < nrows) {
+      const long r = row0 + m;
+      const long t = __ldg(p.permuted_src + r) / p.top_k;
+      const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * K);
+      uint4* dst = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
+      for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+      const uint8_t* ss = p.x_s + (size_t)t * nsb;
+      for (int kk = lane; kk < nk; kk += 32) {
+        const uint32_t w = p.s_vec ? __ldg(reinterpret_cast<const uint32_t*>(ss) + kk)
+                                   : (uint32_t)__ldg(ss + 4 * kk) | ((uint32_t)__ldg(ss + 4 * kk + 1) << 8) |
+                                         ((uint32_t)__ldg(ss + 4 * kk + 2) << 16) |
+                                         ((uint32_t)__ldg(ss + 4 * kk + 3) << 24);
+        *reinterpret_cast<uint32_t*>(blocks + (size_t)kk * kSfBlock + sf_offset(m, 0)) = w;
+      }
+    } else {
+      // rows past the expert's end: finite (2^-127) scales
+      for (int kk = lane; kk < nk; kk += 32)
+        *reinterpret_cast<uint32_t*>(blocks + (size_t)kk * kSfBlock + sf_offset(m, 0)) = 0u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// pack_scales: a weight's UE8M0 scales [E_loc, Mtot, K/32] rearranged into
+// the scale blocks of the GEMM's N tiles: per (expert, N tile, stage) two
+// blocks for tile rows 0..127 and 128..255.  FC1 tiles are NH gate rows
+// followed by the NH matching up rows.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* ws, int Mtot, int K, int I, int fc1,
+                                                          int nh, int n_ntiles, int E_loc, int vec, uint8_t* out) {
+  const int nk = K / kBK, nsb = K / 32;
+  const long nblk = (long)E_loc * n_ntiles * nk;
+  for (long blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    const int kk = (int)(blk % nk);
+    const int ntile = (int)((blk / nk) % n_ntiles);
+    const int e = (int)(blk / ((long)nk * n_ntiles));
+    uint8_t* dst = out + blk * (2 * kSfBlock);
+    const int n = threadIdx.x;   // tile row 0..255
+    int wr;
+    bool v;
+    if (fc1) {
+      const int i = ntile * nh + (n < nh ? n : n - nh);
+      v = n < 2 * nh && i < I;
+      wr = (n < nh ? 0 : I) + i;
+    } else {
+      wr = ntile * nh + n;
+      v = n < nh && wr < Mtot;
+    }
+    uint32_t w = 0u;
+    if (v) {
+      const uint8_t* s = ws + ((size_t)e * Mtot + wr) * nsb + 4 * kk;
+      w = vec ? __ldg(reinterpret_cast<const uint32_t*>(s))
+              : (uint32_t)__ldg(s) | ((uint32_t)__ldg(s + 1) << 8) | ((uint32_t)__ldg(s + 2) << 16) |
+                    ((uint32_t)__ldg(s + 3) << 24);
+    }
+    *reinterpret_cast<uint32_t*>(dst + (n >> 7) * kSfBlock + sf_offset(n, 0)) = w;
   }
 }
 
@@ -468,20 +459,42 @@ cudaError_t launch_fcq_t(const FcqParams& p, const CUtensorMap& a, const CUtenso
   return cudaGetLastError();
 }
 
+int n_tiles_of(int rows, bool fc1) { return (rows + fcq_n_rows(fc1) - 1) / fcq_n_rows(fc1); }
+
 }  // namespace
 
 int fcq_n_rows(bool fc1) { return fc1 ? Cfg<true>::NH : Cfg<false>::NH; }
 
-bool fcq_supported(int H, int I, const void* w1, const void* w2, const void* w1s, const void* w2s) {
+bool fcq_supported(int H, int I, const void* w1, const void* w2) {
   // the 4-bit tensor-map type wants rows of a multiple of 128 codes and a
-  // 32-byte aligned base; the scale stream copies 4-byte words
+  // 32-byte aligned base
   auto al = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
-  return H % kBK == 0 && I % kBK == 0 && al(w1, 32) && al(w2, 32) && al(w1s, 4) && al(w2s, 4);
+  return H % kBK == 0 && I % kBK == 0 && al(w1, 32) && al(w2, 32);
 }
 
-cudaError_t launch_gather8(const Gather8Params& p, cudaStream_t st) {
-  if (p.S <= 0) return cudaSuccess;
-  gather8_kernel<<<(unsigned)((p.S + 7) / 8), 256, 0, st>>>(p);
+size_t fcq_act_scale_bytes(long max_tiles, int K) { return (size_t)max_tiles * (K / kBK) * kSfBlock; }
+
+size_t fcq_packed_scale_bytes(int E_loc, int H, int I, bool fc1) {
+  const int K = fc1 ? H : I;
+  return (size_t)E_loc * n_tiles_of(fc1 ? I : H, fc1) * (K / kBK) * 2 * kSfBlock;
+}
+
+cudaError_t launch_pack_scales(const uint8_t* ws, int E_loc, int H, int I, bool fc1, uint8_t* out,
+                               cudaStream_t st) {
+  const int Mtot = fc1 ? 2 * I : H, K = fc1 ? H : I;
+  const int n_ntiles = n_tiles_of(fc1 ? I : H, fc1);
+  const long nblk = (long)E_loc * n_ntiles * (K / kBK);
+  if (nblk <= 0) return cudaSuccess;
+  const int vec = (reinterpret_cast<uintptr_t>(ws) & 3) == 0;   // rows are 4-byte multiples (K % 128 == 0)
+  const long grid = nblk < 8L * sm_count() ? nblk : 8L * sm_count();
+  pack_scales_kernel<<<(unsigned)grid, 256, 0, st>>>(ws, Mtot, K, I, fc1 ? 1 : 0, fcq_n_rows(fc1), n_ntiles,
+                                                     E_loc, vec, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st) {
+  if (max_tiles <= 0) return cudaSuccess;
+  gather8_kernel<<<(unsigned)max_tiles, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

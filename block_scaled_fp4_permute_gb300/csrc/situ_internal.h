@@ -98,53 +98,60 @@ int fcp_token_tile();
 cudaError_t launch_fcp(const FcpParams& p, const uint16_t* x16, long S, int kpad, const uint8_t* w, int E_loc,
                        bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 
-// Block-scaled tcgen05 path for MXFP8 activations x MXFP4 weights (w4a8):
-// A operand E4M3 rows in expert order [S, K] with UE8M0 scales [S, K/32];
-// K a multiple of 128.  FC1 writes H1 as MXFP8 rows (hq [S, hq_stride],
-// hs [S, hq_stride/32]), FC2 writes fp32 Y [S, Mtot].
+// Block-scaled tcgen05 path for MXFP8 activations x MXFP4 weights (w4a8).
+// A operand: E4M3 rows in expert order [S, K] plus, per 128-token tile, the
+// scale blocks of its rows (xsp [tiles, K/128, 512 B]); B scales packed per
+// (expert, N tile, stage) by launch_pack_scales.  K a multiple of 128.  FC1
+// writes H1 as E4M3 rows (hq [S, hq_stride]) and scale blocks (hsp [tiles,
+// I/128, 512 B]); FC2 writes fp32 Y [S, Mtot].
 struct FcqParams {
   int Mtot, K, I;
-  const uint8_t* ws;             // weight block scales [E_loc, Mtot, K/32]
-  int ws_vec;                    // 1: ws is 4-byte aligned (rows are, K/32 being a multiple of 4)
+  const uint8_t* wsp;            // packed weight scale blocks
+  const uint8_t* xsp;            // activation scale blocks per token tile
   const int32_t* offsets;
   const int32_t* tile_offsets;
   const int2* tile_info;
   int E_loc;
   int n_ntiles;
-  const uint8_t* xs;             // activation scales, xs_stride bytes per row (4-byte aligned)
-  int xs_stride;
   const float* beta;
   const float* beta_lin;
   const float* alpha_g;
   const float* alpha_u;
   uint8_t* hq;
-  uint8_t* hs;
+  uint8_t* hsp;
   int hq_stride;
   const float* alpha2;
   float* y_out;
   int* err;                      // device status word
 };
-bool fcq_supported(int H, int I, const void* w1, const void* w2, const void* w1_scale, const void* w2_scale);
+bool fcq_supported(int H, int I, const void* w1, const void* w2);
 // weight rows per N tile: FC1 gate rows (the tile also holds the matching
 // up rows), FC2 rows of H
 int fcq_n_rows(bool fc1);
+// bytes of the activation scale blocks for max_tiles token tiles, and of
+// one weight's packed scale blocks
+size_t fcq_act_scale_bytes(long max_tiles, int K);
+size_t fcq_packed_scale_bytes(int E_loc, int H, int I, bool fc1);
+cudaError_t launch_pack_scales(const uint8_t* w_scale, int E_loc, int H, int I, bool fc1, uint8_t* out,
+                               cudaStream_t st);
 cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint8_t* w, int E_loc, bool fc1,
                        long max_tiles, cudaStream_t st);
 
-// MXFP8 rows (x_q [T, K], x_s [T, K/32]) copied into expert order
-// (x8 [S, K], x8s [S, K/32]); K a multiple of 16, s_vec = 1 when the scale
-// rows may be copied as 32-bit words.
+// Per token tile: MXFP8 rows (x_q [T, K], x_s [T, K/32]) copied into
+// expert order (x8 [S, K]) and their scales written as the tile's scale
+// blocks (xsp); K a multiple of 128, s_vec = 1 when x_s is 4-byte aligned.
 struct Gather8Params {
   const uint8_t* x_q;
   const uint8_t* x_s;
   const int32_t* permuted_src;
-  const int32_t* meta;
-  int top_k, K, s_vec;
-  long S;
+  const int32_t* offsets;
+  const int32_t* tile_offsets;
+  const int2* tile_info;
+  int E_loc, top_k, K, s_vec;
   uint8_t* x8;
-  uint8_t* x8s;
+  uint8_t* xsp;
 };
-cudaError_t launch_gather8(const Gather8Params& p, cudaStream_t st);
+cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st);
 size_t fcd_smem_bytes(int K, bool nvfp4);
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 

@@ -23,8 +23,30 @@ bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
-  size_t x16, x16s, h16, h16s, total;
+  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, total;
 };
+
+// Decode-like routings (about six or fewer rows per expert) take the
+// 8-token-tile path when its shared-memory staging fits; everything else a
+// tcgen05 prefill path.
+bool decode_like(const situ_moe_args* a) {
+  return (double)a->T * a->top_k / (double)a->num_experts_total <= 6.0;
+}
+constexpr size_t kMaxDecodeSmem = 220 * 1024;
+bool takes_decode_path(const situ_moe_args* a) {
+  const bool nv = a->weight_dtype == SITU_W_NVFP4;
+  return decode_like(a) && fcd_smem_bytes(a->H, nv) <= kMaxDecodeSmem && fcd_smem_bytes(a->I, nv) <= kMaxDecodeSmem;
+}
+// shapes of the block-scaled prefill path (w4a8, K multiples of 128)
+bool block_scaled_shapes(const situ_moe_args* a) {
+  return a->weight_dtype == SITU_W_MXFP4 && a->H % 128 == 0 && a->I % 128 == 0;
+}
+bool takes_block_scaled_path(const situ_moe_args* a) {
+  return a->act_dtype == SITU_ACT_MXFP8 && block_scaled_shapes(a) && !takes_decode_path(a);
+}
+long max_prefill_tiles(const situ_moe_args* a) {
+  return (long)a->T * a->top_k / fcp_token_tile() + a->num_local_experts + 1;
+}
 
 Layout make_layout(const situ_moe_args* a) {
   Layout L;
@@ -47,6 +69,16 @@ Layout make_layout(const situ_moe_args* a) {
   L.x16s = take(4 * S * (size_t)(pad128(a->H) / 32));
   L.h16 = take(2 * S * (size_t)pad128(a->I));
   L.h16s = take(4 * S * (size_t)(pad128(a->I) / 32));
+  // block-scaled path: scale blocks of the token tiles (FC1 input, H1), and
+  // the packed weight scales when the caller keeps none
+  const bool bs = takes_block_scaled_path(a);
+  const long tiles = max_prefill_tiles(a);
+  L.xsp = take(bs ? fcq_act_scale_bytes(tiles, a->H) : 0);
+  L.hsp = take(bs ? fcq_act_scale_bytes(tiles, a->I) : 0);
+  L.wsp = take(bs && !a->scales_packed
+                   ? fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true) +
+                         fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, false)
+                   : 0);
   L.total = o;
   return L;
 }
@@ -88,16 +120,10 @@ situ_status validate(const situ_moe_args* a) {
   for (const void* p : p4)
     if (!aligned_to(p, 4)) return SITU_ERR_MISALIGNED;
   if (!aligned_to(a->w1_scale, 2) || !aligned_to(a->w2_scale, 2)) return SITU_ERR_MISALIGNED;
+  if (!aligned_to(a->scales_packed, 16)) return SITU_ERR_MISALIGNED;
   return SITU_OK;
 }
 
-// Token-tile width of the grouped GEMMs: 8 * ns tokens, chosen from the
-// expected rows per expert (decode: 1-2 rows, prefill: hundreds).
-// Decode-like routings (about six or fewer rows per expert) take the
-// 8-token-tile path; everything else the tcgen05 prefill path.
-bool decode_like(const situ_moe_args* a) {
-  return (double)a->T * a->top_k / (double)a->num_experts_total <= 6.0;
-}
 
 situ_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SITU_OK : SITU_ERR_CUDA; }
 
@@ -184,8 +210,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   uint16_t* h1 = (uint16_t*)(ws + L.h1);
   float* y = (float*)(ws + L.y);
   const bool nv = a->weight_dtype == SITU_W_NVFP4;
-  const bool small_tiles = decode_like(a);
-  const int tile_n = small_tiles ? kDecodeTileTokens : fcp_token_tile();
+  const bool decode_path = takes_decode_path(a);
+  const int tile_n = decode_path ? kDecodeTileTokens : fcp_token_tile();
   const long S = (long)a->T * a->top_k;
   const long max_tiles = S / tile_n + a->num_local_experts + 1;
   auto mark = [&](int i) {
@@ -199,10 +225,6 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   if (err != cudaSuccess) return SITU_ERR_CUDA;
   mark(1);
 
-  // the decode kernel stages the whole K of its token tile in shared memory
-  const size_t kMaxSmem = 220 * 1024;
-  const bool decode_path = small_tiles && fcd_smem_bytes(a->H, nv) <= kMaxSmem &&
-                           fcd_smem_bytes(a->I, nv) <= kMaxSmem;
   if (decode_path) {
     // 8-token tiles: rows are converted once to f16 block rows, then FC1
     // (+SiTU, writing H1 as f16 block rows) and FC2
@@ -263,22 +285,36 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.y_out = y;
     if ((err = launch_fcd(d, false, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(4);
-  } else if (a->act_dtype == SITU_ACT_MXFP8 && !nv &&
-             fcq_supported(a->H, a->I, a->w1, a->w2, a->w1_scale, a->w2_scale)) {
+  } else if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) {
     // w4a8 on the block-scaled tensor cores: MXFP8 rows copied into expert
-    // order, FC1 (+SiTU) writing H1 as MXFP8, FC2 reading it as it stands
+    // order with their tile scale blocks, FC1 (+SiTU) writing H1 as MXFP8,
+    // FC2 reading it as it stands
+    const uint8_t* wsp1 = (const uint8_t*)a->scales_packed;
+    if (!wsp1) {
+      uint8_t* dst = ws + L.wsp;
+      if ((err = launch_pack_scales(a->w1_scale, a->num_local_experts, a->H, a->I, true, dst, st)) !=
+              cudaSuccess ||
+          (err = launch_pack_scales(a->w2_scale, a->num_local_experts, a->H, a->I, false,
+                                    dst + fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true),
+                                    st)) != cudaSuccess)
+        return SITU_ERR_CUDA;
+      wsp1 = dst;
+    }
+    const uint8_t* wsp2 = wsp1 + fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true);
     Gather8Params g8;
-    g8.x_q = (const uint8_t*)a->hidden_states_q;
-    g8.x_s = (const uint8_t*)a->hidden_states_scale;
+    g8.x_q = a->hidden_states_q;
+    g8.x_s = a->hidden_states_scale;
     g8.permuted_src = psrc;
-    g8.meta = meta;
+    g8.offsets = offsets;
+    g8.tile_offsets = tile_offsets;
+    g8.tile_info = tile_info;
+    g8.E_loc = a->num_local_experts;
     g8.top_k = a->top_k;
     g8.K = a->H;
     g8.s_vec = (reinterpret_cast<uintptr_t>(a->hidden_states_scale) & 3) == 0;
-    g8.S = S;
     g8.x8 = ws + L.x16;
-    g8.x8s = ws + L.x16s;
-    if ((err = launch_gather8(g8, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    g8.xsp = ws + L.xsp;
+    if ((err = launch_gather8(g8, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(2);
     FcqParams q;
     std::memset(&q, 0, sizeof(q));
@@ -288,30 +324,26 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.E_loc = a->num_local_experts;
     q.I = a->I;
     q.err = meta + 2;
-    q.ws = a->w1_scale;
-    q.ws_vec = (reinterpret_cast<uintptr_t>(a->w1_scale) & 3) == 0;
+    q.wsp = wsp1;
+    q.xsp = g8.xsp;
     q.Mtot = 2 * a->I;
     q.K = a->H;
     q.n_ntiles = (a->I + fcq_n_rows(true) - 1) / fcq_n_rows(true);
-    q.xs = g8.x8s;
-    q.xs_stride = a->H / 32;
     q.beta = a->gemm1_alpha;
     q.beta_lin = a->gemm1_beta;
     q.alpha_g = a->g1_alphas;
     q.alpha_u = a->g1_alphas_up;
     q.hq = ws + L.h16;
-    q.hs = ws + L.h16s;
+    q.hsp = ws + L.hsp;
     q.hq_stride = a->I;
     if ((err = launch_fcq(q, g8.x8, S, a->w1, a->num_local_experts, true, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(3);
-    q.ws = a->w2_scale;
-    q.ws_vec = (reinterpret_cast<uintptr_t>(a->w2_scale) & 3) == 0;
+    q.wsp = wsp2;
+    q.xsp = q.hsp;
     q.Mtot = a->H;
     q.K = a->I;
     q.n_ntiles = (a->H + fcq_n_rows(false) - 1) / fcq_n_rows(false);
-    q.xs = q.hs;
-    q.xs_stride = a->I / 32;
     q.alpha2 = a->g2_alphas;
     q.y_out = y;
     if ((err = launch_fcq(q, q.hq, S, a->w2, a->num_local_experts, false, max_tiles, st)) != cudaSuccess)
@@ -407,6 +439,29 @@ situ_status situ_moe_forward_profiled(const situ_moe_args* a, void* workspace,
                                       size_t workspace_bytes, void* stream, void* const* events) {
   if (!events) return SITU_ERR_NULL_ARG;
   return forward_impl(a, workspace, workspace_bytes, stream, events);
+}
+
+size_t situ_moe_packed_scales_size(const situ_moe_args* a) {
+  if (!a || a->H <= 0 || a->I <= 0 || a->num_local_experts < 1 || !block_scaled_shapes(a)) return 0;
+  return fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true) +
+         fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, false);
+}
+
+situ_status situ_moe_pack_scales(const situ_moe_args* a, void* packed, size_t packed_bytes, void* stream) {
+  if (!a || !packed) return SITU_ERR_NULL_ARG;
+  if (a->H <= 0 || a->I <= 0 || a->num_local_experts < 1 || a->num_local_experts > SITU_MAX_LOCAL_EXPERTS)
+    return SITU_ERR_BAD_SHAPE;
+  if (!block_scaled_shapes(a)) return SITU_ERR_UNSUPPORTED;
+  if (!a->w1_scale || !a->w2_scale) return SITU_ERR_NULL_ARG;
+  if (!aligned16(packed)) return SITU_ERR_MISALIGNED;
+  const size_t b1 = fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true);
+  if (packed_bytes < situ_moe_packed_scales_size(a)) return SITU_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* out = (uint8_t*)packed;
+  if (launch_pack_scales(a->w1_scale, a->num_local_experts, a->H, a->I, true, out, st) != cudaSuccess ||
+      launch_pack_scales(a->w2_scale, a->num_local_experts, a->H, a->I, false, out + b1, st) != cudaSuccess)
+    return SITU_ERR_CUDA;
+  return SITU_OK;
 }
 
 situ_status situ_moe_device_status(const situ_moe_args* a, const void* workspace, void* stream,

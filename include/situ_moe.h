@@ -225,6 +225,9 @@ typedef struct situ_moe_args {
   const float* g1_alphas_up;      /* fp32 [E_loc] or NULL (1) */
   const float* g2_alphas;         /* fp32 [E_loc] or NULL (1) */
   void* out;                      /* bf16 [T, H] partial output of this shard */
+  const void* scales_packed;      /* optional: situ_moe_pack_scales output for w1_scale /
+                                     w2_scale, or NULL (the forward then packs them into its
+                                     workspace on every call) */
 } situ_moe_args;
 
 /* Workspace bytes situ_moe_forward needs for these shapes (0 on bad args).
@@ -270,6 +273,28 @@ situ_status situ_moe_forward_profiled(const situ_moe_args* args, void* workspace
  * --------------------------------------------------------------------- */
 situ_status situ_moe_device_status(const situ_moe_args* args, const void* workspace, void* stream,
                                    int32_t* code);
+
+/* ------------------------------------------------------------------------
+ * situ_moe_packed_scales_size / situ_moe_pack_scales -- the MXFP4 weight
+ * scales rearranged for the block-scaled tensor-core GEMMs.
+ *
+ * The MXFP8 x MXFP4 (w4a8) prefill path reads each GEMM stage's weight
+ * scales as contiguous blocks: per (local expert, N tile of weight rows,
+ * 128 elements of K) the UE8M0 bytes of the tile's rows, laid out as the
+ * tensor memory copy expects.  Packing depends only on w1_scale, w2_scale,
+ * num_local_experts, H and I, so it is done once per weight set; pass the
+ * result as args->scales_packed.  Without it the forward packs into its
+ * workspace on every call (same result, a little more HBM traffic).
+ * The size is 0 (and pack_scales returns UNSUPPORTED) unless weight_dtype
+ * is MXFP4 and H and I are multiples of 128.  `packed` is a device buffer
+ * of at least that many bytes, 16-byte aligned, owned by the caller;
+ * asynchronous on `stream`.  A layout of this library, not of the pages.
+ * Errors: NULL_ARG, BAD_SHAPE, UNSUPPORTED, MISALIGNED, WORKSPACE_TOO_SMALL
+ * (packed_bytes too small), CUDA.
+ * --------------------------------------------------------------------- */
+size_t situ_moe_packed_scales_size(const situ_moe_args* args);
+situ_status situ_moe_pack_scales(const situ_moe_args* args, void* packed, size_t packed_bytes,
+                                 void* stream);
 
 #ifdef __cplusplus
 }

@@ -97,6 +97,21 @@ def test_device_status_argument_errors(lib):
     assert lib.situ_moe_device_status(ctypes.byref(_args(T=0)), ctypes.c_void_p(16), None, None) == 0
 
 
+def test_packed_scales_size_and_errors(lib):
+    ok = _args(H=256, I=128)
+    n = lib.situ_moe_packed_scales_size(ctypes.byref(ok))
+    assert n > 0
+    assert lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=256, I=96))) == 0   # I % 128
+    assert lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=256, I=128, weight_dtype=1))) == 0
+    assert lib.situ_moe_packed_scales_size(None) == 0
+    buf = ctypes.c_void_p(256)
+    assert lib.situ_moe_pack_scales(None, buf, n, None) == 1
+    assert lib.situ_moe_pack_scales(ctypes.byref(ok), None, n, None) == 1
+    assert lib.situ_moe_pack_scales(ctypes.byref(_args(H=256, I=96)), buf, n, None) == 3
+    assert lib.situ_moe_pack_scales(ctypes.byref(ok), ctypes.c_void_p(264), n, None) == 6
+    assert lib.situ_moe_pack_scales(ctypes.byref(ok), buf, n - 1, None) == 4
+
+
 def test_workspace_size_grows_with_tokens(lib):
     small = lib.situ_moe_workspace_size(ctypes.byref(_args(T=4)))
     big = lib.situ_moe_workspace_size(ctypes.byref(_args(T=400)))

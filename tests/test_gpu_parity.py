@@ -200,11 +200,18 @@ def test_prefill_w4a8_subset():
     dict(T=200, H=384, I=384, E_total=3, E_loc=3, off=0, K=2, act=W.ACT_MXFP8, params="k3_random"),
 ])
 def test_w4a8_block_scaled_shapes(over):
-    """w4a8 shapes on the block-scaled tensor-core path (H, I multiples of 128)."""
+    """w4a8 shapes on the block-scaled tensor-core path (H, I multiples of 128),
+    with the weight scales packed once and packed inside every call."""
     wl = W.make("tiny", device="cuda", **over)
     layer, out = run_layer(wl)
+    assert layer.scales_packed is not None
     assert layer.device_status() == 0
     assert_parity(out, oracle_out(wl), str(over))
+    per_call = binding.Layer(wl, pack_scales=False)
+    out2 = per_call()
+    torch.cuda.synchronize()
+    assert per_call.device_status() == 0
+    assert np.array_equal(out2.float().cpu().numpy(), out)
 
 
 def test_ep_shard_subset_and_filtered_rows():

@@ -82,6 +82,20 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return (uint32_t)d;
 }
 
+// Two E4M3 codes (low byte = first) to fp32, exactly, through the hardware
+// E4M3 -> f16 conversion (every finite E4M3 value is an f16).
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& lo, float& hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)codes));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"((uint16_t)(h2 & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"((uint16_t)(h2 >> 16)));
+}
+__device__ __forceinline__ float e4m3_code_to_f32(uint32_t code) {
+  float lo, hi;
+  e4m3x2_to_f32x2(code & 0xFFu, lo, hi);
+  return lo;
+}
+
 // The MXFP8 block exponent: the smallest e in [-127, 127] with
 // amax * 2^-e <= 448, from the fp32 bits of amax (amax = m * 2^k with
 // m in [1, 2); 448 = 1.75 * 2^8, so e = k - 8 + (m > 1.75)).

@@ -474,22 +474,31 @@ bool fcq_supported(int H, int I, const void* w1, const void* w2) {
 
 size_t fcq_act_scale_bytes(long max_tiles, int K) { return (size_t)max_tiles * (K / kBK) * kSfBlock; }
 
-size_t fcq_packed_scale_bytes(int E_loc, int H, int I, bool fc1) {
+size_t packed_scale_bytes(int E_loc, int H, int I, bool fc1, int nh) {
   const int K = fc1 ? H : I;
-  return (size_t)E_loc * n_tiles_of(fc1 ? I : H, fc1) * (K / kBK) * 2 * kSfBlock;
+  const int n_ntiles = ((fc1 ? I : H) + nh - 1) / nh;
+  return (size_t)E_loc * n_ntiles * (K / kBK) * 2 * kSfBlock;
 }
 
-cudaError_t launch_pack_scales(const uint8_t* ws, int E_loc, int H, int I, bool fc1, uint8_t* out,
-                               cudaStream_t st) {
+size_t fcq_packed_scale_bytes(int E_loc, int H, int I, bool fc1) {
+  return packed_scale_bytes(E_loc, H, I, fc1, fcq_n_rows(fc1));
+}
+
+cudaError_t launch_pack_scales_nh(const uint8_t* ws, int E_loc, int H, int I, bool fc1, int nh, uint8_t* out,
+                                  cudaStream_t st) {
   const int Mtot = fc1 ? 2 * I : H, K = fc1 ? H : I;
-  const int n_ntiles = n_tiles_of(fc1 ? I : H, fc1);
+  const int n_ntiles = ((fc1 ? I : H) + nh - 1) / nh;
   const long nblk = (long)E_loc * n_ntiles * (K / kBK);
   if (nblk <= 0) return cudaSuccess;
   const int vec = (reinterpret_cast<uintptr_t>(ws) & 3) == 0;   // rows are 4-byte multiples (K % 128 == 0)
   const long grid = nblk < 8L * sm_count() ? nblk : 8L * sm_count();
-  pack_scales_kernel<<<(unsigned)grid, 256, 0, st>>>(ws, Mtot, K, I, fc1 ? 1 : 0, fcq_n_rows(fc1), n_ntiles,
-                                                     E_loc, vec, out);
+  pack_scales_kernel<<<(unsigned)grid, 256, 0, st>>>(ws, Mtot, K, I, fc1 ? 1 : 0, nh, n_ntiles, E_loc, vec, out);
   return cudaGetLastError();
+}
+
+cudaError_t launch_pack_scales(const uint8_t* ws, int E_loc, int H, int I, bool fc1, uint8_t* out,
+                               cudaStream_t st) {
+  return launch_pack_scales_nh(ws, E_loc, H, I, fc1, fcq_n_rows(fc1), out, st);
 }
 
 cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st) {

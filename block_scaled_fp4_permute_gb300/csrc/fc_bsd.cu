@@ -1,0 +1,526 @@
+// fc_bsd.cu -- FC1 (gate/up + SiTU) and FC2 for decode-sized token tiles on
+// the block-scaled tensor cores, weights on the MMA's M side.
+//
+// At decode every touched expert's FP4 weights are streamed once for one or
+// two tokens, so the layer is bound by HBM bandwidth, and any per-weight
+// instruction (a register conversion of the codes, a scale multiply) costs
+// issue slots that the stream cannot spare.  Here no instruction touches a
+// weight: TMA copies the packed E2M1 codes from HBM into shared memory (the
+// tensor-map type that widens each 8-byte group of 16 codes into a 16-byte
+// slot, the 4-bit operand layout of the MMA) and
+// tcgen05.mma.kind::mxf8f6f4.block_scale reads them there, with their UE8M0
+// block scales in TMEM.
+//
+// Tokens are the MMA's N side: a tile holds up to 16 expert-ordered rows.
+// The activations enter as E4M3 rows with one UE8M0 scale per 32 elements.
+// An MXFP8 input is that already.  A bf16 input (and the bf16 H1 of w4a16)
+// is held as the sum of two such rows, hi + lo: hi is x rounded to E4M3
+// under the block's MXFP8 scale 2^e, and lo the remainder rounded to E4M3
+// under 2^(e-4).  hi carries the leading four significant bits and lo the
+// next four, so every bf16 value whose exponent lies within 2^-14 of the
+// block's largest is represented exactly; smaller ones keep an absolute error
+// below 2^-22 of the block maximum.  hi and lo rows are stored interleaved
+// (rows 2r and 2r + 1), so one box of 32 rows is the MMA's B operand for 16
+// tokens and the epilogue adds columns 2t and 2t + 1.
+//
+// Weight tiles: FC1 takes 128 gate rows and the 128 matching up rows, FC2
+// 256 rows of H; both are staged as rows of 128 K-codes and covered by two
+// M = 128 MMAs (FC1: gate, up; FC2: rows 0..127 and 128..255).  In FC1 gate
+// row i and up row i are then lane i of the two accumulators, so SiTU runs
+// on one thread's registers.  Each MMA has its block of packed
+// weight scales (pack_scales: per weight tile and stage, 128 rows x four
+// K blocks, laid out as tcgen05.cp.32x128b.warpx4 takes them), copied into
+// four TMEM columns.
+//
+// Token-side scales are rows of 16 bytes per stage, the stage's four UE8M0
+// bytes first (the other twelve unused), so a 16-byte TMA box of the tile's
+// rows lands as the source layout of tcgen05.cp.32x128b.warpx4 with each
+// row's scale word in the first TMEM column of the copy.
+//
+// Warp roles (one CTA per SM, persistent over the (token tile, weight tile)
+// items): warps 0..3 epilogue (thread = TMEM lane = weight row), warp 4 one
+// lane TMA producer, warp 5 TMEM allocation and one lane scale copies + MMA.
+// Two accumulator buffers let an item's epilogue overlap the next item's
+// MMAs; the producer runs ahead across item boundaries.  Every mbarrier wait
+// is bounded; on expiry the CTA records an error code, drains what it issued,
+// releases TMEM and returns.
+#include "situ_internal.h"
+#include "tc_common.cuh"
+
+namespace situ {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kTok = 16;           // tokens per tile
+constexpr int kBK = 128;           // K elements per stage
+constexpr int kNH1 = 128;          // FC1 gate (and up) rows per weight tile
+constexpr int kNH2 = 256;          // FC2 rows per weight tile
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 256;
+constexpr int kSfBlock = 512;
+constexpr int kSfCol0 = 128;       // scale columns start after the two accumulator buffers
+constexpr int kSfColsPerStage = 12;
+
+template <bool FC1, bool LO>
+struct CfgW {
+  static constexpr int kStages = 6;
+  static constexpr int NB = LO ? 2 * kTok : kTok;          // MMA N: token rows (hi, lo interleaved)
+  static constexpr int kABytes = 256 * kBK;                // 32 KB
+  static constexpr int kBBytes = NB * kBK;                 // 4 / 2 KB
+  static constexpr int kSfBytes = 3 * kSfBlock;            // weight blocks (2), token block
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSF = kOffB + kStages * kBBytes;
+  static constexpr int kOffBar = kOffSF + kStages * kSfBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;         // full, empty; acc_full[2], acc_empty[2]; drain
+  static constexpr int kOffTm = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffTm + 16 + 1024;
+  static constexpr uint32_t kTx = (uint32_t)(FC1 ? 2 * kNH1 : kNH2) * (kBK / 2) + (uint32_t)NB * kBK +
+                                  (uint32_t)NB * 16 + 2 * kSfBlock;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+  static_assert(2 * NB <= 64, "accumulator buffer");
+  static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
+  // A = E2M1 (5), B = E4M3 (0), both K-major; N >> 3 at bit 17, UE8M0
+  // scales (bit 23), M >> 4 at bit 24; B / A scale byte selectors at bits
+  // 4..5 / 29..30.
+  static constexpr uint32_t kIdesc =
+      (5u << 7) | (0u << 10) | ((uint32_t)(NB >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+};
+
+__device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// scale block in shared memory: no swizzle, 8-row groups of 128 bytes
+__device__ __forceinline__ uint64_t sf_desc(uint32_t a) {
+  uint64_t d = 0;
+  d |= (uint64_t)((a >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  return d;
+}
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// barrier over the n threads of named barrier id; returns the AND of v
+__device__ __forceinline__ bool bar_red_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %3, 0;\n bar.red.and.pred p, %1, %2, q;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void drain_wait(uint32_t a, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try(a, parity))
+    if (globaltimer() - t0 > kWaitNs) return;
+}
+
+}  // namespace
+
+// The hi/lo MXFP8 pair of one value v (held exactly in fp32) of a block
+// with MXFP8 exponent e; the lo scale exponent is e - c, c = min(4, e + 127).
+// Returns the hi code and sets the lo code.
+__device__ __forceinline__ uint32_t split_hl(float v, int e, int c, uint32_t& lo) {
+  const float x = v * exp2i(-e);
+  const uint32_t h = f32x2_to_e4m3x2(x, 0.f) & 0xFFu;
+  const float r = x - e4m3_code_to_f32(h);
+  lo = f32x2_to_e4m3x2(r * exp2i(c), 0.f) & 0xFFu;
+  return h;
+}
+
+// The same for a whole block of 32 values in one thread: codes to hi[0..7],
+// lo[0..7] (four per word, element 4j + u in byte u of word j); returns the
+// two scale bytes (hi in bits 0..7, lo in bits 8..15).
+__device__ __forceinline__ uint32_t split_hl32(const float* v, uint32_t* hi, uint32_t* lo) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const int e = mxfp8_exponent(amax);
+  const int c = min(4, e + 127);
+  const float s = exp2i(-e), sl = exp2i(c);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float x[4], r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = v[4 * j + u] * s;
+    const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
+    float f[4];
+    e4m3x2_to_f32x2(h01, f[0], f[1]);
+    e4m3x2_to_f32x2(h23, f[2], f[3]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) r[u] = x[u] - f[u];
+    hi[j] = h01 | (h23 << 16);
+    lo[j] = f32x2_to_e4m3x2(r[0] * sl, r[1] * sl) | (f32x2_to_e4m3x2(r[2] * sl, r[3] * sl) << 16);
+  }
+  return (uint32_t)(e + 127) | ((uint32_t)(e - c + 127) << 8);
+}
+
+// byte offset of the UE8M0 scale of 32-element block b in a token scale row
+__device__ __forceinline__ int tok_scale_byte(int b) { return 16 * (b >> 2) + (b & 3); }
+
+template <bool FC1, bool LO>
+__global__ void __launch_bounds__(kThreads, 1)
+fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+           const __grid_constant__ CUtensorMap tmS, const FcwParams p) {
+  using C = CfgW<FC1, LO>;
+  constexpr int kStages = C::kStages;
+  constexpr int NB = C::NB;
+  constexpr int NH = FC1 ? kNH1 : kNH2;
+  constexpr int RM = LO ? 2 : 1;     // token-side rows per token
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const long total = (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
+  if ((long)blockIdx.x >= total) return;
+  if (*reinterpret_cast<volatile int*>(p.err) != 0) return;
+  const int nk = p.K / kBK;
+
+  const uint32_t sbase = saddr(smem);
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto full = [&](int s) { return bar0 + 8 * s; };
+  auto empty = [&](int s) { return bar0 + 8 * (kStages + s); };
+  auto acc_full = [&](int b) { return bar0 + 8 * (2 * kStages + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8 * (2 * kStages + 2 + b); };
+  const uint32_t drain = bar0 + 8 * (2 * kStages + 4);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::kOffTm);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tm_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tm_holder;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      long it = 0;
+      bool ok = true;
+      // the tile of the next item is read one item ahead, so that its
+      // latency hides behind this item's loads
+      int2 ti_next = __ldg(p.tile_info + blockIdx.x / p.n_ntiles);
+      for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const int nt = (int)(item % p.n_ntiles);
+        const int2 ti = ti_next;
+        if (item + gridDim.x < total) ti_next = __ldg(p.tile_info + (item + gridDim.x) / p.n_ntiles);
+        const int e = ti.x, row0 = ti.y;
+        const int wrow = e * p.Mtot + nt * NH;
+        const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + nt) * nk * (2 * kSfBlock);
+        for (int kk = 0; kk < nk; ++kk, ++it) {
+          const int s = (int)(it % kStages);
+          const long r = it / kStages;
+          if (r > 0 && !mbar_wait(empty(s), (uint32_t)((r - 1) & 1), p.err, 41)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full(s), C::kTx);
+          const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
+          const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
+          tma_load_2d(a_smem, &tmW, kk * kBK, wrow, full(s));
+          if (FC1) tma_load_2d(a_smem + kNH1 * kBK, &tmW, kk * kBK, wrow + p.I, full(s));
+          tma_load_2d(sbase + C::kOffB + s * C::kBBytes, &tmX, kk * kBK, RM * row0, full(s));
+          bulk_load(sf_smem, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
+          tma_load_2d(sf_smem + 2 * kSfBlock, &tmS, 16 * kk, RM * row0, full(s));
+        }
+      }
+      for (long j = it - 1; j >= 0 && j >= it - kStages; --j)
+        drain_wait(full((int)(j % kStages)), (uint32_t)((j / kStages) & 1));
+    }
+  } else if (warp == 5) {
+    // ---------------- scale copies + MMA issuer ----------------
+    if (lane == 0) {
+      long it = 0;
+      int li = 0;
+      bool ok = true;
+      for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+        const int buf = li & 1, use = li >> 1;
+        if (use > 0 && !mbar_wait(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 42)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d1 = tmem + (uint32_t)(buf * 64);
+        const uint32_t d2 = d1 + NB;
+        for (int kk = 0; kk < nk; ++kk, ++it) {
+          const int s = (int)(it % kStages);
+          if (!mbar_wait(full(s), (uint32_t)((it / kStages) & 1), p.err, 43)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
+          const uint32_t sfw = tmem + (uint32_t)(kSfCol0 + s * kSfColsPerStage);
+          const uint32_t sft = sfw + 8;
+          tmem_cp_sf(sfw, sf_desc(sf_smem));
+          tmem_cp_sf(sfw + 4, sf_desc(sf_smem + kSfBlock));
+          tmem_cp_sf(sft, sf_desc(sf_smem + 2 * kSfBlock));
+          const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
+          const uint64_t ad1 = sdesc(a_smem);
+          const uint64_t ad2 = sdesc(a_smem + 128 * kBK);
+          const uint64_t bd = sdesc(sbase + C::kOffB + s * C::kBBytes);
+#pragma unroll
+          for (uint32_t k4 = 0; k4 < kBK / 32; ++k4) {
+            const uint32_t idesc = C::kIdesc | (k4 << 4) | (k4 << 29);
+            const uint32_t acc = (kk | (int)k4) != 0;
+            mma_bs(d1, ad1 + 2 * k4, bd + 2 * k4, idesc, sfw, sft, acc);
+            mma_bs(d2, ad2 + 2 * k4, bd + 2 * k4, idesc, sfw + 4, sft, acc);
+          }
+          mma_commit(empty(s));
+        }
+        if (!ok) break;
+        mma_commit(acc_full(buf));
+      }
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else {
+    // ---------------- epilogue: thread = weight row (TMEM lane) ----------------
+    const int l = warp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    for (int li = 0;; ++li) {
+      const long item = blockIdx.x + (long)li * gridDim.x;
+      if (item >= total) break;
+      const int buf = li & 1;
+      const int tile = (int)(item / p.n_ntiles), nt = (int)(item % p.n_ntiles);
+      const int2 ti = __ldg(p.tile_info + tile);
+      const int e = ti.x, row0 = ti.y;
+      const int nrows = min(kTok, __ldg(p.offsets + e + 1) - row0);
+      // every epilogue thread takes the same decision (the waits are
+      // bounded, so all 128 reach the reduction)
+      if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 46))) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * 64);
+      float a1[kTok], a2[kTok];
+      if (LO) {
+        // columns 2t (hi) and 2t + 1 (lo) of token t
+        float v[16];
+#pragma unroll
+        for (int acc = 0; acc < 2; ++acc) {
+          float* a = acc ? a2 : a1;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld16(t1 + (uint32_t)(acc * NB + 16 * h), v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a[8 * h + j] = v[2 * j] + v[2 * j + 1];
+          }
+        }
+      } else {
+        tmem_ld16(t1, a1);
+        tmem_ld16(t1 + NB, a2);
+      }
+      // the accumulator is in registers: hand it back to the MMA warp
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(acc_empty(buf));
+
+      if (FC1) {
+        // gate row i = nt * 128 + l and its up row are lane l of the two
+        // accumulators; warp w holds the 32-element block i0 .. i0 + 31
+        const int i0 = nt * kNH1 + warp * 32;
+        if (i0 < p.I) {
+          const float ag = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
+          const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
+          const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+          const int sbyte = tok_scale_byte(i0 / 32);   // FC2's K block of this warp
+#pragma unroll
+          for (int t = 0; t < kTok; ++t) {
+            if (t >= nrows) break;
+            float h = situ_f(a1[t] * ag, a2[t] * au, bt, btl);
+            if (LO) h = bf16_lo(f32x2_to_bf16x2(h, 0.f));   // w4a16: H1 is bf16
+            const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+            const int ex = mxfp8_exponent(amax);
+            const size_t r = (size_t)RM * (size_t)(row0 + t);
+            if (LO) {
+              const int c = min(4, ex + 127);
+              uint32_t lo;
+              const uint32_t hi = split_hl(h, ex, c, lo);
+              p.h[r * p.I + i0 + lane] = (uint8_t)hi;
+              p.h[(r + 1) * p.I + i0 + lane] = (uint8_t)lo;
+              if (lane == 0) {
+                p.hs[r * p.hs_stride + sbyte] = (uint8_t)(ex + 127);
+                p.hs[(r + 1) * p.hs_stride + sbyte] = (uint8_t)(ex - c + 127);
+              }
+            } else {
+              p.h[r * p.I + i0 + lane] = (uint8_t)(f32x2_to_e4m3x2(h * exp2i(-ex), 0.f) & 0xFFu);
+              if (lane == 0) p.hs[r * p.hs_stride + sbyte] = (uint8_t)(ex + 127);
+            }
+          }
+        }
+      } else {
+        // FC2: row n = nt * 256 + l (first accumulator) and nt * 256 + 128 + l
+        // (second); Y rows leave as 128-byte segments
+        const float a2s = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
+        const int n1 = nt * kNH2 + l, n2 = nt * kNH2 + 128 + l;
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+          if (t >= nrows) break;
+          float* yr = p.y_out + (size_t)(row0 + t) * p.Mtot;
+          if (n1 < p.Mtot) yr[n1] = a1[t] * a2s;
+          if (n2 < p.Mtot) yr[n2] = a2[t] * a2s;
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// gather_hl: the token-side operand of the decode tiles, in expert order.
+// Row r takes token permuted_src[r] / top_k.  A bf16 row becomes hi / lo
+// E4M3 rows 2r, 2r + 1 with their scale rows (one thread per 32-element
+// block); an MXFP8 row is copied to row r with its scales.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) {
+  const long r = blockIdx.x;
+  if (r >= __ldg(p.meta)) return;
+  const int tid = threadIdx.x;
+  const int K = p.K, nb = K / 32;
+  const long t = __ldg(p.permuted_src + r) / p.top_k;
+  if (p.act == 0) {
+    const uint4* xrow = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.x_bf16) + (size_t)t * K * 2);
+    uint4* hrow = reinterpret_cast<uint4*>(p.x + (size_t)(2 * r) * K);
+    uint4* lrow = reinterpret_cast<uint4*>(p.x + (size_t)(2 * r + 1) * K);
+    uint8_t* sh = p.xs + (size_t)(2 * r) * p.s_stride;
+    uint8_t* sl = sh + p.s_stride;
+    for (int b = tid; b < nb; b += 128) {
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = __ldg(xrow + 4 * b + q);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * q + 2 * j] = bf16_lo(u[j]);
+          v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
+        }
+      }
+      uint32_t hi[8], lo[8];
+      const uint32_t sb = split_hl32(v, hi, lo);
+      hrow[2 * b] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      hrow[2 * b + 1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+      lrow[2 * b] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      lrow[2 * b + 1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+      sh[tok_scale_byte(b)] = (uint8_t)(sb & 0xFFu);
+      sl[tok_scale_byte(b)] = (uint8_t)(sb >> 8);
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * K);
+    uint4* dst = reinterpret_cast<uint4*>(p.x + (size_t)r * K);
+    for (int i = tid; i < K / 16; i += 128) dst[i] = __ldg(src + i);
+    const uint8_t* ss = p.x_s + (size_t)t * nb;
+    uint8_t* sh = p.xs + (size_t)r * p.s_stride;
+    for (int b = tid; b < nb; b += 128) sh[tok_scale_byte(b)] = __ldg(ss + b);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+namespace {
+
+int sm_count_w() {
+  static int n[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && n[dev] > 0) return n[dev];
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+  if (dev < 64) n[dev] = v;
+  return v;
+}
+
+template <bool FC1, bool LO>
+cudaError_t launch_fcw_t(const FcwParams& p, const CUtensorMap* m, long max_tiles, cudaStream_t st) {
+  using C = CfgW<FC1, LO>;
+  static int set_for[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || set_for[dev] == 0) {
+    cudaError_t err =
+        cudaFuncSetAttribute(fcw_kernel<FC1, LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) set_for[dev] = 1;
+  }
+  const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
+  const long grid = items < sm_count_w() ? items : sm_count_w();
+  if (grid <= 0) return cudaSuccess;
+  fcw_kernel<FC1, LO><<<(unsigned)grid, kThreads, C::kSmem, st>>>(m[0], m[1], m[2], p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int fcw_token_tile() { return kTok; }
+int fcw_n_rows(bool fc1) { return fc1 ? kNH1 : kNH2; }
+int fcw_scale_stride(int K) { return K / 8; }   // 16 bytes per 128-element stage
+
+cudaError_t launch_gather_hl(const GatherHLParams& p, cudaStream_t st) {
+  if (p.S <= 0) return cudaSuccess;
+  gather_hl_kernel<<<(unsigned)p.S, 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S, int E_loc,
+                       bool fc1, bool lo, long max_tiles, cudaStream_t st) {
+  if (S <= 0) return cudaSuccess;
+  FcwParams q = p;
+  q.w = w;
+  CUtensorMap m[3];
+  const int ss = fcw_scale_stride(p.K);
+  const uint64_t rows = (uint64_t)S * (lo ? 2 : 1);   // token-side rows (hi, lo interleaved)
+  const uint32_t nb = (uint32_t)(lo ? 2 * kTok : kTok);
+  // weights: E2M1 [E_loc * Mtot, K] (K/2 bytes per row), boxes of 128 codes x
+  // the tile's rows, each 16 codes in a 16-byte slot, 128-byte swizzle
+  if (!make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, (uint64_t)p.K, (uint64_t)E_loc * p.Mtot,
+                (uint64_t)(p.K / 2), kBK, (uint32_t)fcw_n_rows(fc1), CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // token rows: E4M3 [rows, K], boxes of 128 bytes x the tile's rows,
+  // 128-byte swizzle; scale rows: [rows, ss] bytes, boxes of 16 bytes
+  if (!make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, x, (uint64_t)p.K, rows, (uint64_t)p.K, kBK, nb,
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, (uint64_t)ss, rows, (uint64_t)ss, 16, nb,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (fc1) return lo ? launch_fcw_t<true, true>(q, m, max_tiles, st) : launch_fcw_t<true, false>(q, m, max_tiles, st);
+  return lo ? launch_fcw_t<false, true>(q, m, max_tiles, st) : launch_fcw_t<false, false>(q, m, max_tiles, st);
+}
+
+}  // namespace situ

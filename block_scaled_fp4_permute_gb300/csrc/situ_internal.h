@@ -132,8 +132,13 @@ int fcq_n_rows(bool fc1);
 // one weight's packed scale blocks
 size_t fcq_act_scale_bytes(long max_tiles, int K);
 size_t fcq_packed_scale_bytes(int E_loc, int H, int I, bool fc1);
+// packed scale blocks for weight tiles of nh rows (FC1: nh gate rows then
+// their nh up rows, nh <= 128; FC2: nh <= 256 rows)
+size_t packed_scale_bytes(int E_loc, int H, int I, bool fc1, int nh);
 cudaError_t launch_pack_scales(const uint8_t* w_scale, int E_loc, int H, int I, bool fc1, uint8_t* out,
                                cudaStream_t st);
+cudaError_t launch_pack_scales_nh(const uint8_t* w_scale, int E_loc, int H, int I, bool fc1, int nh, uint8_t* out,
+                                  cudaStream_t st);
 cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint8_t* w, int E_loc, bool fc1,
                        long max_tiles, cudaStream_t st);
 
@@ -152,6 +157,49 @@ struct Gather8Params {
   uint8_t* xsp;
 };
 cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st);
+// Decode tiles on the block-scaled tensor cores (fc_bsd.cu): weights on
+// the MMA's M side, up to 16 expert-ordered token rows on N.  Token-side
+// rows are E4M3 [rows, K] with scale rows [rows, fcw_scale_stride(K)] bytes
+// (16 bytes per 128-element stage, its four UE8M0 bytes first); a bf16 row
+// r is the sum of the hi row 2r and the lo row 2r + 1 (lo = true), an MXFP8
+// row r is row r.  FC1 writes H1 in the same form for FC2.  The weight
+// scales are packed per weight tile: FC1 tiles of fcw_n_rows(true) gate
+// rows plus their up rows, FC2 tiles as the prefill GEMM's.
+struct GatherHLParams {
+  int act;                       // SITU_ACT_BF16 (hi + lo) or SITU_ACT_MXFP8 (hi)
+  const void* x_bf16;
+  const uint8_t* x_q;
+  const uint8_t* x_s;
+  const int32_t* permuted_src;
+  const int32_t* meta;           // meta[0] = R
+  int top_k, K;
+  long S;
+  uint8_t *x, *xs;
+  int s_stride;
+};
+cudaError_t launch_gather_hl(const GatherHLParams& p, cudaStream_t st);
+struct FcwParams {
+  int Mtot, K, I;
+  const uint8_t* w;              // packed E2M1 [E_loc, Mtot, K/2] (set by launch_fcw)
+  const uint8_t* wsp;            // packed weight scale blocks of this GEMM's weight tiles
+  const int32_t* offsets;
+  const int32_t* tile_offsets;
+  const int2* tile_info;
+  int E_loc, n_ntiles;
+  // FC1
+  const float *beta, *beta_lin, *alpha_g, *alpha_u;
+  uint8_t *h, *hs;               // H1 rows and scale rows, as the token side above
+  int hs_stride;
+  // FC2
+  const float* alpha2;
+  float* y_out;                  // fp32 [S, H]
+  int* err;                      // device status word
+};
+int fcw_token_tile();
+int fcw_n_rows(bool fc1);
+int fcw_scale_stride(int K);
+cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S, int E_loc,
+                       bool fc1, bool lo, long max_tiles, cudaStream_t st);
 size_t fcd_smem_bytes(int K, bool nvfp4);
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 

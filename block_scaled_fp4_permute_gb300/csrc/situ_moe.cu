@@ -23,7 +23,7 @@ bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
-  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, total;
+  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, total;
 };
 
 // Decode-like routings (about six or fewer rows per expert) take the
@@ -41,8 +41,43 @@ bool takes_decode_path(const situ_moe_args* a) {
 bool block_scaled_shapes(const situ_moe_args* a) {
   return a->weight_dtype == SITU_W_MXFP4 && a->H % 128 == 0 && a->I % 128 == 0;
 }
+// decode-like routings with bf16 or MXFP8 activations on MXFP4 weights of
+// those shapes: the block-scaled decode tiles (weights on the MMA M side)
+bool fcw_shapes(const situ_moe_args* a) {
+  return decode_like(a) && block_scaled_shapes(a) &&
+         (a->act_dtype == SITU_ACT_BF16 || a->act_dtype == SITU_ACT_MXFP8);
+}
 bool takes_block_scaled_path(const situ_moe_args* a) {
   return a->act_dtype == SITU_ACT_MXFP8 && block_scaled_shapes(a) && !takes_decode_path(a);
+}
+// packed weight scales: [FC1 prefill tiles | FC2 prefill tiles | FC1 decode
+// tiles | FC2 decode tiles]
+size_t packed_fc1_bytes(const situ_moe_args* a) {
+  return fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true);
+}
+size_t packed_fc2_bytes(const situ_moe_args* a) {
+  return fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, false);
+}
+size_t packed_fc1d_bytes(const situ_moe_args* a) {
+  return packed_scale_bytes(a->num_local_experts, a->H, a->I, true, fcw_n_rows(true));
+}
+size_t packed_fc2d_bytes(const situ_moe_args* a) {
+  return packed_scale_bytes(a->num_local_experts, a->H, a->I, false, fcw_n_rows(false));
+}
+size_t packed_total_bytes(const situ_moe_args* a) {
+  return packed_fc1_bytes(a) + packed_fc2_bytes(a) + packed_fc1d_bytes(a) + packed_fc2d_bytes(a);
+}
+// the four packings into one buffer (layout above)
+cudaError_t pack_all_scales(const situ_moe_args* a, uint8_t* dst, cudaStream_t st) {
+  const int E = a->num_local_experts;
+  cudaError_t e = launch_pack_scales(a->w1_scale, E, a->H, a->I, true, dst, st);
+  dst += packed_fc1_bytes(a);
+  if (e == cudaSuccess) e = launch_pack_scales(a->w2_scale, E, a->H, a->I, false, dst, st);
+  dst += packed_fc2_bytes(a);
+  if (e == cudaSuccess) e = launch_pack_scales_nh(a->w1_scale, E, a->H, a->I, true, fcw_n_rows(true), dst, st);
+  dst += packed_fc1d_bytes(a);
+  if (e == cudaSuccess) e = launch_pack_scales_nh(a->w2_scale, E, a->H, a->I, false, fcw_n_rows(false), dst, st);
+  return e;
 }
 long max_prefill_tiles(const situ_moe_args* a) {
   return (long)a->T * a->top_k / fcp_token_tile() + a->num_local_experts + 1;
@@ -75,10 +110,12 @@ Layout make_layout(const situ_moe_args* a) {
   const long tiles = max_prefill_tiles(a);
   L.xsp = take(bs ? fcq_act_scale_bytes(tiles, a->H) : 0);
   L.hsp = take(bs ? fcq_act_scale_bytes(tiles, a->I) : 0);
-  L.wsp = take(bs && !a->scales_packed
-                   ? fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true) +
-                         fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, false)
-                   : 0);
+  const bool w = fcw_shapes(a);
+  L.wsp = take((bs || w) && !a->scales_packed ? packed_total_bytes(a) : 0);
+  // decode tiles: hi / lo scale rows of the input and of H1 (the E4M3 rows
+  // reuse the x16 / h16 regions)
+  L.wxs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->H) : 0);
+  L.whs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->I) : 0);
   L.total = o;
   return L;
 }
@@ -210,8 +247,9 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   uint16_t* h1 = (uint16_t*)(ws + L.h1);
   float* y = (float*)(ws + L.y);
   const bool nv = a->weight_dtype == SITU_W_NVFP4;
-  const bool decode_path = takes_decode_path(a);
-  const int tile_n = decode_path ? kDecodeTileTokens : fcp_token_tile();
+  const bool fcw = fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2);
+  const bool decode_path = !fcw && takes_decode_path(a);
+  const int tile_n = fcw ? fcw_token_tile() : decode_path ? kDecodeTileTokens : fcp_token_tile();
   const long S = (long)a->T * a->top_k;
   const long max_tiles = S / tile_n + a->num_local_experts + 1;
   auto mark = [&](int i) {
@@ -225,7 +263,76 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   if (err != cudaSuccess) return SITU_ERR_CUDA;
   mark(1);
 
-  if (decode_path) {
+  // the packed weight scales of the block-scaled GEMMs: the caller's, or
+  // packed into the workspace by this call
+  auto packed_scales = [&](const uint8_t*& wsp1, const uint8_t*& wsp2, const uint8_t*& wsp3,
+                           const uint8_t*& wsp4) -> cudaError_t {
+    wsp1 = (const uint8_t*)a->scales_packed;
+    if (!wsp1) {
+      cudaError_t e2 = pack_all_scales(a, ws + L.wsp, st);
+      if (e2 != cudaSuccess) return e2;
+      wsp1 = ws + L.wsp;
+    }
+    wsp2 = wsp1 + packed_fc1_bytes(a);
+    wsp3 = wsp2 + packed_fc2_bytes(a);
+    wsp4 = wsp3 + packed_fc1d_bytes(a);
+    return cudaSuccess;
+  };
+
+  if (fcw) {
+    // 16-token tiles on the block-scaled tensor cores, weights on the MMA M
+    // side: token rows as E4M3 (bf16 as interleaved hi / lo rows), FC1
+    // (+SiTU) writing H1 in the same form, FC2
+    const uint8_t *wsp1, *wsp2, *wsp3, *wsp4;
+    if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
+    const bool lo = a->act_dtype == SITU_ACT_BF16;
+    GatherHLParams g;
+    g.act = a->act_dtype;
+    g.x_bf16 = a->hidden_states;
+    g.x_q = a->hidden_states_q;
+    g.x_s = a->hidden_states_scale;
+    g.permuted_src = psrc;
+    g.meta = meta;
+    g.top_k = a->top_k;
+    g.K = a->H;
+    g.S = S;
+    g.x = ws + L.x16;
+    g.xs = ws + L.wxs;
+    g.s_stride = fcw_scale_stride(a->H);
+    if ((err = launch_gather_hl(g, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(2);
+    FcwParams w;
+    std::memset(&w, 0, sizeof(w));
+    w.offsets = offsets;
+    w.tile_offsets = tile_offsets;
+    w.tile_info = tile_info;
+    w.E_loc = a->num_local_experts;
+    w.I = a->I;
+    w.err = meta + 2;
+    w.wsp = wsp3;
+    w.Mtot = 2 * a->I;
+    w.K = a->H;
+    w.n_ntiles = (a->I + fcw_n_rows(true) - 1) / fcw_n_rows(true);
+    w.beta = a->gemm1_alpha;
+    w.beta_lin = a->gemm1_beta;
+    w.alpha_g = a->g1_alphas;
+    w.alpha_u = a->g1_alphas_up;
+    w.h = ws + L.h16;
+    w.hs = ws + L.whs;
+    w.hs_stride = fcw_scale_stride(a->I);
+    if ((err = launch_fcw(w, a->w1, g.x, g.xs, S, a->num_local_experts, true, lo, max_tiles, st)) != cudaSuccess)
+      return SITU_ERR_CUDA;
+    mark(3);
+    w.wsp = wsp4;
+    w.Mtot = a->H;
+    w.K = a->I;
+    w.n_ntiles = (a->H + fcw_n_rows(false) - 1) / fcw_n_rows(false);
+    w.alpha2 = a->g2_alphas;
+    w.y_out = y;
+    if ((err = launch_fcw(w, a->w2, w.h, w.hs, S, a->num_local_experts, false, lo, max_tiles, st)) != cudaSuccess)
+      return SITU_ERR_CUDA;
+    mark(4);
+  } else if (decode_path) {
     // 8-token tiles: rows are converted once to f16 block rows, then FC1
     // (+SiTU, writing H1 as f16 block rows) and FC2
     Gather16Params g16;
@@ -289,18 +396,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     // w4a8 on the block-scaled tensor cores: MXFP8 rows copied into expert
     // order with their tile scale blocks, FC1 (+SiTU) writing H1 as MXFP8,
     // FC2 reading it as it stands
-    const uint8_t* wsp1 = (const uint8_t*)a->scales_packed;
-    if (!wsp1) {
-      uint8_t* dst = ws + L.wsp;
-      if ((err = launch_pack_scales(a->w1_scale, a->num_local_experts, a->H, a->I, true, dst, st)) !=
-              cudaSuccess ||
-          (err = launch_pack_scales(a->w2_scale, a->num_local_experts, a->H, a->I, false,
-                                    dst + fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true),
-                                    st)) != cudaSuccess)
-        return SITU_ERR_CUDA;
-      wsp1 = dst;
-    }
-    const uint8_t* wsp2 = wsp1 + fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true);
+    const uint8_t *wsp1, *wsp2, *wsp3, *wsp4;
+    if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
     Gather8Params g8;
     g8.x_q = a->hidden_states_q;
     g8.x_s = a->hidden_states_scale;
@@ -443,8 +540,7 @@ situ_status situ_moe_forward_profiled(const situ_moe_args* a, void* workspace,
 
 size_t situ_moe_packed_scales_size(const situ_moe_args* a) {
   if (!a || a->H <= 0 || a->I <= 0 || a->num_local_experts < 1 || !block_scaled_shapes(a)) return 0;
-  return fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true) +
-         fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, false);
+  return packed_total_bytes(a);
 }
 
 situ_status situ_moe_pack_scales(const situ_moe_args* a, void* packed, size_t packed_bytes, void* stream) {
@@ -454,14 +550,8 @@ situ_status situ_moe_pack_scales(const situ_moe_args* a, void* packed, size_t pa
   if (!block_scaled_shapes(a)) return SITU_ERR_UNSUPPORTED;
   if (!a->w1_scale || !a->w2_scale) return SITU_ERR_NULL_ARG;
   if (!aligned16(packed)) return SITU_ERR_MISALIGNED;
-  const size_t b1 = fcq_packed_scale_bytes(a->num_local_experts, a->H, a->I, true);
   if (packed_bytes < situ_moe_packed_scales_size(a)) return SITU_ERR_WORKSPACE_TOO_SMALL;
-  cudaStream_t st = (cudaStream_t)stream;
-  uint8_t* out = (uint8_t*)packed;
-  if (launch_pack_scales(a->w1_scale, a->num_local_experts, a->H, a->I, true, out, st) != cudaSuccess ||
-      launch_pack_scales(a->w2_scale, a->num_local_experts, a->H, a->I, false, out + b1, st) != cudaSuccess)
-    return SITU_ERR_CUDA;
-  return SITU_OK;
+  return cuda_status(pack_all_scales(a, (uint8_t*)packed, (cudaStream_t)stream));
 }
 
 situ_status situ_moe_device_status(const situ_moe_args* a, const void* workspace, void* stream,

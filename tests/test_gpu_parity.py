@@ -183,6 +183,34 @@ def test_decode_w4a8():
     assert_parity(out, oracle_out(wl), "decode w4a8")
 
 
+@pytest.mark.parametrize("over,hot", [
+    # a hot expert (six 16-token tiles), partial last weight tiles of FC1 (I=128: 96 + 32 rows)
+    # and FC2 (H=256: 224 + 32 rows)
+    (dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, params="k3_random"), 3),
+    (dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_MXFP8,
+          params="k3_random"), 3),
+    # a filtered shard, three 128-element stages in FC2
+    (dict(T=24, H=384, I=384, E_total=32, E_loc=8, off=8, K=4, params="k3_random"), None),
+    (dict(T=40, H=512, I=256, E_total=64, E_loc=64, off=0, K=8, act=W.ACT_MXFP8,
+          params="k3_random"), None),
+])
+def test_decode_tile_shapes(over, hot):
+    """Decode-sized routings on the block-scaled decode tiles (16 tokens,
+    weights on the MMA's M side), with the weight scales packed once and
+    packed inside every call."""
+    wl = W.make("tiny", device="cuda", **over)
+    if hot is not None:
+        wl.topk_ids[:, 0] = hot
+    layer, out = run_layer(wl)
+    assert layer.device_status() == 0
+    assert_parity(out, oracle_out(wl), str(over))
+    per_call = binding.Layer(wl, pack_scales=False)
+    out2 = per_call()
+    torch.cuda.synchronize()
+    assert per_call.device_status() == 0
+    assert np.array_equal(out2.float().cpu().numpy(), out)
+
+
 def test_prefill_w4a8_subset():
     wl = wl_("prefill_w4a8")
     layer, out = run_layer(wl)

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             l.situ_moe_packed_scales_size.argtypes = [ctypes.POINTER(SituMoeArgs)]
             l.situ_moe_pack_scales.restype = ctypes.c_int
             l.situ_moe_pack_scales.argtypes = [ctypes.POINTER(SituMoeArgs), vp, sz, vp]
+            l.situ_moe_forward_launches.restype = ctypes.c_int32
+            l.situ_moe_forward_launches.argtypes = [ctypes.POINTER(SituMoeArgs)]
             l.situ_moe_device_status.restype = ctypes.c_int
             l.situ_moe_device_status.argtypes = [ctypes.POINTER(SituMoeArgs), vp, vp,
                                                  ctypes.POINTER(ctypes.c_int32)]
@@ -198,6 +200,11 @@ def situ_moe_pack_scales(args: SituMoeArgs, packed: torch.Tensor, stream=None) -
         ctypes.byref(args), _p(packed), packed.numel() * packed.element_size(), _stream(stream)))
 
 
+def situ_moe_forward_launches(args: SituMoeArgs) -> int:
+    """Kernels situ_moe_forward enqueues for ``args`` (-1: invalid)."""
+    return lib().situ_moe_forward_launches(ctypes.byref(args))
+
+
 def situ_moe_forward(args: SituMoeArgs, workspace: torch.Tensor, stream=None) -> None:
     _check("situ_moe_forward", lib().situ_moe_forward(
         ctypes.byref(args), _p(workspace), workspace.numel() * workspace.element_size(),
@@ -270,6 +277,11 @@ class Layer:
             self.args.scales_packed = self.scales_packed.data_ptr()
         n = situ_moe_workspace_size(self.args)
         self.workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+
+    def launches(self) -> int:
+        """Kernels one __call__ enqueues (the forward, plus the MXFP8
+        quantisation for w4a8)."""
+        return situ_moe_forward_launches(self.args) + (1 if self.wl.act == SITU_ACT_MXFP8 else 0)
 
     def device_status(self, stream=None) -> int:
         """0 when every bounded device wait of the last call completed."""

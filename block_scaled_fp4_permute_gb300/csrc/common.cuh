@@ -13,6 +13,17 @@ namespace situ {
 
 constexpr int kWarp = 32;
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start while its predecessor on the
+// stream is still running; griddep_wait blocks until the predecessor has
+// completed and its writes are visible (a no-op for a normal launch), and
+// griddep_launch_dependents lets the successor start launching once every
+// CTA of this grid has issued it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

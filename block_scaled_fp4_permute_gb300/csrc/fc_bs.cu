@@ -459,8 +459,6 @@ cudaError_t launch_fcq_t(const FcqParams& p, const CUtensorMap& a, const CUtenso
   return cudaGetLastError();
 }
 
-int n_tiles_of(int rows, bool fc1) { return (rows + fcq_n_rows(fc1) - 1) / fcq_n_rows(fc1); }
-
 }  // namespace
 
 int fcq_n_rows(bool fc1) { return fc1 ? Cfg<true>::NH : Cfg<false>::NH; }

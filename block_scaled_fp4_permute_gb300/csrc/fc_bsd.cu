@@ -188,9 +188,6 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const long total = (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
-  if ((long)blockIdx.x >= total) return;
-  if (*reinterpret_cast<volatile int*>(p.err) != 0) return;
   const int nk = p.K / kBK;
 
   const uint32_t sbase = saddr(smem);
@@ -224,8 +221,18 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tm_holder;
+  // the set-up above may overlap the predecessor's tail; everything below
+  // reads its outputs
+  griddep_launch_dependents();
+  griddep_wait();
+  // an earlier CTA that timed out leaves no work (total = 0)
+  const long total = *reinterpret_cast<volatile int*>(p.err) != 0
+                         ? 0
+                         : (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
 
-  if (warp == 4) {
+  if ((long)blockIdx.x >= total) {
+    // no item for this CTA
+  } else if (warp == 4) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       long it = 0;
@@ -408,6 +415,8 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // the permute's outputs
   const long r = blockIdx.x;
   if (r >= __ldg(p.meta)) return;
   const int tid = threadIdx.x;
@@ -482,8 +491,8 @@ cudaError_t launch_fcw_t(const FcwParams& p, const CUtensorMap* m, long max_tile
   const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
   const long grid = items < sm_count_w() ? items : sm_count_w();
   if (grid <= 0) return cudaSuccess;
-  fcw_kernel<FC1, LO><<<(unsigned)grid, kThreads, C::kSmem, st>>>(m[0], m[1], m[2], p);
-  return cudaGetLastError();
+  return launch_pdl(fcw_kernel<FC1, LO>, dim3((unsigned)grid), dim3(kThreads), (size_t)C::kSmem, st, m[0], m[1], m[2],
+                    p);
 }
 
 }  // namespace
@@ -494,8 +503,7 @@ int fcw_scale_stride(int K) { return K / 8; }   // 16 bytes per 128-element stag
 
 cudaError_t launch_gather_hl(const GatherHLParams& p, cudaStream_t st) {
   if (p.S <= 0) return cudaSuccess;
-  gather_hl_kernel<<<(unsigned)p.S, 128, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gather_hl_kernel, dim3((unsigned)p.S), dim3(128), 0, st, p);
 }
 
 cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S, int E_loc,

@@ -307,6 +307,11 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
   return cudaGetLastError();
 }
 
+int permute_launches(int T, int K, int E_loc) {
+  const long S = (long)T * K;
+  return (S <= kPermChunk && E_loc <= kSmallMaxExperts) ? 1 : 3;
+}
+
 size_t permute_scratch_bytes(int T, int K, int E_loc) {
   long S = (long)T * K;
   long nblk = (S + kPermChunk - 1) / kPermChunk;

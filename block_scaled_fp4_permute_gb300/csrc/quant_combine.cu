@@ -54,6 +54,7 @@ cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t*
 __global__ void __launch_bounds__(256)
 combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
                const float* __restrict__ w, int K, int H4, uint2* __restrict__ out) {
+  griddep_wait();   // Y is the predecessor's output
   const int t = blockIdx.x;
   const int h4 = blockIdx.y * blockDim.x + threadIdx.x;
   if (h4 >= H4) return;
@@ -89,8 +90,7 @@ cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const floa
                            int H, void* out, cudaStream_t st) {
   const int H4 = H / 4;
   dim3 grid(T, (H4 + 255) / 256);
-  combine_kernel<<<grid, 256, 0, st>>>((const float4*)y, slot_to_row, w, K, H4, (uint2*)out);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, st, (const float4*)y, slot_to_row, w, K, H4, (uint2*)out);
 }
 
 }  // namespace situ

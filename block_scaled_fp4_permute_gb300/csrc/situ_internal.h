@@ -11,6 +11,23 @@ namespace situ {
 
 constexpr int kPermChunk = 4096;   // routing slots per permute block
 
+// Launches kernel k with the programmatic stream-serialisation attribute
+// (see griddep_wait): its prologue may overlap the predecessor's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 // tile_offsets / tile_info / meta may be null (the standalone permute).
 // tile_info[t] = (local expert, first expert-ordered row) of GEMM token tile t.
 cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off, int tile_n,
@@ -18,6 +35,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
                            int2* tile_info, int32_t* permuted_src, int32_t* slot_to_row,
                            int32_t* meta, int32_t* blk_counts, cudaStream_t st);
 size_t permute_scratch_bytes(int T, int K, int E_loc);
+int permute_launches(int T, int K, int E_loc);   // kernels launch_permute enqueues
 
 cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t* s,
                                cudaStream_t st);

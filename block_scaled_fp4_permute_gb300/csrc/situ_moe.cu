@@ -554,6 +554,17 @@ situ_status situ_moe_pack_scales(const situ_moe_args* a, void* packed, size_t pa
   return cuda_status(pack_all_scales(a, (uint8_t*)packed, (cudaStream_t)stream));
 }
 
+int32_t situ_moe_forward_launches(const situ_moe_args* a) {
+  if (validate(a) != SITU_OK) return -1;
+  if (a->T == 0) return 0;
+  const int perm = permute_launches(a->T, a->top_k, a->num_local_experts);
+  const int pack = a->scales_packed ? 0 : 4;
+  if (fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
+  if (takes_decode_path(a)) return perm + 4;
+  if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
+  return perm + 5;
+}
+
 situ_status situ_moe_device_status(const situ_moe_args* a, const void* workspace, void* stream,
                                    int32_t* code) {
   if (code) *code = 0;

@@ -275,16 +275,27 @@ situ_status situ_moe_device_status(const situ_moe_args* args, const void* worksp
                                    int32_t* code);
 
 /* ------------------------------------------------------------------------
+ * situ_moe_forward_launches -- the number of kernels situ_moe_forward
+ * enqueues for these arguments (0 for T = 0, -1 when validation fails),
+ * e.g. to size a CUDA graph or to count device work.  Host-only; the pages
+ * define no counterpart.
+ * --------------------------------------------------------------------- */
+int32_t situ_moe_forward_launches(const situ_moe_args* args);
+
+/* ------------------------------------------------------------------------
  * situ_moe_packed_scales_size / situ_moe_pack_scales -- the MXFP4 weight
  * scales rearranged for the block-scaled tensor-core GEMMs.
  *
- * The MXFP8 x MXFP4 (w4a8) prefill path reads each GEMM stage's weight
- * scales as contiguous blocks: per (local expert, N tile of weight rows,
- * 128 elements of K) the UE8M0 bytes of the tile's rows, laid out as the
- * tensor memory copy expects.  Packing depends only on w1_scale, w2_scale,
+ * The block-scaled GEMMs (the w4a8 prefill tiles, and the decode tiles of
+ * bf16 and MXFP8 activations) read each stage's weight scales as contiguous
+ * blocks: per (local expert, weight tile, 128 elements of K) the UE8M0
+ * bytes of the tile's rows, laid out as the tensor memory copy expects.
+ * The buffer holds four such packings (the prefill and the decode tiles of
+ * FC1 and of FC2).  Packing depends only on w1_scale, w2_scale,
  * num_local_experts, H and I, so it is done once per weight set; pass the
  * result as args->scales_packed.  Without it the forward packs into its
- * workspace on every call (same result, a little more HBM traffic).
+ * workspace on every call (same result, about 25% more HBM traffic for a
+ * decode step).
  * The size is 0 (and pack_scales returns UNSUPPORTED) unless weight_dtype
  * is MXFP4 and H and I are multiples of 128.  `packed` is a device buffer
  * of at least that many bytes, 16-byte aligned, owned by the caller;

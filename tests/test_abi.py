@@ -141,3 +141,22 @@ def test_permute_and_quant_validation(lib):
 def test_status_strings(lib):
     for s in range(7):
         assert binding.status_string(s).startswith("SITU_")
+
+
+def test_forward_launch_count(lib):
+    n = lambda a: lib.situ_moe_forward_launches(ctypes.byref(a))
+    # H, I not multiples of 128: decode-tile register path, one permute launch
+    assert n(_args()) == 5
+    # block-scaled decode tiles: permute, gather, FC1, FC2, combine, plus four
+    # scale packings when the caller keeps no packed scales
+    assert n(_args(H=256, I=128)) == 9
+    packed = _args(H=256, I=128)
+    packed.scales_packed = 0x4000
+    assert n(packed) == 5
+    # prefill routing (bf16): permute (one block), gather, FC1, H1 gather, FC2, combine
+    assert n(_args(T=400, H=64, I=32)) == 6
+    assert n(_args(T=0)) == 0
+    bad = _args()
+    bad.gemm1_alpha = None
+    assert n(bad) == -1
+    assert lib.situ_moe_forward_launches(None) == -1

@@ -46,6 +46,9 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -53,6 +56,21 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak(wl):
+    """(TFLOP/s, source) of the MMA kind the layer's GEMMs use: MXFP8 x MXFP4
+    block-scaled for w4a8 (the measured bf16 GEMM burst peak times the
+    nominal fp8 : bf16 ratio of 2), bf16 for the others."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    bf16, src = FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
+    if os.path.exists(p):
+        with open(p) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        src = "measured bf16_tflops (MEASURED_PEAKS.json)"
+    if wl.act == 1:
+        return 2.0 * bf16, src + " x 2 (nominal fp8 : bf16 ratio)"
+    return bf16, src
 
 
 def routing_stats(wl):
@@ -351,12 +369,25 @@ def run_ours(args):
     if os.path.exists(tpath):
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
-    roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["gbs"], "peak": hbm,
-            "unit": "GB/s", "frac": stages[dom]["frac_hbm"], "traffic": traffic,
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6.8 TB/s"}
+    # the bound of the dominant kernel and of the layer: the larger of the
+    # HBM time of its algorithmic bytes and the tensor time of its FLOPs
+    tc_peak, tc_src = tensor_peak(wl)
+    kflops = {"fc1": 2.0 * R * wl.H * 2 * wl.I, "fc2": 2.0 * R * wl.I * wl.H}
+    kf = kflops.get(dom, 0.0)
+    hbm_src = (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+               else "fallback 6.8 TB/s")
+    if kf / (tc_peak * 1e12) > nbytes[dom] / (hbm * 1e9):
+        ach = kf / (stages[dom]["ms"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": ach / tc_peak, "traffic": traffic, "peak_source": tc_src}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["gbs"], "peak": hbm,
+                "unit": "GB/s", "frac": stages[dom]["frac_hbm"], "traffic": traffic,
+                "peak_source": hbm_src}
     layer_gbs = nbytes["layer"] / (ms * 1e-3) / 1e9
     flops = layer_flops(wl, R)
+    t_hbm = nbytes["layer"] / (hbm * 1e9)
+    t_tc = flops / (tc_peak * 1e12)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -370,7 +401,10 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": ws * wl.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        # operand types of the GEMMs: E2M1 weights x E4M3 rows (bf16 rows as
+        # hi + lo pairs) on the block-scaled tensor cores, else f16 operands
+        "dtype": "e2m1*e4m3->f32" if args.workload in ("decode", "prefill_w4a8", "tiny") else "f16->f32",
         "data": "synthetic (seeded; weights N(0,0.02) packed to the block-scaled format)",
         "config": {"workload": WORKLOAD_NAMES[args.workload], "T": wl.T, "H": wl.H, "I": wl.I,
                    "E_total": wl.E_total, "E_loc": wl.E_loc, "offset": wl.off, "top_k": wl.K,
@@ -378,9 +412,11 @@ def run_ours(args):
                    "l2": "flushed between steps (256 MiB write, outside the step events)",
                    "parallelism": f"replicas x{ws}, no collective"},
         "roofline": roof,
-        "layer_roofline": {"bound": "hbm", "alg_bytes": int(nbytes["layer"]), "achieved": layer_gbs,
-                           "peak": hbm, "unit": "GB/s", "frac": layer_gbs / hbm,
-                           "tflops": flops / (ms * 1e-3) / 1e12},
+        "layer_roofline": {"bound": "tensor" if t_tc > t_hbm else "hbm", "alg_bytes": int(nbytes["layer"]),
+                           "flops": flops, "roofline_ms": max(t_hbm, t_tc) * 1e3,
+                           "frac": max(t_hbm, t_tc) / (ms * 1e-3),
+                           "gbs": layer_gbs, "frac_hbm": layer_gbs / hbm,
+                           "tflops": flops / (ms * 1e-3) / 1e12, "tensor_peak_tflops": tc_peak},
         "stages": stages,
         "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

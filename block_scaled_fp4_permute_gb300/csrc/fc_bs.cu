@@ -54,17 +54,20 @@ constexpr int kBK = 128;         // K elements per stage
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 constexpr int kSfBlock = 512;    // one scale block: 128 rows x 4 K blocks
-constexpr int kSfColsPerStage = 12;
-
-template <bool FC1>
+// LO: bf16 token rows as hi + lo MXFP8 rows (split_hl32), two A tiles per
+// stage and two MMAs per K block into the same accumulator.
+template <bool FC1, bool LO>
 struct Cfg {
   static constexpr int BN = FC1 ? 192 : 224;        // MMA N
   static constexpr int NH = FC1 ? BN / 2 : BN;      // rows per weight box
-  static constexpr int kStages = FC1 ? 5 : 4;
-  static constexpr int kABytes = kBM * kBK;         // 16 KB of E4M3
+  static constexpr int kNA = LO ? 2 : 1;            // A tiles per stage
+  static constexpr int kStages = LO ? 3 : (FC1 ? 5 : 4);
+  static constexpr int kATile = kBM * kBK;          // 16 KB of E4M3
+  static constexpr int kABytes = kNA * kATile;
   static constexpr int kBBytes = BN * kBK;          // E2M1 in 16-byte slots of 16 codes
   static constexpr int kBTx = BN * kBK / 2;         // bytes the weight loads transfer (packed)
-  static constexpr int kSfBytes = 3 * kSfBlock;     // A block, B rows 0..127, B rows 128..255
+  static constexpr int kSfBytes = (kNA + 2) * kSfBlock;   // A block(s), B rows 0..127, B rows 128..255
+  static constexpr int kSfColsPerStage = 4 * (kNA + 2);
   static constexpr int kTx = kABytes + kBTx + kSfBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -132,10 +135,12 @@ __device__ __forceinline__ uint32_t sf_offset(int r, int kb) {
 
 }  // namespace
 
-template <bool FC1>
+template <bool FC1, bool LO>
 __global__ void __launch_bounds__(kThreads, 1)
-fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const FcqParams p) {
-  using C = Cfg<FC1>;
+fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
+           const __grid_constant__ CUtensorMap tmB, const FcqParams p) {
+  using C = Cfg<FC1, LO>;
+  constexpr int kSfColsPerStage = C::kSfColsPerStage;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -189,6 +194,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const int e = ti.x, row0 = ti.y;
         const int wrow = e * p.Mtot + ntile * C::NH;
         const uint8_t* xsb = p.xsp + (size_t)tile * nk * kSfBlock;
+        const uint8_t* xsb_lo = LO ? p.xsp_lo + (size_t)tile * nk * kSfBlock : nullptr;
         const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + ntile) * nk * (2 * kSfBlock);
         for (int kk = 0; kk < nk; ++kk, ++it) {
           const int s = (int)(it % kStages);
@@ -201,10 +207,12 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           const uint32_t b_smem = sbase + C::kOffB + s * C::kBBytes;
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
           tma_load_2d(sbase + C::kOffA + s * C::kABytes, &tmA, kk * kBK, row0, full(s));
+          if (LO) tma_load_2d(sbase + C::kOffA + s * C::kABytes + C::kATile, &tmAl, kk * kBK, row0, full(s));
           tma_load_2d(b_smem, &tmB, kk * kBK, wrow, full(s));
           if (FC1) tma_load_2d(b_smem + C::NH * kBK, &tmB, kk * kBK, wrow + p.I, full(s));
           bulk_load(sf_smem, xsb + (size_t)kk * kSfBlock, kSfBlock, full(s));
-          bulk_load(sf_smem + kSfBlock, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
+          if (LO) bulk_load(sf_smem + kSfBlock, xsb_lo + (size_t)kk * kSfBlock, kSfBlock, full(s));
+          bulk_load(sf_smem + C::kNA * kSfBlock, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
         }
       }
       // unwind: the loads of the last stages may still be landing
@@ -231,16 +239,20 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
           const uint32_t sfa = tmem + (uint32_t)(C::kSfCol0 + s * kSfColsPerStage);
-          const uint32_t sfb = sfa + 4;
+          const uint32_t sfb = sfa + 4 * C::kNA;
           tmem_cp_sf(sfa, sf_desc(sf_smem));
-          tmem_cp_sf(sfb, sf_desc(sf_smem + kSfBlock));
-          tmem_cp_sf(sfb + 4, sf_desc(sf_smem + 2 * kSfBlock));
+          if (LO) tmem_cp_sf(sfa + 4, sf_desc(sf_smem + kSfBlock));
+          tmem_cp_sf(sfb, sf_desc(sf_smem + C::kNA * kSfBlock));
+          tmem_cp_sf(sfb + 4, sf_desc(sf_smem + (C::kNA + 1) * kSfBlock));
           const uint64_t ad = sdesc(sbase + C::kOffA + s * C::kABytes);
           const uint64_t bd = sdesc(sbase + C::kOffB + s * C::kBBytes);
 #pragma unroll
-          for (uint32_t k4 = 0; k4 < kBK / 32; ++k4)   // +32 bytes along K per instruction
-            mma_bs(d, ad + 2 * k4, bd + 2 * k4, C::kIdesc | (k4 << 4) | (k4 << 29), sfa, sfb,
-                   (kk | (int)k4) != 0);
+          for (uint32_t k4 = 0; k4 < kBK / 32; ++k4) {   // +32 bytes along K per instruction
+            const uint32_t idesc = C::kIdesc | (k4 << 4) | (k4 << 29);
+            mma_bs(d, ad + 2 * k4, bd + 2 * k4, idesc, sfa, sfb, (kk | (int)k4) != 0);
+            // the lo rows of the same tokens add into the same accumulator
+            if (LO) mma_bs(d, ad + (uint64_t)(C::kATile >> 4) + 2 * k4, bd + 2 * k4, idesc, sfa + 4, sfb, 1u);
+          }
           mma_commit(empty(s));
         }
         if (!ok) break;
@@ -289,21 +301,34 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             v[j] = situ_f(gt[j] * ag, up[j] * au, bt, btl);
+            if (LO) v[j] = bf16_lo(f32x2_to_bf16x2(v[j], 0.f));   // w4a16: H1 is bf16
             amax = fmaxf(amax, fabsf(v[j]));
           }
-          // MXFP8 of the 32-element block: the smallest e with amax * 2^-e <= 448
-          const int ex = mxfp8_exponent(amax);
-          const float sc = exp2i(-ex);
+          const int b = i0 / 32;   // K block of FC2
+          const size_t sfo = ((size_t)tile * nkh + b / 4) * kSfBlock + sf_offset(m, b & 3);
           uint32_t qv[8];
+          if (LO) {
+            // bf16 H1 as FC2's hi / lo rows
+            uint32_t ql[8];
+            const uint32_t sb = split_hl32(v, qv, ql);
+            uint4* dl = reinterpret_cast<uint4*>(p.hq_lo + row * p.hq_stride + i0);
+            dl[0] = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+            dl[1] = make_uint4(ql[4], ql[5], ql[6], ql[7]);
+            p.hsp[sfo] = (uint8_t)(sb & 0xFFu);
+            p.hsp_lo[sfo] = (uint8_t)(sb >> 8);
+          } else {
+            // MXFP8 of the 32-element block: the smallest e with amax * 2^-e <= 448
+            const int ex = mxfp8_exponent(amax);
+            const float sc = exp2i(-ex);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            qv[j] = f32x2_to_e4m3x2(v[4 * j] * sc, v[4 * j + 1] * sc) |
-                    (f32x2_to_e4m3x2(v[4 * j + 2] * sc, v[4 * j + 3] * sc) << 16);
+            for (int j = 0; j < 8; ++j)
+              qv[j] = f32x2_to_e4m3x2(v[4 * j] * sc, v[4 * j + 1] * sc) |
+                      (f32x2_to_e4m3x2(v[4 * j + 2] * sc, v[4 * j + 3] * sc) << 16);
+            p.hsp[sfo] = (uint8_t)(ex + 127);
+          }
           uint4* dst = reinterpret_cast<uint4*>(p.hq + row * p.hq_stride + i0);
           dst[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
           dst[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
-          const int b = i0 / 32;   // K block of FC2
-          p.hsp[((size_t)tile * nkh + b / 4) * kSfBlock + sf_offset(m, b & 3)] = (uint8_t)(ex + 127);
         }
       } else {
         const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
@@ -361,6 +386,47 @@ __global__ void __launch_bounds__(256) gather8_kernel(const Gather8Params p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = p.K, n16 = K / 16, nsb = K / 32, nk = K / kBK;
   uint8_t* blocks = p.xsp + (size_t)tile * nk * kSfBlock;
+  if (p.x_bf16) {
+    // bf16 rows: hi / lo E4M3 rows (split_hl32), one lane per 32-element block
+    uint8_t* blocks_lo = p.xsp_lo + (size_t)tile * nk * kSfBlock;
+    for (int m = warp; m < kBM; m += 8) {
+      if (m < nrows) {
+        const long r = row0 + m;
+        const long t = __ldg(p.permuted_src + r) / p.top_k;
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.x_bf16) + (size_t)t * K * 2);
+        uint4* dh = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
+        uint4* dl = reinterpret_cast<uint4*>(p.x8_lo + (size_t)r * K);
+        for (int b = lane; b < nsb; b += 32) {
+          float v[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = __ldg(src + 4 * b + q);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              v[8 * q + 2 * j] = bf16_lo(u[j]);
+              v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
+            }
+          }
+          uint32_t hi[8], lo[8];
+          const uint32_t sb = split_hl32(v, hi, lo);
+          dh[2 * b] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          dh[2 * b + 1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+          dl[2 * b] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          dl[2 * b + 1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+          const size_t o = (size_t)(b / 4) * kSfBlock + sf_offset(m, b & 3);
+          blocks[o] = (uint8_t)(sb & 0xFFu);
+          blocks_lo[o] = (uint8_t)(sb >> 8);
+        }
+      } else {
+        for (int kk = lane; kk < nk; kk += 32) {
+          *reinterpret_cast<uint32_t*>(blocks + (size_t)kk * kSfBlock + sf_offset(m, 0)) = 0u;
+          *reinterpret_cast<uint32_t*>(blocks_lo + (size_t)kk * kSfBlock + sf_offset(m, 0)) = 0u;
+        }
+      }
+    }
+    return;
+  }
   for (int m = warp; m < kBM; m += 8) {
     if (m < nrows) {
       const long r = row0 + m;
@@ -439,29 +505,29 @@ int sm_count() {
   return v;
 }
 
-template <bool FC1>
-cudaError_t launch_fcq_t(const FcqParams& p, const CUtensorMap& a, const CUtensorMap& b, long max_tiles,
-                         cudaStream_t st) {
-  using C = Cfg<FC1>;
+template <bool FC1, bool LO>
+cudaError_t launch_fcq_t(const FcqParams& p, const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b,
+                         long max_tiles, cudaStream_t st) {
+  using C = Cfg<FC1, LO>;
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || set_for[dev] == 0) {
     cudaError_t err =
-        cudaFuncSetAttribute(fcq_kernel<FC1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(fcq_kernel<FC1, LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (err != cudaSuccess) return err;
     if (dev < 64) set_for[dev] = 1;
   }
   const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
   const long grid = items < sm_count() ? items : sm_count();
   if (grid <= 0) return cudaSuccess;
-  fcq_kernel<FC1><<<(unsigned)grid, kThreads, C::kSmem, st>>>(a, b, p);
+  fcq_kernel<FC1, LO><<<(unsigned)grid, kThreads, C::kSmem, st>>>(a, al, b, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int fcq_n_rows(bool fc1) { return fc1 ? Cfg<true>::NH : Cfg<false>::NH; }
+int fcq_n_rows(bool fc1) { return fc1 ? Cfg<true, false>::NH : Cfg<false, false>::NH; }
 
 bool fcq_supported(int H, int I, const void* w1, const void* w2) {
   // the 4-bit tensor-map type wants rows of a multiple of 128 codes and a
@@ -505,12 +571,16 @@ cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint8_t* w, int E_loc, bool fc1,
-                       long max_tiles, cudaStream_t st) {
-  CUtensorMap ma, mb;
+cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, const uint8_t* xq_lo, long S, const uint8_t* w,
+                       int E_loc, bool fc1, long max_tiles, cudaStream_t st) {
+  const bool lo = xq_lo != nullptr;
+  CUtensorMap ma, mal, mb;
   // activations: E4M3 [S, K], boxes of 128 bytes x 128 rows, 128-byte swizzle
+  // (the lo rows of bf16 activations likewise)
   if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)p.K, (uint64_t)S, (uint64_t)p.K, kBK, kBM,
-                CU_TENSOR_MAP_SWIZZLE_128B))
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mal, CU_TENSOR_MAP_DATA_TYPE_UINT8, lo ? xq_lo : xq, (uint64_t)p.K, (uint64_t)S, (uint64_t)p.K, kBK,
+                kBM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // weights: E2M1 [E_loc * Mtot, K] (K/2 bytes per row), boxes of 128 codes x
   // NH rows, each 16 codes landing in a 16-byte slot, 128-byte swizzle
@@ -518,7 +588,11 @@ cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint
   if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, (uint64_t)p.K, (uint64_t)E_loc * p.Mtot,
                 (uint64_t)(p.K / 2), kBK, nh, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  return fc1 ? launch_fcq_t<true>(p, ma, mb, max_tiles, st) : launch_fcq_t<false>(p, ma, mb, max_tiles, st);
+  if (fc1)
+    return lo ? launch_fcq_t<true, true>(p, ma, mal, mb, max_tiles, st)
+              : launch_fcq_t<true, false>(p, ma, mal, mb, max_tiles, st);
+  return lo ? launch_fcq_t<false, true>(p, ma, mal, mb, max_tiles, st)
+            : launch_fcq_t<false, false>(p, ma, mal, mb, max_tiles, st);
 }
 
 }  // namespace situ

@@ -145,33 +145,6 @@ __device__ __forceinline__ uint32_t split_hl(float v, int e, int c, uint32_t& lo
   return h;
 }
 
-// The same for a whole block of 32 values in one thread: codes to hi[0..7],
-// lo[0..7] (four per word, element 4j + u in byte u of word j); returns the
-// two scale bytes (hi in bits 0..7, lo in bits 8..15).
-__device__ __forceinline__ uint32_t split_hl32(const float* v, uint32_t* hi, uint32_t* lo) {
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-  const int e = mxfp8_exponent(amax);
-  const int c = min(4, e + 127);
-  const float s = exp2i(-e), sl = exp2i(c);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float x[4], r[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = v[4 * j + u] * s;
-    const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
-    float f[4];
-    e4m3x2_to_f32x2(h01, f[0], f[1]);
-    e4m3x2_to_f32x2(h23, f[2], f[3]);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) r[u] = x[u] - f[u];
-    hi[j] = h01 | (h23 << 16);
-    lo[j] = f32x2_to_e4m3x2(r[0] * sl, r[1] * sl) | (f32x2_to_e4m3x2(r[2] * sl, r[3] * sl) << 16);
-  }
-  return (uint32_t)(e + 127) | ((uint32_t)(e - c + 127) << 8);
-}
-
 // byte offset of the UE8M0 scale of 32-element block b in a token scale row
 __device__ __forceinline__ int tok_scale_byte(int b) { return 16 * (b >> 2) + (b & 3); }
 

@@ -126,6 +126,7 @@ struct FcqParams {
   int Mtot, K, I;
   const uint8_t* wsp;            // packed weight scale blocks
   const uint8_t* xsp;            // activation scale blocks per token tile
+  const uint8_t* xsp_lo;         // the lo rows' blocks (bf16 activations), else null
   const int32_t* offsets;
   const int32_t* tile_offsets;
   const int2* tile_info;
@@ -137,6 +138,8 @@ struct FcqParams {
   const float* alpha_u;
   uint8_t* hq;
   uint8_t* hsp;
+  uint8_t* hq_lo;                // FC1 of bf16 activations: H1's lo rows and blocks
+  uint8_t* hsp_lo;
   int hq_stride;
   const float* alpha2;
   float* y_out;
@@ -157,13 +160,17 @@ cudaError_t launch_pack_scales(const uint8_t* w_scale, int E_loc, int H, int I, 
                                cudaStream_t st);
 cudaError_t launch_pack_scales_nh(const uint8_t* w_scale, int E_loc, int H, int I, bool fc1, int nh, uint8_t* out,
                                   cudaStream_t st);
-cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, long S, const uint8_t* w, int E_loc, bool fc1,
-                       long max_tiles, cudaStream_t st);
+// xq_lo non-null: bf16 activations as hi (xq) + lo rows, two MMAs per K block
+cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, const uint8_t* xq_lo, long S, const uint8_t* w,
+                       int E_loc, bool fc1, long max_tiles, cudaStream_t st);
 
 // Per token tile: MXFP8 rows (x_q [T, K], x_s [T, K/32]) copied into
 // expert order (x8 [S, K]) and their scales written as the tile's scale
-// blocks (xsp); K a multiple of 128, s_vec = 1 when x_s is 4-byte aligned.
+// blocks (xsp); bf16 rows (x_bf16 non-null) split into hi rows (x8, xsp) and
+// lo rows (x8_lo, xsp_lo) by split_hl32.  K a multiple of 128, s_vec = 1
+// when x_s is 4-byte aligned.
 struct Gather8Params {
+  const void* x_bf16;            // bf16 rows, split into x8 (hi) and x8_lo (lo); null for MXFP8
   const uint8_t* x_q;
   const uint8_t* x_s;
   const int32_t* permuted_src;
@@ -173,6 +180,8 @@ struct Gather8Params {
   int E_loc, top_k, K, s_vec;
   uint8_t* x8;
   uint8_t* xsp;
+  uint8_t* x8_lo;
+  uint8_t* xsp_lo;
 };
 cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st);
 // Decode tiles on the block-scaled tensor cores (fc_bsd.cu): weights on

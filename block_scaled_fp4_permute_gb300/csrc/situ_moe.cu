@@ -47,8 +47,11 @@ bool fcw_shapes(const situ_moe_args* a) {
   return decode_like(a) && block_scaled_shapes(a) &&
          (a->act_dtype == SITU_ACT_BF16 || a->act_dtype == SITU_ACT_MXFP8);
 }
+// prefill-sized routings with MXFP8 or bf16 activations on MXFP4 weights of
+// those shapes: the block-scaled prefill tiles (bf16 rows as hi + lo)
 bool takes_block_scaled_path(const situ_moe_args* a) {
-  return a->act_dtype == SITU_ACT_MXFP8 && block_scaled_shapes(a) && !takes_decode_path(a);
+  return (a->act_dtype == SITU_ACT_MXFP8 || a->act_dtype == SITU_ACT_BF16) && block_scaled_shapes(a) &&
+         !takes_decode_path(a);
 }
 // packed weight scales: [FC1 prefill tiles | FC2 prefill tiles | FC1 decode
 // tiles | FC2 decode tiles]
@@ -108,8 +111,9 @@ Layout make_layout(const situ_moe_args* a) {
   // the packed weight scales when the caller keeps none
   const bool bs = takes_block_scaled_path(a);
   const long tiles = max_prefill_tiles(a);
-  L.xsp = take(bs ? fcq_act_scale_bytes(tiles, a->H) : 0);
-  L.hsp = take(bs ? fcq_act_scale_bytes(tiles, a->I) : 0);
+  const size_t nblk = a->act_dtype == SITU_ACT_BF16 ? 2 : 1;   // hi and lo blocks for bf16
+  L.xsp = take(bs ? nblk * fcq_act_scale_bytes(tiles, a->H) : 0);
+  L.hsp = take(bs ? nblk * fcq_act_scale_bytes(tiles, a->I) : 0);
   const bool w = fcw_shapes(a);
   L.wsp = take((bs || w) && !a->scales_packed ? packed_total_bytes(a) : 0);
   // decode tiles: hi / lo scale rows of the input and of H1 (the E4M3 rows
@@ -393,12 +397,15 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if ((err = launch_fcd(d, false, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(4);
   } else if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) {
-    // w4a8 on the block-scaled tensor cores: MXFP8 rows copied into expert
-    // order with their tile scale blocks, FC1 (+SiTU) writing H1 as MXFP8,
-    // FC2 reading it as it stands
+    // 128-token tiles on the block-scaled tensor cores: MXFP8 rows (w4a8)
+    // or bf16 rows split into hi / lo MXFP8 rows (w4a16) copied into expert
+    // order with their tile scale blocks, FC1 (+SiTU) writing H1 in the same
+    // form (MXFP8, or bf16 as hi / lo), FC2 reading it as it stands
     const uint8_t *wsp1, *wsp2, *wsp3, *wsp4;
     if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
+    const bool lo = a->act_dtype == SITU_ACT_BF16;
     Gather8Params g8;
+    g8.x_bf16 = lo ? a->hidden_states : nullptr;
     g8.x_q = a->hidden_states_q;
     g8.x_s = a->hidden_states_scale;
     g8.permuted_src = psrc;
@@ -411,6 +418,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     g8.s_vec = (reinterpret_cast<uintptr_t>(a->hidden_states_scale) & 3) == 0;
     g8.x8 = ws + L.x16;
     g8.xsp = ws + L.xsp;
+    g8.x8_lo = lo ? g8.x8 + (size_t)S * a->H : nullptr;
+    g8.xsp_lo = lo ? g8.xsp + fcq_act_scale_bytes(max_tiles, a->H) : nullptr;
     if ((err = launch_gather8(g8, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(2);
     FcqParams q;
@@ -423,6 +432,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.err = meta + 2;
     q.wsp = wsp1;
     q.xsp = g8.xsp;
+    q.xsp_lo = g8.xsp_lo;
     q.Mtot = 2 * a->I;
     q.K = a->H;
     q.n_ntiles = (a->I + fcq_n_rows(true) - 1) / fcq_n_rows(true);
@@ -432,18 +442,23 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.alpha_u = a->g1_alphas_up;
     q.hq = ws + L.h16;
     q.hsp = ws + L.hsp;
+    q.hq_lo = lo ? q.hq + (size_t)S * a->I : nullptr;
+    q.hsp_lo = lo ? q.hsp + fcq_act_scale_bytes(max_tiles, a->I) : nullptr;
     q.hq_stride = a->I;
-    if ((err = launch_fcq(q, g8.x8, S, a->w1, a->num_local_experts, true, max_tiles, st)) != cudaSuccess)
+    if ((err = launch_fcq(q, g8.x8, g8.x8_lo, S, a->w1, a->num_local_experts, true, max_tiles, st)) !=
+        cudaSuccess)
       return SITU_ERR_CUDA;
     mark(3);
     q.wsp = wsp2;
     q.xsp = q.hsp;
+    q.xsp_lo = q.hsp_lo;
     q.Mtot = a->H;
     q.K = a->I;
     q.n_ntiles = (a->H + fcq_n_rows(false) - 1) / fcq_n_rows(false);
     q.alpha2 = a->g2_alphas;
     q.y_out = y;
-    if ((err = launch_fcq(q, q.hq, S, a->w2, a->num_local_experts, false, max_tiles, st)) != cudaSuccess)
+    if ((err = launch_fcq(q, q.hq, q.hq_lo, S, a->w2, a->num_local_experts, false, max_tiles, st)) !=
+        cudaSuccess)
       return SITU_ERR_CUDA;
     mark(4);
   } else {

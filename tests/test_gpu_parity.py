@@ -177,19 +177,19 @@ def test_decode_k3_constants():
 
 def test_decode_w4a8():
     """w4a8 at decode size: MXFP8 activations and MXFP8 FC1 output on the
-    8-token-tile path."""
+    block-scaled decode tiles."""
     wl = W.make("prefill_w4a8", device="cuda", T=64)
     _, out = run_layer(wl)
     assert_parity(out, oracle_out(wl), "decode w4a8")
 
 
 @pytest.mark.parametrize("over,hot", [
-    # a hot expert (six 16-token tiles), partial last weight tiles of FC1 (I=128: 96 + 32 rows)
-    # and FC2 (H=256: 224 + 32 rows)
+    # a hot expert (six 16-token tiles), one weight tile in FC1 (I=128) and FC2 (H=256)
     (dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, params="k3_random"), 3),
     (dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_MXFP8,
           params="k3_random"), 3),
-    # a filtered shard, three 128-element stages in FC2
+    # a filtered shard, three 128-element stages in FC2, FC2's last weight tile half full
+    # (H=384: 256 + 128 rows)
     (dict(T=24, H=384, I=384, E_total=32, E_loc=8, off=8, K=4, params="k3_random"), None),
     (dict(T=40, H=512, I=256, E_total=64, E_loc=64, off=0, K=8, act=W.ACT_MXFP8,
           params="k3_random"), None),
@@ -226,10 +226,15 @@ def test_prefill_w4a8_subset():
     dict(T=257, H=640, I=256, E_total=6, E_loc=3, off=2, K=3, act=W.ACT_MXFP8, params="k3_random"),
     # K = 3 stages in both GEMMs, one hot expert
     dict(T=200, H=384, I=384, E_total=3, E_loc=3, off=0, K=2, act=W.ACT_MXFP8, params="k3_random"),
+    # bf16 activations as hi + lo MXFP8 rows: the same shapes
+    dict(T=300, H=256, I=128, E_total=4, E_loc=4, off=0, K=2, params="k3_random"),
+    dict(T=257, H=640, I=256, E_total=6, E_loc=3, off=2, K=3, params="k3_random"),
+    dict(T=200, H=384, I=384, E_total=3, E_loc=3, off=0, K=2, params="k3_random", beta=4.0, beta_lin=25.0),
 ])
-def test_w4a8_block_scaled_shapes(over):
-    """w4a8 shapes on the block-scaled tensor-core path (H, I multiples of 128),
-    with the weight scales packed once and packed inside every call."""
+def test_block_scaled_prefill_shapes(over):
+    """Prefill shapes on the block-scaled tensor-core path (H, I multiples of
+    128; MXFP8 activations, or bf16 ones as hi + lo rows), with the weight
+    scales packed once and packed inside every call."""
     wl = W.make("tiny", device="cuda", **over)
     layer, out = run_layer(wl)
     assert layer.scales_packed is not None

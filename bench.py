@@ -258,7 +258,7 @@ def run_ours(args):
     dev = torch.device(f"cuda:{local}")
     build.build()
     wl = make_workload(args.workload, dev, args.seed + rank, args.tokens)
-    layer = binding.Layer(wl)
+    layer = binding.Layer(wl, fuse_combine=args.fuse_combine)
     R, touched = routing_stats(wl)
     nbytes = algorithmic_bytes(wl, R, touched)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -410,7 +410,9 @@ def run_ours(args):
                    "E_total": wl.E_total, "E_loc": wl.E_loc, "offset": wl.off, "top_k": wl.K,
                    "kept_pairs": R, "touched_experts": touched,
                    "l2": "flushed between steps (256 MiB write, outside the step events)",
-                   "parallelism": f"replicas x{ws}, no collective"},
+                   "parallelism": f"replicas x{ws}, no collective",
+                   "combine": "fused into FC2 (fp32 reductions)" if args.fuse_combine
+                   else "separate kernel, ascending slot order"},
         "roofline": roof,
         "layer_roofline": {"bound": "tensor" if t_tc > t_hbm else "hbm", "alg_bytes": int(nbytes["layer"]),
                            "flops": flops, "roofline_ms": max(t_hbm, t_tc) * 1e3,
@@ -447,6 +449,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fuse-combine", action="store_true",
+                    help="FC2 adds weight * Y into an fp32 accumulator (block-scaled prefill tiles); "
+                         "not bitwise reproducible run to run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -39,7 +39,7 @@ class SituMoeArgs(ctypes.Structure):
             "hidden_states", "hidden_states_q", "hidden_states_scale", "hidden_states_gscale",
             "topk_ids", "topk_weights", "w1", "w1_scale", "w1_gscale", "w2", "w2_scale",
             "w2_gscale", "gemm1_alpha", "gemm1_beta", "g1_alphas", "g1_alphas_up", "g2_alphas",
-            "out", "scales_packed")]
+            "out", "scales_packed")] + [("fuse_combine", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -242,7 +242,7 @@ class Layer:
     forward call is a single C-ABI call (the bench times exactly this)."""
 
     def __init__(self, wl, out: Optional[torch.Tensor] = None, x_q=None, x_scale=None,
-                 pack_scales: bool = True):
+                 pack_scales: bool = True, fuse_combine: bool = False):
         self.wl = wl
         dev = wl.x_bf16.device
         self.out = out if out is not None else torch.empty((wl.T, wl.H), dtype=torch.bfloat16,
@@ -267,6 +267,7 @@ class Layer:
             kw["hidden_states_gscale"] = wl.x_gscale
         self._keep = kw
         self.args = make_args(**kw)
+        self.args.fuse_combine = 1 if fuse_combine else 0
         # weight scales in the block-scaled GEMMs' layout, packed once per
         # weight set (as at weight-load time) when the shapes use it
         self.scales_packed = None

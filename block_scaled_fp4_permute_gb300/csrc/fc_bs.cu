@@ -128,6 +128,12 @@ __device__ __forceinline__ void drain_wait(uint32_t a, uint32_t parity) {
     if (globaltimer() - t0 > kWaitNs) return;
 }
 
+// out[0..3] += v (fp32 vector reduction in L2)
+__device__ __forceinline__ void red_add_v4(float* out, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // byte offset of (row r, K block kb of the stage) inside a scale block
 __device__ __forceinline__ uint32_t sf_offset(int r, int kb) {
   return (uint32_t)((r & 31) * 16 + ((r >> 5) & 3) * 4 + kb);
@@ -335,6 +341,14 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         // this warp's staging block; the warp owns tile rows 32 quarter .. + 31
         uint8_t* yst = smem + C::kOffY + (warp - 4) * 32 * C::kYRow;
         const int wrow0 = quarter * 32;
+        // fused combine: lane l knows the token and routing weight of row wrow0 + l
+        int my_t = 0;
+        float my_w = 0.f;
+        if (p.fuse && wrow0 + lane < nrows) {
+          const int src = __ldg(p.permuted_src + row0 + wrow0 + lane);
+          my_t = src / p.top_k;
+          my_w = __ldg(p.topk_weights + src);
+        }
         for (int c0 = 0; c0 < C::BN; c0 += 32) {
           float acc[32];
           tmem_ld16(trow + c0, acc);
@@ -351,8 +365,14 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           for (int j = 0; j < 8; ++j) {
             const int r = 4 * j + (lane >> 3);
             const float4 v = *reinterpret_cast<const float4*>(yst + r * C::kYRow + 16 * (lane & 7));
-            if (wrow0 + r < nrows && n < p.Mtot)
+            if (p.fuse) {
+              const int t = __shfl_sync(0xffffffffu, my_t, r);
+              const float w = __shfl_sync(0xffffffffu, my_w, r);
+              if (wrow0 + r < nrows && n < p.Mtot)
+                red_add_v4(p.out_acc + (size_t)t * p.Mtot + n, v.x * w, v.y * w, v.z * w, v.w * w);
+            } else if (wrow0 + r < nrows && n < p.Mtot) {
               *reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + wrow0 + r) * p.Mtot + n) = v;
+            }
           }
           __syncwarp();
         }

@@ -93,4 +93,35 @@ cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const floa
   return launch_pdl(combine_kernel, grid, dim3(256), 0, st, (const float4*)y, slot_to_row, w, K, H4, (uint2*)out);
 }
 
+__global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ a, long n4) {
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x)
+    a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void __launch_bounds__(256) acc_to_bf16_kernel(const float4* __restrict__ acc, long n4,
+                                                          uint2* __restrict__ out) {
+  griddep_wait();   // the accumulator is the predecessor's output
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x) {
+    const float4 v = acc[i];
+    out[i] = make_uint2(f32x2_to_bf16x2(v.x, v.y), f32x2_to_bf16x2(v.z, v.w));
+  }
+}
+
+static unsigned grid_for(long n4) {
+  const long b = (n4 + 255) / 256;
+  return (unsigned)(b < 4096 ? (b > 0 ? b : 1) : 4096);
+}
+
+cudaError_t launch_zero_f32(float* a, long n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  zero_f32_kernel<<<grid_for(n / 4), 256, 0, st>>>((float4*)a, n / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_acc_to_bf16(const float* acc, long n, void* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(acc_to_bf16_kernel, dim3(grid_for(n / 4)), dim3(256), 0, st, (const float4*)acc, n / 4,
+                    (uint2*)out);
+}
+
 }  // namespace situ

@@ -42,6 +42,9 @@ cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t*
 
 cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,
                            int H, void* out, cudaStream_t st);
+// fused-combine helpers: zero the fp32 accumulator, round it to bf16 out
+cudaError_t launch_zero_f32(float* a, long n, cudaStream_t st);
+cudaError_t launch_acc_to_bf16(const float* acc, long n, void* out, cudaStream_t st);
 
 // Decode path.  Activation rows for the decode-tile GEMMs are "f16 block
 // rows": f16 mantissas [rows, kpad] (kpad = K rounded up to 128, zero
@@ -143,6 +146,12 @@ struct FcqParams {
   int hq_stride;
   const float* alpha2;
   float* y_out;
+  // fused combine (FC2): add topk_weights[slot] * Y into out_acc [T, Mtot]
+  int fuse;
+  const int32_t* permuted_src;
+  const float* topk_weights;
+  int top_k;
+  float* out_acc;
   int* err;                      // device status word
 };
 bool fcq_supported(int H, int I, const void* w1, const void* w2);

@@ -260,6 +260,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if (events) cudaEventRecord((cudaEvent_t)events[i], st);
   };
 
+  bool fused = false;   // FC2 adds into the output accumulator (block-scaled prefill only)
   mark(0);
   cudaError_t err = launch_permute(a->topk_ids, a->T, a->top_k, a->num_local_experts,
                                    a->local_expert_offset, tile_n, counts, offsets, tile_offsets,
@@ -404,6 +405,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     const uint8_t *wsp1, *wsp2, *wsp3, *wsp4;
     if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
     const bool lo = a->act_dtype == SITU_ACT_BF16;
+    fused = a->fuse_combine != 0;
+    if (fused && (err = launch_zero_f32(y, (long)a->T * a->H, st)) != cudaSuccess) return SITU_ERR_CUDA;
     Gather8Params g8;
     g8.x_bf16 = lo ? a->hidden_states : nullptr;
     g8.x_q = a->hidden_states_q;
@@ -457,6 +460,11 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.n_ntiles = (a->H + fcq_n_rows(false) - 1) / fcq_n_rows(false);
     q.alpha2 = a->g2_alphas;
     q.y_out = y;
+    q.fuse = fused ? 1 : 0;
+    q.permuted_src = psrc;
+    q.topk_weights = a->topk_weights;
+    q.top_k = a->top_k;
+    q.out_acc = y;   // fused: the accumulator [T, H] takes the place of Y
     if ((err = launch_fcq(q, q.hq, q.hq_lo, S, a->w2, a->num_local_experts, false, max_tiles, st)) !=
         cudaSuccess)
       return SITU_ERR_CUDA;
@@ -536,8 +544,11 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     mark(4);
   }
 
-  if ((err = launch_combine(y, s2r, a->topk_weights, a->T, a->top_k, a->H, a->out, st)) != cudaSuccess)
-    return SITU_ERR_CUDA;
+  if (fused)
+    err = launch_acc_to_bf16(y, (long)a->T * a->H, a->out, st);
+  else
+    err = launch_combine(y, s2r, a->topk_weights, a->T, a->top_k, a->H, a->out, st);
+  if (err != cudaSuccess) return SITU_ERR_CUDA;
   mark(5);
   return cuda_status(cudaGetLastError());
 }
@@ -576,7 +587,8 @@ int32_t situ_moe_forward_launches(const situ_moe_args* a) {
   const int pack = a->scales_packed ? 0 : 4;
   if (fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
   if (takes_decode_path(a)) return perm + 4;
-  if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
+  if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2))
+    return perm + pack + 4 + (a->fuse_combine ? 1 : 0);   // + zeroing the accumulator
   return perm + 5;
 }
 

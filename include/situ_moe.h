@@ -228,6 +228,15 @@ typedef struct situ_moe_args {
   const void* scales_packed;      /* optional: situ_moe_pack_scales output for w1_scale /
                                      w2_scale, or NULL (the forward then packs them into its
                                      workspace on every call) */
+  int32_t fuse_combine;           /* 0: FC2 writes each kept slot's row Y and a second kernel
+                                     forms the weighted sums in ascending slot order
+                                     (deterministic).  1: on the block-scaled prefill tiles,
+                                     FC2 adds weight * Y straight into an fp32 accumulator
+                                     with vector reductions (red.global.add) and a last
+                                     kernel rounds it to bf16; this saves the fp32 Y round
+                                     trip through HBM, but the order of the additions varies
+                                     from run to run, so outputs are reproducible only to
+                                     fp32 rounding.  The other paths ignore it. */
 } situ_moe_args;
 
 /* Workspace bytes situ_moe_forward needs for these shapes (0 on bad args).

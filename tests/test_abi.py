@@ -155,6 +155,13 @@ def test_forward_launch_count(lib):
     assert n(packed) == 5
     # prefill routing (bf16): permute (one block), gather, FC1, H1 gather, FC2, combine
     assert n(_args(T=400, H=64, I=32)) == 6
+    # block-scaled prefill (bf16 rows as hi + lo): permute, gather, FC1, FC2, combine;
+    # fused combine: the combine becomes the accumulator's rounding, plus its zeroing
+    pre = _args(T=400, H=256, I=128)
+    pre.scales_packed = 0x4000
+    assert n(pre) == 5
+    pre.fuse_combine = 1
+    assert n(pre) == 6
     assert n(_args(T=0)) == 0
     bad = _args()
     bad.gemm1_alpha = None

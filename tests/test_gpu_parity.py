@@ -336,3 +336,36 @@ def test_repeated_calls_are_deterministic():
     b = layer().clone()
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("over", [
+    dict(T=300, H=256, I=128, E_total=4, E_loc=4, off=0, K=2, act=W.ACT_MXFP8, params="k3_random"),
+    dict(T=257, H=640, I=256, E_total=6, E_loc=3, off=2, K=3, params="k3_random"),
+    dict(T=200, H=384, I=384, E_total=8, E_loc=4, off=4, K=2, params="k3_random"),
+])
+def test_fused_combine_prefill_shapes(over):
+    """FC2 adding weight * Y straight into the fp32 accumulator (fuse_combine):
+    within the parity bar, equal to the two-pass result to fp32 rounding, and
+    rows with no kept slot still exactly zero."""
+    wl = W.make("tiny", device="cuda", **over)
+    layer = binding.Layer(wl, fuse_combine=True)
+    assert layer.launches() == binding.Layer(wl).launches() + 1
+    out = layer().float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert_parity(out, oracle_out(wl), "fused " + str(over))
+    ids = wl.host("topk_ids")
+    none_kept = ~np.any((ids >= wl.off) & (ids < wl.off + wl.E_loc), axis=1)
+    assert np.all(out[none_kept] == 0.0)
+    _, two_pass = run_layer(wl)
+    assert_parity(out, two_pass, "fused vs two-pass " + str(over))
+
+
+def test_fused_combine_prefill_w4a8_subset():
+    wl = wl_("prefill_w4a8")
+    layer = binding.Layer(wl, fuse_combine=True)
+    out = layer().float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    toks = token_subset(wl.T, 128, seed=5)
+    assert_parity(out[toks], oracle_out(wl, toks), "prefill w4a8, fused combine")

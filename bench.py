@@ -97,7 +97,7 @@ def algorithmic_bytes(wl, R, touched):
         "fc1": w1 + R * H * 2 + R * I * 2,
         "fc2": w2 + R * I * 2 + R * H * 2,
         "combine": R * H * 2 + route + out,
-        "quant": T * H * 2 + T * H + T * H // 32,
+        "quant": T * H * 2 + (T * H + T * H // 32 if wl.act == 1 else T * H // 2 + T * H // 16 + 4 * T),
         "layer": w1 + w2 + act_in + route + out,
     }
 
@@ -179,9 +179,8 @@ def oracle_tokens_per_s(wl, budget_s: float, host_kw=None, max_tokens=None):
 
 
 def host_oracle_kwargs(wl):
-    import oracle
     from block_scaled_fp4_permute_gb300 import workloads as W
-    if wl.act == W.ACT_MXFP8:
+    if wl.act in (W.ACT_MXFP8, W.ACT_NVFP4):
         return W.oracle_kwargs(wl), wl.host("x_bf16")
     return W.oracle_kwargs(wl), None
 
@@ -189,13 +188,21 @@ def host_oracle_kwargs(wl):
 def _oracle_run(oracle, W, wl, host_kw, n):
     kw, xbits = host_kw
     toks = np.arange(n, dtype=np.int32)
-    if xbits is not None:   # w4a8: the oracle's own MXFP8 quantisation is part of the step
+    if xbits is not None and wl.act == W.ACT_MXFP8:   # the oracle's own quantisation is part of the step
         q, s = oracle.quant_mxfp8(xbits[:n])
         kw = dict(kw)
         qf = np.zeros((wl.T, wl.H), np.uint8)
         sf = np.zeros((wl.T, wl.H // 32), np.uint8)
         qf[:n], sf[:n] = q, s
         kw["hidden_states_q"], kw["hidden_states_scale"] = qf, sf
+    elif xbits is not None:
+        q, s, g = oracle.quant_nvfp4(xbits[:n])
+        kw = dict(kw)
+        qf = np.zeros((wl.T, wl.H // 2), np.uint8)
+        sf = np.zeros((wl.T, wl.H // 16), np.uint8)
+        gf = np.ones((wl.T,), np.float32)
+        qf[:n], sf[:n], gf[:n] = q, s, g
+        kw["hidden_states_q"], kw["hidden_states_scale"], kw["hidden_states_gscale"] = qf, sf, gf
     return oracle.moe_forward(**kw, tokens=toks)
 
 
@@ -264,7 +271,8 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     nst = len(binding.PROFILE_STAGES)
-    is_w4a8 = wl.act == binding.SITU_ACT_MXFP8
+    is_w4a8 = wl.act != binding.SITU_ACT_BF16   # the step includes the activation quantisation
+    qname = "quant_mxfp8" if wl.act == binding.SITU_ACT_MXFP8 else "quant_nvfp4"
 
     def new_events(n):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -324,10 +332,7 @@ def run_ours(args):
         ms = float(t.item())
 
     # end to end: pinned host inputs -> device, layer, output -> pinned host
-    if wl.act == binding.SITU_ACT_NVFP4:
-        dev_in = [wl.x_q, wl.x_scale, wl.x_gscale, wl.topk_ids, wl.topk_weights]
-    else:
-        dev_in = [wl.x_bf16, wl.topk_ids, wl.topk_weights]
+    dev_in = [wl.x_bf16, wl.topk_ids, wl.topk_weights]
     host_in = [t.cpu().pin_memory() for t in dev_in]
     host_out = torch.empty(layer.out.shape, dtype=layer.out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
@@ -361,7 +366,7 @@ def run_ours(args):
                         "gbs": gbs, "frac_hbm": gbs / hbm if gbs else None}
     if is_w4a8:
         gbs = nbytes["quant"] / (quant_ms * 1e-3) / 1e9
-        stages["quant_mxfp8"] = {"ms": quant_ms, "alg_bytes": int(nbytes["quant"]), "gbs": gbs,
+        stages[qname] = {"ms": quant_ms, "alg_bytes": int(nbytes["quant"]), "gbs": gbs,
                                  "frac_hbm": gbs / hbm}
     dom = max(stages, key=lambda k: stages[k]["ms"])
     traffic = None

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             l.situ_moe_permute_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
             l.situ_moe_quant_mxfp8.restype = ctypes.c_int
             l.situ_moe_quant_mxfp8.argtypes = [vp, i32, i32, vp, vp, vp]
+            l.situ_moe_quant_nvfp4.restype = ctypes.c_int
+            l.situ_moe_quant_nvfp4.argtypes = [vp, i32, i32, vp, vp, vp, vp]
             l.situ_moe_workspace_size.restype = sz
             l.situ_moe_workspace_size.argtypes = [ctypes.POINTER(SituMoeArgs)]
             l.situ_moe_forward.restype = ctypes.c_int
@@ -164,6 +166,20 @@ def situ_moe_quant_mxfp8(x_bf16: torch.Tensor, stream=None, out=None):
     _check("situ_moe_quant_mxfp8", lib().situ_moe_quant_mxfp8(
         _p(x_bf16), T, H, _p(q), _p(s), _stream(stream)))
     return q, s
+
+
+def situ_moe_quant_nvfp4(x_bf16: torch.Tensor, stream=None, out=None):
+    """bf16 [T,H] -> (packed E2M1 uint8 [T,H/2], E4M3 uint8 [T,H/16], fp32 [T])."""
+    T, H = x_bf16.shape
+    if out is None:
+        q = torch.empty((T, H // 2), dtype=torch.uint8, device=x_bf16.device)
+        s = torch.empty((T, H // 16), dtype=torch.uint8, device=x_bf16.device)
+        g = torch.empty((T,), dtype=torch.float32, device=x_bf16.device)
+    else:
+        q, s, g = out
+    _check("situ_moe_quant_nvfp4", lib().situ_moe_quant_nvfp4(
+        _p(x_bf16), T, H, _p(q), _p(s), _p(g), _stream(stream)))
+    return q, s, g
 
 
 def make_args(*, T, H, I, num_experts_total, num_local_experts, local_expert_offset, top_k,
@@ -263,8 +279,12 @@ class Layer:
             self.x_q, self.x_scale = x_q, x_scale
             kw["hidden_states_q"], kw["hidden_states_scale"] = x_q, x_scale
         else:
-            kw["hidden_states_q"], kw["hidden_states_scale"] = wl.x_q, wl.x_scale
-            kw["hidden_states_gscale"] = wl.x_gscale
+            # NVFP4: quantised from the bf16 hidden states on the GPU in every call
+            self.x_q = torch.empty((wl.T, wl.H // 2), dtype=torch.uint8, device=dev)
+            self.x_scale = torch.empty((wl.T, wl.H // 16), dtype=torch.uint8, device=dev)
+            self.x_gscale = torch.empty((wl.T,), dtype=torch.float32, device=dev)
+            kw["hidden_states_q"], kw["hidden_states_scale"] = self.x_q, self.x_scale
+            kw["hidden_states_gscale"] = self.x_gscale
         self._keep = kw
         self.args = make_args(**kw)
         self.args.fuse_combine = 1 if fuse_combine else 0
@@ -280,9 +300,15 @@ class Layer:
         self.workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
 
     def launches(self) -> int:
-        """Kernels one __call__ enqueues (the forward, plus the MXFP8
-        quantisation for w4a8)."""
-        return situ_moe_forward_launches(self.args) + (1 if self.wl.act == SITU_ACT_MXFP8 else 0)
+        """Kernels one __call__ enqueues (the forward, plus the activation
+        quantisation for MXFP8 and NVFP4 activations)."""
+        return situ_moe_forward_launches(self.args) + (0 if self.wl.act == SITU_ACT_BF16 else 1)
+
+    def _quant(self, stream):
+        if self.wl.act == SITU_ACT_MXFP8:
+            situ_moe_quant_mxfp8(self.wl.x_bf16, stream, out=(self.x_q, self.x_scale))
+        elif self.wl.act == SITU_ACT_NVFP4:
+            situ_moe_quant_nvfp4(self.wl.x_bf16, stream, out=(self.x_q, self.x_scale, self.x_gscale))
 
     def device_status(self, stream=None) -> int:
         """0 when every bounded device wait of the last call completed."""
@@ -290,20 +316,19 @@ class Layer:
 
     def profiled(self, events, quant_events=None, stream=None) -> torch.Tensor:
         """Like __call__, recording per-stage events (see situ_moe_forward_profiled);
-        ``quant_events`` (start, end) bracket the MXFP8 quantisation of w4a8."""
-        if self.wl.act == SITU_ACT_MXFP8:
+        ``quant_events`` (start, end) bracket the activation quantisation."""
+        if self.wl.act != SITU_ACT_BF16:
             if quant_events:
                 quant_events[0].record(stream)
-            situ_moe_quant_mxfp8(self.wl.x_bf16, stream, out=(self.x_q, self.x_scale))
+            self._quant(stream)
             if quant_events:
                 quant_events[1].record(stream)
         situ_moe_forward_profiled(self.args, self.workspace, events, stream)
         return self.out
 
     def __call__(self, stream=None) -> torch.Tensor:
-        """One pass of the layer; for w4a8 this includes the MXFP8 activation
-        quantisation of the bf16 hidden states."""
-        if self.wl.act == SITU_ACT_MXFP8:
-            situ_moe_quant_mxfp8(self.wl.x_bf16, stream, out=(self.x_q, self.x_scale))
+        """One pass of the layer; for MXFP8 and NVFP4 activations this includes
+        their quantisation from the bf16 hidden states."""
+        self._quant(stream)
         situ_moe_forward(self.args, self.workspace, stream)
         return self.out

@@ -93,6 +93,87 @@ cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const floa
   return launch_pdl(combine_kernel, grid, dim3(256), 0, st, (const float4*)y, slot_to_row, w, K, H4, (uint2*)out);
 }
 
+// ---------------------------------------------------------------------------
+// Per-token NVFP4 activation quantisation: row global scale gs = amax / 2688
+// (6 * 448; 1 for an all-zero row), E4M3 scale per 16 elements
+// s = E4M3(amax16 / (6 gs)), elements E2M1(x / (value(s) gs)), every step one
+// fp32 operation rounded to nearest even.  One CTA per token row.
+// ---------------------------------------------------------------------------
+
+// eight fp32 values -> eight E2M1 codes in one word, element 2i in the low
+// nibble of byte i (the first operand of each pair conversion is the high
+// nibble); nearest even, saturating to +-6
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float* y) {
+  uint32_t d;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(d)
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+  return d;
+}
+
+__global__ void __launch_bounds__(128) quant_nvfp4_kernel(const uint4* __restrict__ x, int H,
+                                                          uint2* __restrict__ q, uint8_t* __restrict__ s,
+                                                          float* __restrict__ gs) {
+  __shared__ float red[4];
+  const long t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const uint4* xr = x + (size_t)t * (H / 8);
+  float amax = 0.f;
+  for (int i = tid; i < H / 8; i += 128) {
+    const uint4 v = __ldg(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float g = __fdiv_rn(amax, 2688.f);
+  if (!(g > 0.f)) g = 1.f;
+  if (tid == 0) gs[t] = g;
+  const float den6 = __fmul_rn(6.f, g);
+  for (int b = tid; b < H / 16; b += 128) {
+    float v[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = __ldg(xr + 2 * b + h);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[8 * h + 2 * j] = bf16_lo(w[j]);
+        v[8 * h + 2 * j + 1] = bf16_hi(w[j]);
+      }
+    }
+    float ab = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
+    const uint32_t s8 = f32x2_to_e4m3x2(__fdiv_rn(ab, den6), 0.f) & 0xFFu;
+    const float denom = __fmul_rn(e4m3_code_to_f32(s8), g);
+    uint2 out = make_uint2(0u, 0u);
+    if (denom > 0.f) {
+      float y[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = __fdiv_rn(v[i], denom);
+      out = make_uint2(f32x8_to_e2m1x8(y), f32x8_to_e2m1x8(y + 8));
+    }
+    q[(size_t)t * (H / 16) + b] = out;
+    s[(size_t)t * (H / 16) + b] = (uint8_t)s8;
+  }
+}
+
+cudaError_t launch_quant_nvfp4(const void* x, int T, int H, uint8_t* q, uint8_t* s, float* gs, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  quant_nvfp4_kernel<<<(unsigned)T, 128, 0, st>>>((const uint4*)x, H, (uint2*)q, s, gs);
+  return cudaGetLastError();
+}
+
 __global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ a, long n4) {
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x)
     a[i] = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -39,6 +39,7 @@ int permute_launches(int T, int K, int E_loc);   // kernels launch_permute enque
 
 cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t* s,
                                cudaStream_t st);
+cudaError_t launch_quant_nvfp4(const void* x, int T, int H, uint8_t* q, uint8_t* s, float* gs, cudaStream_t st);
 
 cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,
                            int H, void* out, cudaStream_t st);

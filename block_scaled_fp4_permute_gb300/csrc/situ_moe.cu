@@ -222,6 +222,16 @@ situ_status situ_moe_quant_mxfp8(const void* x_bf16, int32_t T, int32_t H, uint8
   return cuda_status(launch_quant_mxfp8(x_bf16, T, H, x_e4m3, x_scale_ue8m0, (cudaStream_t)stream));
 }
 
+situ_status situ_moe_quant_nvfp4(const void* x_bf16, int32_t T, int32_t H, uint8_t* x_e2m1,
+                                 uint8_t* x_scale_e4m3, float* x_gscale, void* stream) {
+  if (T < 0 || H <= 0 || H % 16) return SITU_ERR_BAD_SHAPE;
+  if (T == 0) return SITU_OK;
+  if (!x_bf16 || !x_e2m1 || !x_scale_e4m3 || !x_gscale) return SITU_ERR_NULL_ARG;
+  if (!aligned16(x_bf16) || !aligned_to(x_e2m1, 8) || !aligned_to(x_gscale, 4)) return SITU_ERR_MISALIGNED;
+  return cuda_status(
+      launch_quant_nvfp4(x_bf16, T, H, x_e2m1, x_scale_e4m3, x_gscale, (cudaStream_t)stream));
+}
+
 size_t situ_moe_workspace_size(const situ_moe_args* args) {
   if (!args) return 0;
   if (check_routing(args->T, args->top_k, args->num_experts_total, args->num_local_experts,

@@ -271,9 +271,10 @@ def make(name: str = "tiny", *, device="cpu", seed: int = 0, T: Optional[int] = 
     return wl
 
 
-def oracle_kwargs(wl: Workload, *, x_q=None, x_scale=None) -> dict:
+def oracle_kwargs(wl: Workload, *, x_q=None, x_scale=None, x_gscale=None) -> dict:
     """Host (numpy) keyword arguments for the oracle's ``moe_forward``.  For
-    the MXFP8 chain pass the oracle's own quantised activations."""
+    the MXFP8 chain pass the oracle's own quantised activations; for NVFP4
+    they may be passed too (default: this module's host packing)."""
     kw = dict(T=wl.T, H=wl.H, I=wl.I, num_experts_total=wl.E_total,
               num_local_experts=wl.E_loc, local_expert_offset=wl.off, top_k=wl.K,
               act=wl.act, wt=wl.wt, topk_ids=wl.host("topk_ids"),
@@ -288,7 +289,7 @@ def oracle_kwargs(wl: Workload, *, x_q=None, x_scale=None) -> dict:
     elif wl.act == ACT_MXFP8:
         kw["hidden_states_q"], kw["hidden_states_scale"] = x_q, x_scale
     else:
-        kw["hidden_states_q"] = wl.host("x_q")
-        kw["hidden_states_scale"] = wl.host("x_scale")
-        kw["hidden_states_gscale"] = wl.host("x_gscale")
+        kw["hidden_states_q"] = wl.host("x_q") if x_q is None else x_q
+        kw["hidden_states_scale"] = wl.host("x_scale") if x_scale is None else x_scale
+        kw["hidden_states_gscale"] = wl.host("x_gscale") if x_gscale is None else x_gscale
     return kw

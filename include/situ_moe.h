@@ -166,6 +166,33 @@ situ_status situ_moe_quant_mxfp8(const void* x_bf16, int32_t T, int32_t H, uint8
                                  uint8_t* x_scale_ue8m0, void* stream);
 
 /* ------------------------------------------------------------------------
+ * situ_moe_quant_nvfp4 -- quantise bf16 activations to NVFP4 with
+ * per-token scaling (the NVFP4 variant's hidden_states / hidden_states_scale
+ * / hidden_states_gscale).
+ *
+ * FlashInfer 0.6.18 SM100a+SM103a MoE-LoRA AOT release notes: the NVFP4
+ * path takes "per-token NVFP4 activation scaling" (they note that
+ * TRT-LLM-Gen ships no fused SiTU GEMM1 for it).  The pages do not fix the
+ * rule; this library uses, per token row, with every step one fp32
+ * operation rounded to nearest even:
+ *   gscale = amax_row / 2688 (= 6 * 448; 1 for an all-zero row),
+ *   scale  = E4M3(amax_16 / (6 * gscale)) per 16 consecutive elements,
+ *   code   = E2M1(x / (value(scale) * gscale)), ties to the even code,
+ *            saturating at 6 (0 when that divisor is 0).
+ *
+ *   x_bf16        bf16  [T, H]      (input; finite values; 16-byte aligned)
+ *   x_e2m1        uint8 [T, H/2]    packed codes, element 2i in the low nibble
+ *                                   (8-byte aligned)
+ *   x_scale_e4m3  uint8 [T, H/16]
+ *   x_gscale      fp32  [T]
+ *
+ * Bit-exact.  H must be a positive multiple of 16; T == 0 launches nothing.
+ * Asynchronous on `stream`.  Errors: NULL_ARG, BAD_SHAPE, MISALIGNED, CUDA.
+ * --------------------------------------------------------------------- */
+situ_status situ_moe_quant_nvfp4(const void* x_bf16, int32_t T, int32_t H, uint8_t* x_e2m1,
+                                 uint8_t* x_scale_e4m3, float* x_gscale, void* stream);
+
+/* ------------------------------------------------------------------------
  * situ_moe_forward -- the whole routed-expert layer.
  *
  * For each kept pair (t, j) with local expert e = topk_ids[t,j] - offset:

@@ -76,6 +76,11 @@ def lib():
             l.oracle_mxfp8_exponent.argtypes = [ctypes.c_double]
             l.oracle_situ.restype = ctypes.c_double
             l.oracle_situ.argtypes = [ctypes.c_double] * 4
+            l.oracle_e2m1_encode.restype = ctypes.c_uint
+            l.oracle_e2m1_encode.argtypes = [ctypes.c_double]
+            l.oracle_quant_nvfp4.restype = None
+            l.oracle_quant_nvfp4.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p]
             l.oracle_quant_mxfp8.restype = None
             l.oracle_quant_mxfp8.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_void_p, ctypes.c_void_p]
@@ -141,6 +146,23 @@ def get_threads() -> int:
 
 
 # --- array entry points ----------------------------------------------------
+
+def e2m1_encode(v: float) -> int:
+    return int(lib().oracle_e2m1_encode(float(v)))
+
+
+def quant_nvfp4(x_bf16_bits: np.ndarray):
+    """Per-token NVFP4 quantisation of bf16 rows (uint16 bit patterns [T, H]):
+    returns (packed E2M1 uint8 [T, H/2], E4M3 scales uint8 [T, H/16],
+    fp32 global scales [T])."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    T, H = x.shape
+    q = np.zeros((T, H // 2), np.uint8)
+    s = np.zeros((T, H // 16), np.uint8)
+    g = np.zeros((T,), np.float32)
+    lib().oracle_quant_nvfp4(_ptr(x), T, H, _ptr(q), _ptr(s), _ptr(g))
+    return q, s, g
+
 
 def quant_mxfp8(x_bf16_bits: np.ndarray):
     """x: uint16 bf16 bits [T,H] -> (E4M3 uint8 [T,H], UE8M0 uint8 [T,H/32])."""

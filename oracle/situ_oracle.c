@@ -10,6 +10,9 @@
  * What it computes (each function names the passage it follows):
  *   - the block-scaled number formats the layer consumes: E2M1 (FP4) values,
  *     UE8M0 power-of-two block scales and E4M3 ("fn") values;
+ *   - the per-token NVFP4 activation quantisation of the NVFP4 variant
+ *     (FlashInfer 0.6.18 MoE-LoRA AOT release notes, "per-token NVFP4
+ *     activation scaling"; the rule itself is a reading, see below);
  *   - the per-token MXFP8 activation quantisation of the w4a8 chain
  *     (TokenSpeed SiTU, "Activation precision (w4a16 vs w4a8)" and
  *     "Supported contract": MXFP8 activations with a per-token
@@ -198,6 +201,80 @@ static void quant_row(void* p, long t) {
 void oracle_quant_mxfp8(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s) {
   quant_ctx c = {x, H, q, s};
   parallel_for(T, quant_row, &c);
+}
+
+/* ------------------------------------------------------------------ */
+/* NVFP4 activation quantisation (per-token)                            */
+/* ------------------------------------------------------------------ */
+
+/* Round a value to E2M1 by searching the eight magnitudes: nearest value,
+ * ties to the even code, magnitudes above 6 saturate to 6.  The sign is
+ * kept (bit 3), so a negative value that rounds to zero gives code 8. */
+unsigned oracle_e2m1_encode(double v) {
+  unsigned sign = signbit(v) ? 8u : 0u;
+  double a = fabs(v);
+  if (a >= 6.0) return sign | 7u;
+  unsigned lo = 0;
+  while (lo < 7 && oracle_e2m1_value(lo + 1) <= a) ++lo;   /* value(lo) <= a < value(lo + 1) */
+  unsigned hi = lo + 1;
+  double dlo = a - oracle_e2m1_value(lo), dhi = oracle_e2m1_value(hi) - a;
+  unsigned code;
+  if (dlo < dhi) code = lo;
+  else if (dhi < dlo) code = hi;
+  else code = (lo & 1u) ? hi : lo;
+  return sign | code;
+}
+
+typedef struct { const uint16_t* x; int H; uint8_t* q; uint8_t* s; float* gs; } nvq_ctx;
+
+/* The per-token NVFP4 rule of the layer's NVFP4 activations (a reading:
+ * the FlashInfer notes name per-token NVFP4 activation scaling, and the
+ * pages fix no rule).  Every step is one fp32 operation, rounded to
+ * nearest even, as the device performs it:
+ *   gs     = amax_row / 2688   (2688 = 6 * 448; 1 when the row is all zero)
+ *   s      = E4M3(amax_block16 / (6 * gs))   (round to nearest even)
+ *   denom  = value(s) * gs
+ *   code_i = E2M1(x_i / denom), or 0 when denom is 0. */
+static void nvq_row(void* p, long t) {
+  nvq_ctx* c = (nvq_ctx*)p;
+  const uint16_t* xr = c->x + (size_t)t * c->H;
+  float amax = 0.0f;
+  for (int i = 0; i < c->H; ++i) {
+    float a = fabsf((float)oracle_bf16_value(xr[i]));
+    if (a > amax) amax = a;
+  }
+  float gs = amax / 2688.0f;
+  if (!(gs > 0.0f)) gs = 1.0f;
+  c->gs[t] = gs;
+  for (int b = 0; b < c->H / 16; ++b) {
+    float ab = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      float a = fabsf((float)oracle_bf16_value(xr[b * 16 + i]));
+      if (a > ab) ab = a;
+    }
+    float den6 = 6.0f * gs;
+    float qv = ab / den6;
+    unsigned s8 = oracle_e4m3_encode((double)qv);
+    float denom = (float)oracle_e4m3_value(s8) * gs;
+    c->s[(size_t)t * (c->H / 16) + b] = (uint8_t)s8;
+    for (int i = 0; i < 16; i += 2) {
+      unsigned c0 = 0, c1 = 0;
+      if (denom > 0.0f) {
+        float y0 = (float)oracle_bf16_value(xr[b * 16 + i]) / denom;
+        float y1 = (float)oracle_bf16_value(xr[b * 16 + i + 1]) / denom;
+        c0 = oracle_e2m1_encode((double)y0);
+        c1 = oracle_e2m1_encode((double)y1);
+      }
+      c->q[(size_t)t * (c->H / 2) + (b * 16 + i) / 2] = (uint8_t)(c0 | (c1 << 4));
+    }
+  }
+}
+
+/* x: bf16 [T,H]; q: packed E2M1 [T,H/2] (element 2i in the low nibble);
+ * s: E4M3 [T,H/16]; gs: fp32 [T].  Requires H % 16 == 0, finite inputs. */
+void oracle_quant_nvfp4(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* s, float* gs) {
+  nvq_ctx c = {x, H, q, s, gs};
+  parallel_for(T, nvq_row, &c);
 }
 
 /* ------------------------------------------------------------------ */

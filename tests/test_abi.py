@@ -167,3 +167,12 @@ def test_forward_launch_count(lib):
     bad.gemm1_alpha = None
     assert n(bad) == -1
     assert lib.situ_moe_forward_launches(None) == -1
+
+
+def test_quant_nvfp4_argument_errors(lib):
+    p = ctypes.c_void_p(256)
+    assert lib.situ_moe_quant_nvfp4(p, 4, 40, p, p, p, None) == 2     # H % 16
+    assert lib.situ_moe_quant_nvfp4(p, -1, 64, p, p, p, None) == 2
+    assert lib.situ_moe_quant_nvfp4(p, 0, 64, None, None, None, None) == 0
+    assert lib.situ_moe_quant_nvfp4(None, 4, 64, p, p, p, None) == 1
+    assert lib.situ_moe_quant_nvfp4(ctypes.c_void_p(264), 4, 64, p, p, p, None) == 6

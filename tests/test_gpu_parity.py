@@ -70,9 +70,13 @@ def run_layer(wl):
 
 
 def oracle_out(wl, tokens=None):
+    """The oracle's layer on the oracle's own activation quantisation."""
     if wl.act == W.ACT_MXFP8:
         q, s = oracle.quant_mxfp8(wl.host("x_bf16"))
         kw = W.oracle_kwargs(wl, x_q=q, x_scale=s)
+    elif wl.act == W.ACT_NVFP4:
+        q, s, g = oracle.quant_nvfp4(wl.host("x_bf16"))
+        kw = W.oracle_kwargs(wl, x_q=q, x_scale=s, x_gscale=g)
     else:
         kw = W.oracle_kwargs(wl)
     return oracle.moe_forward(**kw, tokens=tokens)
@@ -151,6 +155,33 @@ def test_quant_bit_exact_special_blocks():
     x[5, 160:192] = torch.nextafter(torch.tensor(448.0), torch.tensor(1e9)).item()
     x[6, :] *= 2.0 ** torch.arange(256, device="cuda").float().sub(128).div(2)
     _check_quant(x.to(torch.bfloat16))
+
+
+def _check_quant_nvfp4(x):
+    q, s, g = binding.situ_moe_quant_nvfp4(x)
+    torch.cuda.synchronize()
+    bits = x.view(torch.int16).cpu().numpy().view(np.uint16)
+    rq, rs, rg = oracle.quant_nvfp4(bits)
+    assert np.array_equal(g.cpu().numpy(), rg)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_quant_nvfp4_bit_exact_on_workload_activations():
+    _check_quant_nvfp4(W.make("nvfp4", device="cuda", T=2048).x_bf16)
+
+
+def test_quant_nvfp4_bit_exact_special_rows():
+    g = torch.Generator(device="cuda").manual_seed(4)
+    x = torch.randn((41, 320), generator=g, device="cuda")
+    x[0] = 0.0                                   # all-zero row: gscale 1, codes 0
+    x[1, :16] = 0.0                              # an all-zero block in a live row
+    x[2] *= 1e-30
+    x[3] *= 1e30
+    x[4, 5] = -0.0
+    x[5, :] = torch.linspace(-6.0, 6.0, 320, device="cuda")       # many E2M1 ties
+    x[6, :] *= 2.0 ** torch.arange(320, device="cuda").float().sub(160).div(8)
+    _check_quant_nvfp4(x.to(torch.bfloat16))
 
 
 # ---------------------------------------------------------------------------

@@ -143,3 +143,70 @@ def test_quant_mxfp8_round_trip_error_bound():
     q2, s2 = oracle.quant_mxfp8(_bf16_bits(dq))
     sc2 = np.repeat(torch.from_numpy(s2).view(torch.float8_e8m0fnu).double().numpy(), 32, axis=1)
     assert np.array_equal(torch.from_numpy(q2).view(torch.float8_e4m3fn).double().numpy() * sc2, dq)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 activation quantisation (per-token global scale, E4M3 per 16, E2M1)
+# ---------------------------------------------------------------------------
+
+def _e2m1_brute(v):
+    """Nearest of the 16 signed E2M1 values by exhaustive comparison, ties to
+    the even code, saturating; a negative value rounding to 0 keeps the sign."""
+    vals = [oracle.e2m1_value(c) for c in range(8)]
+    a = min(abs(v), 6.0)
+    best = min(range(8), key=lambda c: (abs(a - vals[c]), c % 2))
+    return best | (8 if math.copysign(1.0, v) < 0 else 0)
+
+
+def test_e2m1_encode_brute_force_and_ties():
+    rng = np.random.default_rng(11)
+    pts = list(rng.uniform(-7.5, 7.5, 4000))
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    mids = [(grid[i] + grid[i + 1]) / 2 for i in range(7)]     # every tie
+    for m in mids:
+        pts += [m, -m, np.nextafter(m, 0.0), np.nextafter(m, 10.0)]
+    pts += [0.0, -0.0, 6.0, 1e9, -1e9]
+    for v in pts:
+        assert oracle.e2m1_encode(v) == _e2m1_brute(float(v)), v
+
+
+def _bits(x):
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quant_nvfp4_matches_torch_packing():
+    """Against an independent torch formulation of the same fp32 steps
+    (float8_e4m3fn casts and a bucketed E2M1 search): identical bytes."""
+    from block_scaled_fp4_permute_gb300 import workloads as W
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn((48, 512), generator=g) * torch.logspace(-3, 3, 48).unsqueeze(1)
+    x[3, :] = 0.0
+    x[4, 17] = -0.0
+    xb = x.to(torch.bfloat16)
+    q, s, gs = oracle.quant_nvfp4(_bits(xb))
+    xf = xb.float()
+    ref_gs = xf.abs().amax(1) / (6.0 * 448.0)
+    ref_gs = torch.where(ref_gs > 0, ref_gs, torch.ones_like(ref_gs))
+    rq, rs = W.pack_nvfp4(xf, ref_gs)
+    assert np.array_equal(gs, ref_gs.numpy())
+    assert np.array_equal(s, rs.numpy())
+    assert np.array_equal(q, rq.numpy())
+
+
+def test_quant_nvfp4_properties():
+    g = torch.Generator().manual_seed(6)
+    x = (torch.randn((16, 256), generator=g) * 3.0).to(torch.bfloat16)
+    x[0] = 0.0
+    q, s, gs = oracle.quant_nvfp4(_bits(x))
+    assert gs[0] == 1.0 and not q[0].any() and not s[0].any()       # all-zero row
+    xf = x.float().numpy().astype(np.float64)
+    for t in range(1, 16):
+        assert gs[t] == np.float32(np.abs(xf[t]).max() / 2688.0)
+        codes = np.stack([q[t] & 15, q[t] >> 4], 1).reshape(-1)
+        val = np.array([oracle.e2m1_value(int(c)) for c in codes])
+        sc = np.repeat([oracle.e4m3_value(int(b)) for b in s[t]], 16) * float(gs[t])
+        # every element within half a grid step (at most 1 near 6, in units of the block scale)
+        assert np.all(np.abs(val * sc - xf[t]) <= 1.0 * sc + 1e-12)
+        # each block's largest element lands near the top of the E2M1 range
+        blk = np.abs(xf[t]).reshape(-1, 16).max(1)
+        assert np.all(np.abs(val.reshape(-1, 16)).max(1)[blk > 0] >= 4.0)

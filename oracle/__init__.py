@@ -33,6 +33,7 @@ _lib = None
 _lock = threading.Lock()
 
 ACT_BF16, ACT_MXFP8, ACT_NVFP4 = 0, 1, 2
+ACT_FN_SITU, ACT_FN_SWIGLU_BIAS = 0, 1
 W_MXFP4, W_NVFP4 = 0, 1
 
 
@@ -55,6 +56,7 @@ class _Args(ctypes.Structure):
         ("w2", ctypes.c_void_p), ("w2s", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p),
         ("beta", ctypes.c_void_p), ("beta_lin", ctypes.c_void_p),
         ("alpha_g", ctypes.c_void_p), ("alpha_u", ctypes.c_void_p), ("alpha2", ctypes.c_void_p),
+        ("activation", ctypes.c_int), ("topk_in_fc1", ctypes.c_int),
     ]
 
 
@@ -76,6 +78,8 @@ def lib():
             l.oracle_mxfp8_exponent.argtypes = [ctypes.c_double]
             l.oracle_situ.restype = ctypes.c_double
             l.oracle_situ.argtypes = [ctypes.c_double] * 4
+            l.oracle_swiglu_bias.restype = ctypes.c_double
+            l.oracle_swiglu_bias.argtypes = [ctypes.c_double] * 4
             l.oracle_e2m1_encode.restype = ctypes.c_uint
             l.oracle_e2m1_encode.argtypes = [ctypes.c_double]
             l.oracle_quant_nvfp4.restype = None
@@ -137,6 +141,10 @@ def situ(g: float, u: float, beta: float, beta_lin: float) -> float:
     return lib().oracle_situ(g, u, beta, beta_lin)
 
 
+def swiglu_bias(g: float, u: float, alpha: float, beta: float) -> float:
+    return float(lib().oracle_swiglu_bias(g, u, alpha, beta))
+
+
 def set_threads(n: int) -> None:
     lib().oracle_set_threads(int(n))
 
@@ -193,8 +201,14 @@ def moe_forward(*, T, H, I, num_experts_total, num_local_experts, local_expert_o
                 act, wt, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, gemm1_alpha,
                 gemm1_beta, hidden_states=None, hidden_states_q=None, hidden_states_scale=None,
                 hidden_states_gscale=None, w1_gscale=None, w2_gscale=None, g1_alphas=None,
-                g1_alphas_up=None, g2_alphas=None, tokens=None) -> np.ndarray:
+                g1_alphas_up=None, g2_alphas=None, tokens=None, activation=0,
+                apply_topk_in_fc1=0) -> np.ndarray:
     """Reference layer output (fp64 [n_tok, H]) for ``tokens`` (all T if None).
+
+    activation: ACT_FN_SITU (gemm1_alpha / gemm1_beta = beta / linear beta)
+    or ACT_FN_SWIGLU_BIAS (alpha / beta); apply_topk_in_fc1: the routing
+    weight scales H1 (before its rounding) and the un-permute sum is
+    unweighted.
 
     hidden_states: uint16 bf16 bits [T,H] (act=ACT_BF16);
     hidden_states_q / hidden_states_scale: E4M3 [T,H] + UE8M0 [T,H/32]
@@ -227,6 +241,8 @@ def moe_forward(*, T, H, I, num_experts_total, num_local_experts, local_expert_o
     args.alpha_g = c(g1_alphas, np.float32)
     args.alpha_u = c(g1_alphas_up, np.float32)
     args.alpha2 = c(g2_alphas, np.float32)
+    args.activation = int(activation)
+    args.topk_in_fc1 = int(apply_topk_in_fc1)
     if tokens is None:
         n_tok, tok_ptr = T, None
     else:

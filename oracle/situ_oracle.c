@@ -326,6 +326,14 @@ static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 /* [beta * tanh(g/beta) * sigmoid(g)] * [beta_lin * tanh(u/beta_lin)]
  * (TensorRT-LLM PR #17865, golden `_situ_act`).  A cap <= 0 takes the
  * factor's beta -> infinity limit (g*sigmoid(g) resp. u). */
+/* CUTLASS SwigluBias, the variant printed beside SiTU in the golden
+ * reference of TensorRT-LLM PR #17865 (`_swiglu_bias_act`):
+ * gate * sigmoid(gate * alpha) * (linear + beta).  With alpha = 1 and
+ * beta = 0 it is SwiGLU. */
+double oracle_swiglu_bias(double g, double u, double alpha, double beta) {
+  return g * sigmoid(g * alpha) * (u + beta);
+}
+
 double oracle_situ(double g, double u, double beta, double beta_lin) {
   double gate = (beta > 0.0) ? beta * tanh(g / beta) * sigmoid(g) : g * sigmoid(g);
   double up = (beta_lin > 0.0) ? beta_lin * tanh(u / beta_lin) : u;
@@ -338,6 +346,7 @@ double oracle_situ(double g, double u, double beta, double beta_lin) {
 
 enum { ACT_BF16 = 0, ACT_MXFP8 = 1, ACT_NVFP4 = 2 };
 enum { W_MXFP4 = 0, W_NVFP4 = 1 };
+enum { ACT_FN_SITU = 0, ACT_FN_SWIGLU_BIAS = 1 };
 
 typedef struct {
   int T, H, I, E_total, E_loc, off, K, act, wt;
@@ -358,6 +367,8 @@ typedef struct {
   const float* alpha_g;     /* g1_alphas    [E_loc] or NULL (1) */
   const float* alpha_u;     /* g1_alphas_up [E_loc] or NULL (1) */
   const float* alpha2;      /* g2_alphas    [E_loc] or NULL (1) */
+  int activation;           /* ACT_FN_SITU (beta, beta_lin) or ACT_FN_SWIGLU_BIAS (alpha, beta) */
+  int topk_in_fc1;          /* 1: the routing weight scales H1 instead of the FC2 output */
 } oracle_args;
 
 /* Dequantise one packed FP4 matrix row (n elements) with its block scales:
@@ -397,6 +408,7 @@ typedef struct {
   const oracle_args* a;
   int R;                      /* kept pairs in the subset */
   const int32_t* pair_tok;    /* [R] token of each pair */
+  const float* pair_w;        /* [R] routing weight of each pair */
   const int32_t* exp_start;   /* [E_loc+1] pairs grouped by expert */
   double* y;                  /* [R, H] FC2 output per pair */
 } expert_ctx;
@@ -439,7 +451,12 @@ static void run_expert(void* p, long e) {
       for (int k = 0; k < H; ++k) { accg += (double)x[k] * wg[k]; accu += (double)x[k] * wu[k]; }
       double g = ag * g1g * xg * accg;
       double u = au * g1u * xg * accu;
-      hf[i] = (float)oracle_situ(g, u, a->beta[e], a->beta_lin[e]);
+      double h_act = (a->activation == ACT_FN_SWIGLU_BIAS) ? oracle_swiglu_bias(g, u, a->beta[e], a->beta_lin[e])
+                                                           : oracle_situ(g, u, a->beta[e], a->beta_lin[e]);
+      /* apply_topk_in_fc1: the slot's routing weight scales H1 before it is
+       * rounded for FC2, and the un-permute sum is unweighted */
+      if (a->topk_in_fc1) h_act *= (double)c->pair_w[pi];
+      hf[i] = (float)h_act;
     }
     /* The FC1 output as FC2 consumes it. */
     if (a->act == ACT_MXFP8) {
@@ -479,7 +496,7 @@ static void combine_token(void* p, long ti) {
   for (int j = 0; j < K; ++j) {
     int pi = c->slot_pair[(size_t)ti * K + j];
     if (pi < 0) continue;
-    double w = a->wts[(size_t)t * K + j];
+    double w = a->topk_in_fc1 ? 1.0 : a->wts[(size_t)t * K + j];
     const double* y = c->y + (size_t)pi * H;
     for (int n = 0; n < H; ++n) o[n] += w * y[n];
   }
@@ -503,6 +520,7 @@ int oracle_moe_forward(const oracle_args* a, int n_tok, const int32_t* toks, dou
   for (int e = 0; e < E; ++e) exp_start[e + 1] += exp_start[e];
   int R = exp_start[E];
   int32_t* pair_tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+  float* pair_w = (float*)malloc(sizeof(float) * (size_t)(R > 0 ? R : 1));
   int32_t* fill = (int32_t*)calloc((size_t)E + 1, sizeof(int32_t));
   for (int ti = 0; ti < n_tok; ++ti) {
     int t = toks ? toks[ti] : ti;
@@ -513,15 +531,16 @@ int oracle_moe_forward(const oracle_args* a, int n_tok, const int32_t* toks, dou
         int e = id - a->off;
         pi = exp_start[e] + fill[e]++;
         pair_tok[pi] = t;
+        pair_w[pi] = a->wts[(size_t)t * K + j];
       }
       slot_pair[(size_t)ti * K + j] = pi;
     }
   }
   double* y = (double*)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1) * a->H);
-  expert_ctx ec = {a, R, pair_tok, exp_start, y};
+  expert_ctx ec = {a, R, pair_tok, pair_w, exp_start, y};
   parallel_for(E, run_expert, &ec);
   combine_ctx cc = {a, toks, slot_pair, y, out};
   parallel_for(n_tok, combine_token, &cc);
-  free(slot_pair); free(exp_start); free(pair_tok); free(fill); free(y);
+  free(slot_pair); free(exp_start); free(pair_tok); free(pair_w); free(fill); free(y);
   return R;
 }

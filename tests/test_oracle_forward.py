@@ -139,7 +139,11 @@ def _situ_np(g, u, beta, beta_lin):
     return gate * up
 
 
-def brute_force(kw, alpha_power=1):
+def _swiglu_bias_np(g, u, alpha, beta):
+    return g * sigmoid(g * alpha) * (u + beta)
+
+
+def brute_force(kw, alpha_power=1, activation=0, topk_in_fc1=0):
     T, H, I, K = kw["T"], kw["H"], kw["I"], kw["top_k"]
     off, E_loc = kw["local_expert_offset"], kw["num_local_experts"]
     act, nv = kw["act"], kw["wt"] == W.W_NVFP4
@@ -170,10 +174,15 @@ def brute_force(kw, alpha_power=1):
             g2 = kw["w2_gscale"][e] if nv else 1.0
             g = ag[e] ** alpha_power * g1g * xg[t] * (W1[:I] @ X[t])
             u = au[e] ** alpha_power * g1u * xg[t] * (W1[I:] @ X[t])
-            a = _situ_np(g, u, kw["gemm1_alpha"][e], kw["gemm1_beta"][e]).astype(np.float32)
+            fn = _swiglu_bias_np if activation == oracle.ACT_FN_SWIGLU_BIAS else _situ_np
+            a = fn(g, u, kw["gemm1_alpha"][e], kw["gemm1_beta"][e])
+            w = float(kw["topk_weights"][t, j])
+            if topk_in_fc1:
+                a = a * w                  # the routing weight scales H1 before its rounding
+            a = a.astype(np.float32)
             h = _mxfp8_round_trip(a) if act == W.ACT_MXFP8 else _bf16(a)
             y = a2[e] * g2 * (W2 @ h)
-            out[t] += float(kw["topk_weights"][t, j]) * y
+            out[t] += (1.0 if topk_in_fc1 else w) * y
     return out
 
 
@@ -293,3 +302,56 @@ def test_double_applied_alpha_is_detected():
     bad = brute_force(kw, alpha_power=2)
     rms = np.sqrt(np.mean(good ** 2))
     assert np.max(np.abs(bad - good)) > 0.2 * rms
+
+
+# --------------------------------------------------------------------------
+# activation variants: SwigluBias, apply_topk_in_fc1
+# --------------------------------------------------------------------------
+
+def test_swiglu_bias_at_unit_alpha_zero_beta_is_swiglu():
+    """SwigluBias(alpha=1, beta=0) and SiTU with both caps off are both SwiGLU
+    g * sigmoid(g) * u, written as two different oracle functions."""
+    rng = np.random.default_rng(21)
+    for g, u in rng.normal(0, 4, (200, 2)):
+        assert oracle.swiglu_bias(g, u, 1.0, 0.0) == pytest.approx(oracle.situ(g, u, 0.0, 0.0), rel=1e-14, abs=1e-300)
+
+
+def test_swiglu_bias_shift_and_gate_limits():
+    rng = np.random.default_rng(22)
+    for g, u, a, b in rng.normal(0, 2, (200, 4)):
+        a = abs(a) + 0.1
+        # beta shifts the linear input
+        assert oracle.swiglu_bias(g, u, a, b) == pytest.approx(oracle.swiglu_bias(g, u + b, a, 0.0), rel=1e-12)
+    # a steep gate: sigmoid(alpha g) -> step(g)
+    assert oracle.swiglu_bias(2.0, 3.0, 1e4, 0.5) == pytest.approx(2.0 * 3.5, rel=1e-12)
+    assert abs(oracle.swiglu_bias(-2.0, 3.0, 1e4, 0.5)) < 1e-300
+
+
+@pytest.mark.parametrize("act,wt", [(W.ACT_BF16, W.W_MXFP4), (W.ACT_MXFP8, W.W_MXFP4),
+                                    (W.ACT_NVFP4, W.W_NVFP4)])
+@pytest.mark.parametrize("activation,topk_in_fc1", [(1, 0), (0, 1), (1, 1)])
+def test_variants_match_brute_force(act, wt, activation, topk_in_fc1):
+    wl = _small(act, wt, 3)
+    kw = _kwargs(wl)
+    if activation == 1:   # SwigluBias alpha ~ 1.7, beta ~ small
+        kw["gemm1_alpha"] = np.full_like(kw["gemm1_alpha"], 1.702)
+        kw["gemm1_beta"] = np.linspace(-0.5, 0.5, kw["gemm1_beta"].shape[0]).astype(np.float32)
+    got = oracle.moe_forward(**kw, activation=activation, apply_topk_in_fc1=topk_in_fc1)
+    ref = brute_force(kw, activation=activation, topk_in_fc1=topk_in_fc1)
+    _close(got, ref, rel=1e-7)
+    assert np.sqrt(np.mean(ref ** 2)) > 0
+
+
+def test_topk_in_fc1_differs_only_by_rounding_position():
+    """FC2 is linear, so moving the routing weight from the FC2 output to H1
+    changes only where H1 is rounded to bf16: the two outputs differ by
+    rounding-sized amounts, well inside the layer's parity bar (2% of rms),
+    and are not identical."""
+    wl = _small(W.ACT_BF16, W.W_MXFP4, 4)
+    kw = _kwargs(wl)
+    a = oracle.moe_forward(**kw)
+    b = oracle.moe_forward(**kw, apply_topk_in_fc1=1)
+    rms = np.sqrt(np.mean(a ** 2))
+    assert np.max(np.abs(a - b)) <= 2e-2 * rms
+    assert np.sqrt(np.mean((a - b) ** 2)) <= 2.0 ** -8 * rms
+    assert not np.array_equal(a, b)

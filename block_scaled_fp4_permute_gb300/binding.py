@@ -19,6 +19,7 @@ from . import build as _build
 SITU_OK = 0
 SITU_ERR_DEVICE_TIMEOUT = 7
 SITU_ACT_BF16, SITU_ACT_MXFP8, SITU_ACT_NVFP4 = 0, 1, 2
+SITU_ACT_FN_SITU, SITU_ACT_FN_SWIGLU_BIAS = 0, 1
 SITU_W_MXFP4, SITU_W_NVFP4 = 0, 1
 
 _lib = None
@@ -39,7 +40,8 @@ class SituMoeArgs(ctypes.Structure):
             "hidden_states", "hidden_states_q", "hidden_states_scale", "hidden_states_gscale",
             "topk_ids", "topk_weights", "w1", "w1_scale", "w1_gscale", "w2", "w2_scale",
             "w2_gscale", "gemm1_alpha", "gemm1_beta", "g1_alphas", "g1_alphas_up", "g2_alphas",
-            "out", "scales_packed")] + [("fuse_combine", ctypes.c_int32)]
+            "out", "scales_packed")] + [(n, ctypes.c_int32) for n in (
+                "fuse_combine", "activation", "apply_topk_in_fc1")]
 
 
 def library_path() -> str:
@@ -258,7 +260,8 @@ class Layer:
     forward call is a single C-ABI call (the bench times exactly this)."""
 
     def __init__(self, wl, out: Optional[torch.Tensor] = None, x_q=None, x_scale=None,
-                 pack_scales: bool = True, fuse_combine: bool = False):
+                 pack_scales: bool = True, fuse_combine: bool = False, activation: int = 0,
+                 apply_topk_in_fc1: bool = False):
         self.wl = wl
         dev = wl.x_bf16.device
         self.out = out if out is not None else torch.empty((wl.T, wl.H), dtype=torch.bfloat16,
@@ -288,6 +291,8 @@ class Layer:
         self._keep = kw
         self.args = make_args(**kw)
         self.args.fuse_combine = 1 if fuse_combine else 0
+        self.args.activation = int(activation)
+        self.args.apply_topk_in_fc1 = 1 if apply_topk_in_fc1 else 0
         # weight scales in the block-scaled GEMMs' layout, packed once per
         # weight set (as at weight-load time) when the shapes use it
         self.scales_packed = None

@@ -180,4 +180,13 @@ __device__ __forceinline__ float situ_f(float g, float u, float b, float bl) {
   return __fdividef(num, den);
 }
 
+// FC1's gated activation: kind 0 is SiTU (caps p0, p1 as above), kind 1
+// SwigluBias g * sigmoid(p0 * g) * (u + p1) (the exponent argument clamped
+// to [-80, 80], where sigmoid is 0 or 1 to fp32 precision).
+constexpr int kActSitu = 0, kActSwigluBias = 1;
+__device__ __forceinline__ float act_f(int kind, float g, float u, float p0, float p1) {
+  if (kind == kActSwigluBias) return __fdividef(g * (u + p1), 1.f + __expf(-fminf(fmaxf(p0 * g, -80.f), 80.f)));
+  return situ_f(g, u, p0, p1);
+}
+
 }  // namespace situ

@@ -294,6 +294,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
         const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
         const int nkh = p.I / kBK;   // FC2's stages: H1's scale blocks per tile
+        const float rw = (p.topk_fc1 && vrow) ? __ldg(p.topk_weights + __ldg(p.permuted_src + row)) : 1.f;
         for (int c0 = 0; c0 < C::NH; c0 += 32) {
           float gt[32], up[32];
           tmem_ld16(trow + c0, gt);
@@ -306,7 +307,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           float amax = 0.f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            v[j] = situ_f(gt[j] * ag, up[j] * au, bt, btl);
+            v[j] = act_f(p.act_kind, gt[j] * ag, up[j] * au, bt, btl) * rw;
             if (LO) v[j] = bf16_lo(f32x2_to_bf16x2(v[j], 0.f));   // w4a16: H1 is bf16
             amax = fmaxf(amax, fabsf(v[j]));
           }
@@ -347,7 +348,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         if (p.fuse && wrow0 + lane < nrows) {
           const int src = __ldg(p.permuted_src + row0 + wrow0 + lane);
           my_t = src / p.top_k;
-          my_w = __ldg(p.topk_weights + src);
+          my_w = p.topk_fc1 ? 1.f : __ldg(p.topk_weights + src);   // else the weight is in H1
         }
         for (int c0 = 0; c0 < C::BN; c0 += 32) {
           float acc[32];

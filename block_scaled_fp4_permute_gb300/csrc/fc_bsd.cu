@@ -335,7 +335,8 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
 #pragma unroll
           for (int t = 0; t < kTok; ++t) {
             if (t >= nrows) break;
-            float h = situ_f(a1[t] * ag, a2[t] * au, bt, btl);
+            float h = act_f(p.act_kind, a1[t] * ag, a2[t] * au, bt, btl);
+            if (p.topk_fc1) h *= __ldg(p.topk_weights + __ldg(p.permuted_src + row0 + t));
             if (LO) h = bf16_lo(f32x2_to_bf16x2(h, 0.f));   // w4a16: H1 is bf16
             const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
             const int ex = mxfp8_exponent(amax);

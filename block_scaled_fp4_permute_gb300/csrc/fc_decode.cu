@@ -137,6 +137,7 @@ template <bool FC1, bool WNV, bool ABLK>
 __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float s_tok[kNT];       // per-token activation scale (rows without block scales)
+  __shared__ float s_w[kNT];         // routing weight of each row when it scales H1
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
   const int K = p.K;
   const int nkb = K / 32;
@@ -263,7 +264,11 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
       sS[tok * nkb4 + b] = 0.f;
     }
     __syncthreads();
-    if (tid < kNT) s_tok[tid] = (tid < nrows && !ABLK) ? sS[tid * nkb4] : (tid < nrows ? 1.f : 0.f);
+    if (tid < kNT) {
+      s_tok[tid] = (tid < nrows && !ABLK) ? sS[tid * nkb4] : (tid < nrows ? 1.f : 0.f);
+      s_w[tid] = (FC1 && p.topk_fc1 && tid < nrows) ? __ldg(p.topk_weights + __ldg(p.permuted_src + row0 + tid))
+                                                     : 1.f;
+    }
   }
   __syncthreads();
 
@@ -281,8 +286,10 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
         const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
         const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
         const float gg = WNV ? __ldg(p.w1_gs + 2 * e) : 1.f, gu = WNV ? __ldg(p.w1_gs + 2 * e + 1) : 1.f;
-        sH[(2 * c) * 64 + il] = situ_f(acc[0] * (ag * gg * t0), acc[2] * (au * gu * t0), bt, btl);
-        sH[(2 * c + 1) * 64 + il] = situ_f(acc[1] * (ag * gg * t1), acc[3] * (au * gu * t1), bt, btl);
+        sH[(2 * c) * 64 + il] =
+            act_f(p.act_kind, acc[0] * (ag * gg * t0), acc[2] * (au * gu * t0), bt, btl) * s_w[2 * c];
+        sH[(2 * c + 1) * 64 + il] =
+            act_f(p.act_kind, acc[1] * (ag * gg * t1), acc[3] * (au * gu * t1), bt, btl) * s_w[2 * c + 1];
       }
       __syncthreads();
       if (tid < kNT * 2) {

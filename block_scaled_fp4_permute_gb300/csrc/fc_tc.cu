@@ -300,6 +300,7 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         const float ag = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
         const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
         const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+        const float rw = (p.topk_fc1 && vrow) ? __ldg(p.topk_weights + __ldg(p.permuted_src + row)) : 1.f;
         for (int c0 = 0; c0 < kBN / 2; c0 += 32) {
           float gt[32], up[32];
           tmem_ld16(trow + c0, gt);
@@ -311,7 +312,8 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            v[j] = situ_f(gt[j] * (xs * wsc[c0 + j] * ag), up[j] * (xs * wsc[128 + c0 + j] * au), bt, btl);
+            v[j] = act_f(p.act_kind, gt[j] * (xs * wsc[c0 + j] * ag), up[j] * (xs * wsc[128 + c0 + j] * au), bt,
+                         btl) * rw;
           if (p.h_mxfp8) {   // the MXFP8 round trip FC2 consumes (w4a8)
             float amax = 0.f;
 #pragma unroll

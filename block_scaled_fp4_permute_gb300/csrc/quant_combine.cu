@@ -68,7 +68,7 @@ combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ slot_to
     for (int u = 0; u < 4; ++u) {
       const int j = j0 + u;
       r[u] = j < K ? __ldg(slot_to_row + (size_t)t * K + j) : -1;
-      wt[u] = r[u] >= 0 ? __ldg(w + (size_t)t * K + j) : 0.f;
+      wt[u] = r[u] >= 0 ? (w ? __ldg(w + (size_t)t * K + j) : 1.f) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)

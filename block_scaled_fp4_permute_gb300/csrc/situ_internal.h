@@ -86,6 +86,9 @@ struct FcdParams {
   int I;
   const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs;
   int h_mxfp8;                   // H1 is the MXFP8 round trip of h (else bf16 of h)
+  int act_kind, topk_fc1;        // FC1's activation (kActSitu / kActSwigluBias); routing weight in H1
+  const int32_t* permuted_src;   // topk_fc1: row -> slot, and the slots' weights
+  const float* topk_weights;
   uint16_t* h16;                 // f16 block rows [S, pad128(I)]
   float* hs;                     // [S, pad128(I)/32]
   // FC2
@@ -110,6 +113,9 @@ struct FcpParams {
   // FC1
   const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs;
   int h_mxfp8;
+  int act_kind, topk_fc1;
+  const int32_t* permuted_src;
+  const float* topk_weights;
   uint16_t* h_out;               // bf16 [S, I]
   // FC2
   const float *alpha2, *w2_gs;
@@ -140,6 +146,7 @@ struct FcqParams {
   const float* beta_lin;
   const float* alpha_g;
   const float* alpha_u;
+  int act_kind, topk_fc1;        // FC1's activation; routing weight in H1 (uses the fields below)
   uint8_t* hq;
   uint8_t* hsp;
   uint8_t* hq_lo;                // FC1 of bf16 activations: H1's lo rows and blocks
@@ -225,6 +232,9 @@ struct FcwParams {
   int E_loc, n_ntiles;
   // FC1
   const float *beta, *beta_lin, *alpha_g, *alpha_u;
+  int act_kind, topk_fc1;        // FC1's activation; routing weight in H1
+  const int32_t* permuted_src;
+  const float* topk_weights;
   uint8_t *h, *hs;               // H1 rows and scale rows, as the token side above
   int hs_stride;
   // FC2

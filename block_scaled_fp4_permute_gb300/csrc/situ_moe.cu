@@ -143,6 +143,7 @@ situ_status validate(const situ_moe_args* a) {
   const bool w4a8 = a->act_dtype == SITU_ACT_MXFP8 && a->weight_dtype == SITU_W_MXFP4;
   const bool nv = a->act_dtype == SITU_ACT_NVFP4 && a->weight_dtype == SITU_W_NVFP4;
   if (!(w4a16 || w4a8 || nv)) return SITU_ERR_UNSUPPORTED;
+  if (a->activation != SITU_ACT_FN_SITU && a->activation != SITU_ACT_FN_SWIGLU_BIAS) return SITU_ERR_UNSUPPORTED;
   if (a->T == 0) return SITU_OK;
   if (!a->topk_ids || !a->topk_weights || !a->w1 || !a->w1_scale || !a->w2 || !a->w2_scale ||
       !a->gemm1_alpha || !a->gemm1_beta || !a->out)
@@ -332,6 +333,10 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     w.beta_lin = a->gemm1_beta;
     w.alpha_g = a->g1_alphas;
     w.alpha_u = a->g1_alphas_up;
+    w.act_kind = a->activation;
+    w.topk_fc1 = a->apply_topk_in_fc1 != 0;
+    w.permuted_src = psrc;
+    w.topk_weights = a->topk_weights;
     w.h = ws + L.h16;
     w.hs = ws + L.whs;
     w.hs_stride = fcw_scale_stride(a->I);
@@ -388,6 +393,10 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.alpha_u = a->g1_alphas_up;
     d.w1_gs = a->w1_gscale;
     d.h_mxfp8 = a->act_dtype == SITU_ACT_MXFP8;
+    d.act_kind = a->activation;
+    d.topk_fc1 = a->apply_topk_in_fc1 != 0;
+    d.permuted_src = psrc;
+    d.topk_weights = a->topk_weights;
     d.h16 = (uint16_t*)(ws + L.h16);
     d.hs = (float*)(ws + L.h16s);
     if ((err = launch_fcd(d, true, nv, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
@@ -453,6 +462,10 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.beta_lin = a->gemm1_beta;
     q.alpha_g = a->g1_alphas;
     q.alpha_u = a->g1_alphas_up;
+    q.act_kind = a->activation;
+    q.topk_fc1 = a->apply_topk_in_fc1 != 0;
+    q.permuted_src = psrc;
+    q.topk_weights = a->topk_weights;
     q.hq = ws + L.h16;
     q.hsp = ws + L.hsp;
     q.hq_lo = lo ? q.hq + (size_t)S * a->I : nullptr;
@@ -471,8 +484,6 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.alpha2 = a->g2_alphas;
     q.y_out = y;
     q.fuse = fused ? 1 : 0;
-    q.permuted_src = psrc;
-    q.topk_weights = a->topk_weights;
     q.top_k = a->top_k;
     q.out_acc = y;   // fused: the accumulator [T, H] takes the place of Y
     if ((err = launch_fcq(q, q.hq, q.hq_lo, S, a->w2, a->num_local_experts, false, max_tiles, st)) !=
@@ -520,6 +531,10 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     f.alpha_u = a->g1_alphas_up;
     f.w1_gs = a->w1_gscale;
     f.h_mxfp8 = a->act_dtype == SITU_ACT_MXFP8;
+    f.act_kind = a->activation;
+    f.topk_fc1 = a->apply_topk_in_fc1 != 0;
+    f.permuted_src = psrc;
+    f.topk_weights = a->topk_weights;
     f.h_out = h1;
     if ((err = launch_fcp(f, g16.x16, S, pad128(a->H), a->w1, a->num_local_experts, true, nv, max_tiles, st)) !=
         cudaSuccess)
@@ -557,7 +572,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   if (fused)
     err = launch_acc_to_bf16(y, (long)a->T * a->H, a->out, st);
   else
-    err = launch_combine(y, s2r, a->topk_weights, a->T, a->top_k, a->H, a->out, st);
+    err = launch_combine(y, s2r, a->apply_topk_in_fc1 ? nullptr : a->topk_weights, a->T, a->top_k, a->H, a->out,
+                         st);
   if (err != cudaSuccess) return SITU_ERR_CUDA;
   mark(5);
   return cuda_status(cudaGetLastError());

@@ -40,6 +40,7 @@ import numpy as np
 import torch
 
 ACT_BF16, ACT_MXFP8, ACT_NVFP4 = 0, 1, 2
+ACT_FN_SITU, ACT_FN_SWIGLU_BIAS = 0, 1      # FC1 activation kinds
 W_MXFP4, W_NVFP4 = 0, 1
 
 # The workload families; "tiny" is small enough for the oracle in

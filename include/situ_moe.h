@@ -224,6 +224,9 @@ situ_status situ_moe_quant_nvfp4(const void* x_bf16, int32_t T, int32_t H, uint8
  * must lie in [2, 252] so that every dequantised weight is a bf16 normal or
  * zero (the layer's synthetic and real checkpoints are far inside this).
  * --------------------------------------------------------------------- */
+/* FC1's gated activation (situ_moe_args.activation). */
+typedef enum { SITU_ACT_FN_SITU = 0, SITU_ACT_FN_SWIGLU_BIAS = 1 } situ_act_fn;
+
 typedef struct situ_moe_args {
   int32_t T;                      /* tokens */
   int32_t H;                      /* hidden size (FC1 K, FC2 N) */
@@ -264,6 +267,16 @@ typedef struct situ_moe_args {
                                      trip through HBM, but the order of the additions varies
                                      from run to run, so outputs are reproducible only to
                                      fp32 rounding.  The other paths ignore it. */
+  int32_t activation;             /* FC1's gated activation, situ_act_fn: SITU (default; the
+                                     caps gemm1_alpha / gemm1_beta) or SWIGLU_BIAS, CUTLASS's
+                                     g * sigmoid(alpha * g) * (u + beta) printed beside SiTU in
+                                     PR #17865's golden reference, with alpha = gemm1_alpha and
+                                     beta = gemm1_beta per local expert (SwiGLU: SITU with both
+                                     caps <= 0, or SWIGLU_BIAS with alpha 1, beta 0) */
+  int32_t apply_topk_in_fc1;      /* 1: each slot's routing weight scales its H1 row in FC1's
+                                     epilogue, before H1 is rounded for FC2, and the
+                                     un-permute sum is unweighted (the MegaMoE option of PR
+                                     #17865); 0: the weight is applied in the sum */
 } situ_moe_args;
 
 /* Workspace bytes situ_moe_forward needs for these shapes (0 on bad args).

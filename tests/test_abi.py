@@ -176,3 +176,10 @@ def test_quant_nvfp4_argument_errors(lib):
     assert lib.situ_moe_quant_nvfp4(p, 0, 64, None, None, None, None) == 0
     assert lib.situ_moe_quant_nvfp4(None, 4, 64, p, p, p, None) == 1
     assert lib.situ_moe_quant_nvfp4(ctypes.c_void_p(264), 4, 64, p, p, p, None) == 6
+
+
+def test_forward_rejects_unknown_activation(lib):
+    a = _args()
+    a.activation = 2
+    assert _fwd(lib, a) == 3
+    assert lib.situ_moe_forward_launches(ctypes.byref(a)) == -1

@@ -69,8 +69,9 @@ def run_layer(wl):
     return layer, out.float().cpu().numpy()
 
 
-def oracle_out(wl, tokens=None):
-    """The oracle's layer on the oracle's own activation quantisation."""
+def oracle_out(wl, tokens=None, **variant):
+    """The oracle's layer on the oracle's own activation quantisation
+    (``variant``: activation / apply_topk_in_fc1)."""
     if wl.act == W.ACT_MXFP8:
         q, s = oracle.quant_mxfp8(wl.host("x_bf16"))
         kw = W.oracle_kwargs(wl, x_q=q, x_scale=s)
@@ -79,7 +80,7 @@ def oracle_out(wl, tokens=None):
         kw = W.oracle_kwargs(wl, x_q=q, x_scale=s, x_gscale=g)
     else:
         kw = W.oracle_kwargs(wl)
-    return oracle.moe_forward(**kw, tokens=tokens)
+    return oracle.moe_forward(**kw, tokens=tokens, **variant)
 
 
 def token_subset(T, n, seed=0):
@@ -400,3 +401,35 @@ def test_fused_combine_prefill_w4a8_subset():
     assert layer.device_status() == 0
     toks = token_subset(wl.T, 128, seed=5)
     assert_parity(out[toks], oracle_out(wl, toks), "prefill w4a8, fused combine")
+
+
+
+_VARIANT_SHAPES = [
+    ("decode", {}),                                                                  # block-scaled decode, bf16
+    ("tiny", dict(T=64, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_MXFP8)),   # ... MXFP8
+    ("tiny", dict(T=300, H=256, I=128, E_total=4, E_loc=4, off=0, K=2, act=W.ACT_MXFP8)),    # block-scaled prefill
+    ("tiny", dict(T=300, H=256, I=128, E_total=4, E_loc=4, off=0, K=2)),                     # ... bf16 hi + lo
+    ("tiny", dict(T=29, H=320, I=160, E_total=16, E_loc=8, off=8, K=4, act=W.ACT_NVFP4,
+                  wt=W.W_NVFP4)),                                                    # f16 prefill tiles
+    ("tiny", dict(T=5, H=160, I=96, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4,
+                  wt=W.W_NVFP4)),                                                    # register decode tiles
+    ("tiny", dict(T=17, H=160, I=96, E_total=12, E_loc=5, off=4, K=3)),             # ... bf16, odd shapes
+]
+
+
+@pytest.mark.parametrize("name,over", _VARIANT_SHAPES)
+@pytest.mark.parametrize("activation,topk_in_fc1", [(W.ACT_FN_SWIGLU_BIAS, False), (W.ACT_FN_SITU, True),
+                                                    (W.ACT_FN_SWIGLU_BIAS, True)])
+def test_activation_variants_on_every_path(name, over, activation, topk_in_fc1):
+    """SwigluBias (alpha, beta per expert from gemm1_alpha / gemm1_beta) and the
+    routing weight applied in FC1's epilogue, on every GEMM path."""
+    wl = W.make(name, device="cuda", params="k3_random", **over)
+    if activation == W.ACT_FN_SWIGLU_BIAS:
+        wl.gemm1_alpha = torch.full_like(wl.gemm1_alpha, 1.702)
+        wl.gemm1_beta = torch.linspace(-0.5, 0.5, wl.E_loc, device="cuda")
+    layer = binding.Layer(wl, activation=activation, apply_topk_in_fc1=topk_in_fc1)
+    out = layer().float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    ref = oracle_out(wl, activation=activation, apply_topk_in_fc1=int(topk_in_fc1))
+    assert_parity(out, ref, f"{name} {over} activation={activation} topk_in_fc1={topk_in_fc1}")

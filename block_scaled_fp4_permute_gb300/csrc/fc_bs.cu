@@ -454,7 +454,22 @@ __global__ void __launch_bounds__(256) gather8_kernel(const Gather8Params p) {
       const long t = __ldg(p.permuted_src + r) / p.top_k;
       const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * K);
       uint4* dst = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
-      for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+      // all of the lane's loads first, then the stores: one L2 round trip
+      // per row instead of one per 16-byte piece
+      constexpr int kU = 8;
+      for (int i0 = 0; i0 < n16; i0 += 32 * kU) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < n16) v[u] = __ldg(src + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < n16) dst[i] = v[u];
+        }
+      }
       const uint8_t* ss = p.x_s + (size_t)t * nsb;
       for (int kk = lane; kk < nk; kk += 32) {
         const uint32_t w = p.s_vec ? __ldg(reinterpret_cast<const uint32_t*>(ss) + kk)

@@ -91,12 +91,17 @@ def algorithmic_bytes(wl, R, touched):
     act_in = {0: T * H * 2, 1: T * H + T * H // 32, 2: T * H // 2 + T * H // 16 + 4 * T}[wl.act]
     route = T * K * 8
     out = T * H * 2
+    # bytes per element of the FC2 rows Y the combine reads: f16 + a scale byte
+    # per 32 on the block-scaled prefill tiles, fp32 elsewhere
+    blk_prefill = (wl.act in (0, 1) and wl.wt == 0 and H % 128 == 0 and I % 128 == 0
+                   and T * K / max(wl.E_total, 1) > 6.0)
+    y_bytes = 2 + 1 / 32 if blk_prefill else 4
     return {
         "permute": T * K * 4 + 2 * T * K * 4 + 2 * wl.E_loc * 4,
         "gather": act_in * R / max(T, 1) + R * H * 2,
         "fc1": w1 + R * H * 2 + R * I * 2,
         "fc2": w2 + R * I * 2 + R * H * 2,
-        "combine": R * H * 2 + route + out,
+        "combine": R * H * y_bytes + route + out,
         "quant": T * H * 2 + (T * H + T * H // 32 if wl.act == 1 else T * H // 2 + T * H // 16 + 4 * T),
         "layer": w1 + w2 + act_in + route + out,
     }

@@ -93,6 +93,29 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return (uint32_t)d;
 }
 
+// fp32 pair -> f16 pair, round to nearest even; lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float f16_to_f32(uint32_t h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((uint16_t)h));
+  return f;
+}
+
+// Y rows of the block-scaled prefill path: f16 mantissas with one
+// power-of-two scale per 32 elements, 2^(byte - 127), chosen so that the
+// block maximum lies in [2^14, 2^15): 11 significant bits for every element
+// within 2^-28 of the block maximum.
+__device__ __forceinline__ int y16_exponent(float amax) {
+  const int k = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (k == 0) return 0;                 // zero (or an fp32 subnormal block)
+  const int ex = k - 127 - 14;
+  return ex < -127 ? -127 : (ex > 127 ? 127 : ex);
+}
+
 // Two E4M3 codes (low byte = first) to fp32, exactly, through the hardware
 // E4M3 -> f16 conversion (every finite E4M3 value is an f16).
 __device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& lo, float& hi) {

@@ -337,7 +337,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           dst[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
           dst[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
         }
-      } else {
+      } else if (p.y_scale == nullptr) {
         const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
         // this warp's staging block; the warp owns tile rows 32 quarter .. + 31
         uint8_t* yst = smem + C::kOffY + (warp - 4) * 32 * C::kYRow;
@@ -374,6 +374,48 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
             } else if (wrow0 + r < nrows && n < p.Mtot) {
               *reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + wrow0 + r) * p.Mtot + n) = v;
             }
+          }
+          __syncwarp();
+        }
+      } else {
+        // Y as f16 rows with a power-of-two scale per 32 columns: half the
+        // bytes of the fp32 rows that the combine reads back
+        const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
+        uint8_t* yst = smem + C::kOffY + (warp - 4) * 32 * C::kYRow;
+        const int wrow0 = quarter * 32;
+        uint16_t* y16 = reinterpret_cast<uint16_t*>(p.y_out);
+        const int nb = p.Mtot / 32;
+        for (int c0 = 0; c0 < C::BN; c0 += 32) {
+          float acc[32];
+          tmem_ld16(trow + c0, acc);
+          tmem_ld16(trow + c0 + 16, acc + 16);
+          float amax = 0.f;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            acc[q] *= a2;
+            amax = fmaxf(amax, fabsf(acc[q]));
+          }
+          const int ex = y16_exponent(amax);
+          const float inv = exp2i(-ex);
+          // own row (64 bytes) into the staging block ...
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(yst + lane * C::kYRow + 16 * q) =
+                make_uint4(pack_f16x2(acc[8 * q] * inv, acc[8 * q + 1] * inv),
+                           pack_f16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                           pack_f16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
+                           pack_f16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+          const int n0 = nbase + c0;
+          if (m < nrows && n0 < p.Mtot) p.y_scale[(size_t)(row0 + m) * nb + n0 / 32] = (uint8_t)(ex + 127);
+          __syncwarp();
+          // ... and out as 8 rows x 64 bytes per instruction
+          const int n = n0 + 8 * (lane & 3);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 8 * j + (lane >> 2);
+            const uint4 v = *reinterpret_cast<const uint4*>(yst + r * C::kYRow + 16 * (lane & 3));
+            if (wrow0 + r < nrows && n < p.Mtot)
+              *reinterpret_cast<uint4*>(y16 + (size_t)(row0 + wrow0 + r) * p.Mtot + n) = v;
           }
           __syncwarp();
         }

@@ -23,7 +23,7 @@ bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
-  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, total;
+  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, total;
 };
 
 // Decode-like routings (about six or fewer rows per expert) take the
@@ -114,6 +114,7 @@ Layout make_layout(const situ_moe_args* a) {
   const size_t nblk = a->act_dtype == SITU_ACT_BF16 ? 2 : 1;   // hi and lo blocks for bf16
   L.xsp = take(bs ? nblk * fcq_act_scale_bytes(tiles, a->H) : 0);
   L.hsp = take(bs ? nblk * fcq_act_scale_bytes(tiles, a->I) : 0);
+  L.ys = take(bs ? S * (size_t)(a->H / 32) : 0);   // scale bytes of the f16 Y rows
   const bool w = fcw_shapes(a);
   L.wsp = take((bs || w) && !a->scales_packed ? packed_total_bytes(a) : 0);
   // decode tiles: hi / lo scale rows of the input and of H1 (the E4M3 rows
@@ -272,6 +273,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   };
 
   bool fused = false;   // FC2 adds into the output accumulator (block-scaled prefill only)
+  bool y16 = false;     // FC2 writes Y as f16 rows + scale bytes (block-scaled prefill)
   mark(0);
   cudaError_t err = launch_permute(a->topk_ids, a->T, a->top_k, a->num_local_experts,
                                    a->local_expert_offset, tile_n, counts, offsets, tile_offsets,
@@ -485,6 +487,9 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.y_out = y;
     q.fuse = fused ? 1 : 0;
     q.top_k = a->top_k;
+    // unfused: Y as f16 rows with a scale per 32 columns (half the bytes of fp32)
+    q.y_scale = fused ? nullptr : ws + L.ys;
+    y16 = !fused;
     q.out_acc = y;   // fused: the accumulator [T, H] takes the place of Y
     if ((err = launch_fcq(q, q.hq, q.hq_lo, S, a->w2, a->num_local_experts, false, max_tiles, st)) !=
         cudaSuccess)
@@ -571,6 +576,9 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
 
   if (fused)
     err = launch_acc_to_bf16(y, (long)a->T * a->H, a->out, st);
+  else if (y16)
+    err = launch_combine16(y, ws + L.ys, s2r, a->apply_topk_in_fc1 ? nullptr : a->topk_weights, a->T, a->top_k,
+                           a->H, a->out, st);
   else
     err = launch_combine(y, s2r, a->apply_topk_in_fc1 ? nullptr : a->topk_weights, a->T, a->top_k, a->H, a->out,
                          st);

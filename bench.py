@@ -305,10 +305,14 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    graph = layer.capture() if args.graph else None
     for i in range(args.steps):
         flush.zero_()
         bounds[i][0].record(stream)
-        layer()
+        if graph is not None:
+            graph.replay()
+        else:
+            layer()
         bounds[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -421,6 +425,7 @@ def run_ours(args):
                    "kept_pairs": R, "touched_experts": touched,
                    "l2": "flushed between steps (256 MiB write, outside the step events)",
                    "parallelism": f"replicas x{ws}, no collective",
+                   "launch": "CUDA graph replay of the layer call" if args.graph else "eager C-ABI call",
                    "combine": "fused into FC2 (fp32 reductions)" if args.fuse_combine
                    else "separate kernel, ascending slot order"},
         "roofline": roof,
@@ -459,6 +464,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of a CUDA graph of the layer call instead of eager C-ABI calls")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="FC2 adds weight * Y into an fp32 accumulator (block-scaled prefill tiles); "
                          "not bitwise reproducible run to run")

@@ -331,6 +331,24 @@ class Layer:
         situ_moe_forward_profiled(self.args, self.workspace, events, stream)
         return self.out
 
+    def capture(self, warmup: bool = True):
+        """A CUDA graph of one __call__ (the activation quantisation, if any,
+        and the forward's kernels, with their programmatic dependencies).
+        situ_moe_forward never synchronises the host, so a call can be
+        captured; the graph replays on the same buffers.  Returns the
+        torch.cuda.CUDAGraph; ``graph.replay()`` runs one layer pass."""
+        if warmup:   # one eager call first: per-device attribute set-up
+            self()
+            torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self(stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
     def __call__(self, stream=None) -> torch.Tensor:
         """One pass of the layer; for MXFP8 and NVFP4 activations this includes
         their quantisation from the bf16 hidden states."""

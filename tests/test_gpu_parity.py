@@ -433,3 +433,24 @@ def test_activation_variants_on_every_path(name, over, activation, topk_in_fc1):
     assert layer.device_status() == 0
     ref = oracle_out(wl, activation=activation, apply_topk_in_fc1=int(topk_in_fc1))
     assert_parity(out, ref, f"{name} {over} activation={activation} topk_in_fc1={topk_in_fc1}")
+
+
+@pytest.mark.parametrize("name,T", [("decode", None), ("nvfp4", 1), ("prefill_w4a8", 512), ("ep_shard", 256),
+                                    ("tiny", None)])
+def test_cuda_graph_replay_matches_eager(name, T):
+    """One layer call captured in a CUDA graph (no host synchronisation in
+    the forward, programmatic launches included) replays to the same bytes."""
+    wl = W.make(name, device="cuda", T=T) if T else wl_(name)
+    layer = binding.Layer(wl)
+    eager = layer().clone()
+    torch.cuda.synchronize()
+    g = layer.capture()
+    layer.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(layer.out, eager)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(layer.out, eager)
+    assert layer.device_status() == 0

@@ -227,22 +227,24 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     }
   } else if (warp == 1) {
     // ---------------- scale copies + MMA issuer ----------------
-    if (lane == 0) {
-      long it = 0;
-      int li = 0;
-      bool ok = true;
-      for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
-        const int buf = li & 1, use = li >> 1;
-        if (use > 0 && !mbar_wait(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 22)) break;
+    // the whole warp walks the loop; one elected lane issues
+    const bool leader = elect_one();
+    long it = 0;
+    int li = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+      const int buf = li & 1, use = li >> 1;
+      if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 22)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t d = tmem + (uint32_t)(buf * C::BN);
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int s = (int)(it % kStages);
+        if (!mbar_wait_warp(full(s), (uint32_t)((it / kStages) & 1), p.err, 23)) {
+          ok = false;
+          break;
+        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t d = tmem + (uint32_t)(buf * C::BN);
-        for (int kk = 0; kk < nk; ++kk, ++it) {
-          const int s = (int)(it % kStages);
-          if (!mbar_wait(full(s), (uint32_t)((it / kStages) & 1), p.err, 23)) {
-            ok = false;
-            break;
-          }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (leader) {
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
           const uint32_t sfa = tmem + (uint32_t)(C::kSfCol0 + s * kSfColsPerStage);
           const uint32_t sfb = sfa + 4 * C::kNA;
@@ -261,13 +263,18 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           }
           mma_commit(empty(s));
         }
-        if (!ok) break;
-        mma_commit(acc_full(buf));
+        __syncwarp();
       }
-      // unwind: every MMA and scale copy issued so far has completed
+      if (!ok) break;
+      if (leader) mma_commit(acc_full(buf));
+      __syncwarp();
+    }
+    // unwind: every MMA and scale copy issued so far has completed
+    if (leader) {
       mma_commit(drain);
       drain_wait(drain, 0);
     }
+    __syncwarp();
   } else if (warp >= 4) {
     // ---------------- epilogue: thread = token row (TMEM lane) ----------------
     // warpgroup buf drains accumulator buf, i.e. this CTA's items buf, buf + 2, ...

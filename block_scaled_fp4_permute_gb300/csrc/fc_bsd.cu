@@ -242,23 +242,25 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
     }
   } else if (warp == 5) {
     // ---------------- scale copies + MMA issuer ----------------
-    if (lane == 0) {
-      long it = 0;
-      int li = 0;
-      bool ok = true;
-      for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
-        const int buf = li & 1, use = li >> 1;
-        if (use > 0 && !mbar_wait(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 42)) break;
+    // the whole warp walks the loop; one elected lane issues
+    const bool leader = elect_one();
+    long it = 0;
+    int li = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+      const int buf = li & 1, use = li >> 1;
+      if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 42)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t d1 = tmem + (uint32_t)(buf * 64);
+      const uint32_t d2 = d1 + NB;
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int s = (int)(it % kStages);
+        if (!mbar_wait_warp(full(s), (uint32_t)((it / kStages) & 1), p.err, 43)) {
+          ok = false;
+          break;
+        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t d1 = tmem + (uint32_t)(buf * 64);
-        const uint32_t d2 = d1 + NB;
-        for (int kk = 0; kk < nk; ++kk, ++it) {
-          const int s = (int)(it % kStages);
-          if (!mbar_wait(full(s), (uint32_t)((it / kStages) & 1), p.err, 43)) {
-            ok = false;
-            break;
-          }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (leader) {
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
           const uint32_t sfw = tmem + (uint32_t)(kSfCol0 + s * kSfColsPerStage);
           const uint32_t sft = sfw + 8;
@@ -278,12 +280,17 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           }
           mma_commit(empty(s));
         }
-        if (!ok) break;
-        mma_commit(acc_full(buf));
+        __syncwarp();
       }
+      if (!ok) break;
+      if (leader) mma_commit(acc_full(buf));
+      __syncwarp();
+    }
+    if (leader) {
       mma_commit(drain);
       drain_wait(drain, 0);
     }
+    __syncwarp();
   } else {
     // ---------------- epilogue: thread = weight row (TMEM lane) ----------------
     const int l = warp * 32 + lane;

@@ -166,13 +166,15 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      bool ok = true;
-      for (int kk = 0; kk < nk && ok; ++kk) {
-        const int s = kk % kStages, par = (kk / kStages) & 1;
-        ok = mbar_wait(full_a(s), par, p.err, 12) && mbar_wait(full_b(s), par, p.err, 13);
-        if (!ok) break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // the whole warp walks the loop; one elected lane issues
+    const bool leader = elect_one();
+    bool ok = true;
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % kStages, par = (kk / kStages) & 1;
+      ok = mbar_wait_warp(full_a(s), par, p.err, 12) && mbar_wait_warp(full_b(s), par, p.err, 13);
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (leader) {
         const uint64_t ad = sdesc(sbase + kOffA + s * kABytes);
         const uint64_t bd = sdesc(sbase + kOffB + s * kBBytes);
 #pragma unroll
@@ -180,8 +182,10 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           mma_f16_ss(tmem, ad + 2 * k4, bd + 2 * k4, (kk | k4) != 0);
         mma_commit(empty(s));
       }
-      mma_commit(acc_full);
+      __syncwarp();
     }
+    if (leader) mma_commit(acc_full);
+    __syncwarp();
   } else if (warp >= 4) {
     // ---------------- converters, then epilogue ----------------
     const int t = tid - 128;

@@ -56,6 +56,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int* err,
   }
 }
 
+// The same bounded wait taken by every lane of a warp; the outcome is the
+// AND over the lanes, so the warp leaves a loop together.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t a, uint32_t parity, int* err, int code) {
+  return __all_sync(0xffffffffu, mbar_wait(a, parity, err, code));
+}
+
+// One lane of the converged warp, picked by elect.sync. The MMA issuers run
+// their loop on the whole warp and issue the tcgen05 instructions from this
+// lane: issued from a lone lane of a diverged warp (if (lane == 0) ...) the
+// block-scaled MMAs went out at half the rate or less.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b32 r;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),

@@ -191,24 +191,26 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      long it = 0;
-      bool ok = true;
-      for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const int tile = (int)(item / p.n_ntiles), ntile = (int)(item % p.n_ntiles);
-        const int2 ti = __ldg(p.tile_info + tile);
-        const int e = ti.x, row0 = ti.y;
-        const int wrow = e * p.Mtot + ntile * C::NH;
-        const uint8_t* xsb = p.xsp + (size_t)tile * nk * kSfBlock;
-        const uint8_t* xsb_lo = LO ? p.xsp_lo + (size_t)tile * nk * kSfBlock : nullptr;
-        const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + ntile) * nk * (2 * kSfBlock);
-        for (int kk = 0; kk < nk; ++kk, ++it) {
-          const int s = (int)(it % kStages);
-          const long r = it / kStages;
-          if (r > 0 && !mbar_wait(empty(s), (uint32_t)((r - 1) & 1), p.err, 21)) {
-            ok = false;
-            break;
-          }
+    // the whole warp walks the loop; one elected lane issues the copies
+    const bool leader = elect_one();
+    long it = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const int tile = (int)(item / p.n_ntiles), ntile = (int)(item % p.n_ntiles);
+      const int2 ti = __ldg(p.tile_info + tile);
+      const int e = ti.x, row0 = ti.y;
+      const int wrow = e * p.Mtot + ntile * C::NH;
+      const uint8_t* xsb = p.xsp + (size_t)tile * nk * kSfBlock;
+      const uint8_t* xsb_lo = LO ? p.xsp_lo + (size_t)tile * nk * kSfBlock : nullptr;
+      const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + ntile) * nk * (2 * kSfBlock);
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int s = (int)(it % kStages);
+        const long r = it / kStages;
+        if (r > 0 && !mbar_wait_warp(empty(s), (uint32_t)((r - 1) & 1), p.err, 21)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
           mbar_expect_tx(full(s), C::kTx);
           const uint32_t b_smem = sbase + C::kOffB + s * C::kBBytes;
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
@@ -220,11 +222,14 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           if (LO) bulk_load(sf_smem + kSfBlock, xsb_lo + (size_t)kk * kSfBlock, kSfBlock, full(s));
           bulk_load(sf_smem + C::kNA * kSfBlock, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
         }
+        __syncwarp();
       }
-      // unwind: the loads of the last stages may still be landing
+    }
+    // unwind: the loads of the last stages may still be landing
+    if (leader)
       for (long j = it - 1; j >= 0 && j >= it - kStages; --j)
         drain_wait(full((int)(j % kStages)), (uint32_t)((j / kStages) & 1));
-    }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------- scale copies + MMA issuer ----------------
     // the whole warp walks the loop; one elected lane issues

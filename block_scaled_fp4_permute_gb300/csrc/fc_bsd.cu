@@ -207,26 +207,28 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
     // no item for this CTA
   } else if (warp == 4) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      long it = 0;
-      bool ok = true;
-      // the tile of the next item is read one item ahead, so that its
-      // latency hides behind this item's loads
-      int2 ti_next = __ldg(p.tile_info + blockIdx.x / p.n_ntiles);
-      for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const int nt = (int)(item % p.n_ntiles);
-        const int2 ti = ti_next;
-        if (item + gridDim.x < total) ti_next = __ldg(p.tile_info + (item + gridDim.x) / p.n_ntiles);
-        const int e = ti.x, row0 = ti.y;
-        const int wrow = e * p.Mtot + nt * NH;
-        const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + nt) * nk * (2 * kSfBlock);
-        for (int kk = 0; kk < nk; ++kk, ++it) {
-          const int s = (int)(it % kStages);
-          const long r = it / kStages;
-          if (r > 0 && !mbar_wait(empty(s), (uint32_t)((r - 1) & 1), p.err, 41)) {
-            ok = false;
-            break;
-          }
+    // the whole warp walks the loop; one elected lane issues the copies
+    const bool leader = elect_one();
+    long it = 0;
+    bool ok = true;
+    // the tile of the next item is read one item ahead, so that its
+    // latency hides behind this item's loads
+    int2 ti_next = __ldg(p.tile_info + blockIdx.x / p.n_ntiles);
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const int nt = (int)(item % p.n_ntiles);
+      const int2 ti = ti_next;
+      if (item + gridDim.x < total) ti_next = __ldg(p.tile_info + (item + gridDim.x) / p.n_ntiles);
+      const int e = ti.x, row0 = ti.y;
+      const int wrow = e * p.Mtot + nt * NH;
+      const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + nt) * nk * (2 * kSfBlock);
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int s = (int)(it % kStages);
+        const long r = it / kStages;
+        if (r > 0 && !mbar_wait_warp(empty(s), (uint32_t)((r - 1) & 1), p.err, 41)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
           mbar_expect_tx(full(s), C::kTx);
           const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
@@ -236,10 +238,13 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           bulk_load(sf_smem, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
           tma_load_2d(sf_smem + 2 * kSfBlock, &tmS, 16 * kk, RM * row0, full(s));
         }
+        __syncwarp();
       }
+    }
+    if (leader)
       for (long j = it - 1; j >= 0 && j >= it - kStages; --j)
         drain_wait(full((int)(j % kStages)), (uint32_t)((j / kStages) & 1));
-    }
+    __syncwarp();
   } else if (warp == 5) {
     // ---------------- scale copies + MMA issuer ----------------
     // the whole warp walks the loop; one elected lane issues

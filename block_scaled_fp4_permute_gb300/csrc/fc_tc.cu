@@ -148,11 +148,13 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      const int yw = e * p.Mtot + nbase;
-      for (int kk = 0; kk < nk; ++kk) {
-        const int s = kk % kStages, r = kk / kStages;
-        if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1, p.err, 11)) break;
+    // the whole warp walks the loop; one elected lane issues the copies
+    const bool leader = elect_one();
+    const int yw = e * p.Mtot + nbase;
+    for (int kk = 0; kk < nk; ++kk) {
+      const int s = kk % kStages, r = kk / kStages;
+      if (r > 0 && !mbar_wait_warp(empty(s), (r - 1) & 1, p.err, 11)) break;
+      if (leader) {
         mbar_expect_tx(full_a(s), kABytes);
         tma_load_2d(sbase + kOffA + s * kABytes, &tmA, kk * kBK, row0, full_a(s));
         mbar_expect_tx(full_p(s), kPBytes);
@@ -163,6 +165,7 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           tma_load_2d(sbase + kOffP + s * kPBytes, &tmB, kk * (kBK / 2), yw, full_p(s));
         }
       }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------

@@ -182,34 +182,41 @@ __device__ __forceinline__ uint32_t split_hl32(const float* v, uint32_t* hi, uin
 // tanh is +-1 and sigmoid 0 or 1 to within 1.4e-11 absolute, which keeps
 // the product of the three denominators below 4e32.  The error is a few
 // fp32 ulps of the factors' magnitudes (absolute, not relative, near 0).
+// k0 = 2/b and k1 = 2/bl are the expert's constants, 0 for a cap that is
+// off; the body has no branches, so that the element loops of the
+// epilogues interleave many independent chains.
 __device__ __forceinline__ float exp_neg_clamped(float y) { return __expf(-fminf(fmaxf(y, -25.f), 25.f)); }
-__device__ __forceinline__ float situ_f(float g, float u, float b, float bl) {
+__device__ __forceinline__ float situ_k(float g, float u, float b, float k0, float bl, float k1) {
   const float e0 = exp_neg_clamped(g);
-  float num = 1.f, den = 1.f + e0;               // sigmoid(g)
-  if (b > 0.f) {
-    const float e1 = exp_neg_clamped((2.f / b) * g);
-    num = b * (1.f - e1);
-    den *= 1.f + e1;
-  } else {
-    num = g;
-  }
-  if (bl > 0.f) {
-    const float e2 = exp_neg_clamped((2.f / bl) * u);
-    num *= bl * (1.f - e2);
-    den *= 1.f + e2;
-  } else {
-    num *= u;
-  }
-  return __fdividef(num, den);
+  const float e1 = exp_neg_clamped(k0 * g);
+  const float e2 = exp_neg_clamped(k1 * u);
+  const float ng = k0 > 0.f ? b * (1.f - e1) : g;
+  const float dg = k0 > 0.f ? 1.f + e1 : 1.f;
+  const float nu = k1 > 0.f ? bl * (1.f - e2) : u;
+  const float du = k1 > 0.f ? 1.f + e2 : 1.f;
+  return __fdividef(ng * nu, ((1.f + e0) * dg) * du);
+}
+__device__ __forceinline__ float situ_cap_k(float b) { return b > 0.f ? 2.f / b : 0.f; }
+
+// SwigluBias g * sigmoid(alpha * g) * (u + beta), the exponent argument
+// clamped to [-80, 80], where sigmoid is 0 or 1 to fp32 precision.
+__device__ __forceinline__ float swiglu_bias_f(float g, float u, float alpha, float beta) {
+  return __fdividef(g * (u + beta), 1.f + __expf(-fminf(fmaxf(alpha * g, -80.f), 80.f)));
 }
 
-// FC1's gated activation: kind 0 is SiTU (caps p0, p1 as above), kind 1
-// SwigluBias g * sigmoid(p0 * g) * (u + p1) (the exponent argument clamped
-// to [-80, 80], where sigmoid is 0 or 1 to fp32 precision).
+// FC1's gated activation: kind 0 is SiTU (caps p0 = b, p1 = bl), kind 1
+// SwigluBias (p0 = alpha, p1 = beta).  with_act(kind, p0, p1, body) picks
+// the kind once and runs body(act), act(g, u) being the activation of that
+// kind, so the element loops inside body carry no per-element branch.
 constexpr int kActSitu = 0, kActSwigluBias = 1;
-__device__ __forceinline__ float act_f(int kind, float g, float u, float p0, float p1) {
-  if (kind == kActSwigluBias) return __fdividef(g * (u + p1), 1.f + __expf(-fminf(fmaxf(p0 * g, -80.f), 80.f)));
-  return situ_f(g, u, p0, p1);
+template <class Body>
+__device__ __forceinline__ void with_act(int kind, float p0, float p1, Body&& body) {
+  if (kind == kActSwigluBias) {
+    body([=](float g, float u) { return swiglu_bias_f(g, u, p0, p1); });
+  } else {
+    const float k0 = situ_cap_k(p0), k1 = situ_cap_k(p1);
+    body([=](float g, float u) { return situ_k(g, u, p0, k0, p1, k1); });
+  }
 }
 
 }  // namespace situ

@@ -317,12 +317,14 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           if (!vrow || i0 >= p.I) continue;
           float v[32];
           float amax = 0.f;
+          with_act(p.act_kind, bt, btl, [&](auto act) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] = act_f(p.act_kind, gt[j] * ag, up[j] * au, bt, btl) * rw;
-            if (LO) v[j] = bf16_lo(f32x2_to_bf16x2(v[j], 0.f));   // w4a16: H1 is bf16
-            amax = fmaxf(amax, fabsf(v[j]));
-          }
+            for (int j = 0; j < 32; ++j) {
+              v[j] = act(gt[j] * ag, up[j] * au) * rw;
+              if (LO) v[j] = bf16_lo(f32x2_to_bf16x2(v[j], 0.f));   // w4a16: H1 is bf16
+              amax = fmaxf(amax, fabsf(v[j]));
+            }
+          });
           const int b = i0 / 32;   // K block of FC2
           const size_t sfo = ((size_t)tile * nkh + b / 4) * kSfBlock + sf_offset(m, b & 3);
           uint32_t qv[8];

@@ -344,10 +344,18 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
           const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
           const int sbyte = tok_scale_byte(i0 / 32);   // FC2's K block of this warp
+          // the activation of all 16 token columns first (independent
+          // chains; the columns past nrows hold other rows or zeros and are
+          // not stored), then the per-token block scales and stores
+          float hv[kTok];
+          with_act(p.act_kind, bt, btl, [&](auto act) {
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) hv[t] = act(a1[t] * ag, a2[t] * au);
+          });
 #pragma unroll
           for (int t = 0; t < kTok; ++t) {
             if (t >= nrows) break;
-            float h = act_f(p.act_kind, a1[t] * ag, a2[t] * au, bt, btl);
+            float h = hv[t];
             if (p.topk_fc1) h *= __ldg(p.topk_weights + __ldg(p.permuted_src + row0 + t));
             if (LO) h = bf16_lo(f32x2_to_bf16x2(h, 0.f));   // w4a16: H1 is bf16
             const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));

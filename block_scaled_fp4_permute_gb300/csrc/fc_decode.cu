@@ -286,10 +286,10 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
         const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
         const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
         const float gg = WNV ? __ldg(p.w1_gs + 2 * e) : 1.f, gu = WNV ? __ldg(p.w1_gs + 2 * e + 1) : 1.f;
-        sH[(2 * c) * 64 + il] =
-            act_f(p.act_kind, acc[0] * (ag * gg * t0), acc[2] * (au * gu * t0), bt, btl) * s_w[2 * c];
-        sH[(2 * c + 1) * 64 + il] =
-            act_f(p.act_kind, acc[1] * (ag * gg * t1), acc[3] * (au * gu * t1), bt, btl) * s_w[2 * c + 1];
+        with_act(p.act_kind, bt, btl, [&](auto act) {
+          sH[(2 * c) * 64 + il] = act(acc[0] * (ag * gg * t0), acc[2] * (au * gu * t0)) * s_w[2 * c];
+          sH[(2 * c + 1) * 64 + il] = act(acc[1] * (ag * gg * t1), acc[3] * (au * gu * t1)) * s_w[2 * c + 1];
+        });
       }
       __syncthreads();
       if (tid < kNT * 2) {

@@ -317,10 +317,11 @@ fcp_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           const int i0 = nbase + c0;
           if (!vrow || i0 >= p.I) continue;
           float v[32];
+          with_act(p.act_kind, bt, btl, [&](auto act) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            v[j] = act_f(p.act_kind, gt[j] * (xs * wsc[c0 + j] * ag), up[j] * (xs * wsc[128 + c0 + j] * au), bt,
-                         btl) * rw;
+            for (int j = 0; j < 32; ++j)
+              v[j] = act(gt[j] * (xs * wsc[c0 + j] * ag), up[j] * (xs * wsc[128 + c0 + j] * au)) * rw;
+          });
           if (p.h_mxfp8) {   // the MXFP8 round trip FC2 consumes (w4a8)
             float amax = 0.f;
 #pragma unroll

@@ -398,7 +398,6 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         uint8_t* yst = smem + C::kOffY + (warp - 4) * 32 * C::kYRow;
         const int wrow0 = quarter * 32;
         uint16_t* y16 = reinterpret_cast<uint16_t*>(p.y_out);
-        const int nb = p.Mtot / 32;
         for (int c0 = 0; c0 < C::BN; c0 += 32) {
           float acc[32];
           tmem_ld16(trow + c0, acc);
@@ -420,7 +419,8 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
                            pack_f16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
                            pack_f16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
           const int n0 = nbase + c0;
-          if (m < nrows && n0 < p.Mtot) p.y_scale[(size_t)(row0 + m) * nb + n0 / 32] = (uint8_t)(ex + 127);
+          // block-major scales: the warp's 32 rows are 32 consecutive bytes
+          if (m < nrows && n0 < p.Mtot) p.y_scale[(size_t)(n0 / 32) * p.ys_rows + (row0 + m)] = (uint8_t)(ex + 127);
           __syncwarp();
           // ... and out as 8 rows x 64 bytes per instruction
           const int n = n0 + 8 * (lane & 3);

@@ -87,13 +87,14 @@ combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ slot_to
 }
 
 __global__ void __launch_bounds__(256)
-combine16_kernel(const uint2* __restrict__ y, const uint8_t* __restrict__ ys, const int32_t* __restrict__ slot_to_row,
+combine16_kernel(const uint2* __restrict__ y, const uint8_t* __restrict__ ys, long ys_rows,
+                 const int32_t* __restrict__ slot_to_row,
                  const float* __restrict__ w, int K, int H4, uint2* __restrict__ out) {
   griddep_wait();   // Y is the predecessor's output
   const int t = blockIdx.x;
   const int h4 = blockIdx.y * blockDim.x + threadIdx.x;
   if (h4 >= H4) return;
-  const int nb = H4 / 8, b = h4 >> 3;   // 32-element blocks per row, this thread's block
+  const int b = h4 >> 3;   // this thread's 32-element block
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int j0 = 0; j0 < K; j0 += 4) {
     int r[4];
@@ -109,7 +110,7 @@ combine16_kernel(const uint2* __restrict__ y, const uint8_t* __restrict__ ys, co
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       v[u] = r[u] >= 0 ? __ldg(y + (size_t)r[u] * H4 + h4) : make_uint2(0u, 0u);
-      sb[u] = r[u] >= 0 ? __ldg(ys + (size_t)r[u] * nb + b) : 127u;
+      sb[u] = r[u] >= 0 ? __ldg(ys + (size_t)b * ys_rows + r[u]) : 127u;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -125,12 +126,12 @@ combine16_kernel(const uint2* __restrict__ y, const uint8_t* __restrict__ ys, co
   out[(size_t)t * H4 + h4] = make_uint2(f32x2_to_bf16x2(acc.x, acc.y), f32x2_to_bf16x2(acc.z, acc.w));
 }
 
-cudaError_t launch_combine16(const void* y16, const uint8_t* ys, const int32_t* slot_to_row, const float* w,
-                             int T, int K, int H, void* out, cudaStream_t st) {
+cudaError_t launch_combine16(const void* y16, const uint8_t* ys, long ys_rows, const int32_t* slot_to_row,
+                             const float* w, int T, int K, int H, void* out, cudaStream_t st) {
   const int H4 = H / 4;
   dim3 grid(T, (H4 + 255) / 256);
-  return launch_pdl(combine16_kernel, grid, dim3(256), 0, st, (const uint2*)y16, ys, slot_to_row, w, K, H4,
-                    (uint2*)out);
+  return launch_pdl(combine16_kernel, grid, dim3(256), 0, st, (const uint2*)y16, ys, ys_rows, slot_to_row, w, K,
+                    H4, (uint2*)out);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,

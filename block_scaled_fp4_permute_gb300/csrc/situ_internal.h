@@ -44,7 +44,7 @@ cudaError_t launch_quant_nvfp4(const void* x, int T, int H, uint8_t* q, uint8_t*
 cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,
                            int H, void* out, cudaStream_t st);
 // the same over Y as f16 rows [S, H] with scale bytes [S, H/32] (y16_exponent)
-cudaError_t launch_combine16(const void* y16, const uint8_t* ys, const int32_t* slot_to_row, const float* w,
+cudaError_t launch_combine16(const void* y16, const uint8_t* ys, long ys_rows, const int32_t* slot_to_row, const float* w,
                              int T, int K, int H, void* out, cudaStream_t st);
 // fused-combine helpers: zero the fp32 accumulator, round it to bf16 out
 cudaError_t launch_zero_f32(float* a, long n, cudaStream_t st);
@@ -157,7 +157,9 @@ struct FcqParams {
   int hq_stride;
   const float* alpha2;
   float* y_out;
-  uint8_t* y_scale;              // non-null: Y as f16 rows [S, Mtot] (at y_out) + these scale bytes
+  uint8_t* y_scale;              // non-null: Y as f16 rows [S, Mtot] (at y_out) + these scale bytes,
+                                 // block-major: byte of (row r, 32-column block b) at b * ys_rows + r
+  long ys_rows;
   // fused combine (FC2): add topk_weights[slot] * Y into out_acc [T, Mtot]
   int fuse;
   const int32_t* permuted_src;

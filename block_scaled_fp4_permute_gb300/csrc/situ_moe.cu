@@ -489,6 +489,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     q.top_k = a->top_k;
     // unfused: Y as f16 rows with a scale per 32 columns (half the bytes of fp32)
     q.y_scale = fused ? nullptr : ws + L.ys;
+    q.ys_rows = S;
     y16 = !fused;
     q.out_acc = y;   // fused: the accumulator [T, H] takes the place of Y
     if ((err = launch_fcq(q, q.hq, q.hq_lo, S, a->w2, a->num_local_experts, false, max_tiles, st)) !=
@@ -577,7 +578,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   if (fused)
     err = launch_acc_to_bf16(y, (long)a->T * a->H, a->out, st);
   else if (y16)
-    err = launch_combine16(y, ws + L.ys, s2r, a->apply_topk_in_fc1 ? nullptr : a->topk_weights, a->T, a->top_k,
+    err = launch_combine16(y, ws + L.ys, S, s2r, a->apply_topk_in_fc1 ? nullptr : a->topk_weights, a->T, a->top_k,
                            a->H, a->out, st);
   else
     err = launch_combine(y, s2r, a->apply_topk_in_fc1 ? nullptr : a->topk_weights, a->T, a->top_k, a->H, a->out,

@@ -46,6 +46,7 @@
 // releases TMEM and returns.
 #include "situ_internal.h"
 #include "tc_common.cuh"
+#include <cuda_fp16.h>
 
 namespace situ {
 
@@ -54,22 +55,35 @@ using namespace tc;
 namespace {
 
 constexpr int kTok = 16;           // tokens per tile
-constexpr int kBK = 128;           // K elements per stage
+constexpr int kRowB = 128;         // bytes of one operand row per stage (one 128-byte swizzle row)
+constexpr int kBK = 128;           // K elements per stage of 8-bit containers (MXFP4 x E4M3)
+constexpr int kBKnv = 256;         // K elements per stage of packed E2M1 (NVFP4 x NVFP4)
 constexpr int kNH1 = 128;          // FC1 gate (and up) rows per weight tile
 constexpr int kNH2 = 256;          // FC2 rows per weight tile
 constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;
 constexpr int kSfBlock = 512;
 constexpr int kSfCol0 = 128;       // scale columns start after the two accumulator buffers
-constexpr int kSfColsPerStage = 12;
 
-template <bool FC1, bool LO>
+// NV: NVFP4 FC1 (E2M1 x E2M1, E4M3 scales per 16, kind::mxf4nvf4 with
+// scale_vec::4X).  A stage is then 256 elements of K (128 packed bytes per
+// row), four K = 64 MMAs per accumulator; each MMA reads four E4M3 bytes
+// per row, so every MMA has its own 512-byte scale block (four TMEM
+// columns) on both sides: two weight accumulators x four MMAs, and four
+// token blocks (the gather writes each row's stage scales as four 16-byte
+// chunks, one per MMA, its word first).
+template <bool FC1, bool LO, bool NV = false>
 struct CfgW {
-  static constexpr int kStages = 6;
+  static_assert(!NV || (FC1 && !LO), "the NVFP4 tiles are FC1 on NVFP4 token rows");
+  static constexpr int kStages = NV ? 5 : 6;
   static constexpr int NB = LO ? 2 * kTok : kTok;          // MMA N: token rows (hi, lo interleaved)
-  static constexpr int kABytes = 256 * kBK;                // 32 KB
-  static constexpr int kBBytes = NB * kBK;                 // 4 / 2 KB
-  static constexpr int kSfBytes = 3 * kSfBlock;            // weight blocks (2), token block
+  static constexpr int kKS = NV ? kBKnv : kBK;             // K elements per stage
+  static constexpr int kABytes = 256 * kRowB;              // 32 KB
+  static constexpr int kBBytes = NB * kRowB;               // 4 / 2 KB
+  static constexpr int kWSf = NV ? 8 : 2;                  // weight scale blocks per stage
+  static constexpr int kTSf = NV ? 4 : 1;                  // token scale blocks per stage
+  static constexpr int kSfBytes = (kWSf + kTSf) * kSfBlock;
+  static constexpr int kTmemCols = NV ? 512 : 256;
+  static constexpr int kSfColsPerStage = 4 * (kWSf + kTSf);
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffSF = kOffB + kStages * kBBytes;
@@ -77,17 +91,22 @@ struct CfgW {
   static constexpr int kNumBars = 2 * kStages + 5;         // full, empty; acc_full[2], acc_empty[2]; drain
   static constexpr int kOffTm = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffTm + 16 + 1024;
-  static constexpr uint32_t kTx = (uint32_t)(FC1 ? 2 * kNH1 : kNH2) * (kBK / 2) + (uint32_t)NB * kBK +
-                                  (uint32_t)NB * 16 + 2 * kSfBlock;
+  // bytes a stage's copies deliver: the 4-bit map of the MXFP4 weights
+  // counts the packed bytes (half the widened tile), the NVFP4 map is bytes
+  static constexpr uint32_t kTx = NV ? (uint32_t)(2 * kNH1 * kRowB + NB * kRowB + kTSf * NB * 16 + kWSf * kSfBlock)
+                                     : (uint32_t)(FC1 ? 2 * kNH1 : kNH2) * (kBK / 2) + (uint32_t)NB * kBK +
+                                           (uint32_t)NB * 16 + 2 * kSfBlock;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
   static_assert(2 * NB <= 64, "accumulator buffer");
   static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
   // A = E2M1 (5), B = E4M3 (0), both K-major; N >> 3 at bit 17, UE8M0
   // scales (bit 23), M >> 4 at bit 24; B / A scale byte selectors at bits
-  // 4..5 / 29..30.
+  // 4..5 / 29..30.  NVFP4: A = B = E2M1 (1 in the fp4 kinds' encoding),
+  // UE4M3 scales (bit 23 clear), selectors 0 (all four bytes are used).
   static constexpr uint32_t kIdesc =
-      (5u << 7) | (0u << 10) | ((uint32_t)(NB >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24);
+      NV ? ((1u << 7) | (1u << 10) | ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(128 >> 4) << 24))
+         : ((5u << 7) | (0u << 10) | ((uint32_t)(NB >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24));
 };
 
 __device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
@@ -95,6 +114,16 @@ __device__ __forceinline__ void mma_bs(uint32_t d_tmem, uint64_t a, uint64_t b, 
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
       " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_nv(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
           d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
@@ -148,11 +177,11 @@ __device__ __forceinline__ uint32_t split_hl(float v, int e, int c, uint32_t& lo
 // byte offset of the UE8M0 scale of 32-element block b in a token scale row
 __device__ __forceinline__ int tok_scale_byte(int b) { return 16 * (b >> 2) + (b & 3); }
 
-template <bool FC1, bool LO>
+template <bool FC1, bool LO, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
 fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
            const __grid_constant__ CUtensorMap tmS, const FcwParams p) {
-  using C = CfgW<FC1, LO>;
+  using C = CfgW<FC1, LO, NV>;
   constexpr int kStages = C::kStages;
   constexpr int NB = C::NB;
   constexpr int NH = FC1 ? kNH1 : kNH2;
@@ -161,7 +190,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int nk = p.K / kBK;
+  const int nk = p.K / C::kKS;
 
   const uint32_t sbase = saddr(smem);
   const uint32_t bar0 = sbase + C::kOffBar;
@@ -186,7 +215,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   }
   if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tm_holder)),
-                 "r"(kTmemCols)
+                 "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -220,7 +249,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       if (item + gridDim.x < total) ti_next = __ldg(p.tile_info + (item + gridDim.x) / p.n_ntiles);
       const int e = ti.x, row0 = ti.y;
       const int wrow = e * p.Mtot + nt * NH;
-      const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + nt) * nk * (2 * kSfBlock);
+      const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + nt) * nk * (C::kWSf * kSfBlock);
       for (int kk = 0; kk < nk; ++kk, ++it) {
         const int s = (int)(it % kStages);
         const long r = it / kStages;
@@ -232,11 +261,15 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           mbar_expect_tx(full(s), C::kTx);
           const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
-          tma_load_2d(a_smem, &tmW, kk * kBK, wrow, full(s));
-          if (FC1) tma_load_2d(a_smem + kNH1 * kBK, &tmW, kk * kBK, wrow + p.I, full(s));
-          tma_load_2d(sbase + C::kOffB + s * C::kBBytes, &tmX, kk * kBK, RM * row0, full(s));
-          bulk_load(sf_smem, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
-          tma_load_2d(sf_smem + 2 * kSfBlock, &tmS, 16 * kk, RM * row0, full(s));
+          // x = kk * 128: codes of the MXFP4 map, bytes of the E4M3 / packed
+          // NVFP4 maps; either way one 128-byte row of the stage
+          tma_load_2d(a_smem, &tmW, kk * kRowB, wrow, full(s));
+          if (FC1) tma_load_2d(a_smem + kNH1 * kRowB, &tmW, kk * kRowB, wrow + p.I, full(s));
+          tma_load_2d(sbase + C::kOffB + s * C::kBBytes, &tmX, kk * kRowB, RM * row0, full(s));
+          bulk_load(sf_smem, wsb + (size_t)kk * C::kWSf * kSfBlock, C::kWSf * kSfBlock, full(s));
+#pragma unroll
+          for (int b = 0; b < C::kTSf; ++b)
+            tma_load_2d(sf_smem + (C::kWSf + b) * kSfBlock, &tmS, 16 * (C::kTSf * kk + b), RM * row0, full(s));
         }
         __syncwarp();
       }
@@ -267,21 +300,29 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (leader) {
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
-          const uint32_t sfw = tmem + (uint32_t)(kSfCol0 + s * kSfColsPerStage);
-          const uint32_t sft = sfw + 8;
-          tmem_cp_sf(sfw, sf_desc(sf_smem));
-          tmem_cp_sf(sfw + 4, sf_desc(sf_smem + kSfBlock));
-          tmem_cp_sf(sft, sf_desc(sf_smem + 2 * kSfBlock));
+          const uint32_t sfw = tmem + (uint32_t)(kSfCol0 + s * C::kSfColsPerStage);
+          const uint32_t sft = sfw + 4 * C::kWSf;
+#pragma unroll
+          for (int b = 0; b < C::kWSf + C::kTSf; ++b) tmem_cp_sf(sfw + 4 * b, sf_desc(sf_smem + b * kSfBlock));
           const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
           const uint64_t ad1 = sdesc(a_smem);
-          const uint64_t ad2 = sdesc(a_smem + 128 * kBK);
+          const uint64_t ad2 = sdesc(a_smem + 128 * kRowB);
           const uint64_t bd = sdesc(sbase + C::kOffB + s * C::kBBytes);
+          // four MMAs per accumulator, 32 bytes of each row apart (K = 32
+          // 8-bit containers, or K = 64 packed E2M1)
 #pragma unroll
-          for (uint32_t k4 = 0; k4 < kBK / 32; ++k4) {
-            const uint32_t idesc = C::kIdesc | (k4 << 4) | (k4 << 29);
+          for (uint32_t k4 = 0; k4 < 4; ++k4) {
             const uint32_t acc = (kk | (int)k4) != 0;
-            mma_bs(d1, ad1 + 2 * k4, bd + 2 * k4, idesc, sfw, sft, acc);
-            mma_bs(d2, ad2 + 2 * k4, bd + 2 * k4, idesc, sfw + 4, sft, acc);
+            if (NV) {
+              // scale block k4 of each accumulator and of the tokens
+              mma_nv(d1, ad1 + 2 * k4, bd + 2 * k4, C::kIdesc, sfw + 4 * k4, sft + 4 * k4, acc);
+              mma_nv(d2, ad2 + 2 * k4, bd + 2 * k4, C::kIdesc, sfw + 16 + 4 * k4, sft + 4 * k4, acc);
+            } else {
+              // one block per accumulator, byte k4 of each scale word
+              const uint32_t idesc = C::kIdesc | (k4 << 4) | (k4 << 29);
+              mma_bs(d1, ad1 + 2 * k4, bd + 2 * k4, idesc, sfw, sft, acc);
+              mma_bs(d2, ad2 + 2 * k4, bd + 2 * k4, idesc, sfw + 4, sft, acc);
+            }
           }
           mma_commit(empty(s));
         }
@@ -335,7 +376,42 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       mbar_arrive(acc_empty(buf));
 
-      if (FC1) {
+      if constexpr (NV) {
+        // NVFP4: the accumulators hold sum(code * scale) products; the
+        // expert's gate / up global scale and the token's global scale make
+        // them dot products.  H1 is bf16, written as f16 block rows (f16
+        // mantissas of the bf16 values under a power-of-two scale per 32
+        // columns that puts the block maximum in [2^14, 2^15)), the form the
+        // register-tile FC2 reads.
+        const int i0 = nt * kNH1 + warp * 32;
+        if (i0 < p.I) {
+          const float ag = (p.alpha_g ? __ldg(p.alpha_g + e) : 1.f) * __ldg(p.w1_gs + 2 * e);
+          const float au = (p.alpha_u ? __ldg(p.alpha_u + e) : 1.f) * __ldg(p.w1_gs + 2 * e + 1);
+          const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+          const int ipad = pad128(p.I);
+          float hv[kTok];
+          with_act(p.act_kind, bt, btl, [&](auto act) {
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) {
+              const float gx = t < nrows ? __ldg(p.xg + row0 + t) : 0.f;
+              hv[t] = act(a1[t] * (ag * gx), a2[t] * (au * gx));
+            }
+          });
+#pragma unroll
+          for (int t = 0; t < kTok; ++t) {
+            if (t >= nrows) break;
+            float h = hv[t];
+            if (p.topk_fc1) h *= __ldg(p.topk_weights + __ldg(p.permuted_src + row0 + t));
+            h = bf16_lo(f32x2_to_bf16x2(h, 0.f));
+            const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+            int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
+            ex = ex < -126 ? -126 : ex;
+            const size_t r = (size_t)(row0 + t);
+            p.h16[r * ipad + i0 + lane] = __half_as_ushort(__float2half_rn(h * exp2i(-ex)));
+            if (lane == 0) p.h16s[r * (ipad / 32) + i0 / 32] = exp2i(ex);
+          }
+        }
+      } else if (FC1) {
         // gate row i = nt * 128 + l and its up row are lane l of the two
         // accumulators; warp w holds the 32-element block i0 .. i0 + 31
         const int i0 = nt * kNH1 + warp * 32;
@@ -397,7 +473,8 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   if (warp == 5) {
     __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols)
+                 : "memory");
   }
 }
 
@@ -405,7 +482,8 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
 // gather_hl: the token-side operand of the decode tiles, in expert order.
 // Row r takes token permuted_src[r] / top_k.  A bf16 row becomes hi / lo
 // E4M3 rows 2r, 2r + 1 with their scale rows (one thread per 32-element
-// block); an MXFP8 row is copied to row r with its scales.
+// block); an MXFP8 row is copied to row r with its scales; an NVFP4 row is
+// copied to row r with its scale row and global scale.
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) {
@@ -443,6 +521,22 @@ __global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) 
       sh[tok_scale_byte(b)] = (uint8_t)(sb & 0xFFu);
       sl[tok_scale_byte(b)] = (uint8_t)(sb >> 8);
     }
+  } else if (p.act == 2) {
+    // NVFP4: packed codes (16-byte rows) copied as they are; the E4M3
+    // scales of each 64-element K step (one MMA) as a 16-byte chunk, its
+    // four bytes first (scale row of K/4 bytes; the caller's scale rows are
+    // read bytewise, they need no alignment); the token's global scale
+    const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * (K / 2));
+    uint4* dst = reinterpret_cast<uint4*>(p.x + (size_t)r * (K / 2));
+    for (int i = tid; i < K / 32; i += 128) dst[i] = __ldg(src + i);
+    const uint8_t* ss = p.x_s + (size_t)t * (K / 16);
+    uint4* sd = reinterpret_cast<uint4*>(p.xs + (size_t)r * (K / 4));
+    for (int c = tid; c < K / 64; c += 128) {
+      const uint32_t v = (uint32_t)__ldg(ss + 4 * c) | ((uint32_t)__ldg(ss + 4 * c + 1) << 8) |
+                         ((uint32_t)__ldg(ss + 4 * c + 2) << 16) | ((uint32_t)__ldg(ss + 4 * c + 3) << 24);
+      sd[c] = make_uint4(v, 0u, 0u, 0u);
+    }
+    if (tid == 0) p.xg[r] = __ldg(p.x_gs + t);
   } else {
     const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * K);
     uint4* dst = reinterpret_cast<uint4*>(p.x + (size_t)r * K);
@@ -470,23 +564,23 @@ int sm_count_w() {
   return v;
 }
 
-template <bool FC1, bool LO>
+template <bool FC1, bool LO, bool NV = false>
 cudaError_t launch_fcw_t(const FcwParams& p, const CUtensorMap* m, long max_tiles, cudaStream_t st) {
-  using C = CfgW<FC1, LO>;
+  using C = CfgW<FC1, LO, NV>;
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || set_for[dev] == 0) {
     cudaError_t err =
-        cudaFuncSetAttribute(fcw_kernel<FC1, LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(fcw_kernel<FC1, LO, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (err != cudaSuccess) return err;
     if (dev < 64) set_for[dev] = 1;
   }
   const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
   const long grid = items < sm_count_w() ? items : sm_count_w();
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(fcw_kernel<FC1, LO>, dim3((unsigned)grid), dim3(kThreads), (size_t)C::kSmem, st, m[0], m[1], m[2],
-                    p);
+  return launch_pdl(fcw_kernel<FC1, LO, NV>, dim3((unsigned)grid), dim3(kThreads), (size_t)C::kSmem, st, m[0], m[1],
+                    m[2], p);
 }
 
 }  // namespace
@@ -523,6 +617,73 @@ cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, c
     return cudaErrorInvalidValue;
   if (fc1) return lo ? launch_fcw_t<true, true>(q, m, max_tiles, st) : launch_fcw_t<true, false>(q, m, max_tiles, st);
   return lo ? launch_fcw_t<false, true>(q, m, max_tiles, st) : launch_fcw_t<false, false>(q, m, max_tiles, st);
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 FC1 on the decode tiles
+// ---------------------------------------------------------------------------
+
+// Packed NVFP4 weight scales of the FC1 decode tiles: per (expert, weight
+// tile nt, stage kk of 256 elements, accumulator a (gate, up), MMA k) a
+// 512-byte block; in it the four E4M3 bytes of tile row r = i + 32q (K
+// blocks 16kk + 4k .. + 3 of source row a * I + nt * 128 + r) sit at byte
+// 16i + 4q, the layout tcgen05.cp.32x128b.warpx4 spreads over the four
+// TMEM columns the MMA reads.  One thread per 4-byte word.
+__global__ void pack_scales_nv_kernel(const uint8_t* __restrict__ ws, int H, int I, int n_nt, int nk, long n_words,
+                                      uint32_t* __restrict__ out) {
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_words) return;
+  const int w = (int)(idx & 127);
+  const int i = w >> 2, q = w & 3;
+  long b = idx >> 7;
+  const int k = (int)(b & 3);
+  b >>= 2;
+  const int a = (int)(b & 1);
+  b >>= 1;
+  const int kk = (int)(b % nk);
+  b /= nk;
+  const int nt = (int)(b % n_nt);
+  const long e = b / n_nt;
+  const int ir = nt * kNH1 + i + 32 * q;   // gate / up row within the half
+  uint32_t v = 0;
+  if (ir < I) {
+    const uint8_t* src = ws + ((size_t)e * 2 * I + (size_t)a * I + ir) * (size_t)(H / 16) + 16 * kk + 4 * k;
+    v = (uint32_t)src[0] | ((uint32_t)src[1] << 8) | ((uint32_t)src[2] << 16) | ((uint32_t)src[3] << 24);
+  }
+  out[idx] = v;
+}
+
+size_t packed_scale_bytes_nv(int E_loc, int H, int I) {
+  const size_t n_nt = (size_t)(I + kNH1 - 1) / kNH1, nk = (size_t)H / kBKnv;
+  return (size_t)E_loc * n_nt * nk * 8 * kSfBlock;
+}
+
+cudaError_t launch_pack_scales_nv(const uint8_t* w1_scale, int E_loc, int H, int I, uint8_t* out, cudaStream_t st) {
+  const int n_nt = (I + kNH1 - 1) / kNH1, nk = H / kBKnv;
+  const long n_words = (long)(packed_scale_bytes_nv(E_loc, H, I) / 4);
+  if (n_words <= 0) return cudaSuccess;
+  pack_scales_nv_kernel<<<(unsigned)((n_words + 255) / 256), 256, 0, st>>>(w1_scale, H, I, n_nt, nk, n_words,
+                                                                          reinterpret_cast<uint32_t*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
+                          int E_loc, long max_tiles, cudaStream_t st) {
+  if (S <= 0) return cudaSuccess;
+  FcwParams q = p;
+  q.w = w;
+  CUtensorMap m[3];
+  // weights and token rows: packed E2M1 as bytes [rows, K/2], boxes of 128
+  // bytes (256 codes) x the tile's rows, 128-byte swizzle; token scale rows
+  // [rows, K/4] bytes (a 16-byte chunk per 64 elements), boxes of 16 bytes
+  if (!make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)(p.K / 2), (uint64_t)E_loc * p.Mtot,
+                (uint64_t)(p.K / 2), kRowB, kNH1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, x, (uint64_t)(p.K / 2), (uint64_t)S, (uint64_t)(p.K / 2), kRowB,
+                kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, (uint64_t)(p.K / 4), (uint64_t)S, (uint64_t)(p.K / 4), 16,
+                kTok, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  return launch_fcw_t<true, false, true>(q, m, max_tiles, st);
 }
 
 }  // namespace situ

@@ -85,6 +85,7 @@ struct FcdParams {
   const int32_t* tile_offsets;
   const int2* tile_info;
   int E_loc, n_mtiles, mg;
+  int tile_split;                // listed tiles hold up to 8 * tile_split rows (each CTA takes 8)
   // FC1
   int I;
   const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs;
@@ -216,10 +217,12 @@ cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t 
 // scales are packed per weight tile: FC1 tiles of fcw_n_rows(true) gate
 // rows plus their up rows, FC2 tiles as the prefill GEMM's.
 struct GatherHLParams {
-  int act;                       // SITU_ACT_BF16 (hi + lo) or SITU_ACT_MXFP8 (hi)
+  int act;                       // SITU_ACT_BF16 (hi + lo), SITU_ACT_MXFP8 (hi) or SITU_ACT_NVFP4
   const void* x_bf16;
   const uint8_t* x_q;
   const uint8_t* x_s;
+  const float* x_gs;             // NVFP4: per-token global scale, copied to xg [S] in row order
+  float* xg;
   const int32_t* permuted_src;
   const int32_t* meta;           // meta[0] = R
   int top_k, K;
@@ -243,6 +246,12 @@ struct FcwParams {
   const float* topk_weights;
   uint8_t *h, *hs;               // H1 rows and scale rows, as the token side above
   int hs_stride;
+  // NVFP4 FC1 (kind::mxf4nvf4): global scales, and H1 as f16 block rows
+  // (FcdParams::h16 / hs) for the register-tile FC2
+  const float* w1_gs;            // [E_loc, 2] gate / up global scale
+  const float* xg;               // [S] the row's per-token global scale
+  uint16_t* h16;                 // [S, pad128(I)]
+  float* h16s;                   // [S, pad128(I) / 32]
   // FC2
   const float* alpha2;
   float* y_out;                  // fp32 [S, H]
@@ -253,6 +262,15 @@ int fcw_n_rows(bool fc1);
 int fcw_scale_stride(int K);
 cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S, int E_loc,
                        bool fc1, bool lo, long max_tiles, cudaStream_t st);
+// NVFP4 FC1 on the decode tiles: both operands E2M1 with E4M3 scales per 16
+// (tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X).  Token rows: packed
+// E2M1 [rows, K/2] with their scale rows [rows, K/16] in expert order (gather
+// act = NVFP4); weight scales packed by launch_pack_scales_nv.  K a multiple
+// of 256, I of 128.
+cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
+                          int E_loc, long max_tiles, cudaStream_t st);
+size_t packed_scale_bytes_nv(int E_loc, int H, int I);
+cudaError_t launch_pack_scales_nv(const uint8_t* w1_scale, int E_loc, int H, int I, uint8_t* out, cudaStream_t st);
 size_t fcd_smem_bytes(int K, bool nvfp4);
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);
 

@@ -6,6 +6,8 @@
 // No host synchronisation: the number of kept rows and the GEMM token tiles
 // live on the device (written by the permute) and every later kernel reads
 // them there; grids are sized for the worst case and surplus CTAs exit.
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/situ_moe.h"
@@ -23,7 +25,7 @@ bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
-  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, total;
+  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, total;
 };
 
 // Decode-like routings (about six or fewer rows per expert) take the
@@ -47,6 +49,17 @@ bool fcw_shapes(const situ_moe_args* a) {
   return decode_like(a) && block_scaled_shapes(a) &&
          (a->act_dtype == SITU_ACT_BF16 || a->act_dtype == SITU_ACT_MXFP8);
 }
+// NVFP4 weights whose FC1 fits the NVFP4 decode tiles (stages of 256
+// elements of H, gate / up tiles of 128 rows)
+bool nv_tile_shapes(const situ_moe_args* a) {
+  return a->weight_dtype == SITU_W_NVFP4 && a->H % 256 == 0 && a->I % 128 == 0;
+}
+// decode-like routings of NVFP4 activations on those weights: FC1 on the
+// block-scaled decode tiles (kind::mxf4nvf4), FC2 on the register tiles
+bool fcw_nv_shapes(const situ_moe_args* a) {
+  return decode_like(a) && nv_tile_shapes(a) && a->act_dtype == SITU_ACT_NVFP4 &&
+         fcd_smem_bytes(a->I, true) <= kMaxDecodeSmem;
+}
 // prefill-sized routings with MXFP8 or bf16 activations on MXFP4 weights of
 // those shapes: the block-scaled prefill tiles (bf16 rows as hi + lo)
 bool takes_block_scaled_path(const situ_moe_args* a) {
@@ -67,12 +80,15 @@ size_t packed_fc1d_bytes(const situ_moe_args* a) {
 size_t packed_fc2d_bytes(const situ_moe_args* a) {
   return packed_scale_bytes(a->num_local_experts, a->H, a->I, false, fcw_n_rows(false));
 }
+// NVFP4: one packing, the FC1 decode tiles
 size_t packed_total_bytes(const situ_moe_args* a) {
+  if (a->weight_dtype == SITU_W_NVFP4) return packed_scale_bytes_nv(a->num_local_experts, a->H, a->I);
   return packed_fc1_bytes(a) + packed_fc2_bytes(a) + packed_fc1d_bytes(a) + packed_fc2d_bytes(a);
 }
 // the four packings into one buffer (layout above)
 cudaError_t pack_all_scales(const situ_moe_args* a, uint8_t* dst, cudaStream_t st) {
   const int E = a->num_local_experts;
+  if (a->weight_dtype == SITU_W_NVFP4) return launch_pack_scales_nv(a->w1_scale, E, a->H, a->I, dst, st);
   cudaError_t e = launch_pack_scales(a->w1_scale, E, a->H, a->I, true, dst, st);
   dst += packed_fc1_bytes(a);
   if (e == cudaSuccess) e = launch_pack_scales(a->w2_scale, E, a->H, a->I, false, dst, st);
@@ -115,12 +131,15 @@ Layout make_layout(const situ_moe_args* a) {
   L.xsp = take(bs ? nblk * fcq_act_scale_bytes(tiles, a->H) : 0);
   L.hsp = take(bs ? nblk * fcq_act_scale_bytes(tiles, a->I) : 0);
   L.ys = take(bs ? S * (size_t)(a->H / 32) : 0);   // scale bytes of the f16 Y rows
-  const bool w = fcw_shapes(a);
-  L.wsp = take((bs || w) && !a->scales_packed ? packed_total_bytes(a) : 0);
+  const bool w = fcw_shapes(a), wnv = fcw_nv_shapes(a);
+  L.wsp = take((bs || w || wnv) && !a->scales_packed ? packed_total_bytes(a) : 0);
   // decode tiles: hi / lo scale rows of the input and of H1 (the E4M3 rows
-  // reuse the x16 / h16 regions)
-  L.wxs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->H) : 0);
+  // reuse the x16 / h16 regions); NVFP4 tiles: the input's E4M3 scales in
+  // 16-byte chunks per 64 elements (its packed codes reuse x16) and per-row
+  // global scales
+  L.wxs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->H) : wnv ? S * (size_t)(a->H / 4) : 0);
   L.whs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->I) : 0);
+  L.xg = take(wnv ? 4 * S : 0);
   L.total = o;
   return L;
 }
@@ -264,12 +283,23 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   float* y = (float*)(ws + L.y);
   const bool nv = a->weight_dtype == SITU_W_NVFP4;
   const bool fcw = fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2);
-  const bool decode_path = !fcw && takes_decode_path(a);
-  const int tile_n = fcw ? fcw_token_tile() : decode_path ? kDecodeTileTokens : fcp_token_tile();
+  const bool fcwnv = fcw_nv_shapes(a);
+  const bool decode_path = !fcw && !fcwnv && takes_decode_path(a);
+  const int tile_n = fcw || fcwnv ? fcw_token_tile() : decode_path ? kDecodeTileTokens : fcp_token_tile();
   const long S = (long)a->T * a->top_k;
   const long max_tiles = S / tile_n + a->num_local_experts + 1;
+  // SITU_MOE_DEBUG_SYNC set: synchronise after every stage and name the
+  // first one whose kernels failed (a debugging aid; it serialises the call)
+  static const bool debug_sync = std::getenv("SITU_MOE_DEBUG_SYNC") != nullptr;
   auto mark = [&](int i) {
     if (events) cudaEventRecord((cudaEvent_t)events[i], st);
+    if (debug_sync && i > 0) {
+      static const char* names[] = {"start", "permute", "gather", "FC1", "FC2", "combine"};
+      const cudaError_t e = cudaStreamSynchronize(st);
+      if (e != cudaSuccess)
+        std::fprintf(stderr, "situ_moe_forward: stage %s failed: %s\n", i < 6 ? names[i] : "?",
+                     cudaGetErrorString(e));
+    }
   };
 
   bool fused = false;   // FC2 adds into the output accumulator (block-scaled prefill only)
@@ -354,6 +384,77 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if ((err = launch_fcw(w, a->w2, w.h, w.hs, S, a->num_local_experts, false, lo, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(4);
+  } else if (fcwnv) {
+    // NVFP4 at decode: FC1 (+SiTU) on 16-token block-scaled tiles with both
+    // operands E2M1 (kind::mxf4nvf4), writing H1 as f16 block rows; FC2 on
+    // the 8-token register tiles, two per 16-token tile
+    const uint8_t *wsp1, *wsp2, *wsp3, *wsp4;
+    if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
+    GatherHLParams g;
+    std::memset(&g, 0, sizeof(g));
+    g.act = SITU_ACT_NVFP4;
+    g.x_q = a->hidden_states_q;
+    g.x_s = a->hidden_states_scale;
+    g.x_gs = a->hidden_states_gscale;
+    g.xg = (float*)(ws + L.xg);
+    g.permuted_src = psrc;
+    g.meta = meta;
+    g.top_k = a->top_k;
+    g.K = a->H;
+    g.S = S;
+    g.x = ws + L.x16;
+    g.xs = ws + L.wxs;
+    if ((err = launch_gather_hl(g, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(2);
+    FcwParams w;
+    std::memset(&w, 0, sizeof(w));
+    w.offsets = offsets;
+    w.tile_offsets = tile_offsets;
+    w.tile_info = tile_info;
+    w.E_loc = a->num_local_experts;
+    w.I = a->I;
+    w.err = meta + 2;
+    w.wsp = wsp1;
+    w.Mtot = 2 * a->I;
+    w.K = a->H;
+    w.n_ntiles = (a->I + fcw_n_rows(true) - 1) / fcw_n_rows(true);
+    w.beta = a->gemm1_alpha;
+    w.beta_lin = a->gemm1_beta;
+    w.alpha_g = a->g1_alphas;
+    w.alpha_u = a->g1_alphas_up;
+    w.act_kind = a->activation;
+    w.topk_fc1 = a->apply_topk_in_fc1 != 0;
+    w.permuted_src = psrc;
+    w.topk_weights = a->topk_weights;
+    w.w1_gs = a->w1_gscale;
+    w.xg = g.xg;
+    w.h16 = (uint16_t*)(ws + L.h16);
+    w.h16s = (float*)(ws + L.h16s);
+    if ((err = launch_fcw_nv(w, a->w1, g.x, g.xs, S, a->num_local_experts, max_tiles, st)) != cudaSuccess)
+      return SITU_ERR_CUDA;
+    mark(3);
+    FcdParams d;
+    std::memset(&d, 0, sizeof(d));
+    d.offsets = offsets;
+    d.tile_offsets = tile_offsets;
+    d.tile_info = tile_info;
+    d.E_loc = a->num_local_experts;
+    d.tile_split = fcw_token_tile() / kDecodeTileTokens;
+    d.I = a->I;
+    d.w = a->w2;
+    d.ws = a->w2_scale;
+    d.Mtot = a->H;
+    d.K = a->I;
+    d.x16 = w.h16;
+    d.xs = w.h16s;
+    d.ablk = 1;
+    d.n_mtiles = (a->H + 127) / 128;
+    d.mg = 4;
+    d.alpha2 = a->g2_alphas;
+    d.w2_gs = a->w2_gscale;
+    d.y_out = y;
+    if ((err = launch_fcd(d, false, true, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    mark(4);
   } else if (decode_path) {
     // 8-token tiles: rows are converted once to f16 block rows, then FC1
     // (+SiTU, writing H1 as f16 block rows) and FC2
@@ -379,6 +480,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.tile_offsets = tile_offsets;
     d.tile_info = tile_info;
     d.E_loc = a->num_local_experts;
+    d.tile_split = 1;
     d.I = a->I;
     d.w = a->w1;
     d.ws = a->w1_scale;
@@ -600,7 +702,8 @@ situ_status situ_moe_forward_profiled(const situ_moe_args* a, void* workspace,
 }
 
 size_t situ_moe_packed_scales_size(const situ_moe_args* a) {
-  if (!a || a->H <= 0 || a->I <= 0 || a->num_local_experts < 1 || !block_scaled_shapes(a)) return 0;
+  if (!a || a->H <= 0 || a->I <= 0 || a->num_local_experts < 1 || !(block_scaled_shapes(a) || nv_tile_shapes(a)))
+    return 0;
   return packed_total_bytes(a);
 }
 
@@ -608,7 +711,7 @@ situ_status situ_moe_pack_scales(const situ_moe_args* a, void* packed, size_t pa
   if (!a || !packed) return SITU_ERR_NULL_ARG;
   if (a->H <= 0 || a->I <= 0 || a->num_local_experts < 1 || a->num_local_experts > SITU_MAX_LOCAL_EXPERTS)
     return SITU_ERR_BAD_SHAPE;
-  if (!block_scaled_shapes(a)) return SITU_ERR_UNSUPPORTED;
+  if (!(block_scaled_shapes(a) || nv_tile_shapes(a))) return SITU_ERR_UNSUPPORTED;
   if (!a->w1_scale || !a->w2_scale) return SITU_ERR_NULL_ARG;
   if (!aligned16(packed)) return SITU_ERR_MISALIGNED;
   if (packed_bytes < situ_moe_packed_scales_size(a)) return SITU_ERR_WORKSPACE_TOO_SMALL;
@@ -621,6 +724,7 @@ int32_t situ_moe_forward_launches(const situ_moe_args* a) {
   const int perm = permute_launches(a->T, a->top_k, a->num_local_experts);
   const int pack = a->scales_packed ? 0 : 4;
   if (fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
+  if (fcw_nv_shapes(a)) return perm + (a->scales_packed ? 0 : 1) + 4;
   if (takes_decode_path(a)) return perm + 4;
   if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2))
     return perm + pack + 4 + (a->fuse_combine ? 1 : 0);   // + zeroing the accumulator

@@ -287,7 +287,10 @@ size_t situ_moe_workspace_size(const situ_moe_args* args);
 
 /* Errors: NULL_ARG (args, required pointers, gemm1_alpha / gemm1_beta --
  * the SiTU caps have no default), BAD_SHAPE, UNSUPPORTED, MISALIGNED,
- * WORKSPACE_TOO_SMALL, CUDA.  T == 0 launches nothing. */
+ * WORKSPACE_TOO_SMALL, CUDA.  T == 0 launches nothing.
+ * Debugging aid: with the environment variable SITU_MOE_DEBUG_SYNC set, the
+ * call synchronises its stream after every stage and prints the first stage
+ * whose kernels failed to stderr (this serialises the call: not for timing). */
 situ_status situ_moe_forward(const situ_moe_args* args, void* workspace, size_t workspace_bytes,
                              void* stream);
 
@@ -332,21 +335,24 @@ situ_status situ_moe_device_status(const situ_moe_args* args, const void* worksp
 int32_t situ_moe_forward_launches(const situ_moe_args* args);
 
 /* ------------------------------------------------------------------------
- * situ_moe_packed_scales_size / situ_moe_pack_scales -- the MXFP4 weight
- * scales rearranged for the block-scaled tensor-core GEMMs.
+ * situ_moe_packed_scales_size / situ_moe_pack_scales -- the weight scales
+ * rearranged for the block-scaled tensor-core GEMMs.
  *
- * The block-scaled GEMMs (the w4a8 prefill tiles, and the decode tiles of
- * bf16 and MXFP8 activations) read each stage's weight scales as contiguous
- * blocks: per (local expert, weight tile, 128 elements of K) the UE8M0
- * bytes of the tile's rows, laid out as the tensor memory copy expects.
- * The buffer holds four such packings (the prefill and the decode tiles of
- * FC1 and of FC2).  Packing depends only on w1_scale, w2_scale,
- * num_local_experts, H and I, so it is done once per weight set; pass the
- * result as args->scales_packed.  Without it the forward packs into its
- * workspace on every call (same result, about 25% more HBM traffic for a
- * decode step).
+ * The block-scaled GEMMs read each stage's weight scales as contiguous
+ * blocks laid out as the tensor memory copy expects.  MXFP4 (the w4a8
+ * prefill tiles, and the decode tiles of bf16 and MXFP8 activations): per
+ * (local expert, weight tile, 128 elements of K) the UE8M0 bytes of the
+ * tile's rows; the buffer holds four such packings (the prefill and the
+ * decode tiles of FC1 and of FC2).  NVFP4 (the decode tiles of NVFP4
+ * activations, FC1 only): per (local expert, 128 gate + 128 up rows, 256
+ * elements of K) eight blocks of the E4M3 bytes, one per K = 64 MMA and W1
+ * half.  Packing depends only on w1_scale, w2_scale, num_local_experts, H
+ * and I, so it is done once per weight set; pass the result as
+ * args->scales_packed.  Without it the forward packs into its workspace on
+ * every call (same result, about 25% more HBM traffic for a decode step).
  * The size is 0 (and pack_scales returns UNSUPPORTED) unless weight_dtype
- * is MXFP4 and H and I are multiples of 128.  `packed` is a device buffer
+ * is MXFP4 with H and I multiples of 128, or NVFP4 with H a multiple of 256
+ * and I of 128.  `packed` is a device buffer
  * of at least that many bytes, 16-byte aligned, owned by the caller;
  * asynchronous on `stream`.  A layout of this library, not of the pages.
  * Errors: NULL_ARG, BAD_SHAPE, UNSUPPORTED, MISALIGNED, WORKSPACE_TOO_SMALL

@@ -102,7 +102,11 @@ def test_packed_scales_size_and_errors(lib):
     n = lib.situ_moe_packed_scales_size(ctypes.byref(ok))
     assert n > 0
     assert lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=256, I=96))) == 0   # I % 128
-    assert lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=256, I=128, weight_dtype=1))) == 0
+    # NVFP4: one packing, for the FC1 decode tiles (H a multiple of 256, I of 128):
+    # E_loc x I/128 weight tiles x H/256 stages x 4 KB
+    nv = lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=512, I=256, act_dtype=2, weight_dtype=1)))
+    assert nv == 8 * 2 * 2 * 4096
+    assert lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=384, I=128, act_dtype=2, weight_dtype=1))) == 0
     assert lib.situ_moe_packed_scales_size(None) == 0
     buf = ctypes.c_void_p(256)
     assert lib.situ_moe_pack_scales(None, buf, n, None) == 1
@@ -162,6 +166,14 @@ def test_forward_launch_count(lib):
     assert n(pre) == 5
     pre.fuse_combine = 1
     assert n(pre) == 6
+    # NVFP4 decode tiles: permute, gather, FC1 (mxf4nvf4), FC2 (register tiles), combine,
+    # plus one scale packing
+    nv = _args(H=256, I=128, act_dtype=2, weight_dtype=1)
+    for f in ("hidden_states_q", "hidden_states_scale", "hidden_states_gscale", "w1_gscale", "w2_gscale"):
+        setattr(nv, f, 0x1000)
+    assert n(nv) == 6
+    nv.scales_packed = 0x4000
+    assert n(nv) == 5
     assert n(_args(T=0)) == 0
     bad = _args()
     bad.gemm1_alpha = None

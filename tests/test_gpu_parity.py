@@ -225,6 +225,15 @@ def test_decode_w4a8():
     (dict(T=24, H=384, I=384, E_total=32, E_loc=8, off=8, K=4, params="k3_random"), None),
     (dict(T=40, H=512, I=256, E_total=64, E_loc=64, off=0, K=8, act=W.ACT_MXFP8,
           params="k3_random"), None),
+    # NVFP4 x NVFP4 FC1 tiles (kind::mxf4nvf4, stages of 256): a hot expert over six
+    # 16-token tiles that FC2 takes in 8-row halves; a filtered shard with two stages and
+    # two weight tiles; three stages and three weight tiles
+    (dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+          params="k3_random"), 3),
+    (dict(T=24, H=512, I=256, E_total=32, E_loc=8, off=8, K=4, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+          params="k3_random"), None),
+    (dict(T=40, H=768, I=384, E_total=64, E_loc=64, off=0, K=8, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+          params="k3_random"), None),
 ])
 def test_decode_tile_shapes(over, hot):
     """Decode-sized routings on the block-scaled decode tiles (16 tokens,
@@ -413,6 +422,8 @@ _VARIANT_SHAPES = [
                   wt=W.W_NVFP4)),                                                    # f16 prefill tiles
     ("tiny", dict(T=5, H=160, I=96, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4,
                   wt=W.W_NVFP4)),                                                    # register decode tiles
+    ("tiny", dict(T=64, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_NVFP4,
+                  wt=W.W_NVFP4)),                                                    # NVFP4 decode tiles
     ("tiny", dict(T=17, H=160, I=96, E_total=12, E_loc=5, off=4, K=3)),             # ... bf16, odd shapes
 ]
 

@@ -89,6 +89,11 @@ def algorithmic_bytes(wl, R, touched):
     w1 = touched * (2 * I * H // 2 + 2 * I * H // bs) + (touched * 8 if wl.wt == 1 else 0)
     w2 = touched * (H * I // 2 + H * I // bs) + (touched * 4 if wl.wt == 1 else 0)
     act_in = {0: T * H * 2, 1: T * H + T * H // 32, 2: T * H // 2 + T * H // 16 + 4 * T}[wl.act]
+    # one token row as the GEMMs read it: the FC1 input in its contract format
+    # (bf16, MXFP8 with its scale bytes, NVFP4 with its scales and global
+    # scale) and H1 (MXFP8 for w4a8, bf16 otherwise)
+    x_row = act_in / max(T, 1)
+    h_row = I + I / 32 if wl.act == 1 else 2 * I
     route = T * K * 8
     out = T * H * 2
     # bytes per element of the FC2 rows Y the combine reads: f16 + a scale byte
@@ -98,13 +103,23 @@ def algorithmic_bytes(wl, R, touched):
     y_bytes = 2 + 1 / 32 if blk_prefill else 4
     return {
         "permute": T * K * 4 + 2 * T * K * 4 + 2 * wl.E_loc * 4,
-        "gather": act_in * R / max(T, 1) + R * H * 2,
-        "fc1": w1 + R * H * 2 + R * I * 2,
-        "fc2": w2 + R * I * 2 + R * H * 2,
+        "gather": 2 * R * x_row,
+        "fc1": w1 + R * x_row + R * h_row,
+        "fc2": w2 + R * h_row + R * H * y_bytes,
         "combine": R * H * y_bytes + route + out,
         "quant": T * H * 2 + (T * H + T * H // 32 if wl.act == 1 else T * H // 2 + T * H // 16 + 4 * T),
         "layer": w1 + w2 + act_in + route + out,
     }
+
+
+def gemm_dtype(wl):
+    """Operand types the layer's GEMMs compute in, by the path the shapes take."""
+    decode_like = wl.T * wl.K / max(wl.E_total, 1) <= 6.0
+    if wl.wt == 0 and wl.H % 128 == 0 and wl.I % 128 == 0:
+        return "e2m1*e4m3->f32"
+    if wl.wt == 1 and wl.act == 2 and decode_like and wl.H % 256 == 0 and wl.I % 128 == 0:
+        return "e2m1*e2m1->f32 (FC1), f16->f32 (FC2)"
+    return "f16->f32"
 
 
 def layer_flops(wl, R):
@@ -417,8 +432,9 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         # operand types of the GEMMs: E2M1 weights x E4M3 rows (bf16 rows as
-        # hi + lo pairs) on the block-scaled tensor cores, else f16 operands
-        "dtype": "e2m1*e4m3->f32" if args.workload in ("decode", "prefill_w4a8", "tiny") else "f16->f32",
+        # hi + lo pairs) on the block-scaled tensor cores for MXFP4 weights;
+        # NVFP4: E2M1 x E2M1 in FC1 at decode sizes, f16 operands otherwise
+        "dtype": gemm_dtype(wl),
         "data": "synthetic (seeded; weights N(0,0.02) packed to the block-scaled format)",
         "config": {"workload": WORKLOAD_NAMES[args.workload], "T": wl.T, "H": wl.H, "I": wl.I,
                    "E_total": wl.E_total, "E_loc": wl.E_loc, "offset": wl.off, "top_k": wl.K,

@@ -379,16 +379,13 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       if constexpr (NV) {
         // NVFP4: the accumulators hold sum(code * scale) products; the
         // expert's gate / up global scale and the token's global scale make
-        // them dot products.  H1 is bf16, written as f16 block rows (f16
-        // mantissas of the bf16 values under a power-of-two scale per 32
-        // columns that puts the block maximum in [2^14, 2^15)), the form the
-        // register-tile FC2 reads.
+        // them dot products.  H1 is bf16 rows [S, I] (the NVFP4 variant keeps
+        // H1 in bf16), which the FC2 of NVFP4 weights reads.
         const int i0 = nt * kNH1 + warp * 32;
         if (i0 < p.I) {
           const float ag = (p.alpha_g ? __ldg(p.alpha_g + e) : 1.f) * __ldg(p.w1_gs + 2 * e);
           const float au = (p.alpha_u ? __ldg(p.alpha_u + e) : 1.f) * __ldg(p.w1_gs + 2 * e + 1);
           const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
-          const int ipad = pad128(p.I);
           float hv[kTok];
           with_act(p.act_kind, bt, btl, [&](auto act) {
 #pragma unroll
@@ -402,13 +399,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
             if (t >= nrows) break;
             float h = hv[t];
             if (p.topk_fc1) h *= __ldg(p.topk_weights + __ldg(p.permuted_src + row0 + t));
-            h = bf16_lo(f32x2_to_bf16x2(h, 0.f));
-            const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
-            int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
-            ex = ex < -126 ? -126 : ex;
-            const size_t r = (size_t)(row0 + t);
-            p.h16[r * ipad + i0 + lane] = __half_as_ushort(__float2half_rn(h * exp2i(-ex)));
-            if (lane == 0) p.h16s[r * (ipad / 32) + i0 / 32] = exp2i(ex);
+            p.h_bf16[(size_t)(row0 + t) * p.I + i0 + lane] = (uint16_t)(f32x2_to_bf16x2(h, 0.f) & 0xFFFFu);
           }
         }
       } else if (FC1) {
@@ -684,6 +675,318 @@ cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x
                 kTok, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   return launch_fcw_t<true, false, true>(q, m, max_tiles, st);
+}
+
+// ---------------------------------------------------------------------------
+// fcv_kernel: FC2 of NVFP4 weights on the decode tiles, bf16 H1.
+//
+// The FC2 input H1 is bf16 (the NVFP4 variant keeps H1 in bf16), which no
+// fp4 x fp4 MMA can take, and NVFP4's E4M3 scales per 16 fit no UE8M0
+// block-scaled kind.  So the weights are expanded in shared memory: a code
+// times its block scale is E2M1 x E4M3, at most six significant bits, held
+// exactly by bf16; tcgen05.mma.kind::f16 multiplies it with the bf16 H1 in
+// fp32.  The per-expert global scale and alpha2 go to the epilogue.
+//
+// Tiles as fcw's FC2: 256 rows of H (two M = 128 accumulators) x up to 16
+// expert-ordered tokens (N = 16), K = I in stages of 64.  Per stage TMA
+// loads the packed codes of the 256 rows (32 bytes each, no swizzle) and the
+// tokens' bf16 H1 rows (128 bytes each, 128-byte swizzle); eight converter
+// warps (one weight row per thread) write the stage's bf16 A operand in the
+// 128-byte-swizzled K-major layout, reading the row's four E4M3 scale bytes
+// from global memory one stage ahead.  Warp roles: 0..3 epilogue (thread =
+// TMEM lane = weight row), 4 TMA producer, 5 TMEM allocation + MMA issuer,
+// 6..13 converters.  Persistent over (token tile, weight tile) items, two
+// accumulator buffers; every wait bounded, as in fcw_kernel.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr int kVStages = 5;
+constexpr int kVBK = 64;                        // K elements per stage
+constexpr int kVThreads = 448;
+constexpr int kVTmemCols = 64;
+constexpr int kVABytes = 256 * 128;             // bf16 A operand: 256 rows x 64 elements
+constexpr int kVXBytes = kTok * 128;            // bf16 token rows
+constexpr int kVRBytes = 256 * 32;              // packed codes
+constexpr int kVOffA = 0;
+constexpr int kVOffX = kVOffA + kVStages * kVABytes;
+constexpr int kVOffR = kVOffX + kVStages * kVXBytes;
+constexpr int kVOffBar = kVOffR + kVStages * kVRBytes;
+constexpr int kVNumBars = 3 * kVStages + 5;     // full, conv, empty; acc_full[2], acc_empty[2]; drain
+constexpr int kVOffTm = kVOffBar + kVNumBars * 8;
+constexpr int kVSmem = kVOffTm + 16 + 1024;
+constexpr uint32_t kVTx = kVXBytes + kVRBytes;
+static_assert(kVSmem <= 227 * 1024, "shared memory budget");
+static_assert(kVOffX % 1024 == 0 && kVXBytes % 1024 == 0, "swizzle atoms");
+// kind::f16: fp32 accumulator (bit 4), A = B = bf16 (1 at bits 7 and 10),
+// both K-major, N >> 3 at bit 17, M >> 4 at bit 24
+constexpr uint32_t kVIdesc =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kVIdesc), "r"(accumulate)
+      : "memory");
+}
+// eight E2M1 codes (one 32-bit word, byte j = elements 2j, 2j + 1) -> f16 pairs
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t* d) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t e4m3_pair_f16(uint32_t b) {   // one E4M3 code in both halves
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)(b | (b << 8))));
+  return d;
+}
+// code x scale as an exact f16 pair, then as a bf16 pair (at most six
+// significant bits and magnitudes in [2^-10, 2688]: exact in both)
+__device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t codes_f16x2, uint32_t scale_f16x2) {
+  uint32_t v;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(codes_f16x2), "r"(scale_f16x2));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+  return f32x2_to_bf16x2(lo, hi);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kVThreads, 1)
+fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const FcvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nk = p.K / kVBK;
+  const int nsb = p.K / 16;                     // E4M3 scales per weight row
+
+  const uint32_t sbase = saddr(smem);
+  const uint32_t bar0 = sbase + kVOffBar;
+  auto full = [&](int s) { return bar0 + 8 * s; };
+  auto conv = [&](int s) { return bar0 + 8 * (kVStages + s); };
+  auto empty = [&](int s) { return bar0 + 8 * (2 * kVStages + s); };
+  auto acc_full = [&](int b) { return bar0 + 8 * (3 * kVStages + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8 * (3 * kVStages + 2 + b); };
+  const uint32_t drain = bar0 + 8 * (3 * kVStages + 4);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + kVOffTm);
+
+  if (tid == 0) {
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(conv(s), 256);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tm_holder)),
+                 "r"(kVTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tm_holder;
+  griddep_launch_dependents();
+  griddep_wait();
+  const long total = *reinterpret_cast<volatile int*>(p.err) != 0
+                         ? 0
+                         : (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
+
+  if ((long)blockIdx.x >= total) {
+    // no item for this CTA
+  } else if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    const bool leader = elect_one();
+    long it = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const int nt = (int)(item % p.n_ntiles);
+      const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
+      const int wrow = ti.x * p.Mtot + nt * kNH2;
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int s = (int)(it % kVStages);
+        const long r = it / kVStages;
+        if (r > 0 && !mbar_wait_warp(empty(s), (uint32_t)((r - 1) & 1), p.err, 51)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          mbar_expect_tx(full(s), kVTx);
+          tma_load_2d(sbase + kVOffR + s * kVRBytes, &tmW, kk * (kVBK / 2), wrow, full(s));
+          tma_load_2d(sbase + kVOffX + s * kVXBytes, &tmX, kk * kVBK, ti.y, full(s));
+        }
+        __syncwarp();
+      }
+    }
+    if (leader)
+      for (long j = it - 1; j >= 0 && j >= it - kVStages; --j)
+        drain_wait(full((int)(j % kVStages)), (uint32_t)((j / kVStages) & 1));
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ---------------- converters: thread = weight row n of the tile ----------------
+    const int n = tid - 192;
+    long it = 0;
+    for (long item = blockIdx.x; item < total; item += gridDim.x) {
+      const int nt = (int)(item % p.n_ntiles);
+      const int e = __ldg(p.tile_info + item / p.n_ntiles).x;
+      const int grow = nt * kNH2 + n;
+      const bool valid = grow < p.Mtot;
+      const uint8_t* srow = p.ws + ((size_t)e * p.Mtot + (valid ? grow : 0)) * (size_t)nsb;
+      // the row's four scale bytes of a stage (its 16-element blocks)
+      auto load_sc = [&](int kk) -> uint32_t {
+        if (!valid || kk >= nk) return 0u;
+        const uint8_t* q = srow + 4 * kk;
+        return (uint32_t)__ldg(q) | ((uint32_t)__ldg(q + 1) << 8) | ((uint32_t)__ldg(q + 2) << 16) |
+               ((uint32_t)__ldg(q + 3) << 24);
+      };
+      uint32_t sc = load_sc(0);
+      bool ok = true;
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const uint32_t sc_next = load_sc(kk + 1);
+        const int s = (int)(it % kVStages);
+        if (!mbar_wait(full(s), (uint32_t)((it / kVStages) & 1), p.err, 54)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* raw = smem + kVOffR + s * kVRBytes + n * 32;
+        uint8_t* arow = smem + kVOffA + s * kVABytes + n * 128;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(raw);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 16);
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint32_t f[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) f[b] = e4m3_pair_f16((sc >> (8 * b)) & 0xFFu);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {   // 16-byte chunk j = elements 8j .. 8j + 7 (block j / 2)
+          uint32_t d[4];
+          e2m1x8_f16(w[j], d);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d[i] = scaled_bf16x2(d[i], f[j >> 1]);
+          *reinterpret_cast<uint4*>(arow + ((j ^ (n & 7)) << 4)) = make_uint4(d[0], d[1], d[2], d[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(conv(s));
+        sc = sc_next;
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    const bool leader = elect_one();
+    long it = 0;
+    int li = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+      const int buf = li & 1, use = li >> 1;
+      if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 52)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t d1 = tmem + (uint32_t)(buf * 32);
+      const uint32_t d2 = d1 + kTok;
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int s = (int)(it % kVStages);
+        const uint32_t par = (uint32_t)((it / kVStages) & 1);
+        if (!mbar_wait_warp(full(s), par, p.err, 53) || !mbar_wait_warp(conv(s), par, p.err, 55)) {
+          ok = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (leader) {
+          const uint64_t ad1 = sdesc(sbase + kVOffA + s * kVABytes);
+          const uint64_t ad2 = sdesc(sbase + kVOffA + s * kVABytes + 128 * 128);
+          const uint64_t bd = sdesc(sbase + kVOffX + s * kVXBytes);
+#pragma unroll
+          for (uint32_t k4 = 0; k4 < kVBK / 16; ++k4) {   // K = 16 per MMA, 32 bytes of each row
+            const uint32_t acc = (kk | (int)k4) != 0;
+            mma_bf16(d1, ad1 + 2 * k4, bd + 2 * k4, acc);
+            mma_bf16(d2, ad2 + 2 * k4, bd + 2 * k4, acc);
+          }
+          mma_commit(empty(s));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (leader) mma_commit(acc_full(buf));
+      __syncwarp();
+    }
+    if (leader) {
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: thread = weight row (TMEM lane) ----------------
+    const int l = warp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    for (int li = 0;; ++li) {
+      const long item = blockIdx.x + (long)li * gridDim.x;
+      if (item >= total) break;
+      const int buf = li & 1;
+      const int nt = (int)(item % p.n_ntiles);
+      const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
+      const int e = ti.x, row0 = ti.y;
+      const int nrows = min(kTok, __ldg(p.offsets + e + 1) - row0);
+      if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 56))) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * 32);
+      float a1[kTok], a2[kTok];
+      tmem_ld16(t1, a1);
+      tmem_ld16(t1 + kTok, a2);
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(acc_empty(buf));
+      const float sc = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * __ldg(p.gs + e);
+      const int n1 = nt * kNH2 + l, n2 = n1 + 128;
+#pragma unroll
+      for (int t = 0; t < kTok; ++t) {
+        if (t >= nrows) break;
+        float* yr = p.y_out + (size_t)(row0 + t) * p.Mtot;
+        if (n1 < p.Mtot) yr[n1] = a1[t] * sc;
+        if (n2 < p.Mtot) yr[n2] = a2[t] * sc;
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kVTmemCols) : "memory");
+  }
+}
+
+cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, long max_tiles,
+                       cudaStream_t st) {
+  if (S <= 0) return cudaSuccess;
+  CUtensorMap m[2];
+  // packed codes [E_loc * Mtot, K/2] bytes, boxes of 32 bytes (64 codes) x
+  // 256 rows, no swizzle; H1 bf16 [S, K], boxes of 64 elements x 16 rows,
+  // 128-byte swizzle
+  if (!make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w, (uint64_t)(p.K / 2), (uint64_t)E_loc * p.Mtot,
+                (uint64_t)(p.K / 2), kVBK / 2, kNH2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h_bf16, (uint64_t)p.K, (uint64_t)S, (uint64_t)p.K * 2,
+                kVBK, kTok, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  static int set_for[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || set_for[dev] == 0) {
+    cudaError_t err = cudaFuncSetAttribute(fcv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) set_for[dev] = 1;
+  }
+  const long items = max_tiles * p.n_ntiles;
+  const long grid = items < sm_count_w() ? items : sm_count_w();
+  if (grid <= 0) return cudaSuccess;
+  return launch_pdl(fcv_kernel, dim3((unsigned)grid), dim3(kVThreads), (size_t)kVSmem, st, m[0], m[1], p);
 }
 
 }  // namespace situ

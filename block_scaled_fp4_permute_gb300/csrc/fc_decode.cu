@@ -150,17 +150,13 @@ __global__ void __launch_bounds__(kThreads, 2) fcd_kernel(const FcdParams p) {
 
   const int ngroups = (p.n_mtiles + p.mg - 1) / p.mg;
   const int grp = blockIdx.x % ngroups;
-  // a listed tile of up to 8 * tile_split rows is taken 8 rows per CTA
-  const int split = p.tile_split > 1 ? p.tile_split : 1;
-  const int sub = (blockIdx.x / ngroups) % split;
-  const int tile = blockIdx.x / ngroups / split;
+  const int tile = blockIdx.x / ngroups;
   const int total = __ldg(p.tile_offsets + p.E_loc);
   if (tile >= total) return;
   const int2 ti = __ldg(p.tile_info + tile);
   const int e = ti.x;
-  const int row0 = ti.y + kNT * sub;
+  const int row0 = ti.y;
   const int nrows = min(kNT, __ldg(p.offsets + e + 1) - row0);
-  if (nrows <= 0) return;
   const int mt0 = grp * p.mg;
   const int mcount = min(p.mg, p.n_mtiles - mt0);
   const int nch = (nkb + 3) / 4;
@@ -561,7 +557,7 @@ static cudaError_t launch_fcd_t(const FcdParams& p, long max_tiles, cudaStream_t
     if (dev < 64) set_for[dev] = (int)smem;
   }
   const long ngroups = (p.n_mtiles + p.mg - 1) / p.mg;
-  const long grid = max_tiles * (p.tile_split > 1 ? p.tile_split : 1) * ngroups;
+  const long grid = max_tiles * ngroups;
   if (grid <= 0) return cudaSuccess;
   fcd_kernel<FC1, WNV, ABLK><<<(unsigned)grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();

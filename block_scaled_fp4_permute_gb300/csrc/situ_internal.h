@@ -85,7 +85,6 @@ struct FcdParams {
   const int32_t* tile_offsets;
   const int2* tile_info;
   int E_loc, n_mtiles, mg;
-  int tile_split;                // listed tiles hold up to 8 * tile_split rows (each CTA takes 8)
   // FC1
   int I;
   const float *beta, *beta_lin, *alpha_g, *alpha_u, *w1_gs;
@@ -246,12 +245,11 @@ struct FcwParams {
   const float* topk_weights;
   uint8_t *h, *hs;               // H1 rows and scale rows, as the token side above
   int hs_stride;
-  // NVFP4 FC1 (kind::mxf4nvf4): global scales, and H1 as f16 block rows
-  // (FcdParams::h16 / hs) for the register-tile FC2
+  // NVFP4 FC1 (kind::mxf4nvf4): global scales, and H1 as bf16 rows for
+  // the NVFP4 FC2 (launch_fcv)
   const float* w1_gs;            // [E_loc, 2] gate / up global scale
   const float* xg;               // [S] the row's per-token global scale
-  uint16_t* h16;                 // [S, pad128(I)]
-  float* h16s;                   // [S, pad128(I) / 32]
+  uint16_t* h_bf16;              // [S, I]
   // FC2
   const float* alpha2;
   float* y_out;                  // fp32 [S, H]
@@ -270,6 +268,25 @@ cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, c
 cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
                           int E_loc, long max_tiles, cudaStream_t st);
 size_t packed_scale_bytes_nv(int E_loc, int H, int I);
+// NVFP4 FC2 on the decode tiles: the weights expanded to exact bf16 (code x
+// E4M3 block scale) in shared memory by converter warps, times the bf16 H1
+// rows [S, K] on tcgen05.mma.kind::f16; 256 rows of H per weight tile, up to
+// 16 tokens; Y fp32 [S, Mtot] = alpha2 * gs * acc.  K a multiple of 64.
+struct FcvParams {
+  int Mtot, K;
+  const uint8_t* w;              // packed E2M1 [E_loc, Mtot, K/2]
+  const uint8_t* ws;             // E4M3 block scales [E_loc, Mtot, K/16]
+  const float* gs;               // [E_loc] global scale
+  const float* alpha2;           // [E_loc] or null
+  const int32_t* offsets;
+  const int32_t* tile_offsets;
+  const int2* tile_info;
+  int E_loc, n_ntiles;
+  float* y_out;
+  int* err;
+};
+cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, long max_tiles,
+                       cudaStream_t st);
 cudaError_t launch_pack_scales_nv(const uint8_t* w1_scale, int E_loc, int H, int I, uint8_t* out, cudaStream_t st);
 size_t fcd_smem_bytes(int K, bool nvfp4);
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);

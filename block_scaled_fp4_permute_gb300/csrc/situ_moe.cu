@@ -55,10 +55,10 @@ bool nv_tile_shapes(const situ_moe_args* a) {
   return a->weight_dtype == SITU_W_NVFP4 && a->H % 256 == 0 && a->I % 128 == 0;
 }
 // decode-like routings of NVFP4 activations on those weights: FC1 on the
-// block-scaled decode tiles (kind::mxf4nvf4), FC2 on the register tiles
+// block-scaled decode tiles (kind::mxf4nvf4), FC2 on the same tiles with
+// the weights expanded to bf16 (kind::f16)
 bool fcw_nv_shapes(const situ_moe_args* a) {
-  return decode_like(a) && nv_tile_shapes(a) && a->act_dtype == SITU_ACT_NVFP4 &&
-         fcd_smem_bytes(a->I, true) <= kMaxDecodeSmem;
+  return decode_like(a) && nv_tile_shapes(a) && a->act_dtype == SITU_ACT_NVFP4;
 }
 // prefill-sized routings with MXFP8 or bf16 activations on MXFP4 weights of
 // those shapes: the block-scaled prefill tiles (bf16 rows as hi + lo)
@@ -386,8 +386,9 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     mark(4);
   } else if (fcwnv) {
     // NVFP4 at decode: FC1 (+SiTU) on 16-token block-scaled tiles with both
-    // operands E2M1 (kind::mxf4nvf4), writing H1 as f16 block rows; FC2 on
-    // the 8-token register tiles, two per 16-token tile
+    // operands E2M1 (kind::mxf4nvf4), writing H1 as bf16 rows; FC2 on the
+    // same tiles with the weights expanded to bf16 in shared memory
+    // (kind::f16)
     const uint8_t *wsp1, *wsp2, *wsp3, *wsp4;
     if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
     GatherHLParams g;
@@ -428,32 +429,26 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     w.topk_weights = a->topk_weights;
     w.w1_gs = a->w1_gscale;
     w.xg = g.xg;
-    w.h16 = (uint16_t*)(ws + L.h16);
-    w.h16s = (float*)(ws + L.h16s);
+    w.h_bf16 = h1;
     if ((err = launch_fcw_nv(w, a->w1, g.x, g.xs, S, a->num_local_experts, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(3);
-    FcdParams d;
-    std::memset(&d, 0, sizeof(d));
-    d.offsets = offsets;
-    d.tile_offsets = tile_offsets;
-    d.tile_info = tile_info;
-    d.E_loc = a->num_local_experts;
-    d.tile_split = fcw_token_tile() / kDecodeTileTokens;
-    d.I = a->I;
-    d.w = a->w2;
-    d.ws = a->w2_scale;
-    d.Mtot = a->H;
-    d.K = a->I;
-    d.x16 = w.h16;
-    d.xs = w.h16s;
-    d.ablk = 1;
-    d.n_mtiles = (a->H + 127) / 128;
-    d.mg = 4;
-    d.alpha2 = a->g2_alphas;
-    d.w2_gs = a->w2_gscale;
-    d.y_out = y;
-    if ((err = launch_fcd(d, false, true, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    FcvParams v;
+    std::memset(&v, 0, sizeof(v));
+    v.Mtot = a->H;
+    v.K = a->I;
+    v.w = a->w2;
+    v.ws = a->w2_scale;
+    v.gs = a->w2_gscale;
+    v.alpha2 = a->g2_alphas;
+    v.offsets = offsets;
+    v.tile_offsets = tile_offsets;
+    v.tile_info = tile_info;
+    v.E_loc = a->num_local_experts;
+    v.n_ntiles = (a->H + fcw_n_rows(false) - 1) / fcw_n_rows(false);
+    v.y_out = y;
+    v.err = meta + 2;
+    if ((err = launch_fcv(v, h1, S, a->num_local_experts, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(4);
   } else if (decode_path) {
     // 8-token tiles: rows are converted once to f16 block rows, then FC1
@@ -480,7 +475,6 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.tile_offsets = tile_offsets;
     d.tile_info = tile_info;
     d.E_loc = a->num_local_experts;
-    d.tile_split = 1;
     d.I = a->I;
     d.w = a->w1;
     d.ws = a->w1_scale;

@@ -397,7 +397,10 @@ def run_ours(args):
     tpath = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
-            traffic = json.load(f).get(dom)
+            tj = json.load(f)
+        # counters of a capture at this token count only
+        if tj.get("T") == wl.T:
+            traffic = tj.get(dom)
     # the bound of the dominant kernel and of the layer: the larger of the
     # HBM time of its algorithmic bytes and the tensor time of its FLOPs
     tc_peak, tc_src = tensor_peak(wl)

@@ -196,7 +196,9 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
   int32_t* offs = cnt + E_loc;               // [E_loc]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kPerWarp = kPermChunk / kSmallWarps;   // 128
-  for (int i = threadIdx.x; i < kSmallWarps * E_loc; i += blockDim.x) wcnt[i] = 0;
+  // only the warps that own slots keep counts (8 of 32 at 1,024 slots)
+  const int nw = (S + kPerWarp - 1) / kPerWarp;
+  for (int i = threadIdx.x; i < nw * E_loc; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   for (int r = 0; r < kPerWarp; r += kWarp) {
     const int s = warp * kPerWarp + r + lane;
@@ -208,7 +210,7 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
   __syncthreads();
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
     int run = 0;
-    for (int w = 0; w < kSmallWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       const int v = wcnt[w * E_loc + e];
       wcnt[w * E_loc + e] = run;
       run += v;

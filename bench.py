@@ -226,6 +226,18 @@ def _oracle_run(oracle, W, wl, host_kw, n):
     return oracle.moe_forward(**kw, tokens=toks)
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself on one rank or without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -350,10 +362,7 @@ def run_ours(args):
     quant_ms /= n_prof
     step_ms = np.array([b[0].elapsed_time(b[1]) for b in bounds])
     ms = float(step_ms.mean())
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     # end to end: pinned host inputs -> device, layer, output -> pinned host
     dev_in = [wl.x_bf16, wl.topk_ids, wl.topk_weights]
@@ -377,10 +386,7 @@ def run_ours(args):
         if i >= max(args.warmup, 1):
             e_ms.append(e0.elapsed_time(e1))
     e2e_ms = float(np.mean(e_ms))
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     hbm, peak_kind = peaks()
     stages = {}

@@ -701,33 +701,39 @@ cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x
 
 namespace {
 
-constexpr int kVStages = 5;
 constexpr int kVBK = 64;                        // K elements per stage
 constexpr int kVThreads = 448;
-constexpr int kVTmemCols = 64;
 constexpr int kVABytes = 256 * 128;             // bf16 A operand: 256 rows x 64 elements
-constexpr int kVXBytes = kTok * 128;            // bf16 token rows
 constexpr int kVRBytes = 256 * 32;              // packed codes
-constexpr int kVOffA = 0;
-constexpr int kVOffX = kVOffA + kVStages * kVABytes;
-constexpr int kVOffR = kVOffX + kVStages * kVXBytes;
-constexpr int kVOffBar = kVOffR + kVStages * kVRBytes;
-constexpr int kVNumBars = 3 * kVStages + 5;     // full, conv, empty; acc_full[2], acc_empty[2]; drain
-constexpr int kVOffTm = kVOffBar + kVNumBars * 8;
-constexpr int kVSmem = kVOffTm + 16 + 1024;
-constexpr uint32_t kVTx = kVXBytes + kVRBytes;
-static_assert(kVSmem <= 227 * 1024, "shared memory budget");
-static_assert(kVOffX % 1024 == 0 && kVXBytes % 1024 == 0, "swizzle atoms");
-// kind::f16: fp32 accumulator (bit 4), A = B = bf16 (1 at bits 7 and 10),
-// both K-major, N >> 3 at bit 17, M >> 4 at bit 24
-constexpr uint32_t kVIdesc =
-    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTok >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// NB: token rows per tile (MMA N), 16, or 64 when experts hold more rows
+template <int NB>
+struct CfgV {
+  static constexpr int kStages = NB > 16 ? 4 : 5;
+  static constexpr int kTmemCols = NB > 16 ? 256 : 64;   // two buffers of two NB-column accumulators
+  static constexpr int kXBytes = NB * 128;              // bf16 token rows
+  static constexpr int kOffA = 0;
+  static constexpr int kOffX = kOffA + kStages * kVABytes;
+  static constexpr int kOffR = kOffX + kStages * kXBytes;
+  static constexpr int kOffBar = kOffR + kStages * kVRBytes;
+  static constexpr int kNumBars = 3 * kStages + 5;     // full, conv, empty; acc_full[2], acc_empty[2]; drain
+  static constexpr int kOffTm = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffTm + 16 + 1024;
+  static constexpr uint32_t kTx = kXBytes + kVRBytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kOffX % 1024 == 0 && kXBytes % 1024 == 0, "swizzle atoms");
+  static_assert(4 * NB <= kTmemCols, "TMEM budget");
+  // kind::f16: fp32 accumulator (bit 4), A = B = bf16 (1 at bits 7 and 10),
+  // both K-major, N >> 3 at bit 17, M >> 4 at bit 24
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+};
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(kVIdesc), "r"(accumulate)
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // eight E2M1 codes (one 32-bit word, byte j = elements 2j, 2j + 1) -> f16 pairs
@@ -755,23 +761,26 @@ __device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t codes_f16x2, uint32_t
 
 }  // namespace
 
+template <int NB>
 __global__ void __launch_bounds__(kVThreads, 1)
 fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const FcvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using C = CfgV<NB>;
+  constexpr int kVStages = C::kStages;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nk = p.K / kVBK;
   const int nsb = p.K / 16;                     // E4M3 scales per weight row
 
   const uint32_t sbase = saddr(smem);
-  const uint32_t bar0 = sbase + kVOffBar;
+  const uint32_t bar0 = sbase + C::kOffBar;
   auto full = [&](int s) { return bar0 + 8 * s; };
   auto conv = [&](int s) { return bar0 + 8 * (kVStages + s); };
   auto empty = [&](int s) { return bar0 + 8 * (2 * kVStages + s); };
   auto acc_full = [&](int b) { return bar0 + 8 * (3 * kVStages + b); };
   auto acc_empty = [&](int b) { return bar0 + 8 * (3 * kVStages + 2 + b); };
   const uint32_t drain = bar0 + 8 * (3 * kVStages + 4);
-  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + kVOffTm);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::kOffTm);
 
   if (tid == 0) {
     for (int s = 0; s < kVStages; ++s) {
@@ -788,7 +797,7 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   }
   if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tm_holder)),
-                 "r"(kVTmemCols)
+                 "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -821,9 +830,9 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           break;
         }
         if (leader) {
-          mbar_expect_tx(full(s), kVTx);
-          tma_load_2d(sbase + kVOffR + s * kVRBytes, &tmW, kk * (kVBK / 2), wrow, full(s));
-          tma_load_2d(sbase + kVOffX + s * kVXBytes, &tmX, kk * kVBK, ti.y, full(s));
+          mbar_expect_tx(full(s), C::kTx);
+          tma_load_2d(sbase + C::kOffR + s * kVRBytes, &tmW, kk * (kVBK / 2), wrow, full(s));
+          tma_load_2d(sbase + C::kOffX + s * C::kXBytes, &tmX, kk * kVBK, ti.y, full(s));
         }
         __syncwarp();
       }
@@ -858,8 +867,8 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + kVOffR + s * kVRBytes + n * 32;
-        uint8_t* arow = smem + kVOffA + s * kVABytes + n * 128;
+        const uint8_t* raw = smem + C::kOffR + s * kVRBytes + n * 32;
+        uint8_t* arow = smem + C::kOffA + s * kVABytes + n * 128;
         const uint4 q0 = *reinterpret_cast<const uint4*>(raw);
         const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 16);
         const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -890,8 +899,8 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int buf = li & 1, use = li >> 1;
       if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 52)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t d1 = tmem + (uint32_t)(buf * 32);
-      const uint32_t d2 = d1 + kTok;
+      const uint32_t d1 = tmem + (uint32_t)(buf * 2 * NB);
+      const uint32_t d2 = d1 + NB;
       for (int kk = 0; kk < nk; ++kk, ++it) {
         const int s = (int)(it % kVStages);
         const uint32_t par = (uint32_t)((it / kVStages) & 1);
@@ -901,14 +910,14 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (leader) {
-          const uint64_t ad1 = sdesc(sbase + kVOffA + s * kVABytes);
-          const uint64_t ad2 = sdesc(sbase + kVOffA + s * kVABytes + 128 * 128);
-          const uint64_t bd = sdesc(sbase + kVOffX + s * kVXBytes);
+          const uint64_t ad1 = sdesc(sbase + C::kOffA + s * kVABytes);
+          const uint64_t ad2 = sdesc(sbase + C::kOffA + s * kVABytes + 128 * 128);
+          const uint64_t bd = sdesc(sbase + C::kOffX + s * C::kXBytes);
 #pragma unroll
           for (uint32_t k4 = 0; k4 < kVBK / 16; ++k4) {   // K = 16 per MMA, 32 bytes of each row
             const uint32_t acc = (kk | (int)k4) != 0;
-            mma_bf16(d1, ad1 + 2 * k4, bd + 2 * k4, acc);
-            mma_bf16(d2, ad2 + 2 * k4, bd + 2 * k4, acc);
+            mma_bf16(d1, ad1 + 2 * k4, bd + 2 * k4, C::kIdesc, acc);
+            mma_bf16(d2, ad2 + 2 * k4, bd + 2 * k4, C::kIdesc, acc);
           }
           mma_commit(empty(s));
         }
@@ -934,24 +943,27 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int nt = (int)(item % p.n_ntiles);
       const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
       const int e = ti.x, row0 = ti.y;
-      const int nrows = min(kTok, __ldg(p.offsets + e + 1) - row0);
+      const int nrows = min(NB, __ldg(p.offsets + e + 1) - row0);
       if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 56))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * 32);
-      float a1[kTok], a2[kTok];
-      tmem_ld16(t1, a1);
-      tmem_ld16(t1 + kTok, a2);
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      mbar_arrive(acc_empty(buf));
+      const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * 2 * NB);
       const float sc = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * __ldg(p.gs + e);
       const int n1 = nt * kNH2 + l, n2 = n1 + 128;
+      // 16 token columns at a time from each accumulator
+      for (int c0 = 0; c0 < NB; c0 += 16) {
+        float a1[16], a2[16];
+        tmem_ld16(t1 + c0, a1);
+        tmem_ld16(t1 + NB + c0, a2);
 #pragma unroll
-      for (int t = 0; t < kTok; ++t) {
-        if (t >= nrows) break;
-        float* yr = p.y_out + (size_t)(row0 + t) * p.Mtot;
-        if (n1 < p.Mtot) yr[n1] = a1[t] * sc;
-        if (n2 < p.Mtot) yr[n2] = a2[t] * sc;
+        for (int t = 0; t < 16; ++t) {
+          if (c0 + t >= nrows) break;
+          float* yr = p.y_out + (size_t)(row0 + c0 + t) * p.Mtot;
+          if (n1 < p.Mtot) yr[n1] = a1[t] * sc;
+          if (n2 < p.Mtot) yr[n2] = a2[t] * sc;
+        }
       }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(acc_empty(buf));
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -959,34 +971,43 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   if (warp == 5) {
     __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kVTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
 }
 
-cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, long max_tiles,
-                       cudaStream_t st) {
-  if (S <= 0) return cudaSuccess;
+template <int NB>
+cudaError_t launch_fcv_t(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, long max_tiles,
+                         cudaStream_t st) {
+  using C = CfgV<NB>;
   CUtensorMap m[2];
   // packed codes [E_loc * Mtot, K/2] bytes, boxes of 32 bytes (64 codes) x
-  // 256 rows, no swizzle; H1 bf16 [S, K], boxes of 64 elements x 16 rows,
+  // 256 rows, no swizzle; H1 bf16 [S, K], boxes of 64 elements x NB rows,
   // 128-byte swizzle
   if (!make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w, (uint64_t)(p.K / 2), (uint64_t)E_loc * p.Mtot,
                 (uint64_t)(p.K / 2), kVBK / 2, kNH2, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h_bf16, (uint64_t)p.K, (uint64_t)S, (uint64_t)p.K * 2,
-                kVBK, kTok, CU_TENSOR_MAP_SWIZZLE_128B))
+                kVBK, NB, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || set_for[dev] == 0) {
-    cudaError_t err = cudaFuncSetAttribute(fcv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+    cudaError_t err = cudaFuncSetAttribute(fcv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (err != cudaSuccess) return err;
     if (dev < 64) set_for[dev] = 1;
   }
   const long items = max_tiles * p.n_ntiles;
   const long grid = items < sm_count_w() ? items : sm_count_w();
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(fcv_kernel, dim3((unsigned)grid), dim3(kVThreads), (size_t)kVSmem, st, m[0], m[1], p);
+  return launch_pdl(fcv_kernel<NB>, dim3((unsigned)grid), dim3(kVThreads), (size_t)C::kSmem, st, m[0], m[1], p);
+}
+
+cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, int tile_rows, long max_tiles,
+                       cudaStream_t st) {
+  if (S <= 0) return cudaSuccess;
+  if (tile_rows == 64) return launch_fcv_t<64>(p, h_bf16, S, E_loc, max_tiles, st);
+  if (tile_rows == kTok) return launch_fcv_t<kTok>(p, h_bf16, S, E_loc, max_tiles, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace situ

@@ -234,6 +234,10 @@ def test_decode_w4a8():
           params="k3_random"), None),
     (dict(T=40, H=768, I=384, E_total=64, E_loc=64, off=0, K=8, act=W.ACT_NVFP4, wt=W.W_NVFP4,
           params="k3_random"), None),
+    # 25 rows per expert: FC2 on 64-token tiles of its own tile table, a hot expert over
+    # four of them and 13 16-token FC1 tiles
+    (dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+          params="k3_random"), 5),
 ])
 def test_decode_tile_shapes(over, hot):
     """Decode-sized routings on the block-scaled decode tiles (16 tokens,

@@ -117,7 +117,7 @@ def gemm_dtype(wl):
     rows_per_expert = wl.T * wl.K / max(wl.E_total, 1)
     if wl.wt == 0 and wl.H % 128 == 0 and wl.I % 128 == 0:
         return "e2m1*e4m3->f32"
-    if wl.wt == 1 and wl.act == 2 and rows_per_expert <= 64.0 and wl.H % 256 == 0 and wl.I % 128 == 0:
+    if wl.wt == 1 and wl.act == 2 and rows_per_expert <= 512.0 and wl.H % 256 == 0 and wl.I % 128 == 0:
         return "e2m1*e2m1->f32 (FC1), bf16->f32 (FC2)"
     return "f16->f32"
 

@@ -54,13 +54,13 @@ bool fcw_shapes(const situ_moe_args* a) {
 bool nv_tile_shapes(const situ_moe_args* a) {
   return a->weight_dtype == SITU_W_NVFP4 && a->H % 256 == 0 && a->I % 128 == 0;
 }
-// NVFP4 activations on those weights with up to 64 kept rows per expert on
-// average: FC1 on the block-scaled 16-token tiles (kind::mxf4nvf4), FC2 on
-// the same tiles with the weights expanded to bf16 (kind::f16).  Each tile
-// streams its expert's weights, which beats the 128-token f16 prefill tiles
-// (whose dequantisation runs per tile over mostly empty rows) until the
-// experts hold a few hundred rows.
-constexpr double kNvTileMaxRowsPerExpert = 64.0;
+// NVFP4 activations on those weights with up to 512 kept rows per expert on
+// average: FC1 on the block-scaled 16-token tiles (kind::mxf4nvf4), FC2 with
+// the weights expanded to bf16 (kind::f16) on the same tiles or on 64-token
+// ones.  Each tile streams its expert's weights, which beats the 128-token
+// f16 prefill tiles (whose dequantisation runs per tile over mostly empty
+// rows) until the experts hold a few hundred rows.
+constexpr double kNvTileMaxRowsPerExpert = 512.0;
 bool fcw_nv_shapes(const situ_moe_args* a) {
   return (double)a->T * a->top_k / (double)a->num_experts_total <= kNvTileMaxRowsPerExpert && nv_tile_shapes(a) &&
          a->act_dtype == SITU_ACT_NVFP4;

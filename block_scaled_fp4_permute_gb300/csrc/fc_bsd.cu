@@ -62,7 +62,6 @@ constexpr int kNH1 = 128;          // FC1 gate (and up) rows per weight tile
 constexpr int kNH2 = 256;          // FC2 rows per weight tile
 constexpr int kThreads = 192;
 constexpr int kSfBlock = 512;
-constexpr int kSfCol0 = 128;       // scale columns start after the two accumulator buffers
 
 // NV: NVFP4 FC1 (E2M1 x E2M1, E4M3 scales per 16, kind::mxf4nvf4 with
 // scale_vec::4X).  A stage is then 256 elements of K (128 packed bytes per
@@ -70,19 +69,28 @@ constexpr int kSfCol0 = 128;       // scale columns start after the two accumula
 // per row, so every MMA has its own 512-byte scale block (four TMEM
 // columns) on both sides: two weight accumulators x four MMAs, and four
 // token blocks (the gather writes each row's stage scales as four 16-byte
-// chunks, one per MMA, its word first).
-template <bool FC1, bool LO, bool NV = false>
+// chunks, one per MMA, its word first).  TT: token rows per tile, 16, or
+// 64 for NVFP4 when experts hold more rows; a 64-row token scale block
+// spans two TMEM columns (rows 0..31, then 32..63): the MMA warp first moves
+// row i + 32's word into word 1 of row i in shared memory, so one
+// tcgen05.cp (its TMEM destination 4-column aligned, as the copy requires)
+// lays both columns.
+template <bool FC1, bool LO, bool NV = false, int TT = kTok>
 struct CfgW {
   static_assert(!NV || (FC1 && !LO), "the NVFP4 tiles are FC1 on NVFP4 token rows");
-  static constexpr int kStages = NV ? 5 : 6;
-  static constexpr int NB = LO ? 2 * kTok : kTok;          // MMA N: token rows (hi, lo interleaved)
+  static_assert(TT == kTok || (NV && TT == 64), "64-row tiles are NVFP4 only");
+  static constexpr int kStages = NV ? (TT > 32 ? 4 : 5) : 6;
+  static constexpr int NB = LO ? 2 * TT : TT;              // MMA N: token rows (hi, lo interleaved)
   static constexpr int kKS = NV ? kBKnv : kBK;             // K elements per stage
   static constexpr int kABytes = 256 * kRowB;              // 32 KB
-  static constexpr int kBBytes = NB * kRowB;               // 4 / 2 KB
+  static constexpr int kBBytes = NB * kRowB;               // 2 / 4 / 8 KB
   static constexpr int kWSf = NV ? 8 : 2;                  // weight scale blocks per stage
   static constexpr int kTSf = NV ? 4 : 1;                  // token scale blocks per stage
-  static constexpr int kSfBytes = (kWSf + kTSf) * kSfBlock;
+  static constexpr int kTSfBytes = TT * 16 > kSfBlock ? TT * 16 : kSfBlock;
+  static constexpr int kSfBytes = kWSf * kSfBlock + kTSf * kTSfBytes;
   static constexpr int kTmemCols = NV ? 512 : 256;
+  static constexpr int kAccStride = 2 * NB > 64 ? 2 * NB : 64;   // columns per accumulator buffer
+  static constexpr int kSfCol0 = 2 * kAccStride;            // scale columns after the two buffers
   static constexpr int kSfColsPerStage = 4 * (kWSf + kTSf);
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -93,12 +101,12 @@ struct CfgW {
   static constexpr int kSmem = kOffTm + 16 + 1024;
   // bytes a stage's copies deliver: the 4-bit map of the MXFP4 weights
   // counts the packed bytes (half the widened tile), the NVFP4 map is bytes
-  static constexpr uint32_t kTx = NV ? (uint32_t)(2 * kNH1 * kRowB + NB * kRowB + kTSf * NB * 16 + kWSf * kSfBlock)
+  static constexpr uint32_t kTx = NV ? (uint32_t)(2 * kNH1 * kRowB + NB * kRowB + kTSf * TT * 16 + kWSf * kSfBlock)
                                      : (uint32_t)(FC1 ? 2 * kNH1 : kNH2) * (kBK / 2) + (uint32_t)NB * kBK +
                                            (uint32_t)NB * 16 + 2 * kSfBlock;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
-  static_assert(2 * NB <= 64, "accumulator buffer");
+  static_assert(2 * NB <= kAccStride, "accumulator buffer");
   static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0, "swizzle atoms");
   // A = E2M1 (5), B = E4M3 (0), both K-major; N >> 3 at bit 17, UE8M0
   // scales (bit 23), M >> 4 at bit 24; B / A scale byte selectors at bits
@@ -177,11 +185,11 @@ __device__ __forceinline__ uint32_t split_hl(float v, int e, int c, uint32_t& lo
 // byte offset of the UE8M0 scale of 32-element block b in a token scale row
 __device__ __forceinline__ int tok_scale_byte(int b) { return 16 * (b >> 2) + (b & 3); }
 
-template <bool FC1, bool LO, bool NV>
+template <bool FC1, bool LO, bool NV, int TT>
 __global__ void __launch_bounds__(kThreads, 1)
 fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
            const __grid_constant__ CUtensorMap tmS, const FcwParams p) {
-  using C = CfgW<FC1, LO, NV>;
+  using C = CfgW<FC1, LO, NV, TT>;
   constexpr int kStages = C::kStages;
   constexpr int NB = C::NB;
   constexpr int NH = FC1 ? kNH1 : kNH2;
@@ -269,7 +277,8 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           bulk_load(sf_smem, wsb + (size_t)kk * C::kWSf * kSfBlock, C::kWSf * kSfBlock, full(s));
 #pragma unroll
           for (int b = 0; b < C::kTSf; ++b)
-            tma_load_2d(sf_smem + (C::kWSf + b) * kSfBlock, &tmS, 16 * (C::kTSf * kk + b), RM * row0, full(s));
+            tma_load_2d(sf_smem + C::kWSf * kSfBlock + b * C::kTSfBytes, &tmS, 16 * (C::kTSf * kk + b), RM * row0,
+                        full(s));
         }
         __syncwarp();
       }
@@ -289,7 +298,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int buf = li & 1, use = li >> 1;
       if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 42)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t d1 = tmem + (uint32_t)(buf * 64);
+      const uint32_t d1 = tmem + (uint32_t)(buf * C::kAccStride);
       const uint32_t d2 = d1 + NB;
       for (int kk = 0; kk < nk; ++kk, ++it) {
         const int s = (int)(it % kStages);
@@ -298,12 +307,27 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (TT > 32) {
+          // 64-row token scale blocks: lane i puts row i + 32's scale word
+          // beside row i's (word 1 of its 16-byte row)
+          uint32_t* tb = reinterpret_cast<uint32_t*>(smem + C::kOffSF + s * C::kSfBytes + C::kWSf * kSfBlock);
+#pragma unroll
+          for (int b = 0; b < C::kTSf; ++b) {
+            uint32_t* blk = tb + b * (C::kTSfBytes / 4);
+            blk[4 * lane + 1] = blk[4 * (lane + 32)];
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
         if (leader) {
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
-          const uint32_t sfw = tmem + (uint32_t)(kSfCol0 + s * C::kSfColsPerStage);
+          const uint32_t sfw = tmem + (uint32_t)(C::kSfCol0 + s * C::kSfColsPerStage);
           const uint32_t sft = sfw + 4 * C::kWSf;
+          const uint32_t sf_tok = sf_smem + C::kWSf * kSfBlock;
 #pragma unroll
-          for (int b = 0; b < C::kWSf + C::kTSf; ++b) tmem_cp_sf(sfw + 4 * b, sf_desc(sf_smem + b * kSfBlock));
+          for (int b = 0; b < C::kWSf; ++b) tmem_cp_sf(sfw + 4 * b, sf_desc(sf_smem + b * kSfBlock));
+#pragma unroll
+          for (int b = 0; b < C::kTSf; ++b) tmem_cp_sf(sft + 4 * b, sf_desc(sf_tok + b * C::kTSfBytes));
           const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
           const uint64_t ad1 = sdesc(a_smem);
           const uint64_t ad2 = sdesc(a_smem + 128 * kRowB);
@@ -348,14 +372,16 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int tile = (int)(item / p.n_ntiles), nt = (int)(item % p.n_ntiles);
       const int2 ti = __ldg(p.tile_info + tile);
       const int e = ti.x, row0 = ti.y;
-      const int nrows = min(kTok, __ldg(p.offsets + e + 1) - row0);
+      const int nrows = min(TT, __ldg(p.offsets + e + 1) - row0);
       // every epilogue thread takes the same decision (the waits are
       // bounded, so all 128 reach the reduction)
       if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 46))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * 64);
+      const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * C::kAccStride);
       float a1[kTok], a2[kTok];
-      if (LO) {
+      if (NV) {
+        // read 16 token columns at a time below
+      } else if (LO) {
         // columns 2t (hi) and 2t + 1 (lo) of token t
         float v[16];
 #pragma unroll
@@ -372,36 +398,46 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         tmem_ld16(t1, a1);
         tmem_ld16(t1 + NB, a2);
       }
-      // the accumulator is in registers: hand it back to the MMA warp
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      mbar_arrive(acc_empty(buf));
+      if (!NV) {
+        // the accumulator is in registers: hand it back to the MMA warp
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(acc_empty(buf));
+      }
 
       if constexpr (NV) {
         // NVFP4: the accumulators hold sum(code * scale) products; the
         // expert's gate / up global scale and the token's global scale make
         // them dot products.  H1 is bf16 rows [S, I] (the NVFP4 variant keeps
         // H1 in bf16), which the FC2 of NVFP4 weights reads.
+        // The tile's token columns 16 at a time.
         const int i0 = nt * kNH1 + warp * 32;
-        if (i0 < p.I) {
-          const float ag = (p.alpha_g ? __ldg(p.alpha_g + e) : 1.f) * __ldg(p.w1_gs + 2 * e);
-          const float au = (p.alpha_u ? __ldg(p.alpha_u + e) : 1.f) * __ldg(p.w1_gs + 2 * e + 1);
-          const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
-          float hv[kTok];
+        const float ag = (p.alpha_g ? __ldg(p.alpha_g + e) : 1.f) * __ldg(p.w1_gs + 2 * e);
+        const float au = (p.alpha_u ? __ldg(p.alpha_u + e) : 1.f) * __ldg(p.w1_gs + 2 * e + 1);
+        const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+        for (int c0 = 0; c0 < TT; c0 += 16) {
+          tmem_ld16(t1 + c0, a1);
+          tmem_ld16(t1 + NB + c0, a2);
+          if (c0 >= nrows || i0 >= p.I) continue;
+          float hv[16];
           with_act(p.act_kind, bt, btl, [&](auto act) {
 #pragma unroll
-            for (int t = 0; t < kTok; ++t) {
-              const float gx = t < nrows ? __ldg(p.xg + row0 + t) : 0.f;
-              hv[t] = act(a1[t] * (ag * gx), a2[t] * (au * gx));
+            for (int j = 0; j < 16; ++j) {
+              const float gx = c0 + j < nrows ? __ldg(p.xg + row0 + c0 + j) : 0.f;
+              hv[j] = act(a1[j] * (ag * gx), a2[j] * (au * gx));
             }
           });
 #pragma unroll
-          for (int t = 0; t < kTok; ++t) {
+          for (int j = 0; j < 16; ++j) {
+            const int t = c0 + j;
             if (t >= nrows) break;
-            float h = hv[t];
+            float h = hv[j];
             if (p.topk_fc1) h *= __ldg(p.topk_weights + __ldg(p.permuted_src + row0 + t));
             p.h_bf16[(size_t)(row0 + t) * p.I + i0 + lane] = (uint16_t)(f32x2_to_bf16x2(h, 0.f) & 0xFFFFu);
           }
         }
+        // every column is in registers or stored: hand the accumulator back
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(acc_empty(buf));
       } else if (FC1) {
         // gate row i = nt * 128 + l and its up row are lane l of the two
         // accumulators; warp w holds the 32-element block i0 .. i0 + 31
@@ -555,23 +591,23 @@ int sm_count_w() {
   return v;
 }
 
-template <bool FC1, bool LO, bool NV = false>
+template <bool FC1, bool LO, bool NV = false, int TT = kTok>
 cudaError_t launch_fcw_t(const FcwParams& p, const CUtensorMap* m, long max_tiles, cudaStream_t st) {
-  using C = CfgW<FC1, LO, NV>;
+  using C = CfgW<FC1, LO, NV, TT>;
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || set_for[dev] == 0) {
     cudaError_t err =
-        cudaFuncSetAttribute(fcw_kernel<FC1, LO, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(fcw_kernel<FC1, LO, NV, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (err != cudaSuccess) return err;
     if (dev < 64) set_for[dev] = 1;
   }
   const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
   const long grid = items < sm_count_w() ? items : sm_count_w();
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(fcw_kernel<FC1, LO, NV>, dim3((unsigned)grid), dim3(kThreads), (size_t)C::kSmem, st, m[0], m[1],
-                    m[2], p);
+  return launch_pdl(fcw_kernel<FC1, LO, NV, TT>, dim3((unsigned)grid), dim3(kThreads), (size_t)C::kSmem, st, m[0],
+                    m[1], m[2], p);
 }
 
 }  // namespace
@@ -659,8 +695,9 @@ cudaError_t launch_pack_scales_nv(const uint8_t* w1_scale, int E_loc, int H, int
 }
 
 cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
-                          int E_loc, long max_tiles, cudaStream_t st) {
+                          int E_loc, int tile_rows, long max_tiles, cudaStream_t st) {
   if (S <= 0) return cudaSuccess;
+  if (tile_rows != kTok && tile_rows != 64) return cudaErrorInvalidValue;
   FcwParams q = p;
   q.w = w;
   CUtensorMap m[3];
@@ -670,11 +707,12 @@ cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x
   if (!make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)(p.K / 2), (uint64_t)E_loc * p.Mtot,
                 (uint64_t)(p.K / 2), kRowB, kNH1, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, x, (uint64_t)(p.K / 2), (uint64_t)S, (uint64_t)(p.K / 2), kRowB,
-                kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                (uint32_t)tile_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&m[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, (uint64_t)(p.K / 4), (uint64_t)S, (uint64_t)(p.K / 4), 16,
-                kTok, CU_TENSOR_MAP_SWIZZLE_NONE))
+                (uint32_t)tile_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  return launch_fcw_t<true, false, true>(q, m, max_tiles, st);
+  if (tile_rows == 64) return launch_fcw_t<true, false, true, 64>(q, m, max_tiles, st);
+  return launch_fcw_t<true, false, true, kTok>(q, m, max_tiles, st);
 }
 
 // ---------------------------------------------------------------------------

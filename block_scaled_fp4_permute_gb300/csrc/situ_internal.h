@@ -35,10 +35,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
                            int2* tile_info, int32_t* permuted_src, int32_t* slot_to_row,
                            int32_t* meta, int32_t* blk_counts, cudaStream_t st);
 size_t permute_scratch_bytes(int T, int K, int E_loc);
-// a second tile table (tiles of tile_n rows) over the permute's expert
-// offsets [E_loc + 1], for a GEMM with another token tile
-cudaError_t launch_tile_table(const int32_t* offsets, int E_loc, int tile_n, int32_t* tile_offsets, int2* tile_info,
-                              cudaStream_t st);
+
 int permute_launches(int T, int K, int E_loc);   // kernels launch_permute enqueues
 
 cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t* s,
@@ -269,8 +266,9 @@ cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, c
 // E2M1 [rows, K/2] with their scale rows [rows, K/16] in expert order (gather
 // act = NVFP4); weight scales packed by launch_pack_scales_nv.  K a multiple
 // of 256, I of 128.
+// tile_rows: token rows per tile, 16 or 64 (the tile table's)
 cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
-                          int E_loc, long max_tiles, cudaStream_t st);
+                          int E_loc, int tile_rows, long max_tiles, cudaStream_t st);
 size_t packed_scale_bytes_nv(int E_loc, int H, int I);
 // NVFP4 FC2 on the decode tiles: the weights expanded to exact bf16 (code x
 // E4M3 block scale) in shared memory by converter warps, times the bf16 H1

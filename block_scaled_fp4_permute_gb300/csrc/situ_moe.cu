@@ -25,7 +25,7 @@ bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
-  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, t2off, t2info, total;
+  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, total;
 };
 
 // Decode-like routings (about six or fewer rows per expert) take the
@@ -65,11 +65,11 @@ bool fcw_nv_shapes(const situ_moe_args* a) {
   return (double)a->T * a->top_k / (double)a->num_experts_total <= kNvTileMaxRowsPerExpert && nv_tile_shapes(a) &&
          a->act_dtype == SITU_ACT_NVFP4;
 }
-// Above 16 rows per expert on average the NVFP4 FC2 takes 64-token tiles (a
-// second tile table): its small-N MMAs cost about the same per instruction
-// at N = 64 as at 16, so wider tiles cut their count per weight byte.
-constexpr int kNvFc2WideTile = 64;
-bool nv_wide_fc2(const situ_moe_args* a) {
+// Above 16 rows per expert on average the NVFP4 tiles are 64 tokens wide:
+// their small-N MMAs cost about the same per instruction at N = 64 as at 16,
+// so wider tiles cut the MMAs and the weight re-reads per weight byte.
+constexpr int kNvWideTile = 64;
+bool nv_wide(const situ_moe_args* a) {
   return fcw_nv_shapes(a) && (double)a->T * a->top_k / (double)a->num_experts_total > 16.0;
 }
 // prefill-sized routings with MXFP8 or bf16 activations on MXFP4 weights of
@@ -152,10 +152,6 @@ Layout make_layout(const situ_moe_args* a) {
   L.wxs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->H) : wnv ? S * (size_t)(a->H / 4) : 0);
   L.whs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->I) : 0);
   L.xg = take(wnv ? 4 * S : 0);
-  // NVFP4 FC2 on 64-token tiles: its own tile table
-  const bool wide = nv_wide_fc2(a);
-  L.t2off = take(wide ? 4 * (E + 1) : 0);
-  L.t2info = take(wide ? 8 * (S / kNvFc2WideTile + E + 2) : 0);
   L.total = o;
   return L;
 }
@@ -301,7 +297,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   const bool fcw = fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2);
   const bool fcwnv = fcw_nv_shapes(a);
   const bool decode_path = !fcw && !fcwnv && takes_decode_path(a);
-  const int tile_n = fcw || fcwnv ? fcw_token_tile() : decode_path ? kDecodeTileTokens : fcp_token_tile();
+  const int tile_n = fcwnv ? (nv_wide(a) ? kNvWideTile : fcw_token_tile())
+                     : fcw ? fcw_token_tile() : decode_path ? kDecodeTileTokens : fcp_token_tile();
   const long S = (long)a->T * a->top_k;
   const long max_tiles = S / tile_n + a->num_local_experts + 1;
   // SITU_MOE_DEBUG_SYNC set: synchronise after every stage and name the
@@ -324,9 +321,6 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   cudaError_t err = launch_permute(a->topk_ids, a->T, a->top_k, a->num_local_experts,
                                    a->local_expert_offset, tile_n, counts, offsets, tile_offsets,
                                    tile_info, psrc, s2r, meta, (int32_t*)(ws + L.blk), st);
-  if (err == cudaSuccess && fcwnv && nv_wide_fc2(a))
-    err = launch_tile_table(offsets, a->num_local_experts, kNvFc2WideTile, (int32_t*)(ws + L.t2off),
-                            (int2*)(ws + L.t2info), st);
   if (err != cudaSuccess) return SITU_ERR_CUDA;
   mark(1);
 
@@ -449,7 +443,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     w.w1_gs = a->w1_gscale;
     w.xg = g.xg;
     w.h_bf16 = h1;
-    if ((err = launch_fcw_nv(w, a->w1, g.x, g.xs, S, a->num_local_experts, max_tiles, st)) != cudaSuccess)
+    if ((err = launch_fcw_nv(w, a->w1, g.x, g.xs, S, a->num_local_experts, tile_n, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(3);
     FcvParams v;
@@ -467,15 +461,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     v.n_ntiles = (a->H + fcw_n_rows(false) - 1) / fcw_n_rows(false);
     v.y_out = y;
     v.err = meta + 2;
-    int fc2_tile = fcw_token_tile();
-    long fc2_tiles = max_tiles;
-    if (nv_wide_fc2(a)) {
-      fc2_tile = kNvFc2WideTile;
-      fc2_tiles = S / kNvFc2WideTile + a->num_local_experts + 1;
-      v.tile_offsets = (const int32_t*)(ws + L.t2off);
-      v.tile_info = (const int2*)(ws + L.t2info);
-    }
-    if ((err = launch_fcv(v, h1, S, a->num_local_experts, fc2_tile, fc2_tiles, st)) != cudaSuccess)
+    if ((err = launch_fcv(v, h1, S, a->num_local_experts, tile_n, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(4);
   } else if (decode_path) {
@@ -746,7 +732,7 @@ int32_t situ_moe_forward_launches(const situ_moe_args* a) {
   const int perm = permute_launches(a->T, a->top_k, a->num_local_experts);
   const int pack = a->scales_packed ? 0 : 4;
   if (fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
-  if (fcw_nv_shapes(a)) return perm + (nv_wide_fc2(a) ? 1 : 0) + (a->scales_packed ? 0 : 1) + 4;
+  if (fcw_nv_shapes(a)) return perm + (a->scales_packed ? 0 : 1) + 4;
   if (takes_decode_path(a)) return perm + 4;
   if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2))
     return perm + pack + 4 + (a->fuse_combine ? 1 : 0);   // + zeroing the accumulator

@@ -234,8 +234,8 @@ def test_decode_w4a8():
           params="k3_random"), None),
     (dict(T=40, H=768, I=384, E_total=64, E_loc=64, off=0, K=8, act=W.ACT_NVFP4, wt=W.W_NVFP4,
           params="k3_random"), None),
-    # 25 rows per expert: FC2 on 64-token tiles of its own tile table, a hot expert over
-    # four of them and 13 16-token FC1 tiles
+    # 25 rows per expert: both GEMMs on 64-token tiles (two TMEM columns of token scales per
+    # MMA in FC1), a hot expert over four of them
     (dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
           params="k3_random"), 5),
 ])

@@ -336,12 +336,22 @@ def test_all_slots_on_one_expert():
     assert_parity(out, oracle_out(wl), "two hot experts")
 
 
-def test_no_kept_slot_gives_zero_output():
-    wl = W.make("tiny", device="cuda", T=8, E_total=16, E_loc=4, off=12)
+@pytest.mark.parametrize("over", [
+    dict(),                                                              # register decode tiles (bf16)
+    dict(H=256, I=128),                                                  # block-scaled decode tiles
+    dict(H=256, I=128, act=W.ACT_MXFP8),
+    dict(H=256, I=128, act=W.ACT_NVFP4, wt=W.W_NVFP4),                   # NVFP4 tiles
+])
+def test_no_kept_slot_gives_zero_output(over):
+    """Every slot outside the shard: no tile, no GEMM work, and an all-zero
+    partial output on every decode-tile path."""
+    wl = W.make("tiny", device="cuda", T=8, E_total=16, E_loc=4, off=12, **over)
     wl.topk_ids[:] = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
     layer = binding.Layer(wl)
     layer.out.fill_(1.0)
     out = layer().float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
     assert np.all(out == 0.0)
 
 

@@ -337,8 +337,8 @@ def test_all_slots_on_one_expert():
 
 
 @pytest.mark.parametrize("over", [
-    dict(),                                                              # register decode tiles (bf16)
-    dict(H=256, I=128),                                                  # block-scaled decode tiles
+    dict(H=160, I=96),                                                   # register decode tiles
+    dict(H=256, I=128),                                                  # block-scaled decode tiles (bf16)
     dict(H=256, I=128, act=W.ACT_MXFP8),
     dict(H=256, I=128, act=W.ACT_NVFP4, wt=W.W_NVFP4),                   # NVFP4 tiles
 ])

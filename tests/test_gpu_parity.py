@@ -238,6 +238,10 @@ def test_decode_w4a8():
     # MMA in FC1), a hot expert over four of them
     (dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
           params="k3_random"), 5),
+    # 64-token NVFP4 tiles on a filtered shard (experts 4..11 of 16), two stages, two FC1
+    # weight tiles
+    (dict(T=300, H=512, I=256, E_total=16, E_loc=8, off=4, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+          params="k3_random"), None),
 ])
 def test_decode_tile_shapes(over, hot):
     """Decode-sized routings on the block-scaled decode tiles (16 tokens,
@@ -438,6 +442,8 @@ _VARIANT_SHAPES = [
                   wt=W.W_NVFP4)),                                                    # register decode tiles
     ("tiny", dict(T=64, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_NVFP4,
                   wt=W.W_NVFP4)),                                                    # NVFP4 decode tiles
+    ("tiny", dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4,
+                  wt=W.W_NVFP4)),                                                    # ... 64 tokens wide
     ("tiny", dict(T=17, H=160, I=96, E_total=12, E_loc=5, off=4, K=3)),             # ... bf16, odd shapes
 ]
 

@@ -743,11 +743,11 @@ constexpr int kVBK = 64;                        // K elements per stage
 constexpr int kVThreads = 448;
 constexpr int kVABytes = 256 * 128;             // bf16 A operand: 256 rows x 64 elements
 constexpr int kVRBytes = 256 * 32;              // packed codes
-// NB: token rows per tile (MMA N), 16, or 64 when experts hold more rows
+// NB: token rows per tile (MMA N), 16, 64 or 128 as experts hold more rows
 template <int NB>
 struct CfgV {
-  static constexpr int kStages = NB > 16 ? 4 : 5;
-  static constexpr int kTmemCols = NB > 16 ? 256 : 64;   // two buffers of two NB-column accumulators
+  static constexpr int kStages = NB > 64 ? 3 : NB > 16 ? 4 : 5;
+  static constexpr int kTmemCols = NB > 16 ? 4 * NB : 64;   // two buffers of two NB-column accumulators
   static constexpr int kXBytes = NB * 128;              // bf16 token rows
   static constexpr int kOffA = 0;
   static constexpr int kOffX = kOffA + kStages * kVABytes;
@@ -1043,6 +1043,7 @@ cudaError_t launch_fcv_t(const FcvParams& p, const uint16_t* h_bf16, long S, int
 cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, int tile_rows, long max_tiles,
                        cudaStream_t st) {
   if (S <= 0) return cudaSuccess;
+  if (tile_rows == 128) return launch_fcv_t<128>(p, h_bf16, S, E_loc, max_tiles, st);
   if (tile_rows == 64) return launch_fcv_t<64>(p, h_bf16, S, E_loc, max_tiles, st);
   if (tile_rows == kTok) return launch_fcv_t<kTok>(p, h_bf16, S, E_loc, max_tiles, st);
   return cudaErrorInvalidValue;

@@ -268,6 +268,35 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
   for (int r = R + threadIdx.x; r < S; r += blockDim.x) permuted_src[r] = -1;
 }
 
+// A second GEMM tile table over the same expert-ordered rows, for a GEMM
+// whose token tiles are tile_n rows (offsets from the permute): one block,
+// each thread a contiguous run of experts, an exclusive scan of their tile
+// counts, then tile_info[t] = (expert, first row).
+__global__ void __launch_bounds__(1024)
+tile_table_kernel(const int32_t* __restrict__ offsets, int E_loc, int tile_n, int32_t* __restrict__ tile_offsets,
+                  int2* __restrict__ tile_info) {
+  const int per = (E_loc + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(E_loc, (int)threadIdx.x * per), e1 = min(E_loc, e0 + per);
+  int st = 0;
+  for (int e = e0; e < e1; ++e) st += (__ldg(offsets + e + 1) - __ldg(offsets + e) + tile_n - 1) / tile_n;
+  int tiles;
+  int pt = block_exclusive_scan(st, &tiles);
+  for (int e = e0; e < e1; ++e) {
+    const int r0 = __ldg(offsets + e);
+    const int nt = (__ldg(offsets + e + 1) - r0 + tile_n - 1) / tile_n;
+    tile_offsets[e] = pt;
+    for (int k = 0; k < nt; ++k) tile_info[pt + k] = make_int2(e, r0 + k * tile_n);
+    pt += nt;
+  }
+  if (threadIdx.x == 0) tile_offsets[E_loc] = tiles;
+}
+
+cudaError_t launch_tile_table(const int32_t* offsets, int E_loc, int tile_n, int32_t* tile_offsets, int2* tile_info,
+                              cudaStream_t st) {
+  tile_table_kernel<<<1, 1024, 0, st>>>(offsets, E_loc, tile_n, tile_offsets, tile_info);
+  return cudaGetLastError();
+}
+
 static int g_scatter_smem_set[64];
 static int g_small_smem_set[64];
 

@@ -35,6 +35,10 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
                            int2* tile_info, int32_t* permuted_src, int32_t* slot_to_row,
                            int32_t* meta, int32_t* blk_counts, cudaStream_t st);
 size_t permute_scratch_bytes(int T, int K, int E_loc);
+// a second tile table (tiles of tile_n rows) over the permute's expert
+// offsets [E_loc + 1], for a GEMM with another token tile
+cudaError_t launch_tile_table(const int32_t* offsets, int E_loc, int tile_n, int32_t* tile_offsets, int2* tile_info,
+                              cudaStream_t st);
 
 int permute_launches(int T, int K, int E_loc);   // kernels launch_permute enqueues
 
@@ -287,7 +291,7 @@ struct FcvParams {
   float* y_out;
   int* err;
 };
-// tile_rows: the token tile of p's tile table, 16 or 64
+// tile_rows: the token tile of p's tile table, 16, 64 or 128
 cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, int tile_rows, long max_tiles,
                        cudaStream_t st);
 cudaError_t launch_pack_scales_nv(const uint8_t* w1_scale, int E_loc, int H, int I, uint8_t* out, cudaStream_t st);

@@ -25,7 +25,7 @@ bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
-  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, total;
+  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, t2off, t2info, total;
 };
 
 // Decode-like routings (about six or fewer rows per expert) take the
@@ -71,6 +71,13 @@ bool fcw_nv_shapes(const situ_moe_args* a) {
 constexpr int kNvWideTile = 64;
 bool nv_wide(const situ_moe_args* a) {
   return fcw_nv_shapes(a) && (double)a->T * a->top_k / (double)a->num_experts_total > 16.0;
+}
+// Above 64 rows per expert FC2 takes 128-token tiles of a second tile table:
+// its converter warps expand an expert's weights once per tile, so wider
+// tiles expand them fewer times.
+constexpr int kNvFc2WideTile = 128;
+bool nv_wide_fc2(const situ_moe_args* a) {
+  return fcw_nv_shapes(a) && (double)a->T * a->top_k / (double)a->num_experts_total > 64.0;
 }
 // prefill-sized routings with MXFP8 or bf16 activations on MXFP4 weights of
 // those shapes: the block-scaled prefill tiles (bf16 rows as hi + lo)
@@ -152,6 +159,10 @@ Layout make_layout(const situ_moe_args* a) {
   L.wxs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->H) : wnv ? S * (size_t)(a->H / 4) : 0);
   L.whs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->I) : 0);
   L.xg = take(wnv ? 4 * S : 0);
+  // NVFP4 FC2 on 128-token tiles: its own tile table
+  const bool wide2 = nv_wide_fc2(a);
+  L.t2off = take(wide2 ? 4 * (E + 1) : 0);
+  L.t2info = take(wide2 ? 8 * (S / kNvFc2WideTile + E + 2) : 0);
   L.total = o;
   return L;
 }
@@ -321,6 +332,9 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   cudaError_t err = launch_permute(a->topk_ids, a->T, a->top_k, a->num_local_experts,
                                    a->local_expert_offset, tile_n, counts, offsets, tile_offsets,
                                    tile_info, psrc, s2r, meta, (int32_t*)(ws + L.blk), st);
+  if (err == cudaSuccess && fcwnv && nv_wide_fc2(a))
+    err = launch_tile_table(offsets, a->num_local_experts, kNvFc2WideTile, (int32_t*)(ws + L.t2off),
+                            (int2*)(ws + L.t2info), st);
   if (err != cudaSuccess) return SITU_ERR_CUDA;
   mark(1);
 
@@ -461,7 +475,15 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     v.n_ntiles = (a->H + fcw_n_rows(false) - 1) / fcw_n_rows(false);
     v.y_out = y;
     v.err = meta + 2;
-    if ((err = launch_fcv(v, h1, S, a->num_local_experts, tile_n, max_tiles, st)) != cudaSuccess)
+    int fc2_tile = tile_n;
+    long fc2_tiles = max_tiles;
+    if (nv_wide_fc2(a)) {
+      fc2_tile = kNvFc2WideTile;
+      fc2_tiles = S / kNvFc2WideTile + a->num_local_experts + 1;
+      v.tile_offsets = (const int32_t*)(ws + L.t2off);
+      v.tile_info = (const int2*)(ws + L.t2info);
+    }
+    if ((err = launch_fcv(v, h1, S, a->num_local_experts, fc2_tile, fc2_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(4);
   } else if (decode_path) {
@@ -732,7 +754,7 @@ int32_t situ_moe_forward_launches(const situ_moe_args* a) {
   const int perm = permute_launches(a->T, a->top_k, a->num_local_experts);
   const int pack = a->scales_packed ? 0 : 4;
   if (fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
-  if (fcw_nv_shapes(a)) return perm + (a->scales_packed ? 0 : 1) + 4;
+  if (fcw_nv_shapes(a)) return perm + (nv_wide_fc2(a) ? 1 : 0) + (a->scales_packed ? 0 : 1) + 4;
   if (takes_decode_path(a)) return perm + 4;
   if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2))
     return perm + pack + 4 + (a->fuse_combine ? 1 : 0);   // + zeroing the accumulator

@@ -238,6 +238,10 @@ def test_decode_w4a8():
     # MMA in FC1), a hot expert over four of them
     (dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
           params="k3_random"), 5),
+    # 75 rows per expert: FC2 on 128-token tiles of a second tile table, a hot expert over
+    # five of them
+    (dict(T=600, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+          params="k3_random"), 9),
     # 64-token NVFP4 tiles on a filtered shard (experts 4..11 of 16), two stages, two FC1
     # weight tiles
     (dict(T=300, H=512, I=256, E_total=16, E_loc=8, off=4, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,

@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
             l.situ_moe_device_status.restype = ctypes.c_int
             l.situ_moe_device_status.argtypes = [ctypes.POINTER(SituMoeArgs), vp, vp,
                                                  ctypes.POINTER(ctypes.c_int32)]
+            l.situ_moe_wait_selftest.restype = ctypes.c_int
+            l.situ_moe_wait_selftest.argtypes = [vp, vp]
             _lib = l
     return _lib
 
@@ -227,6 +229,16 @@ def situ_moe_forward(args: SituMoeArgs, workspace: torch.Tensor, stream=None) ->
     _check("situ_moe_forward", lib().situ_moe_forward(
         ctypes.byref(args), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+SITU_SELFTEST_WAIT_CODE = 99   # include/situ_moe.h
+
+
+def situ_moe_wait_selftest(status: torch.Tensor, stream=None) -> None:
+    """One bounded device wait made to run out (the failure path): after the
+    wait limit the kernel records SITU_SELFTEST_WAIT_CODE in ``status`` (an
+    int32 tensor on the device, zeroed by the caller) and returns."""
+    _check("situ_moe_wait_selftest", lib().situ_moe_wait_selftest(_p(status), _stream(stream)))
 
 
 def situ_moe_device_status(args: SituMoeArgs, workspace: torch.Tensor, stream=None) -> int:

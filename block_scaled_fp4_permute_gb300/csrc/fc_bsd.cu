@@ -1049,4 +1049,24 @@ cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E
   return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------
+// The failure path's self-test: the bounded wait of the GEMM kernels on a
+// barrier phase that no arrival completes.  It gives up after kWaitNs,
+// records `code` in *status and returns.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int* status, int code) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(saddr(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (mbar_wait(saddr(&bar), 0, status, code)) atomicExch(status, -1);   // cannot complete
+  }
+}
+
+cudaError_t launch_wait_selftest(int* status, int code, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, code);
+  return cudaGetLastError();
+}
+
 }  // namespace situ

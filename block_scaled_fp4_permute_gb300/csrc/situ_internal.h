@@ -260,6 +260,9 @@ struct FcwParams {
   float* y_out;                  // fp32 [S, H]
   int* err;                      // device status word
 };
+// one bounded mbarrier wait that nothing completes: records `code` in
+// *status after the wait limit and returns (the failure path's self-test)
+cudaError_t launch_wait_selftest(int* status, int code, cudaStream_t st);
 int fcw_token_tile();
 int fcw_n_rows(bool fc1);
 int fcw_scale_stride(int K);

@@ -748,6 +748,12 @@ situ_status situ_moe_pack_scales(const situ_moe_args* a, void* packed, size_t pa
   return cuda_status(pack_all_scales(a, (uint8_t*)packed, (cudaStream_t)stream));
 }
 
+situ_status situ_moe_wait_selftest(int32_t* device_status, void* stream) {
+  if (!device_status) return SITU_ERR_NULL_ARG;
+  if (!aligned_to(device_status, 4)) return SITU_ERR_MISALIGNED;
+  return cuda_status(launch_wait_selftest(device_status, SITU_SELFTEST_WAIT_CODE, (cudaStream_t)stream));
+}
+
 int32_t situ_moe_forward_launches(const situ_moe_args* a) {
   if (validate(a) != SITU_OK) return -1;
   if (a->T == 0) return 0;

@@ -327,6 +327,22 @@ situ_status situ_moe_device_status(const situ_moe_args* args, const void* worksp
                                    int32_t* code);
 
 /* ------------------------------------------------------------------------
+ * situ_moe_wait_selftest -- the bounded wait of the tensor-core kernels,
+ * made to run out.
+ *
+ * Launches one small kernel that waits, with the same bounded mbarrier wait
+ * every GEMM kernel of this library uses (200 ms of the GPU's global timer),
+ * for a barrier phase that nothing completes.  The wait gives up, records
+ * SITU_SELFTEST_WAIT_CODE in *device_status (one int32 in device memory,
+ * which the caller sets to 0 first) and the kernel returns: no trap, no
+ * hang, and the CUDA context stays usable.  A test of the failure path;
+ * the pages define no counterpart.  Asynchronous on `stream`.
+ * Errors: NULL_ARG (device_status), MISALIGNED (not 4-byte aligned), CUDA.
+ * --------------------------------------------------------------------- */
+#define SITU_SELFTEST_WAIT_CODE 99
+situ_status situ_moe_wait_selftest(int32_t* device_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * situ_moe_forward_launches -- the number of kernels situ_moe_forward
  * enqueues for these arguments (0 for T = 0, -1 when validation fails),
  * e.g. to size a CUDA graph or to count device work.  Host-only; the pages

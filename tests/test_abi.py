@@ -116,6 +116,11 @@ def test_packed_scales_size_and_errors(lib):
     assert lib.situ_moe_pack_scales(ctypes.byref(ok), buf, n - 1, None) == 4
 
 
+def test_wait_selftest_argument_errors(lib):
+    assert lib.situ_moe_wait_selftest(None, None) == 1
+    assert lib.situ_moe_wait_selftest(ctypes.c_void_p(0x1002), None) == 6
+
+
 def test_workspace_size_grows_with_tokens(lib):
     small = lib.situ_moe_workspace_size(ctypes.byref(_args(T=4)))
     big = lib.situ_moe_workspace_size(ctypes.byref(_args(T=400)))

@@ -1,6 +1,14 @@
 // fc_bsd.cu -- FC1 (gate/up + SiTU) and FC2 for decode-sized token tiles on
 // the block-scaled tensor cores, weights on the MMA's M side.
 //
+// Kernels here: fcw_kernel (MXFP4 weights, kind::mxf8f6f4; and the NVFP4
+// FC1, kind::mxf4nvf4, 16 or 64 tokens per tile), gather_hl_kernel (the
+// token rows in expert order), fcv_kernel (the NVFP4 FC2: weights expanded
+// to bf16 in shared memory, kind::f16, 16, 64 or 128 tokens per tile; its
+// 128-token tile table comes from tile_table_kernel in permute.cu),
+// pack_scales_nv_kernel, and wait_selftest_kernel (the bounded wait made to
+// run out).
+//
 // At decode every touched expert's FP4 weights are streamed once for one or
 // two tokens, so the layer is bound by HBM bandwidth, and any per-weight
 // instruction (a register conversion of the codes, a scale multiply) costs

@@ -264,6 +264,37 @@ def test_decode_tile_shapes(over, hot):
     assert np.array_equal(out2.float().cpu().numpy(), out)
 
 
+def _at_byte_offset(t, off):
+    buf = torch.empty(t.numel() + 16, dtype=torch.uint8, device=t.device)
+    v = buf[off:off + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("over", [
+    dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+         params="k3_random"),
+    dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4, wt=W.W_NVFP4,
+         params="k3_random"),
+    dict(T=24, H=512, I=256, E_total=32, E_loc=8, off=8, K=4, params="k3_random"),
+])
+def test_weight_scales_two_byte_aligned(over):
+    """The contract asks the weight scale arrays for 2-byte alignment only:
+    at addresses 2 mod 4 the layer gives the same bytes as at aligned ones,
+    with the scales packed once and packed inside the call."""
+    wl = W.make("tiny", device="cuda", **over)
+    _, ref = run_layer(wl)
+    wl.w1_scale = _at_byte_offset(wl.w1_scale, 2)
+    wl.w2_scale = _at_byte_offset(wl.w2_scale, 6)
+    assert wl.w1_scale.data_ptr() % 4 == 2 and wl.w2_scale.data_ptr() % 4 == 2
+    for pack in (True, False):
+        layer = binding.Layer(wl, pack_scales=pack)
+        out = layer()
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        assert np.array_equal(out.float().cpu().numpy(), ref)
+
+
 def test_prefill_w4a8_subset():
     wl = wl_("prefill_w4a8")
     layer, out = run_layer(wl)

@@ -66,8 +66,9 @@ bool fcw_nv_shapes(const situ_moe_args* a) {
          a->act_dtype == SITU_ACT_NVFP4;
 }
 // Above 16 rows per expert on average the NVFP4 tiles are 64 tokens wide:
-// their small-N MMAs cost about the same per instruction at N = 64 as at 16,
-// so wider tiles cut the MMAs and the weight re-reads per weight byte.
+// a K stage of these tiles takes about as long with 64 tokens as with 16
+// (measured on both GEMMs), so wider tiles cut the stages and the weight
+// re-reads per weight byte.
 constexpr int kNvWideTile = 64;
 bool nv_wide(const situ_moe_args* a) {
   return fcw_nv_shapes(a) && (double)a->T * a->top_k / (double)a->num_experts_total > 16.0;

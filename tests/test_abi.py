@@ -186,6 +186,24 @@ def test_forward_launch_count(lib):
     assert lib.situ_moe_forward_launches(None) == -1
 
 
+@pytest.mark.parametrize("T,launches", [
+    (50, 6),     # 12.5 rows per expert: 16-token tiles, one tile table
+    (100, 6),    # 25: both GEMMs on 64-token tiles, still one tile table
+    (300, 7),    # 75: FC2 on 128-token tiles of a second tile table
+    (2048, 7),   # 512: the widest routing still on the NVFP4 tiles (4,096 slots, one permute launch)
+    (2056, 8),   # 514: the f16 prefill tiles, and three permute launches from 4,097 slots on
+])
+def test_nvfp4_path_choice_by_rows_per_expert(lib, T, launches):
+    """The host picks the NVFP4 kernels from T * top_k / E_total alone:
+    per-launch counts pin the 16 / 64 / 128-token tile thresholds and the
+    hand-over to the f16 prefill tiles above 512 rows per expert."""
+    a = _args(T=T, H=256, I=128, num_experts_total=8, num_local_experts=8, top_k=2, act_dtype=2,
+              weight_dtype=1)
+    for f in ("hidden_states_q", "hidden_states_scale", "hidden_states_gscale", "w1_gscale", "w2_gscale"):
+        setattr(a, f, 0x1000)
+    assert lib.situ_moe_forward_launches(ctypes.byref(a)) == launches
+
+
 def test_quant_nvfp4_argument_errors(lib):
     p = ctypes.c_void_p(256)
     assert lib.situ_moe_quant_nvfp4(p, 4, 40, p, p, p, None) == 2     # H % 16

@@ -204,6 +204,24 @@ def test_nvfp4_path_choice_by_rows_per_expert(lib, T, launches):
     assert lib.situ_moe_forward_launches(ctypes.byref(a)) == launches
 
 
+@pytest.mark.parametrize("T,fuse,w1,launches", [
+    (24, 1, 0x1000, 5),   # 6 rows per expert: block-scaled decode tiles (no fused combine there)
+    (28, 1, 0x1000, 6),   # 7: block-scaled prefill tiles, combine fused (+ accumulator zeroing)
+    (28, 0, 0x1000, 5),   # 7: block-scaled prefill tiles, separate combine
+    (24, 0, 0x1010, 5),   # W1 not 32-byte aligned: no 4-bit tensor map; decode register tiles
+    (28, 0, 0x1010, 6),   # ... and above 6 rows per expert the f16 prefill tiles (+ H1 gather)
+])
+def test_mxfp4_path_choice(lib, T, fuse, w1, launches):
+    """MXFP4 weights with H, I multiples of 128: up to six rows per expert the
+    decode tiles, above them the prefill tiles; weights the 4-bit tensor maps
+    cannot address (base not 32-byte aligned) take the register / f16 paths."""
+    a = _args(T=T, H=256, I=128, num_experts_total=8, num_local_experts=8, top_k=2)
+    a.scales_packed = 0x4000
+    a.fuse_combine = fuse
+    a.w1 = w1
+    assert lib.situ_moe_forward_launches(ctypes.byref(a)) == launches
+
+
 def test_quant_nvfp4_argument_errors(lib):
     p = ctypes.c_void_p(256)
     assert lib.situ_moe_quant_nvfp4(p, 4, 40, p, p, p, None) == 2     # H % 16

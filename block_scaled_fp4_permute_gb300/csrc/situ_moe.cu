@@ -225,7 +225,7 @@ const char* situ_status_string(situ_status s) {
     case SITU_ERR_UNSUPPORTED: return "SITU_ERR_UNSUPPORTED: unsupported format pair";
     case SITU_ERR_WORKSPACE_TOO_SMALL: return "SITU_ERR_WORKSPACE_TOO_SMALL";
     case SITU_ERR_CUDA: return "SITU_ERR_CUDA: a CUDA launch or call failed";
-    case SITU_ERR_MISALIGNED: return "SITU_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+    case SITU_ERR_MISALIGNED: return "SITU_ERR_MISALIGNED: a pointer is below the alignment its argument requires";
     case SITU_ERR_DEVICE_TIMEOUT: return "SITU_ERR_DEVICE_TIMEOUT: a kernel gave up a bounded wait";
   }
   return "unknown situ_status";

@@ -16,7 +16,10 @@
  *     must be 16-byte aligned, block-scale arrays 2-byte aligned, fp32 and
  *     int32 vectors 4-byte aligned (SITU_ERR_MISALIGNED otherwise).  For
  *     situ_moe_permute and situ_moe_quant_mxfp8 every pointer must be
- *     16-byte aligned.  The caller owns every buffer,
+ *     16-byte aligned.  Packed MXFP4 weights (w1, w2) whose bases are
+ *     16- but not 32-byte aligned are accepted, but the block-scaled tcgen05
+ *     kernels need 32 (their 4-bit tensor maps), so such calls run on the
+ *     slower register / f16 kernels.  The caller owns every buffer,
  *     including the workspace; the library allocates no device memory and
  *     keeps no state between calls.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
@@ -50,7 +53,7 @@ typedef enum situ_status {
   SITU_ERR_UNSUPPORTED = 3,        /* unsupported (activation, weight) format pair or limit */
   SITU_ERR_WORKSPACE_TOO_SMALL = 4,
   SITU_ERR_CUDA = 5,               /* a CUDA launch or runtime call failed */
-  SITU_ERR_MISALIGNED = 6,         /* a pointer is not 16-byte aligned */
+  SITU_ERR_MISALIGNED = 6,         /* a pointer is below the alignment its argument requires */
   SITU_ERR_DEVICE_TIMEOUT = 7      /* a kernel gave up a bounded wait (see situ_moe_device_status) */
 } situ_status;
 

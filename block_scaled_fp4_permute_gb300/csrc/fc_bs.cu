@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* ws, int
 namespace {
 
 int sm_count() {
-  static int n[64];
+  static std::atomic<int> n[64];   // SM count per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && n[dev] > 0) return n[dev];
@@ -604,11 +604,14 @@ cudaError_t launch_fcq_t(const FcqParams& p, const CUtensorMap& a, const CUtenso
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 64 || set_for[dev] == 0) {
-    cudaError_t err =
-        cudaFuncSetAttribute(fcq_kernel<FC1, LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (err != cudaSuccess) return err;
-    if (dev < 64) set_for[dev] = 1;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (dev >= 64 || set_for[dev] == 0) {
+      cudaError_t err =
+          cudaFuncSetAttribute(fcq_kernel<FC1, LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) set_for[dev] = 1;
+    }
   }
   const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
   const long grid = items < sm_count() ? items : sm_count();

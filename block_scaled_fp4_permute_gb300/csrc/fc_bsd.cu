@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) 
 namespace {
 
 int sm_count_w() {
-  static int n[64];
+  static std::atomic<int> n[64];   // SM count per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && n[dev] > 0) return n[dev];
@@ -605,11 +605,14 @@ cudaError_t launch_fcw_t(const FcwParams& p, const CUtensorMap* m, long max_tile
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 64 || set_for[dev] == 0) {
-    cudaError_t err =
-        cudaFuncSetAttribute(fcw_kernel<FC1, LO, NV, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (err != cudaSuccess) return err;
-    if (dev < 64) set_for[dev] = 1;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (dev >= 64 || set_for[dev] == 0) {
+      cudaError_t err =
+          cudaFuncSetAttribute(fcw_kernel<FC1, LO, NV, TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) set_for[dev] = 1;
+    }
   }
   const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
   const long grid = items < sm_count_w() ? items : sm_count_w();
@@ -1037,10 +1040,13 @@ cudaError_t launch_fcv_t(const FcvParams& p, const uint16_t* h_bf16, long S, int
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 64 || set_for[dev] == 0) {
-    cudaError_t err = cudaFuncSetAttribute(fcv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (err != cudaSuccess) return err;
-    if (dev < 64) set_for[dev] = 1;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (dev >= 64 || set_for[dev] == 0) {
+      cudaError_t err = cudaFuncSetAttribute(fcv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) set_for[dev] = 1;
+    }
   }
   const long items = max_tiles * p.n_ntiles;
   const long grid = items < sm_count_w() ? items : sm_count_w();

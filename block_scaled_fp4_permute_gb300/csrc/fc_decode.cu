@@ -550,11 +550,14 @@ static cudaError_t launch_fcd_t(const FcdParams& p, long max_tiles, cudaStream_t
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (smem > 48 * 1024 && (dev >= 64 || set_for[dev] < (int)smem)) {
-    cudaError_t err = cudaFuncSetAttribute(fcd_kernel<FC1, WNV, ABLK>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    if (dev < 64) set_for[dev] = (int)smem;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (smem > 48 * 1024 && (dev >= 64 || set_for[dev] < (int)smem)) {
+      cudaError_t err = cudaFuncSetAttribute(fcd_kernel<FC1, WNV, ABLK>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) set_for[dev] = (int)smem;
+    }
   }
   const long ngroups = (p.n_mtiles + p.mg - 1) / p.mg;
   const long grid = max_tiles * ngroups;

@@ -379,11 +379,14 @@ cudaError_t launch_fcp_t(const FcpParams& p, const CUtensorMap& a, const CUtenso
   static int set_for[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 64 || set_for[dev] == 0) {
-    cudaError_t err = cudaFuncSetAttribute(fcp_kernel<FC1, WNV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kSmemBytes);
-    if (err != cudaSuccess) return err;
-    if (dev < 64) set_for[dev] = 1;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (dev >= 64 || set_for[dev] == 0) {
+      cudaError_t err = cudaFuncSetAttribute(fcp_kernel<FC1, WNV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) set_for[dev] = 1;
+    }
   }
   const long grid = max_tiles * p.n_ntiles;
   if (grid <= 0) return cudaSuccess;

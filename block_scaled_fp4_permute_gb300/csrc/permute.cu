@@ -312,23 +312,29 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
   cudaGetDevice(&dev);
   if (nblk == 1 && E_loc <= kSmallMaxExperts) {
     const size_t smem = sizeof(int32_t) * (size_t)(kSmallWarps + 2) * E_loc;
-    if (dev < 0 || dev >= 64 || g_small_smem_set[dev] < (int)smem) {
-      cudaError_t err = cudaFuncSetAttribute(permute_small_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (err != cudaSuccess) return err;
-      if (dev >= 0 && dev < 64) g_small_smem_set[dev] = (int)smem;
+    {
+      std::lock_guard<std::mutex> lock(attr_mutex());
+      if (dev < 0 || dev >= 64 || g_small_smem_set[dev] < (int)smem) {
+        cudaError_t err = cudaFuncSetAttribute(permute_small_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        if (dev >= 0 && dev < 64) g_small_smem_set[dev] = (int)smem;
+      }
     }
     permute_small_kernel<<<1, kSmallThreads, smem, st>>>(ids, (int)S, E_loc, off, tile_n, counts,
                                                          offsets, tile_offsets, tile_info,
                                                          permuted_src, slot_to_row, meta);
     return cudaGetLastError();
   }
-  if (dev >= 0 && dev < 64 && g_scatter_smem_set[dev] < (int)wcnt_smem) {
-    cudaError_t err = cudaFuncSetAttribute(permute_scatter_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)wcnt_smem);
-    if (err != cudaSuccess) return err;
-    g_scatter_smem_set[dev] = (int)wcnt_smem;
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (dev >= 0 && dev < 64 && g_scatter_smem_set[dev] < (int)wcnt_smem) {
+      cudaError_t err = cudaFuncSetAttribute(permute_scatter_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)wcnt_smem);
+      if (err != cudaSuccess) return err;
+      g_scatter_smem_set[dev] = (int)wcnt_smem;
+    }
   }
   permute_count_kernel<<<nblk, kPermThreads, hist_smem, st>>>(ids, S, E_loc, off, blk_counts);
   permute_scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, E_loc, S, tile_n, counts, offsets,

@@ -5,11 +5,23 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace situ {
 
 constexpr int kPermChunk = 4096;   // routing slots per permute block
+
+// Serialises the launchers' per-device caches of kernel attributes (each
+// raises cudaFuncAttributeMaxDynamicSharedMemorySize once per device and
+// kernel).  Unserialised, two host threads could both find a cache unset,
+// or one could lower a limit that the other has just raised for its launch.
+inline std::mutex& attr_mutex() {
+  static std::mutex m;
+  return m;
+}
 
 // Launches kernel k with the programmatic stream-serialisation attribute
 // (see griddep_wait): its prologue may overlap the predecessor's tail.

@@ -1,21 +1,30 @@
 #!/usr/bin/env python3
 """Benchmark of the SiTU routed-MoE expert layer on GB300.
 
-Default workload: the Kimi-K3 TP8 decode layer, w4a16 (T=64 tokens, hidden
-3584, intermediate 384, 896 local experts, top-16 uniform routing, bf16
-activations, MXFP4 weights).  One step = one pass of the whole layer
-(permute -> gather -> FC1 + SiTU -> FC2 -> combine; for the w4a8 workload
-also the MXFP8 activation quantisation) over one batch already resident in
-HBM.  Prints one JSON line.
+The headline line is the Kimi-K3 TP8 decode layer, w4a16 (T=64 tokens,
+hidden 3584, intermediate 384, 896 local experts, top-16 uniform routing,
+bf16 activations, MXFP4 weights); the same JSON line carries a second
+record, ``prefill_w4a8_8192``, for the Kimi-K3 TP8 prefill layer, w4a8
+(T=8192, top-16 Zipf(1.0), MXFP8 activations quantised from bf16 inside the
+step).  One step = one pass of the whole layer (permute -> gather -> FC1 +
+SiTU -> FC2 -> combine; for MXFP8 / NVFP4 activations also their
+quantisation) over one batch already resident in HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
   python bench.py --impl reference ...     # the CPU oracle as reference arm
+  python bench.py --peaks-only             # just the tensor-core peaks (JSON)
 
 Timing: CUDA events on the launching stream around each step, a 256 MiB
 write between steps flushes L2 (the events exclude it), max over ranks.
 Under torchrun each rank runs its own replica of the layer (its own seed);
 the layer needs no collective (each EP/TP rank produces a partial output
 the caller all-reduces), so scaling is weak.
+
+Roofline peaks: HBM from MEASURED_PEAKS.json; the tensor-core peak of each
+GEMM is that of the MMA kind it runs (kind::mxf8f6f4 for the MXFP4 GEMMs,
+kind::mxf4nvf4 for the NVFP4 FC1, kind::f16 bf16 for the NVFP4 FC2),
+measured in the same run by the library's MMA-throughput kernel
+(situ_tc_peak, one CTA per SM issuing back-to-back M=128 N=256 MMAs).
 """
 from __future__ import annotations
 
@@ -47,6 +56,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 FALLBACK_BF16_TFLOPS = 1900.0
+TC_PEAKS_FILE = os.path.join(ROOT, "profiles", "tc_peaks.json")
 
 
 def peaks():
@@ -58,19 +68,76 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def tensor_peak(wl):
-    """(TFLOP/s, source) of the MMA kind the layer's GEMMs use: MXFP8 x MXFP4
-    block-scaled for w4a8 (the measured bf16 GEMM burst peak times the
-    nominal fp8 : bf16 ratio of 2), bf16 for the others."""
+def measure_tc_peaks(dev, reps: int = 8, target_ms: float = 20.0):
+    """Dense TFLOP/s of each MMA kind on this GPU: ``reps`` launches of the
+    library's MMA-throughput kernel, each sized to about ``target_ms``; the
+    best launch is the burst peak, the median is reported beside it."""
+    import torch
+    from block_scaled_fp4_permute_gb300 import binding
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    def timed(kind, m):
+        e0.record(stream)
+        f = binding.situ_tc_peak(kind, m, status)
+        e1.record(stream)
+        e1.synchronize()
+        return f, e0.elapsed_time(e1)
+
+    out = {}
+    for kind, name in binding.TC_KIND_NAMES.items():
+        m = 4096
+        timed(kind, m)                       # first launch: attributes, module load
+        _, ms = timed(kind, m)
+        m = int(max(4, min(1 << 30, m * target_ms / max(ms, 1e-3)))) // 4 * 4
+        rates, times = [], []
+        for _ in range(reps):
+            f, ms = timed(kind, m)
+            rates.append(f / (ms * 1e-3) / 1e12)
+            times.append(ms)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"situ_tc_peak({name}): device status {int(status.item())}")
+        out[name] = {"tflops": max(rates), "tflops_median": float(np.median(rates)),
+                     "mmas_per_sm": m, "launch_ms": float(np.median(times))}
+    return out
+
+
+def load_tc_peaks():
+    """The committed microbenchmark result (used when no live measurement)."""
+    if os.path.exists(TC_PEAKS_FILE):
+        with open(TC_PEAKS_FILE) as f:
+            return json.load(f).get("kinds")
+    return None
+
+
+def gemm_kinds(wl):
+    """The tensor-core MMA kind each GEMM of the layer runs on, by the path
+    the shapes take (mirrors the library's host-side path choice)."""
+    rows_per_expert = wl.T * wl.K / max(wl.E_total, 1)
+    if wl.wt == 0 and wl.H % 128 == 0 and wl.I % 128 == 0:
+        return {"fc1": "mxf8f6f4", "fc2": "mxf8f6f4"}
+    if wl.wt == 1 and wl.act == 2 and rows_per_expert <= 512.0 and wl.H % 256 == 0 and wl.I % 128 == 0:
+        return {"fc1": "mxf4nvf4", "fc2": "bf16"}
+    return {"fc1": "f16", "fc2": "f16"}
+
+
+def tensor_peak_of(kind, tc):
+    """(TFLOP/s, source) of one MMA kind: the live (or committed)
+    microbenchmark for the block-scaled kinds, MEASURED_PEAKS.json's cuBLAS
+    bf16 GEMM for bf16 / f16."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    bf16, src = FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
+    bf16, bsrc = FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
     if os.path.exists(p):
         with open(p) as f:
             bf16 = float(json.load(f)["bf16_tflops"])
-        src = "measured bf16_tflops (MEASURED_PEAKS.json)"
-    if wl.act == 1:
-        return 2.0 * bf16, src + " x 2 (nominal fp8 : bf16 ratio)"
-    return bf16, src
+        bsrc = "measured bf16_tflops (MEASURED_PEAKS.json, cuBLAS bf16 GEMM burst)"
+    if kind in ("bf16", "f16"):
+        return bf16, bsrc
+    if tc and kind in tc:
+        return float(tc[kind]["tflops"]), f"measured kind::{kind} (situ_tc_peak microbenchmark, {tc.get('_source', 'this run')})"
+    return 2.0 * bf16, bsrc + " x 2 (nominal fp8 : bf16 ratio; no microbenchmark result)"
 
 
 def routing_stats(wl):
@@ -112,14 +179,27 @@ def algorithmic_bytes(wl, R, touched):
     }
 
 
-def gemm_dtype(wl):
-    """Operand types the layer's GEMMs compute in, by the path the shapes take."""
-    rows_per_expert = wl.T * wl.K / max(wl.E_total, 1)
-    if wl.wt == 0 and wl.H % 128 == 0 and wl.I % 128 == 0:
-        return "e2m1*e4m3->f32"
-    if wl.wt == 1 and wl.act == 2 and rows_per_expert <= 512.0 and wl.H % 256 == 0 and wl.I % 128 == 0:
-        return "e2m1*e2m1->f32 (FC1), bf16->f32 (FC2)"
-    return "f16->f32"
+def layer_dtype(wl):
+    """The operand types the layer computes in (what the contract's formats
+    are, not the tensor-core containers): bf16 or MXFP8 or NVFP4 activations
+    times MXFP4 / NVFP4 weights, fp32 accumulation."""
+    act = {0: "bf16", 1: "mxfp8", 2: "nvfp4"}[wl.act]
+    w = {0: "mxfp4", 1: "nvfp4"}[wl.wt]
+    h1 = "mxfp8" if wl.act == 1 else "bf16"
+    return f"{act}x{w}->f32 (FC1), {h1}x{w}->f32 (FC2)"
+
+
+def mma_containers(wl):
+    """How the tensor cores see the operands, per GEMM."""
+    k = gemm_kinds(wl)
+    if k["fc1"] == "mxf8f6f4":
+        rows = "bf16 rows as E4M3 hi + lo pairs (two MMAs per K block)" if wl.act == 0 else "E4M3 rows"
+        return {"fc1": f"kind::mxf8f6f4, {rows} x E2M1 weights", "fc2": f"kind::mxf8f6f4, H1 as "
+                + ("E4M3 hi + lo pairs" if wl.act == 0 else "E4M3 rows") + " x E2M1 weights"}
+    if k["fc1"] == "mxf4nvf4":
+        return {"fc1": "kind::mxf4nvf4, E2M1 x E2M1, E4M3 scales per 16",
+                "fc2": "kind::f16, bf16 H1 x bf16-expanded NVFP4 weights"}
+    return {"fc1": "kind::f16 / mma.sync on f16-expanded operands", "fc2": "same"}
 
 
 def layer_flops(wl, R):
@@ -285,25 +365,21 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+def measure_workload(name, args, dev, rank, ws, tc, sampler_dev, cpu_budget):
+    """Times one workload: the plain C-ABI forward for ``args.steps`` steps
+    (events around each), per-stage times from the profiled call, and the
+    end-to-end call with host buffers.  Returns the record (dict)."""
     import torch
-    import torch.distributed as dist
-    from block_scaled_fp4_permute_gb300 import binding, build
+    from block_scaled_fp4_permute_gb300 import binding
 
-    ws, rank, local = dist_env()
-    if ws > 1:
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
-    torch.cuda.set_device(local)
-    dev = torch.device(f"cuda:{local}")
-    build.build()
-    wl = make_workload(args.workload, dev, args.seed + rank, args.tokens)
+    wl = make_workload(name, dev, args.seed + rank, args.tokens if name == args.workload else None)
     layer = binding.Layer(wl, fuse_combine=args.fuse_combine)
     R, touched = routing_stats(wl)
     nbytes = algorithmic_bytes(wl, R, touched)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     nst = len(binding.PROFILE_STAGES)
-    is_w4a8 = wl.act != binding.SITU_ACT_BF16   # the step includes the activation quantisation
+    is_q = wl.act != binding.SITU_ACT_BF16   # the step includes the activation quantisation
     qname = "quant_mxfp8" if wl.act == binding.SITU_ACT_MXFP8 else "quant_nvfp4"
 
     def new_events(n):
@@ -318,17 +394,17 @@ def run_ours(args):
     bounds = [new_events(2) for _ in range(args.steps)]
     n_prof = min(args.steps, 50)
     steps = [new_events(nst + 1) for _ in range(n_prof)]
-    qevs = [new_events(2) for _ in range(n_prof)] if is_w4a8 else None
+    qevs = [new_events(2) for _ in range(n_prof)] if is_q else None
     for _ in range(args.warmup):
         flush.zero_()
         layer()
     torch.cuda.synchronize()
 
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-    sampler = ClockSampler(vis.split(",")[local].strip() if vis else local)
+    sampler = ClockSampler(sampler_dev)
     sampler.start()
     time.sleep(0.25)
     if ws > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -344,25 +420,27 @@ def run_ours(args):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if ws > 1:
+        import torch.distributed as dist
         dist.barrier()
     clocks = sampler.stop()
+    if layer.device_status() != 0:
+        raise RuntimeError(f"{name}: a kernel gave up a bounded wait (device status {layer.device_status()})")
     for i in range(n_prof):
         flush.zero_()
-        layer.profiled(steps[i], qevs[i] if is_w4a8 else None)
+        layer.profiled(steps[i], qevs[i] if is_q else None)
     torch.cuda.synchronize()
 
     stage_ms = np.zeros(nst)
     quant_ms = 0.0
     for i, evs in enumerate(steps):
-        for s in range(nst):
-            stage_ms[s] += evs[s].elapsed_time(evs[s + 1])
-        if is_w4a8:
+        for s_ in range(nst):
+            stage_ms[s_] += evs[s_].elapsed_time(evs[s_ + 1])
+        if is_q:
             quant_ms += qevs[i][0].elapsed_time(qevs[i][1])
     stage_ms /= n_prof
     quant_ms /= n_prof
     step_ms = np.array([b[0].elapsed_time(b[1]) for b in bounds])
-    ms = float(step_ms.mean())
-    ms = max_over_ranks(ms, dev)
+    ms = max_over_ranks(float(step_ms.mean()), dev)
 
     # end to end: pinned host inputs -> device, layer, output -> pinned host
     dev_in = [wl.x_bf16, wl.topk_ids, wl.topk_weights]
@@ -385,39 +463,49 @@ def run_ours(args):
         e1.synchronize()
         if i >= max(args.warmup, 1):
             e_ms.append(e0.elapsed_time(e1))
-    e2e_ms = float(np.mean(e_ms))
-    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_ms = max_over_ranks(float(np.mean(e_ms)), dev)
 
     hbm, peak_kind = peaks()
     stages = {}
-    for s, name in enumerate(binding.PROFILE_STAGES):
-        gbs = nbytes[name] / (stage_ms[s] * 1e-3) / 1e9 if stage_ms[s] > 0 else None
-        stages[name] = {"ms": float(stage_ms[s]), "alg_bytes": int(nbytes[name]),
-                        "gbs": gbs, "frac_hbm": gbs / hbm if gbs else None}
-    if is_w4a8:
+    for s_, sname in enumerate(binding.PROFILE_STAGES):
+        gbs = nbytes[sname] / (stage_ms[s_] * 1e-3) / 1e9 if stage_ms[s_] > 0 else None
+        stages[sname] = {"ms": float(stage_ms[s_]), "alg_bytes": int(nbytes[sname]),
+                         "gbs": gbs, "frac_hbm": gbs / hbm if gbs else None}
+    if is_q:
         gbs = nbytes["quant"] / (quant_ms * 1e-3) / 1e9
-        stages[qname] = {"ms": quant_ms, "alg_bytes": int(nbytes["quant"]), "gbs": gbs,
-                                 "frac_hbm": gbs / hbm}
+        stages[qname] = {"ms": quant_ms, "alg_bytes": int(nbytes["quant"]), "gbs": gbs, "frac_hbm": gbs / hbm}
+    kinds = gemm_kinds(wl)
+    kflops = {"fc1": 2.0 * R * wl.H * 2 * wl.I, "fc2": 2.0 * R * wl.I * wl.H}
+    for g in ("fc1", "fc2"):
+        pk, _ = tensor_peak_of(kinds[g], tc)
+        stages[g]["tflops"] = kflops[g] / (stage_ms[binding.PROFILE_STAGES.index(g)] * 1e-3) / 1e12 \
+            if stages[g]["ms"] > 0 else None
+        stages[g]["mma_kind"] = kinds[g]
+        stages[g]["frac_tensor"] = stages[g]["tflops"] / pk if stages[g]["tflops"] else None
     dom = max(stages, key=lambda k: stages[k]["ms"])
     traffic = None
-    tpath = os.path.join(ROOT, "profiles", f"traffic_{args.workload}.json")
+    tpath = os.path.join(ROOT, "profiles", f"traffic_{name}.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
-        # counters of a capture at this token count only
-        if tj.get("T") == wl.T:
+        # counters of a capture at this token count, of the current kernels only
+        if tj.get("T") == wl.T and not tj.get("stale"):
             traffic = tj.get(dom)
     # the bound of the dominant kernel and of the layer: the larger of the
-    # HBM time of its algorithmic bytes and the tensor time of its FLOPs
-    tc_peak, tc_src = tensor_peak(wl)
-    kflops = {"fc1": 2.0 * R * wl.H * 2 * wl.I, "fc2": 2.0 * R * wl.I * wl.H}
-    kf = kflops.get(dom, 0.0)
+    # HBM time of its algorithmic bytes and the tensor time of its FLOPs (each
+    # GEMM against the peak of its own MMA kind)
     hbm_src = (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                else "fallback 6.8 TB/s")
+    kf = kflops.get(dom, 0.0)
+    if dom in kinds:
+        tc_peak, tc_src = tensor_peak_of(kinds[dom], tc)
+    else:
+        tc_peak, tc_src = float("inf"), "-"
     if kf / (tc_peak * 1e12) > nbytes[dom] / (hbm * 1e9):
         ach = kf / (stages[dom]["ms"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tc_peak,
-                "unit": "TFLOP/s", "frac": ach / tc_peak, "traffic": traffic, "peak_source": tc_src}
+                "unit": "TFLOP/s", "frac": ach / tc_peak, "traffic": traffic, "peak_source": tc_src,
+                "mma_kind": kinds[dom]}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["gbs"], "peak": hbm,
                 "unit": "GB/s", "frac": stages[dom]["frac_hbm"], "traffic": traffic,
@@ -425,49 +513,106 @@ def run_ours(args):
     layer_gbs = nbytes["layer"] / (ms * 1e-3) / 1e9
     flops = layer_flops(wl, R)
     t_hbm = nbytes["layer"] / (hbm * 1e9)
-    t_tc = flops / (tc_peak * 1e12)
+    t_tc = sum(kflops[g] / (tensor_peak_of(kinds[g], tc)[0] * 1e12) for g in ("fc1", "fc2"))
+    # one number for "the" tensor peak of the layer: its FLOPs over the
+    # per-kind tensor time
+    layer_tc_peak = flops / t_tc / 1e12
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        tps, n, dt, threads = oracle_tokens_per_s(wl, args.cpu_budget)
+        tps, n, dt, threads = oracle_tokens_per_s(wl, cpu_budget)
         cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} of {wl.T} tokens of the same workload, {dt:.1f} s"}
 
-    launches_per_step = layer.launches()
-    line = {
-        "metric": METRIC, "value": ws * wl.T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        # operand types of the GEMMs: E2M1 weights x E4M3 rows (bf16 rows as
-        # hi + lo pairs) on the block-scaled tensor cores for MXFP4 weights;
-        # NVFP4: E2M1 x E2M1 in FC1 at decode sizes, f16 operands otherwise
-        "dtype": gemm_dtype(wl),
-        "data": "synthetic (seeded; weights N(0,0.02) packed to the block-scaled format)",
-        "config": {"workload": WORKLOAD_NAMES[args.workload], "T": wl.T, "H": wl.H, "I": wl.I,
+    rec = {
+        "value": ws * wl.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+        "dtype": layer_dtype(wl), "mma": mma_containers(wl),
+        "config": {"workload": WORKLOAD_NAMES[name], "T": wl.T, "H": wl.H, "I": wl.I,
                    "E_total": wl.E_total, "E_loc": wl.E_loc, "offset": wl.off, "top_k": wl.K,
                    "kept_pairs": R, "touched_experts": touched,
                    "l2": "flushed between steps (256 MiB write, outside the step events)",
                    "parallelism": f"replicas x{ws}, no collective",
                    "launch": "CUDA graph replay of the layer call" if args.graph else "eager C-ABI call",
                    "combine": "fused into FC2 (fp32 reductions)" if args.fuse_combine
-                   else "separate kernel, ascending slot order"},
+                   else "separate kernel, ascending slot order",
+                   "step": ("MXFP8 quantisation of the bf16 input + " if wl.act == 1 else
+                            "NVFP4 quantisation of the bf16 input + " if wl.act == 2 else "")
+                   + "the whole layer"},
         "roofline": roof,
         "layer_roofline": {"bound": "tensor" if t_tc > t_hbm else "hbm", "alg_bytes": int(nbytes["layer"]),
                            "flops": flops, "roofline_ms": max(t_hbm, t_tc) * 1e3,
                            "frac": max(t_hbm, t_tc) / (ms * 1e-3),
                            "gbs": layer_gbs, "frac_hbm": layer_gbs / hbm,
-                           "tflops": flops / (ms * 1e-3) / 1e12, "tensor_peak_tflops": tc_peak},
+                           "tflops": flops / (ms * 1e-3) / 1e12, "tensor_peak_tflops": layer_tc_peak,
+                           "frac_tensor": flops / (ms * 1e-3) / 1e12 / layer_tc_peak,
+                           "t_hbm_ms": t_hbm * 1e3, "t_tensor_ms": t_tc * 1e3},
         "stages": stages,
         "e2e": {"value": ws * wl.T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "stage_times": f"per-kernel ms from {n_prof} further steps of the profiled call (events between kernels)",
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": layer.launches() * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,
     }
+    del layer, wl, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from block_scaled_fp4_permute_gb300 import build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    build.build()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler_dev = vis.split(",")[local].strip() if vis else local
+
+    # tensor-core peaks of the MMA kinds, measured on this GPU now
+    tc, tc_clocks = None, None
+    if not args.no_tc_peaks:
+        sampler = ClockSampler(sampler_dev)
+        sampler.start()
+        tc = measure_tc_peaks(dev)
+        tc_clocks = sampler.stop()
+        tc["_source"] = "this run"
+    else:
+        tc = load_tc_peaks()
+        if tc:
+            tc["_source"] = "profiles/tc_peaks.json"
+    if args.peaks_only:
+        if rank == 0:
+            print(json.dumps({"kinds": {k: v for k, v in tc.items() if not k.startswith("_")},
+                              "clocks": tc_clocks, "gpu": torch.cuda.get_device_name(dev),
+                              "how": "situ_tc_peak: one CTA per SM, back-to-back M=128 N=256 MMAs into one TMEM "
+                                     "accumulator, operands in shared memory; best (and median) of 8 launches of "
+                                     "about 20 ms, CUDA events"}), flush=True)
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    main = measure_workload(args.workload, args, dev, rank, ws, tc, sampler_dev, args.cpu_budget)
+    line = {"metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "data": "synthetic (seeded; weights N(0,0.02) packed to "
+            "the block-scaled format)"}
+    line.update({k: v for k, v in main.items() if k not in ("value", "unit", "ms_per_step")})
+    if tc:
+        line["tc_peaks"] = {k: v for k, v in tc.items() if not k.startswith("_")}
+        line["tc_peaks_clocks"] = tc_clocks
+    # the second half of the metric (T=8192 prefill) rides on the same line
+    if args.workload == "decode" and not args.no_prefill and args.tokens is None:
+        rec = measure_workload("prefill_w4a8", args, dev, rank, ws, tc, sampler_dev, args.cpu_budget)
+        rec["steps"], rec["warmup"] = args.steps, args.warmup
+        line["prefill_w4a8_8192"] = rec
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -489,6 +634,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="leave out the T=8192 w4a8 prefill record of the decode line")
+    ap.add_argument("--no-tc-peaks", action="store_true",
+                    help="take the tensor-core peaks from profiles/tc_peaks.json instead of measuring them")
+    ap.add_argument("--peaks-only", action="store_true",
+                    help="measure the tensor-core peaks of the MMA kinds and print them as JSON")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph of the layer call instead of eager C-ABI calls")
     ap.add_argument("--fuse-combine", action="store_true",

@@ -41,7 +41,7 @@ class SituMoeArgs(ctypes.Structure):
             "topk_ids", "topk_weights", "w1", "w1_scale", "w1_gscale", "w2", "w2_scale",
             "w2_gscale", "gemm1_alpha", "gemm1_beta", "g1_alphas", "g1_alphas_up", "g2_alphas",
             "out", "scales_packed")] + [(n, ctypes.c_int32) for n in (
-                "fuse_combine", "activation", "apply_topk_in_fc1")]
+                "fuse_combine", "activation", "apply_topk_in_fc1")] + [("tactic", ctypes.c_int32 * 2)]
 
 
 def library_path() -> str:
@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.POINTER(ctypes.c_int32)]
             l.situ_moe_wait_selftest.restype = ctypes.c_int
             l.situ_moe_wait_selftest.argtypes = [vp, vp]
+            l.situ_tc_peak.restype = ctypes.c_int
+            l.situ_tc_peak.argtypes = [i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
             _lib = l
     return _lib
 
@@ -147,12 +149,21 @@ def situ_moe_permute_noalloc(topk_ids: torch.Tensor, num_experts_total: int,
     (the C entry point itself never allocates)."""
     T, K = topk_ids.shape
     dev = topk_ids.device
+    if topk_ids.dtype != torch.int32:
+        raise TypeError("topk_ids must be int32")
+    topk_ids = topk_ids.contiguous()   # a strided view would be read as if packed
     if out is None:
         out = (torch.empty(num_local_experts, dtype=torch.int32, device=dev),
                torch.empty(num_local_experts + 1, dtype=torch.int32, device=dev),
                torch.empty(max(T * K, 1), dtype=torch.int32, device=dev),
                torch.empty(max(T * K, 1), dtype=torch.int32, device=dev))
     counts, offsets, psrc, s2r = out
+    # the kernels write every element of these: check what they will be given
+    for t, n, what in ((counts, num_local_experts, "expert_counts"),
+                       (offsets, num_local_experts + 1, "expert_offsets"),
+                       (psrc, T * K, "permuted_src"), (s2r, T * K, "slot_to_row")):
+        if t.dtype != torch.int32 or t.device != dev or not t.is_contiguous() or t.numel() < n:
+            raise ValueError(f"{what}: needs a contiguous int32 tensor of >= {n} elements on {dev}")
     _check("situ_moe_permute_noalloc", lib().situ_moe_permute_noalloc(
         _p(topk_ids), T, K, num_experts_total, num_local_experts, local_expert_offset,
         _p(counts), _p(offsets), _p(psrc), _p(s2r), _stream(stream)))
@@ -194,6 +205,7 @@ def make_args(*, T, H, I, num_experts_total, num_local_experts, local_expert_off
     a = SituMoeArgs(T=T, H=H, I=I, num_experts_total=num_experts_total,
                     num_local_experts=num_local_experts, local_expert_offset=local_expert_offset,
                     top_k=top_k, act_dtype=act_dtype, weight_dtype=weight_dtype)
+    a.tactic[0] = a.tactic[1] = -1   # auto
     for name, t in dict(hidden_states=hidden_states, hidden_states_q=hidden_states_q,
                         hidden_states_scale=hidden_states_scale,
                         hidden_states_gscale=hidden_states_gscale, topk_ids=topk_ids,
@@ -239,6 +251,20 @@ def situ_moe_wait_selftest(status: torch.Tensor, stream=None) -> None:
     wait limit the kernel records SITU_SELFTEST_WAIT_CODE in ``status`` (an
     int32 tensor on the device, zeroed by the caller) and returns."""
     _check("situ_moe_wait_selftest", lib().situ_moe_wait_selftest(_p(status), _stream(stream)))
+
+
+SITU_TC_MXF8F6F4, SITU_TC_MXF4NVF4, SITU_TC_BF16 = 0, 1, 2
+TC_KIND_NAMES = {SITU_TC_MXF8F6F4: "mxf8f6f4", SITU_TC_MXF4NVF4: "mxf4nvf4", SITU_TC_BF16: "bf16"}
+
+
+def situ_tc_peak(kind: int, mmas_per_sm: int, status: torch.Tensor, stream=None) -> float:
+    """Enqueues the MMA-throughput kernel of ``kind`` (SITU_TC_*) with
+    ``mmas_per_sm`` MMAs per SM; returns the launch's dense FLOPs.  ``status``
+    is an int32 device tensor zeroed by the caller (98 after a timed-out wait)."""
+    flops = ctypes.c_double(0.0)
+    _check("situ_tc_peak", lib().situ_tc_peak(int(kind), int(mmas_per_sm), _p(status),
+                                              ctypes.byref(flops), _stream(stream)))
+    return float(flops.value)
 
 
 def situ_moe_device_status(args: SituMoeArgs, workspace: torch.Tensor, stream=None) -> int:

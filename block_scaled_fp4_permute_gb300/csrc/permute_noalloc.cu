@@ -5,6 +5,8 @@
 // int32) lives in a fixed array compiled into the library instead of in a
 // caller-provided workspace.  Nothing here calls cudaMalloc, cudaFree or any
 // other allocating routine.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/situ_moe.h"
@@ -19,23 +21,59 @@ static __device__ __align__(256) int32_t g_permute_scratch[SITU_NOALLOC_SCRATCH_
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int32_t* g_scratch_addr[kMaxDevices];   // device address of the array, per device
+// per device: the device address of the array and the ID of the context it
+// was looked up in (0: none yet)
+int32_t* g_scratch_addr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// The driver's cuCtxGetCurrent / cuCtxGetId, looked up once through the
+// runtime (the library links only the runtime).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+template <class F>
+F driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
+// ID of the calling thread's current context (0 if there is none yet).
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch in the current device's context, looked up
+// once per device and context (with that device current) and cached.  A
+// context created anew on a device (after cudaDeviceReset, say) has a new
+// ID, so its first call looks the address up again.
 cudaError_t scratch_address(int32_t** out) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (dev >= 0 && dev < kMaxDevices && g_scratch_addr[dev]) {
+  unsigned long long ctx = current_context_id();
+  const bool cacheable = dev >= 0 && dev < kMaxDevices;
+  if (cacheable && ctx != 0 && g_scratch_ctx[dev] == ctx && g_scratch_addr[dev]) {
     *out = g_scratch_addr[dev];
     return cudaSuccess;
   }
   void* p = nullptr;
-  err = cudaGetSymbolAddress(&p, g_permute_scratch);
+  err = cudaGetSymbolAddress(&p, g_permute_scratch);   // also makes the primary context current
   if (err != cudaSuccess) return err;
-  if (dev >= 0 && dev < kMaxDevices) g_scratch_addr[dev] = (int32_t*)p;
+  if (ctx == 0) ctx = current_context_id();
+  if (cacheable) {
+    g_scratch_addr[dev] = (int32_t*)p;
+    g_scratch_ctx[dev] = ctx;   // 0 (unknown) is never matched above
+  }
   *out = (int32_t*)p;
   return cudaSuccess;
 }

@@ -188,6 +188,9 @@ situ_status validate(const situ_moe_args* a) {
   const bool nv = a->act_dtype == SITU_ACT_NVFP4 && a->weight_dtype == SITU_W_NVFP4;
   if (!(w4a16 || w4a8 || nv)) return SITU_ERR_UNSUPPORTED;
   if (a->activation != SITU_ACT_FN_SITU && a->activation != SITU_ACT_FN_SWIGLU_BIAS) return SITU_ERR_UNSUPPORTED;
+  // one configuration per shape: -1 (auto) or 0 (the first valid one) select it
+  for (int g = 0; g < 2; ++g)
+    if (a->tactic[g] != -1 && a->tactic[g] != 0) return SITU_ERR_UNSUPPORTED;
   if (a->T == 0) return SITU_OK;
   if (!a->topk_ids || !a->topk_weights || !a->w1 || !a->w1_scale || !a->w2 || !a->w2_scale ||
       !a->gemm1_alpha || !a->gemm1_beta || !a->out)

@@ -134,8 +134,11 @@ situ_status situ_moe_permute(const int32_t* topk_ids, int32_t T, int32_t top_k,
  *
  * The first call on each device looks up the array's device address with
  * that device current (cudaGetSymbolAddress), so make that first call before
- * any stream capture.  All calls share the one array, which keeps whatever
- * the last call left in it; nothing in it has to start at zero, because
+ * any stream capture.  The address is cached per device and context: the
+ * first call in a context created anew on a device (after cudaDeviceReset,
+ * for instance) looks it up again.  All calls share the one array, which
+ * keeps whatever the last call left in it; nothing in it has to start at
+ * zero, because
  * each call writes every entry it later reads.  Calls whose kernels can
  * overlap on the GPU (different streams, or unordered host threads) race on
  * the array and must be serialised by the caller.
@@ -280,6 +283,11 @@ typedef struct situ_moe_args {
                                      epilogue, before H1 is rounded for FC2, and the
                                      un-permute sum is unweighted (the MegaMoE option of PR
                                      #17865); 0: the weight is applied in the sum */
+  int32_t tactic[2];              /* kernel configuration of FC1 / FC2, as the TokenSpeed SiTU
+                                     runtime API's `tactic` pair: -1 = auto, the first valid
+                                     configuration.  This library has one configuration per
+                                     shape (its path choice), so -1 and 0 both select it; any
+                                     other value returns SITU_ERR_UNSUPPORTED. */
 } situ_moe_args;
 
 /* Workspace bytes situ_moe_forward needs for these shapes (0 on bad args).
@@ -289,7 +297,8 @@ typedef struct situ_moe_args {
 size_t situ_moe_workspace_size(const situ_moe_args* args);
 
 /* Errors: NULL_ARG (args, required pointers, gemm1_alpha / gemm1_beta --
- * the SiTU caps have no default), BAD_SHAPE, UNSUPPORTED, MISALIGNED,
+ * the SiTU caps have no default), BAD_SHAPE, UNSUPPORTED (format pair,
+ * activation kind, a tactic other than -1 / 0), MISALIGNED,
  * WORKSPACE_TOO_SMALL, CUDA.  T == 0 launches nothing.
  * Debugging aid: with the environment variable SITU_MOE_DEBUG_SYNC set, the
  * call synchronises its stream after every stage and prints the first stage
@@ -344,6 +353,33 @@ situ_status situ_moe_device_status(const situ_moe_args* args, const void* worksp
  * --------------------------------------------------------------------- */
 #define SITU_SELFTEST_WAIT_CODE 99
 situ_status situ_moe_wait_selftest(int32_t* device_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * situ_tc_peak -- dense throughput of one tensor-core MMA kind on this GPU.
+ *
+ * Enqueues one kernel with one CTA per SM.  Each CTA fills a 128-row A tile
+ * and a 256-row B tile in shared memory (a fixed byte pattern, scales 1.0),
+ * then issues `mmas_per_sm` MMAs of M = 128, N = 256 into one TMEM
+ * accumulator back to back, as a GEMM's K loop does but without memory
+ * traffic:
+ *   SITU_TC_MXF8F6F4  tcgen05.mma.kind::mxf8f6f4.block_scale, E4M3 x E2M1
+ *                     with UE8M0 per 32, K = 32 (the MXFP4 GEMMs);
+ *   SITU_TC_MXF4NVF4  kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 x E2M1
+ *                     with E4M3 per 16, K = 64 (the NVFP4 FC1);
+ *   SITU_TC_BF16      kind::f16 with bf16 operands, K = 16 (the NVFP4 FC2).
+ * *flops receives the dense FLOPs of the launch (2*M*N*K per MMA, times
+ * mmas_per_sm and the SM count); time the launch with events on `stream`
+ * to get the rate.  The final wait is bounded: if it runs out the kernel
+ * records 98 in *device_status (one int32 in device memory that the caller
+ * sets to 0) and returns.  A measurement aid: the pages define no
+ * counterpart; the roofline of each GEMM is taken against its own kind.
+ * Errors: NULL_ARG, MISALIGNED (device_status not 4-byte aligned),
+ * UNSUPPORTED (kind), BAD_SHAPE (mmas_per_sm not a positive multiple of 4),
+ * CUDA.
+ * --------------------------------------------------------------------- */
+typedef enum { SITU_TC_MXF8F6F4 = 0, SITU_TC_MXF4NVF4 = 1, SITU_TC_BF16 = 2 } situ_tc_kind;
+situ_status situ_tc_peak(int32_t kind, int32_t mmas_per_sm, int32_t* device_status, double* flops,
+                         void* stream);
 
 /* ------------------------------------------------------------------------
  * situ_moe_forward_launches -- the number of kernels situ_moe_forward

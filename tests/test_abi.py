@@ -147,6 +147,38 @@ def test_permute_and_quant_validation(lib):
     assert lib.situ_moe_permute_workspace_size(100, 16, 896) >= 4 * 896
 
 
+def test_permute_noalloc_rejects_without_launch(lib):
+    """Every rejection of the allocation-free permute returns before any
+    CUDA call (the fake pointers are never dereferenced), so these run on
+    the CPU: bad shapes, NULL and misaligned pointers, and a request beyond
+    the fixed scratch (ceil(T*K/4096) * E_loc > SITU_NOALLOC_SCRATCH_INTS)."""
+    vp = ctypes.c_void_p
+    p = vp(0x1000)
+    f = lib.situ_moe_permute_noalloc
+    assert f(p, 4, 0, 8, 8, 0, p, p, p, p, None) == 2            # top_k 0
+    assert f(p, 4, 17, 8, 8, 0, p, p, p, p, None) == 2           # top_k > 16
+    assert f(p, -1, 2, 8, 8, 0, p, p, p, p, None) == 2           # T < 0
+    assert f(p, 4, 2, 8, 8, 1, p, p, p, p, None) == 2            # shard beyond E_total
+    assert f(p, 4, 2, 8, 0, 0, p, p, p, p, None) == 2            # no local expert
+    assert f(None, 4, 2, 8, 8, 0, p, p, p, p, None) == 1
+    assert f(p, 4, 2, 8, 8, 0, p, p, None, p, None) == 1
+    assert f(vp(0x1004), 4, 2, 8, 8, 0, p, p, p, p, None) == 6
+    assert f(p, 4, 2, 8, 8, 0, p, p, p, vp(0x1008), None) == 6
+    assert f(p, 300_000, 16, 1024, 1024, 0, p, p, p, p, None) == 4
+    assert f(None, 0, 2, 8, 8, 0, None, None, None, None, None) == 0   # T == 0: nothing
+
+
+def test_tc_peak_argument_errors(lib):
+    vp = ctypes.c_void_p
+    d = ctypes.c_double(0.0)
+    assert lib.situ_tc_peak(0, 64, None, ctypes.byref(d), None) == 1
+    assert lib.situ_tc_peak(0, 64, vp(0x1000), None, None) == 1
+    assert lib.situ_tc_peak(0, 64, vp(0x1002), ctypes.byref(d), None) == 6
+    assert lib.situ_tc_peak(3, 64, vp(0x1000), ctypes.byref(d), None) == 3
+    assert lib.situ_tc_peak(0, 6, vp(0x1000), ctypes.byref(d), None) == 2
+    assert lib.situ_tc_peak(0, 0, vp(0x1000), ctypes.byref(d), None) == 2
+
+
 def test_status_strings(lib):
     for s in range(7):
         assert binding.status_string(s).startswith("SITU_")
@@ -171,7 +203,8 @@ def test_forward_launch_count(lib):
     assert n(pre) == 5
     pre.fuse_combine = 1
     assert n(pre) == 6
-    # NVFP4 decode tiles: permute, gather, FC1 (mxf4nvf4), FC2 (register tiles), combine,
+    # NVFP4 tiles: permute, gather, FC1 (mxf4nvf4), FC2 (fcv_kernel, bf16-expanded weights on
+    # kind::f16), combine,
     # plus one scale packing
     nv = _args(H=256, I=128, act_dtype=2, weight_dtype=1)
     for f in ("hidden_states_q", "hidden_states_scale", "hidden_states_gscale", "w1_gscale", "w2_gscale"):
@@ -229,6 +262,19 @@ def test_quant_nvfp4_argument_errors(lib):
     assert lib.situ_moe_quant_nvfp4(p, 0, 64, None, None, None, None) == 0
     assert lib.situ_moe_quant_nvfp4(None, 4, 64, p, p, p, None) == 1
     assert lib.situ_moe_quant_nvfp4(ctypes.c_void_p(264), 4, 64, p, p, p, None) == 6
+
+
+def test_forward_tactic_field(lib):
+    # TokenSpeed SiTU's runtime API: tactic = (-1, -1) is the first valid
+    # configuration; this library has one per shape, selected by -1 or 0
+    for t in ((-1, -1), (0, 0), (-1, 0)):
+        a = _args()
+        a.tactic[0], a.tactic[1] = t
+        assert lib.situ_moe_forward_launches(ctypes.byref(a)) == 5
+    for t in ((1, -1), (-1, 2), (-2, -1)):
+        a = _args()
+        a.tactic[0], a.tactic[1] = t
+        assert _fwd(lib, a) == 3
 
 
 def test_forward_rejects_unknown_activation(lib):

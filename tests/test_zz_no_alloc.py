@@ -37,7 +37,8 @@ def _both(ids_np, E_total, E_loc, off):
 
 
 def test_two_calls_match_the_workspace_permute():
-    # call 1: the Kimi-K3 prefill routing (131,072 slots, 896 local experts)
+    # call 1: the Kimi-K3 prefill routing (131,072 slots, 896 local experts;
+    # the three-launch count / scan / scatter path)
     cfg = W.CONFIGS["prefill_w4a8"]
     ids1, _ = W.routing(cfg["T"], cfg["K"], cfg["E_total"], cfg["routing"], 0)
     _both(ids1, cfg["E_total"], cfg["E_loc"], cfg["off"])
@@ -49,12 +50,19 @@ def test_two_calls_match_the_workspace_permute():
     assert int(offsets[-1]) == int(((ids2 >= 336) & (ids2 < 448)).sum())
 
 
-def test_too_large_request_is_rejected_without_launch():
-    # ceil(T*K/4096) * E_loc > SITU_NOALLOC_SCRATCH_INTS (1 << 20)
-    T, K, E = 300_000, 16, 1024
-    ids = torch.zeros((1, K), dtype=torch.int32, device="cuda")   # never read
-    dummy = torch.empty(16, dtype=torch.int32, device="cuda")
-    st = binding.lib().situ_moe_permute_noalloc(
-        binding._p(ids), T, K, E, E, 0, binding._p(dummy), binding._p(dummy),
-        binding._p(dummy), binding._p(dummy), binding._stream(None))
-    assert st == 4          # SITU_ERR_WORKSPACE_TOO_SMALL
+def test_decode_routing_single_launch_path():
+    # the Kimi-K3 decode routing (1,024 slots, 896 local experts) takes the
+    # one-CTA permute, twice in a row, and a strided view of a wider routing
+    # tensor is read as its own elements
+    cfg = W.CONFIGS["decode"]
+    ids, _ = W.routing(cfg["T"], cfg["K"], cfg["E_total"], cfg["routing"], 3)
+    _both(ids, cfg["E_total"], cfg["E_loc"], cfg["off"])
+    _both(ids[::-1].copy(), cfg["E_total"], cfg["E_loc"], cfg["off"])
+    wide = torch.from_numpy(np.concatenate([ids, ids + 1], axis=1)).cuda()
+    view = wide[:, :cfg["K"]]
+    assert not view.is_contiguous()
+    got = binding.situ_moe_permute_noalloc(view, cfg["E_total"], cfg["E_loc"], cfg["off"])
+    ref = binding.situ_moe_permute(torch.from_numpy(ids).cuda(), cfg["E_total"], cfg["E_loc"], cfg["off"])
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)

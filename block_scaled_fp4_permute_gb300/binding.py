@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             l.situ_moe_permute.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
             l.situ_moe_permute_noalloc.restype = ctypes.c_int
             l.situ_moe_permute_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+            l.situ_moe_route_topk.restype = ctypes.c_int
+            l.situ_moe_route_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
             l.situ_moe_quant_mxfp8.restype = ctypes.c_int
             l.situ_moe_quant_mxfp8.argtypes = [vp, i32, i32, vp, vp, vp]
             l.situ_moe_quant_nvfp4.restype = ctypes.c_int
@@ -168,6 +170,25 @@ def situ_moe_permute_noalloc(topk_ids: torch.Tensor, num_experts_total: int,
         _p(topk_ids), T, K, num_experts_total, num_local_experts, local_expert_offset,
         _p(counts), _p(offsets), _p(psrc), _p(s2r), _stream(stream)))
     return counts, offsets, psrc[:T * K], s2r[:T * K]
+
+
+def situ_moe_route_topk(router_logits: torch.Tensor, top_k: int, renormalize: bool = True, stream=None,
+                        out=None):
+    """Router logits fp32 [T, E] -> (int32 topk_ids [T, K], fp32 topk_weights
+    [T, K]): the K largest logits (ties to the lower ID) and a softmax over
+    them (renormalize) or their softmax probabilities over all E."""
+    if router_logits.dtype != torch.float32:
+        raise TypeError("router_logits must be fp32")
+    logits = router_logits.contiguous()
+    T, E = logits.shape
+    if out is None:
+        ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+        w = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
+    else:
+        ids, w = out
+    _check("situ_moe_route_topk", lib().situ_moe_route_topk(
+        _p(logits), T, E, int(top_k), 1 if renormalize else 0, _p(ids), _p(w), _stream(stream)))
+    return ids, w
 
 
 def situ_moe_quant_mxfp8(x_bf16: torch.Tensor, stream=None, out=None):

@@ -151,6 +151,40 @@ situ_status situ_moe_permute_noalloc(const int32_t* topk_ids, int32_t T, int32_t
                                      int32_t* slot_to_row, void* stream);
 
 /* ------------------------------------------------------------------------
+ * situ_moe_route_topk -- the top-k routing of router logits, upstream of
+ * situ_moe_permute.
+ *
+ * The golden reference MoE of TensorRT-LLM PR #17865 (review comment on
+ * test_kimi_k3_situ_moe.py, `_reference_moe`) starts from router logits and
+ * `routing_method.apply(router_logits)`; TokenSpeed SiTU ("Supported
+ * contract") consumes the resulting top-k IDs and weights.  The pages name
+ * no routing method; this call implements top-k selection with a softmax:
+ *   topk_ids[t, j]      the K largest logits of token t in descending order,
+ *                       two equal logits taken lower expert ID first (+0 and
+ *                       -0 are equal);
+ *   topk_weights[t, j]  renormalize = 1: exp(l_j - m) / sum over the K
+ *                       selected of exp(l_i - m), m the largest logit (a
+ *                       softmax over the selected logits, the definition the
+ *                       layer's routing weights follow); renormalize = 0:
+ *                       the same numerator over the sum across all E logits
+ *                       (the selected experts' softmax probabilities).
+ *
+ *   router_logits  fp32  [T, num_experts_total]  (finite values)
+ *   topk_ids       int32 [T, top_k]              global expert IDs
+ *   topk_weights   fp32  [T, top_k]
+ *
+ * The IDs are exact (comparisons of the fp32 logits); the weights are fp32
+ * (expf and one division, a few ulps from the exactly rounded value).
+ * Pointers 4-byte aligned.  T == 0 launches nothing.  Asynchronous on
+ * `stream`.  Errors: NULL_ARG, BAD_SHAPE (T < 0, num_experts_total < 1,
+ * top_k not in 1..min(16, num_experts_total)), UNSUPPORTED (renormalize
+ * not 0 or 1), MISALIGNED, CUDA.
+ * --------------------------------------------------------------------- */
+situ_status situ_moe_route_topk(const float* router_logits, int32_t T, int32_t num_experts_total,
+                                int32_t top_k, int32_t renormalize, int32_t* topk_ids,
+                                float* topk_weights, void* stream);
+
+/* ------------------------------------------------------------------------
  * situ_moe_quant_mxfp8 -- quantise bf16 activations to MXFP8 (w4a8 chain).
  *
  * TokenSpeed SiTU, "Activation precision (w4a16 vs w4a8)" and "Supported

@@ -88,6 +88,8 @@ def lib():
             l.oracle_quant_mxfp8.restype = None
             l.oracle_quant_mxfp8.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_void_p, ctypes.c_void_p]
+            l.oracle_route_topk.restype = ctypes.c_int
+            l.oracle_route_topk.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2
             l.oracle_permute.restype = ctypes.c_int
             l.oracle_permute.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 4
             l.oracle_moe_forward.restype = ctypes.c_int
@@ -180,6 +182,20 @@ def quant_mxfp8(x_bf16_bits: np.ndarray):
     s = np.empty((T, H // 32), np.uint8)
     lib().oracle_quant_mxfp8(_ptr(x), T, H, _ptr(q), _ptr(s))
     return q, s
+
+
+def route_topk(logits: np.ndarray, top_k: int, renormalize: bool = True):
+    """Router logits (fp32 [T, E]) -> (int32 ids [T, K] in descending logit
+    order, ties to the lower ID; fp32 weights [T, K]: a softmax over the K
+    selected logits, or with renormalize=False the selected experts'
+    probabilities under a softmax over all E)."""
+    x = _c(logits, np.float32)
+    T, E = x.shape
+    ids = np.empty((T, top_k), np.int32)
+    w = np.empty((T, top_k), np.float32)
+    if lib().oracle_route_topk(_ptr(x), T, E, int(top_k), 1 if renormalize else 0, _ptr(ids), _ptr(w)) != 0:
+        raise ValueError("oracle_route_topk: bad sizes")
+    return ids, w
 
 
 def permute(topk_ids: np.ndarray, num_experts_total: int, num_local_experts: int,

@@ -17,6 +17,9 @@
  *     (TokenSpeed SiTU, "Activation precision (w4a16 vs w4a8)" and
  *     "Supported contract": MXFP8 activations with a per-token
  *     hidden_states_scale block-scale tensor);
+ *   - the routing step upstream of the layer, top-k of router logits with
+ *     softmax weights (the golden reference MoE of TensorRT-LLM PR #17865
+ *     applies a routing method to router logits; the method is a reading);
  *   - the expert permute with local-shard filtering (TokenSpeed SiTU,
  *     "Supported contract": top-k IDs stay global, experts outside the rank's
  *     contiguous shard are filtered, the output is a partial sum);
@@ -315,6 +318,54 @@ int oracle_permute(const int32_t* ids, int T, int K, int E_total, int E_loc, int
   }
   free(fill);
   return offsets[E_loc];
+}
+
+/* ------------------------------------------------------------------ */
+/* Routing from router logits                                          */
+/* ------------------------------------------------------------------ */
+
+/* The routing step upstream of the layer: the golden reference MoE of
+ * TensorRT-LLM PR #17865 (`_reference_moe`) starts from router logits and
+ * `routing_method.apply(router_logits)`, and TokenSpeed SiTU ("Supported
+ * contract") takes the resulting top-k.  The pages name no routing method;
+ * the reading taken is the one the workloads' routing weights follow:
+ *   ids[t, 0..K-1]  the K largest logits of token t, in descending order of
+ *                   logit, ties taken by the lower expert ID first;
+ *   w[t, j]         renormalize = 1: exp(l_j) / sum over the K selected of
+ *                   exp(l_i) (a softmax over the selected logits);
+ *                   renormalize = 0: exp(l_j) / sum over all E logits (the
+ *                   softmax probabilities of the selected experts).
+ * Logits are finite fp32.  The weights are computed in fp64 with the
+ * maximum subtracted first and rounded once to fp32.  Returns 0, or -1 for
+ * bad sizes (K < 1 or K > E). */
+int oracle_route_topk(const float* logits, int T, int E, int K, int renormalize, int32_t* ids, float* w) {
+  if (T < 0 || E < 1 || K < 1 || K > E) return -1;
+  char* taken = (char*)malloc((size_t)E);
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (size_t)t * E;
+    memset(taken, 0, (size_t)E);
+    /* K rounds of "the largest logit not taken yet, lowest ID among equals" */
+    for (int j = 0; j < K; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e;   /* strict: an equal later ID loses */
+      }
+      taken[best] = 1;
+      ids[(size_t)t * K + j] = best;
+    }
+    const double m = l[ids[(size_t)t * K]];   /* the largest logit of the row */
+    double den = 0.0;
+    if (renormalize) {
+      for (int j = 0; j < K; ++j) den += exp((double)l[ids[(size_t)t * K + j]] - m);
+    } else {
+      for (int e = 0; e < E; ++e) den += exp((double)l[e] - m);
+    }
+    for (int j = 0; j < K; ++j)
+      w[(size_t)t * K + j] = (float)(exp((double)l[ids[(size_t)t * K + j]] - m) / den);
+  }
+  free(taken);
+  return 0;
 }
 
 /* ------------------------------------------------------------------ */

@@ -168,6 +168,22 @@ def test_permute_noalloc_rejects_without_launch(lib):
     assert f(None, 0, 2, 8, 8, 0, None, None, None, None, None) == 0   # T == 0: nothing
 
 
+def test_route_topk_argument_errors(lib):
+    vp = ctypes.c_void_p
+    p = vp(0x1000)
+    f = lib.situ_moe_route_topk
+    assert f(p, 4, 8, 0, 1, p, p, None) == 2       # top_k 0
+    assert f(p, 4, 8, 9, 1, p, p, None) == 2       # top_k > E
+    assert f(p, 4, 32, 17, 1, p, p, None) == 2     # top_k > 16
+    assert f(p, -1, 8, 2, 1, p, p, None) == 2
+    assert f(p, 4, 0, 1, 1, p, p, None) == 2
+    assert f(p, 4, 8, 2, 2, p, p, None) == 3       # renormalize not 0 / 1
+    assert f(None, 4, 8, 2, 1, p, p, None) == 1
+    assert f(p, 4, 8, 2, 1, p, None, None) == 1
+    assert f(vp(0x1002), 4, 8, 2, 1, p, p, None) == 6
+    assert f(None, 0, 8, 2, 1, None, None, None) == 0   # T == 0: nothing
+
+
 def test_tc_peak_argument_errors(lib):
     vp = ctypes.c_void_p
     d = ctypes.c_double(0.0)

@@ -520,3 +520,59 @@ def test_cuda_graph_replay_matches_eager(name, T):
     torch.cuda.synchronize()
     assert torch.equal(layer.out, eager)
     assert layer.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# routing from router logits (bit-exact IDs, weights at fp32 rounding)
+# ---------------------------------------------------------------------------
+
+def _check_route(logits_np, K, renormalize=True):
+    logits = torch.from_numpy(logits_np).cuda()
+    ids, w = binding.situ_moe_route_topk(logits, K, renormalize)
+    torch.cuda.synchronize()
+    rid, rw = oracle.route_topk(logits_np, K, renormalize)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    # expf and one division in fp32 against one rounding of the fp64 value
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=4e-6, atol=1e-9)
+    return ids, w
+
+
+@pytest.mark.parametrize("T,E,K", [(64, 896, 16), (8192, 896, 16), (4096, 896, 16), (16, 8, 2),
+                                   (1, 1, 1), (37, 100, 7), (5, 16, 16), (300, 4096, 16), (3, 33, 13)])
+@pytest.mark.parametrize("renormalize", [True, False])
+def test_route_topk_random_logits(T, E, K, renormalize):
+    rng = np.random.default_rng(T * 7 + E + K)
+    _check_route((rng.standard_normal((T, E)) * 3.0).astype(np.float32), K, renormalize)
+
+
+def test_route_topk_ties_and_extremes():
+    rng = np.random.default_rng(11)
+    # integer logits from a small set: ties everywhere, broken by the lower ID
+    _check_route(rng.integers(-2, 3, (500, 896)).astype(np.float32), 16)
+    # every logit equal: IDs 0..K-1, weights 1/K
+    ids, w = _check_route(np.zeros((8, 64), np.float32), 16)
+    assert np.array_equal(ids.cpu().numpy(), np.tile(np.arange(16), (8, 1)))
+    # signed zeros and huge magnitudes (the maximum is subtracted first)
+    l = np.zeros((4, 40), np.float32)
+    l[:, 1::2] = -0.0
+    l[1, 5] = 3e38
+    l[2, :] = -3e38
+    l[3, 7] = -1e30
+    _check_route(l, 16)
+    _check_route(l, 16, renormalize=False)
+
+
+def test_route_topk_feeds_the_layer():
+    """Route from logits, then the layer: the same as the oracle routing
+    step followed by the oracle layer."""
+    wl = W.make("decode", device="cuda")
+    rng = np.random.default_rng(5)
+    logits_np = rng.standard_normal((wl.T, wl.E_total)).astype(np.float32)
+    ids, w = binding.situ_moe_route_topk(torch.from_numpy(logits_np).cuda(), wl.K)
+    wl.topk_ids.copy_(ids)
+    wl.topk_weights.copy_(w)
+    _, out = run_layer(wl)
+    rid, rw = oracle.route_topk(logits_np, wl.K)
+    kw = W.oracle_kwargs(wl)
+    kw["topk_ids"], kw["topk_weights"] = rid, rw
+    assert_parity(out, oracle.moe_forward(**kw), "routed from logits, decode")

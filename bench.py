@@ -267,14 +267,20 @@ def oracle_tokens_per_s(wl, budget_s: float, host_kw=None, max_tokens=None):
     if host_kw is None:
         host_kw = host_oracle_kwargs(wl)
     T = wl.T
-    n0 = min(T, 2)
-    t0 = time.perf_counter()
-    _oracle_run(oracle, W, wl, host_kw, n0)
-    dt0 = time.perf_counter() - t0
-    n = int(max(1, min(max_tokens or T, T, round(budget_s / max(dt0 / n0, 1e-6)))))
+    cap = min(max_tokens or T, T)
+    # the oracle works expert by expert, so a small sample's time per token
+    # overstates a large one's: size the sample in two steps
+    n = min(T, 2)
     t0 = time.perf_counter()
     _oracle_run(oracle, W, wl, host_kw, n)
     dt = time.perf_counter() - t0
+    for _ in range(2):
+        if dt >= 0.5 * budget_s or n >= cap:
+            break
+        n = int(max(1, min(cap, round(n * budget_s / max(dt, 1e-6)))))
+        t0 = time.perf_counter()
+        _oracle_run(oracle, W, wl, host_kw, n)
+        dt = time.perf_counter() - t0
     return n / dt, n, dt, oracle.get_threads()
 
 

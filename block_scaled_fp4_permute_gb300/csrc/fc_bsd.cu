@@ -582,6 +582,54 @@ __global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) 
   }
 }
 
+// bf16 token rows by token: each thread splits one 32-element block of
+// token t into hi + lo E4M3 blocks once and writes them to the rows of all
+// the token's kept slots (up to top_k), so a token's row is read and split
+// once instead of once per kept slot.
+constexpr int kGatherTokThreads = 32;
+__global__ void __launch_bounds__(kGatherTokThreads) gather_hl_tok_kernel(const GatherHLParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // the permute's outputs
+  const long t = blockIdx.x;
+  const int lane = threadIdx.x;
+  const int K = p.K, nb = K / 32;
+  const int b = blockIdx.y * kGatherTokThreads + lane;
+  // lane j holds the row of slot j
+  const int my_row = lane < p.top_k ? __ldg(p.slot_to_row + t * p.top_k + lane) : -1;
+  // every lane stays for the row shuffles below; lanes past the row's last
+  // block only take part in them
+  const bool valid = b < nb;
+  const uint4* xrow = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.x_bf16) + (size_t)t * K * 2);
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = valid ? __ldg(xrow + 4 * b + q) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * q + 2 * j] = bf16_lo(u[j]);
+      v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
+    }
+  }
+  uint32_t hi[8], lo[8];
+  const uint32_t sb = split_hl32(v, hi, lo);
+  const uint4 h0 = make_uint4(hi[0], hi[1], hi[2], hi[3]), h1 = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+  const uint4 l0 = make_uint4(lo[0], lo[1], lo[2], lo[3]), l1 = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  for (int j = 0; j < p.top_k; ++j) {
+    const int r = __shfl_sync(0xffffffffu, my_row, j);
+    if (r < 0 || !valid) continue;
+    uint4* hrow = reinterpret_cast<uint4*>(p.x + (size_t)(2 * r) * K);
+    uint4* lrow = reinterpret_cast<uint4*>(p.x + (size_t)(2 * r + 1) * K);
+    hrow[2 * b] = h0;
+    hrow[2 * b + 1] = h1;
+    lrow[2 * b] = l0;
+    lrow[2 * b + 1] = l1;
+    uint8_t* sh = p.xs + (size_t)(2 * r) * p.s_stride;
+    sh[tok_scale_byte(b)] = (uint8_t)(sb & 0xFFu);
+    sh[p.s_stride + tok_scale_byte(b)] = (uint8_t)(sb >> 8);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -629,6 +677,11 @@ int fcw_scale_stride(int K) { return K / 8; }   // 16 bytes per 128-element stag
 
 cudaError_t launch_gather_hl(const GatherHLParams& p, cudaStream_t st) {
   if (p.S <= 0) return cudaSuccess;
+  if (p.act == 0 && p.slot_to_row) {
+    const int nb = p.K / 32;
+    const dim3 grid((unsigned)p.T, (unsigned)((nb + kGatherTokThreads - 1) / kGatherTokThreads));
+    return launch_pdl(gather_hl_tok_kernel, grid, dim3(kGatherTokThreads), 0, st, p);
+  }
   return launch_pdl(gather_hl_kernel, dim3((unsigned)p.S), dim3(128), 0, st, p);
 }
 

@@ -10,9 +10,10 @@
 //     instead of rescaling every weight;
 //   * activations arrive as "f16 block rows" (mantissa * per-32-block fp32
 //     scale), built once per row: gather16 converts the token-major input
-//     in expert order (bf16 rows take one power-of-two scale per row that
-//     puts the row maximum in [2^14, 2^15), exact for every element within
-//     2^-28 of it; MXFP8 rows convert exactly and keep their block scales;
+//     in expert order (bf16 rows take one power-of-two scale per 32-element
+//     block that puts the block maximum in [2^14, 2^15), exact for every
+//     element within 2^-28 of it; MXFP8 rows convert exactly and keep their
+//     block scales;
 //     NVFP4 rows convert exactly with the E4M3 block scales folded in and
 //     the per-token fp32 scale as the row scale), and FC1's epilogue writes
 //     H1 the same way for FC2.
@@ -459,7 +460,38 @@ __global__ void __launch_bounds__(128) gather16_kernel(const Gather16Params p) {
   uint4* orow = reinterpret_cast<uint4*>(p.x16 + (size_t)r * kpad);
   float* srow = p.xs + (size_t)r * nkb4;
   float row_scale = 0.f;
-  if (p.act == 0) {
+  if (p.act == 0 && !p.row_scale) {
+    // one power-of-two scale per 32-element block, putting the block maximum
+    // in [2^14, 2^15): exact for every element within 2^-28 of its block's
+    // maximum, whatever the other blocks of the row hold.  Lanes 4b..4b+3 of
+    // a warp hold block b; every thread runs the same number of iterations,
+    // so the shuffles see the whole warp.
+    const uint4* xrow = reinterpret_cast<const uint4*>(p.x_bf16) + (size_t)t * k8n;
+    for (int base = 0; base < k8n; base += 128) {
+      const int k8 = base + tid;
+      const bool valid = k8 < k8n;
+      const uint4 v = valid ? __ldg(xrow + k8) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      // clamped at -126 so that 2^-ex stays an fp32 normal: a block whose
+      // maximum is below 2^-112 then maps into [2^-14, 2^14), where every
+      // bf16 value, subnormals included, is an exact f16
+      int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
+      ex = ex < -126 ? -126 : ex;
+      const float inv = exp2i(-ex);
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = f32x2_to_f16x2(bf16_lo(w[i]) * inv, bf16_hi(w[i]) * inv);
+      if (valid) {
+        orow[k8] = make_uint4(o[0], o[1], o[2], o[3]);
+        if ((k8 & 3) == 0) srow[k8 >> 2] = exp2i(ex);
+      }
+    }
+  } else if (p.act == 0) {
     const uint4* xrow = reinterpret_cast<const uint4*>(p.x_bf16) + (size_t)t * k8n;
     float amax = 0.f;
     for (int k8 = tid; k8 < k8n; k8 += 128) {
@@ -526,7 +558,9 @@ __global__ void __launch_bounds__(128) gather16_kernel(const Gather16Params p) {
     row_scale = __ldg(p.x_gs + t);
   }
   for (int k8 = k8n + tid; k8 < kpad / 8; k8 += 128) orow[k8] = make_uint4(0, 0, 0, 0);
+  const bool block_scaled_bf16 = p.act == 0 && !p.row_scale;   // written above, per block
   for (int b = tid; b < nkb4; b += 128) {
+    if (block_scaled_bf16 && b < nkb) continue;
     float v = 0.f;
     if (b < nkb) v = (p.act == 1 && !p.row_scale) ? exp2i((int)__ldg(p.x_s + (size_t)t * nkb + b) - 127) : row_scale;
     srow[b] = v;

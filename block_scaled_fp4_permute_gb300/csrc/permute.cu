@@ -191,13 +191,14 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
                      int32_t* __restrict__ permuted_src, int32_t* __restrict__ slot_to_row,
                      int32_t* __restrict__ meta) {
   extern __shared__ int32_t sm[];
-  int32_t* wcnt = sm;                        // [kSmallWarps][E_loc]
-  int32_t* cnt = sm + kSmallWarps * E_loc;   // [E_loc]
-  int32_t* offs = cnt + E_loc;               // [E_loc]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kPerWarp = kPermChunk / kSmallWarps;   // 128
-  // only the warps that own slots keep counts (8 of 32 at 1,024 slots)
+  // only the warps that own slots keep counts (8 of 32 at 1,024 slots), and
+  // the launch sizes shared memory for them alone
   const int nw = (S + kPerWarp - 1) / kPerWarp;
+  int32_t* wcnt = sm;                  // [nw][E_loc]
+  int32_t* cnt = sm + nw * E_loc;      // [E_loc]
+  int32_t* offs = cnt + E_loc;         // [E_loc]
   for (int i = threadIdx.x; i < nw * E_loc; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   for (int r = 0; r < kPerWarp; r += kWarp) {
@@ -311,7 +312,10 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
   int dev = 0;
   cudaGetDevice(&dev);
   if (nblk == 1 && E_loc <= kSmallMaxExperts) {
-    const size_t smem = sizeof(int32_t) * (size_t)(kSmallWarps + 2) * E_loc;
+    // per-warp counts of the warps that own slots, counts and offsets; a
+    // small request keeps the SM's shared-memory split as it is
+    const long nw = (S + kPermChunk / kSmallWarps - 1) / (kPermChunk / kSmallWarps);
+    const size_t smem = sizeof(int32_t) * (size_t)(nw + 2) * E_loc;
     {
       std::lock_guard<std::mutex> lock(attr_mutex());
       if (dev < 0 || dev >= 64 || g_small_smem_set[dev] < (int)smem) {

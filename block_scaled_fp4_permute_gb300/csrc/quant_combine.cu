@@ -7,11 +7,13 @@
 // two shuffles, and each lane stores its 8 E4M3 codes with one 64-bit store.
 //
 // combine: the top-k-weighted un-permute sum out[t] = sum_j w[t,j] * Y[row]
-// over the kept slots in ascending j, from the fp32 FC2 output, accumulated
-// in fp32 and rounded to bf16 once (the golden loop of TensorRT-LLM PR #17865 adds
+// over the kept slots in ascending j, from the FC2 output (fp32 rows, or f16
+// rows with a power-of-two scale per 32 columns), accumulated in fp32 and
+// rounded to bf16 once (the golden loop of TensorRT-LLM PR #17865 adds
 // weight * expert output per slot); a token with no kept slot gets 0.  Each
-// thread owns 4 consecutive hidden elements (one 128-bit load per kept
-// slot, four slots in flight), so each row of Y is read fully coalesced.
+// thread owns one 16-byte piece of the rows and has all K slots' loads in
+// flight at once, so each row of Y is read fully coalesced.
+#include "../../include/situ_moe.h"
 #include "situ_internal.h"
 
 namespace situ {
@@ -51,94 +53,88 @@ cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t*
   return cudaGetLastError();
 }
 
-__global__ void __launch_bounds__(256)
-combine_kernel(const float4* __restrict__ y, const int32_t* __restrict__ slot_to_row,
-               const float* __restrict__ w, int K, int H4, uint2* __restrict__ out) {
-  griddep_wait();   // Y is the predecessor's output
-  const int t = blockIdx.x;
-  const int h4 = blockIdx.y * blockDim.x + threadIdx.x;
-  if (h4 >= H4) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  // slots in ascending j; four row loads in flight at a time
-  for (int j0 = 0; j0 < K; j0 += 4) {
-    int r[4];
-    float wt[4];
-    float4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u;
-      r[u] = j < K ? __ldg(slot_to_row + (size_t)t * K + j) : -1;
-      wt[u] = r[u] >= 0 ? (w ? __ldg(w + (size_t)t * K + j) : 1.f) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      v[u] = r[u] >= 0 ? __ldg(y + (size_t)r[u] * H4 + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (r[u] >= 0) {
-        acc.x = fmaf(wt[u], v[u].x, acc.x);
-        acc.y = fmaf(wt[u], v[u].y, acc.y);
-        acc.z = fmaf(wt[u], v[u].z, acc.z);
-        acc.w = fmaf(wt[u], v[u].w, acc.w);
-      }
-    }
-  }
-  out[(size_t)t * H4 + h4] = make_uint2(f32x2_to_bf16x2(acc.x, acc.y), f32x2_to_bf16x2(acc.z, acc.w));
-}
+// One thread owns 16 bytes of one token's Y rows (4 fp32 or 8 f16 columns)
+// and issues the loads of all K slots before the first multiply-add, so a
+// thread keeps K 16-byte loads in flight; the sums still run in ascending j.
+// F16: Y rows are f16 mantissas with a scale byte per 32 columns
+// (y16_exponent), block-major (byte of row r, block b at b * ys_rows + r).
+// Threads per CTA: 64 for f16 rows, 128 for fp32 rows (the Kimi-K3 row of
+// 3584 columns is then exactly 7 CTAs of 16-byte pieces either way).
+template <bool F16>
+constexpr int combine_threads() { return F16 ? 64 : 128; }
 
-__global__ void __launch_bounds__(256)
-combine16_kernel(const uint2* __restrict__ y, const uint8_t* __restrict__ ys, long ys_rows,
-                 const int32_t* __restrict__ slot_to_row,
-                 const float* __restrict__ w, int K, int H4, uint2* __restrict__ out) {
+template <bool F16>
+__global__ void __launch_bounds__(combine_threads<F16>())
+combine_kernel(const uint4* __restrict__ y, const uint8_t* __restrict__ ys, long ys_rows,
+               const int32_t* __restrict__ slot_to_row, const float* __restrict__ w, int K, int n16,
+               uint4* __restrict__ out) {
   griddep_wait();   // Y is the predecessor's output
   const int t = blockIdx.x;
-  const int h4 = blockIdx.y * blockDim.x + threadIdx.x;
-  if (h4 >= H4) return;
-  const int b = h4 >> 3;   // this thread's 32-element block
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < K; j0 += 4) {
-    int r[4];
-    float wt[4];
-    uint2 v[4];
-    uint32_t sb[4];
+  const int c = blockIdx.y * combine_threads<F16>() + threadIdx.x;   // 16-byte column piece
+  if (c >= n16) return;
+  int r[SITU_MAX_TOP_K];
+  float wt[SITU_MAX_TOP_K];
+  uint4 v[SITU_MAX_TOP_K];
+  uint32_t sb[SITU_MAX_TOP_K];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u;
-      r[u] = j < K ? __ldg(slot_to_row + (size_t)t * K + j) : -1;
-      wt[u] = r[u] >= 0 ? (w ? __ldg(w + (size_t)t * K + j) : 1.f) : 0.f;
-    }
+  for (int j = 0; j < SITU_MAX_TOP_K; ++j) {
+    r[j] = j < K ? __ldg(slot_to_row + (size_t)t * K + j) : -1;
+    wt[j] = r[j] >= 0 ? (w ? __ldg(w + (size_t)t * K + j) : 1.f) : 0.f;
+  }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      v[u] = r[u] >= 0 ? __ldg(y + (size_t)r[u] * H4 + h4) : make_uint2(0u, 0u);
-      sb[u] = r[u] >= 0 ? __ldg(ys + (size_t)b * ys_rows + r[u]) : 127u;
-    }
+  for (int j = 0; j < SITU_MAX_TOP_K; ++j) {
+    v[j] = r[j] >= 0 ? __ldg(y + (size_t)r[j] * n16 + c) : make_uint4(0u, 0u, 0u, 0u);
+    if (F16) sb[j] = r[j] >= 0 ? __ldg(ys + (size_t)(c >> 2) * ys_rows + r[j]) : 127u;
+  }
+  if (!F16) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (r[u] >= 0) {
-        const float s = wt[u] * exp2i((int)sb[u] - 127);
-        acc.x = fmaf(s, f16_to_f32(v[u].x & 0xFFFFu), acc.x);
-        acc.y = fmaf(s, f16_to_f32(v[u].x >> 16), acc.y);
-        acc.z = fmaf(s, f16_to_f32(v[u].y & 0xFFFFu), acc.z);
-        acc.w = fmaf(s, f16_to_f32(v[u].y >> 16), acc.w);
+    for (int j = 0; j < SITU_MAX_TOP_K; ++j) {
+      if (r[j] >= 0) {
+        acc.x = fmaf(wt[j], __uint_as_float(v[j].x), acc.x);
+        acc.y = fmaf(wt[j], __uint_as_float(v[j].y), acc.y);
+        acc.z = fmaf(wt[j], __uint_as_float(v[j].z), acc.z);
+        acc.w = fmaf(wt[j], __uint_as_float(v[j].w), acc.w);
       }
     }
+    // 4 bf16 of this thread's 4 columns: 8 bytes (two threads fill 16)
+    reinterpret_cast<uint2*>(out)[(size_t)t * n16 + c] =
+        make_uint2(f32x2_to_bf16x2(acc.x, acc.y), f32x2_to_bf16x2(acc.z, acc.w));
+  } else {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < SITU_MAX_TOP_K; ++j) {
+      if (r[j] >= 0) {
+        const float s = wt[j] * exp2i((int)sb[j] - 127);
+        const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(s, f16_to_f32(u[q] & 0xFFFFu), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(s, f16_to_f32(u[q] >> 16), acc[2 * q + 1]);
+        }
+      }
+    }
+    out[(size_t)t * n16 + c] = make_uint4(f32x2_to_bf16x2(acc[0], acc[1]), f32x2_to_bf16x2(acc[2], acc[3]),
+                                          f32x2_to_bf16x2(acc[4], acc[5]), f32x2_to_bf16x2(acc[6], acc[7]));
   }
-  out[(size_t)t * H4 + h4] = make_uint2(f32x2_to_bf16x2(acc.x, acc.y), f32x2_to_bf16x2(acc.z, acc.w));
 }
 
 cudaError_t launch_combine16(const void* y16, const uint8_t* ys, long ys_rows, const int32_t* slot_to_row,
                              const float* w, int T, int K, int H, void* out, cudaStream_t st) {
-  const int H4 = H / 4;
-  dim3 grid(T, (H4 + 255) / 256);
-  return launch_pdl(combine16_kernel, grid, dim3(256), 0, st, (const uint2*)y16, ys, ys_rows, slot_to_row, w, K,
-                    H4, (uint2*)out);
+  const int n16 = H / 8;   // 16-byte pieces of an f16 row (H is a multiple of 32)
+  constexpr int nt = combine_threads<true>();
+  dim3 grid(T, (n16 + nt - 1) / nt);
+  return launch_pdl(combine_kernel<true>, grid, dim3(nt), 0, st, (const uint4*)y16, ys, ys_rows,
+                    slot_to_row, w, K, n16, (uint4*)out);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* slot_to_row, const float* w, int T, int K,
                            int H, void* out, cudaStream_t st) {
-  const int H4 = H / 4;
-  dim3 grid(T, (H4 + 255) / 256);
-  return launch_pdl(combine_kernel, grid, dim3(256), 0, st, (const float4*)y, slot_to_row, w, K, H4, (uint2*)out);
+  const int n16 = H / 4;   // 16-byte pieces of an fp32 row
+  constexpr int nt = combine_threads<false>();
+  dim3 grid(T, (n16 + nt - 1) / nt);
+  return launch_pdl(combine_kernel<false>, grid, dim3(nt), 0, st, (const uint4*)y,
+                    (const uint8_t*)nullptr, 0L, slot_to_row, w, K, n16, (uint4*)out);
 }
 
 // ---------------------------------------------------------------------------

@@ -240,6 +240,8 @@ struct GatherHLParams {
   const float* x_gs;             // NVFP4: per-token global scale, copied to xg [S] in row order
   float* xg;
   const int32_t* permuted_src;
+  const int32_t* slot_to_row;    // bf16 rows are gathered per token: slot -> row (-1 dropped)
+  int T;
   const int32_t* meta;           // meta[0] = R
   int top_k, K;
   long S;

@@ -366,11 +366,14 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
     const bool lo = a->act_dtype == SITU_ACT_BF16;
     GatherHLParams g;
+    std::memset(&g, 0, sizeof(g));
     g.act = a->act_dtype;
     g.x_bf16 = a->hidden_states;
     g.x_q = a->hidden_states_q;
     g.x_s = a->hidden_states_scale;
     g.permuted_src = psrc;
+    g.slot_to_row = s2r;
+    g.T = a->T;
     g.meta = meta;
     g.top_k = a->top_k;
     g.K = a->H;
@@ -522,7 +525,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     d.K = a->H;
     d.x16 = g16.x16;
     d.xs = g16.xs;
-    d.ablk = a->act_dtype == SITU_ACT_MXFP8;
+    d.ablk = a->act_dtype != SITU_ACT_NVFP4;   // bf16 and MXFP8 rows carry a scale per 32-block
     d.n_mtiles = (a->I + 63) / 64;
     d.mg = 1;
     d.beta = a->gemm1_alpha;

@@ -112,14 +112,14 @@ def load_tc_peaks():
     return None
 
 
-def gemm_kinds(wl):
+def gemm_kinds(wl, h1_nvfp4=False):
     """The tensor-core MMA kind each GEMM of the layer runs on, by the path
     the shapes take (mirrors the library's host-side path choice)."""
     rows_per_expert = wl.T * wl.K / max(wl.E_total, 1)
     if wl.wt == 0 and wl.H % 128 == 0 and wl.I % 128 == 0:
         return {"fc1": "mxf8f6f4", "fc2": "mxf8f6f4"}
     if wl.wt == 1 and wl.act == 2 and rows_per_expert <= 512.0 and wl.H % 256 == 0 and wl.I % 128 == 0:
-        return {"fc1": "mxf4nvf4", "fc2": "bf16"}
+        return {"fc1": "mxf4nvf4", "fc2": "mxf4nvf4" if h1_nvfp4 else "bf16"}
     return {"fc1": "f16", "fc2": "f16"}
 
 
@@ -148,7 +148,7 @@ def routing_stats(wl):
     return R, touched
 
 
-def algorithmic_bytes(wl, R, touched):
+def algorithmic_bytes(wl, R, touched, h1_nvfp4=False):
     """Bytes each stage must move at minimum (weights of touched experts
     once, activations and outputs once)."""
     H, I, T, K = wl.H, wl.I, wl.T, wl.K
@@ -161,6 +161,8 @@ def algorithmic_bytes(wl, R, touched):
     # scale) and H1 (MXFP8 for w4a8, bf16 otherwise)
     x_row = act_in / max(T, 1)
     h_row = I + I / 32 if wl.act == 1 else 2 * I
+    # FC2 reads H1 as FC1 writes it, or as its NVFP4 requantisation
+    h_in = I / 2 + I / 16 + 4 if h1_nvfp4 else h_row
     route = T * K * 8
     out = T * H * 2
     # bytes per element of the FC2 rows Y the combine reads: f16 + a scale byte
@@ -172,33 +174,34 @@ def algorithmic_bytes(wl, R, touched):
         "permute": T * K * 4 + 2 * T * K * 4 + 2 * wl.E_loc * 4,
         "gather": 2 * R * x_row,
         "fc1": w1 + R * x_row + R * h_row,
-        "fc2": w2 + R * h_row + R * H * y_bytes,
+        "fc2": w2 + R * h_in + R * H * y_bytes,
         "combine": R * H * y_bytes + route + out,
         "quant": T * H * 2 + (T * H + T * H // 32 if wl.act == 1 else T * H // 2 + T * H // 16 + 4 * T),
         "layer": w1 + w2 + act_in + route + out,
     }
 
 
-def layer_dtype(wl):
+def layer_dtype(wl, h1_nvfp4=False):
     """The operand types the layer computes in (what the contract's formats
     are, not the tensor-core containers): bf16 or MXFP8 or NVFP4 activations
     times MXFP4 / NVFP4 weights, fp32 accumulation."""
     act = {0: "bf16", 1: "mxfp8", 2: "nvfp4"}[wl.act]
     w = {0: "mxfp4", 1: "nvfp4"}[wl.wt]
-    h1 = "mxfp8" if wl.act == 1 else "bf16"
+    h1 = "mxfp8" if wl.act == 1 else "nvfp4" if h1_nvfp4 else "bf16"
     return f"{act}x{w}->f32 (FC1), {h1}x{w}->f32 (FC2)"
 
 
-def mma_containers(wl):
+def mma_containers(wl, h1_nvfp4=False):
     """How the tensor cores see the operands, per GEMM."""
-    k = gemm_kinds(wl)
+    k = gemm_kinds(wl, h1_nvfp4)
     if k["fc1"] == "mxf8f6f4":
         rows = "bf16 rows as E4M3 hi + lo pairs (two MMAs per K block)" if wl.act == 0 else "E4M3 rows"
         return {"fc1": f"kind::mxf8f6f4, {rows} x E2M1 weights", "fc2": f"kind::mxf8f6f4, H1 as "
                 + ("E4M3 hi + lo pairs" if wl.act == 0 else "E4M3 rows") + " x E2M1 weights"}
     if k["fc1"] == "mxf4nvf4":
         return {"fc1": "kind::mxf4nvf4, E2M1 x E2M1, E4M3 scales per 16",
-                "fc2": "kind::f16, bf16 H1 x bf16-expanded NVFP4 weights"}
+                "fc2": ("kind::mxf4nvf4, requantised NVFP4 H1 x NVFP4 weights" if h1_nvfp4 else
+                        "kind::f16, bf16 H1 x bf16-expanded NVFP4 weights")}
     return {"fc1": "kind::f16 / mma.sync on f16-expanded operands", "fc2": "same"}
 
 
@@ -379,9 +382,10 @@ def measure_workload(name, args, dev, rank, ws, tc, sampler_dev, cpu_budget):
     from block_scaled_fp4_permute_gb300 import binding
 
     wl = make_workload(name, dev, args.seed + rank, args.tokens if name == args.workload else None)
-    layer = binding.Layer(wl, fuse_combine=args.fuse_combine)
+    layer = binding.Layer(wl, fuse_combine=args.fuse_combine, h1_nvfp4=args.h1_nvfp4 and wl.act == 2)
     R, touched = routing_stats(wl)
-    nbytes = algorithmic_bytes(wl, R, touched)
+    h1nv = bool(args.h1_nvfp4 and wl.act == 2)
+    nbytes = algorithmic_bytes(wl, R, touched, h1nv)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     nst = len(binding.PROFILE_STAGES)
@@ -480,7 +484,7 @@ def measure_workload(name, args, dev, rank, ws, tc, sampler_dev, cpu_budget):
     if is_q:
         gbs = nbytes["quant"] / (quant_ms * 1e-3) / 1e9
         stages[qname] = {"ms": quant_ms, "alg_bytes": int(nbytes["quant"]), "gbs": gbs, "frac_hbm": gbs / hbm}
-    kinds = gemm_kinds(wl)
+    kinds = gemm_kinds(wl, h1nv)
     kflops = {"fc1": 2.0 * R * wl.H * 2 * wl.I, "fc2": 2.0 * R * wl.I * wl.H}
     for g in ("fc1", "fc2"):
         pk, _ = tensor_peak_of(kinds[g], tc)
@@ -534,7 +538,7 @@ def measure_workload(name, args, dev, rank, ws, tc, sampler_dev, cpu_budget):
 
     rec = {
         "value": ws * wl.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-        "dtype": layer_dtype(wl), "mma": mma_containers(wl),
+        "dtype": layer_dtype(wl, h1nv), "mma": mma_containers(wl, h1nv),
         "config": {"workload": WORKLOAD_NAMES[name], "T": wl.T, "H": wl.H, "I": wl.I,
                    "E_total": wl.E_total, "E_loc": wl.E_loc, "offset": wl.off, "top_k": wl.K,
                    "kept_pairs": R, "touched_experts": touched,
@@ -543,6 +547,8 @@ def measure_workload(name, args, dev, rank, ws, tc, sampler_dev, cpu_budget):
                    "launch": "CUDA graph replay of the layer call" if args.graph else "eager C-ABI call",
                    "combine": "fused into FC2 (fp32 reductions)" if args.fuse_combine
                    else "separate kernel, ascending slot order",
+                   "h1": ("NVFP4, requantised per token (opt-in)" if args.h1_nvfp4 and wl.act == 2 else
+                          "MXFP8" if wl.act == 1 else "bf16"),
                    "step": ("MXFP8 quantisation of the bf16 input + " if wl.act == 1 else
                             "NVFP4 quantisation of the bf16 input + " if wl.act == 2 else "")
                    + "the whole layer"},
@@ -648,6 +654,8 @@ def main():
                     help="measure the tensor-core peaks of the MMA kinds and print them as JSON")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph of the layer call instead of eager C-ABI calls")
+    ap.add_argument("--h1-nvfp4", action="store_true",
+                    help="NVFP4 workload: requantise H1 per token to NVFP4 and run FC2 as NVFP4 x NVFP4")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="FC2 adds weight * Y into an fp32 accumulator (block-scaled prefill tiles); "
                          "not bitwise reproducible run to run")

@@ -41,7 +41,7 @@ class SituMoeArgs(ctypes.Structure):
             "topk_ids", "topk_weights", "w1", "w1_scale", "w1_gscale", "w2", "w2_scale",
             "w2_gscale", "gemm1_alpha", "gemm1_beta", "g1_alphas", "g1_alphas_up", "g2_alphas",
             "out", "scales_packed")] + [(n, ctypes.c_int32) for n in (
-                "fuse_combine", "activation", "apply_topk_in_fc1")] + [("tactic", ctypes.c_int32 * 2)]
+                "fuse_combine", "activation", "apply_topk_in_fc1", "h1_nvfp4")] + [("tactic", ctypes.c_int32 * 2)]
 
 
 def library_path() -> str:
@@ -320,7 +320,7 @@ class Layer:
 
     def __init__(self, wl, out: Optional[torch.Tensor] = None, x_q=None, x_scale=None,
                  pack_scales: bool = True, fuse_combine: bool = False, activation: int = 0,
-                 apply_topk_in_fc1: bool = False):
+                 apply_topk_in_fc1: bool = False, h1_nvfp4: bool = False):
         self.wl = wl
         dev = wl.x_bf16.device
         self.out = out if out is not None else torch.empty((wl.T, wl.H), dtype=torch.bfloat16,
@@ -352,6 +352,7 @@ class Layer:
         self.args.fuse_combine = 1 if fuse_combine else 0
         self.args.activation = int(activation)
         self.args.apply_topk_in_fc1 = 1 if apply_topk_in_fc1 else 0
+        self.args.h1_nvfp4 = 1 if h1_nvfp4 else 0
         # weight scales in the block-scaled GEMMs' layout, packed once per
         # weight set (as at weight-load time) when the shapes use it
         self.scales_packed = None

@@ -85,7 +85,7 @@ constexpr int kSfBlock = 512;
 // lays both columns.
 template <bool FC1, bool LO, bool NV = false, int TT = kTok>
 struct CfgW {
-  static_assert(!NV || (FC1 && !LO), "the NVFP4 tiles are FC1 on NVFP4 token rows");
+  static_assert(!NV || !LO, "the NVFP4 tiles take NVFP4 token rows");
   static_assert(TT == kTok || (NV && TT == 64), "64-row tiles are NVFP4 only");
   static constexpr int kStages = NV ? (TT > 32 ? 4 : 5) : 6;
   static constexpr int NB = LO ? 2 * TT : TT;              // MMA N: token rows (hi, lo interleaved)
@@ -206,7 +206,9 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int nk = p.K / C::kKS;
+  // K stages; the NVFP4 FC2 (K = I, a multiple of 128) may end in a half
+  // stage, whose missing half TMA fills with zeros and whose MMAs are skipped
+  const int nk = (p.K + C::kKS - 1) / C::kKS;
 
   const uint32_t sbase = saddr(smem);
   const uint32_t bar0 = sbase + C::kOffBar;
@@ -280,7 +282,8 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           // x = kk * 128: codes of the MXFP4 map, bytes of the E4M3 / packed
           // NVFP4 maps; either way one 128-byte row of the stage
           tma_load_2d(a_smem, &tmW, kk * kRowB, wrow, full(s));
-          if (FC1) tma_load_2d(a_smem + kNH1 * kRowB, &tmW, kk * kRowB, wrow + p.I, full(s));
+          // FC1: the up half; NVFP4 FC2: rows 128..255 (its map's boxes are 128 rows)
+          if (FC1 || NV) tma_load_2d(a_smem + kNH1 * kRowB, &tmW, kk * kRowB, wrow + (FC1 ? p.I : kNH1), full(s));
           tma_load_2d(sbase + C::kOffB + s * C::kBBytes, &tmX, kk * kRowB, RM * row0, full(s));
           bulk_load(sf_smem, wsb + (size_t)kk * C::kWSf * kSfBlock, C::kWSf * kSfBlock, full(s));
 #pragma unroll
@@ -342,9 +345,11 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           const uint64_t bd = sdesc(sbase + C::kOffB + s * C::kBBytes);
           // four MMAs per accumulator, 32 bytes of each row apart (K = 32
           // 8-bit containers, or K = 64 packed E2M1)
+          const int n64 = NV ? min(4, (p.K - kk * C::kKS) / 64) : 4;   // K = 64 steps in this stage
 #pragma unroll
           for (uint32_t k4 = 0; k4 < 4; ++k4) {
             const uint32_t acc = (kk | (int)k4) != 0;
+            if (NV && (int)k4 >= n64) break;
             if (NV) {
               // scale block k4 of each accumulator and of the tokens
               mma_nv(d1, ad1 + 2 * k4, bd + 2 * k4, C::kIdesc, sfw + 4 * k4, sft + 4 * k4, acc);
@@ -412,7 +417,30 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         mbar_arrive(acc_empty(buf));
       }
 
-      if constexpr (NV) {
+      if constexpr (NV && !FC1) {
+        // NVFP4 FC2 on the requantised H1: the accumulators hold sum(code *
+        // scale) products of W2 rows n1 = nt * 256 + l and n2 = n1 + 128; the
+        // expert's global scale, alpha2 and the row's H1 global scale make them
+        // Y.  Y rows leave as 128-byte segments (a warp's 32 consecutive n).
+        const float a2s = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * __ldg(p.w2_gs + e);
+        const int n1 = nt * kNH2 + l, n2 = n1 + 128;
+        for (int c0 = 0; c0 < TT; c0 += 16) {
+          tmem_ld16(t1 + c0, a1);
+          tmem_ld16(t1 + NB + c0, a2);
+          if (c0 >= nrows) continue;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = c0 + j;
+            if (t >= nrows) break;
+            const float sc = a2s * __ldg(p.xg + row0 + t);
+            float* yr = p.y_out + (size_t)(row0 + t) * p.Mtot;
+            if (n1 < p.Mtot) yr[n1] = a1[j] * sc;
+            if (n2 < p.Mtot) yr[n2] = a2[j] * sc;
+          }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(acc_empty(buf));
+      } else if constexpr (NV) {
         // NVFP4: the accumulators hold sum(code * scale) products; the
         // expert's gate / up global scale and the token's global scale make
         // them dot products.  H1 is bf16 rows [S, I] (the NVFP4 variant keeps
@@ -756,6 +784,72 @@ cudaError_t launch_pack_scales_nv(const uint8_t* w1_scale, int E_loc, int H, int
   pack_scales_nv_kernel<<<(unsigned)((n_words + 255) / 256), 256, 0, st>>>(w1_scale, H, I, n_nt, nk, n_words,
                                                                           reinterpret_cast<uint32_t*>(out));
   return cudaGetLastError();
+}
+
+// Packed NVFP4 weight scales of the FC2 tiles: per (expert, 256-row tile
+// nt, stage kk of 256 elements of I, half a (rows 0..127, 128..255), MMA k)
+// a 512-byte block laid out as pack_scales_nv's, from W2's E4M3 scales
+// [E_loc, H, I/16]; the blocks of K steps past I (a last half stage) are 0.
+__global__ void pack_scales_nv2_kernel(const uint8_t* __restrict__ ws, int H, int I, int n_nt, int nk, long n_words,
+                                       uint32_t* __restrict__ out) {
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n_words) return;
+  const int w = (int)(idx & 127);
+  const int i = w >> 2, q = w & 3;
+  long b = idx >> 7;
+  const int k = (int)(b & 3);
+  b >>= 2;
+  const int a = (int)(b & 1);
+  b >>= 1;
+  const int kk = (int)(b % nk);
+  b /= nk;
+  const int nt = (int)(b % n_nt);
+  const long e = b / n_nt;
+  const int row = nt * kNH2 + a * 128 + i + 32 * q;   // row of H
+  const int kb = 16 * kk + 4 * k;                     // first 16-element block of the MMA
+  uint32_t v = 0;
+  if (row < H && kb < I / 16) {
+    const uint8_t* src = ws + ((size_t)e * H + row) * (size_t)(I / 16) + kb;
+    v = (uint32_t)src[0] | ((uint32_t)src[1] << 8) | ((uint32_t)src[2] << 16) | ((uint32_t)src[3] << 24);
+  }
+  out[idx] = v;
+}
+
+size_t packed_scale_bytes_nv2(int E_loc, int H, int I) {
+  const size_t n_nt = (size_t)(H + kNH2 - 1) / kNH2, nk = (size_t)(I + kBKnv - 1) / kBKnv;
+  return (size_t)E_loc * n_nt * nk * 8 * kSfBlock;
+}
+
+cudaError_t launch_pack_scales_nv2(const uint8_t* w2_scale, int E_loc, int H, int I, uint8_t* out, cudaStream_t st) {
+  const int n_nt = (H + kNH2 - 1) / kNH2, nk = (I + kBKnv - 1) / kBKnv;
+  const long n_words = (long)(packed_scale_bytes_nv2(E_loc, H, I) / 4);
+  if (n_words <= 0) return cudaSuccess;
+  pack_scales_nv2_kernel<<<(unsigned)((n_words + 255) / 256), 256, 0, st>>>(w2_scale, H, I, n_nt, nk, n_words,
+                                                                           reinterpret_cast<uint32_t*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fcw_nv2(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
+                           int E_loc, int tile_rows, long max_tiles, cudaStream_t st) {
+  if (S <= 0) return cudaSuccess;
+  if (tile_rows != kTok && tile_rows != 64) return cudaErrorInvalidValue;
+  if (p.K % 128 != 0) return cudaErrorInvalidValue;
+  FcwParams q = p;
+  q.w = w;
+  CUtensorMap m[3];
+  // W2 and the H1 rows: packed E2M1 as bytes [rows, K/2], boxes of 128
+  // bytes x 128 weight rows / the tile's token rows, 128-byte swizzle (a box
+  // past the row end of a half stage reads zeros); H1 scale rows [S, K/4]
+  // bytes, boxes of 16 bytes
+  if (!make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)(p.K / 2), (uint64_t)E_loc * p.Mtot,
+                (uint64_t)(p.K / 2), kRowB, kNH1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, x, (uint64_t)(p.K / 2), (uint64_t)S, (uint64_t)(p.K / 2), kRowB,
+                (uint32_t)tile_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, xs, (uint64_t)(p.K / 4), (uint64_t)S, (uint64_t)(p.K / 4), 16,
+                (uint32_t)tile_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (tile_rows == 64) return launch_fcw_t<false, false, true, 64>(q, m, max_tiles, st);
+  return launch_fcw_t<false, false, true, kTok>(q, m, max_tiles, st);
 }
 
 cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,

@@ -61,7 +61,7 @@ cudaError_t launch_quant_mxfp8(const void* x, int T, int H, uint8_t* q, uint8_t*
 // Threads per CTA: 64 for f16 rows, 128 for fp32 rows (the Kimi-K3 row of
 // 3584 columns is then exactly 7 CTAs of 16-byte pieces either way).
 template <bool F16>
-constexpr int combine_threads() { return F16 ? 64 : 128; }
+__host__ __device__ constexpr int combine_threads() { return F16 ? 64 : 128; }
 
 template <bool F16>
 __global__ void __launch_bounds__(combine_threads<F16>())
@@ -216,6 +216,77 @@ cudaError_t launch_quant_nvfp4(const void* x, int T, int H, uint8_t* q, uint8_t*
   if (T <= 0) return cudaSuccess;
   quant_nvfp4_kernel<<<(unsigned)T, 128, 0, st>>>((const uint4*)x, H, (uint2*)q, s, gs);
   return cudaGetLastError();
+}
+
+// The bf16 H1 rows in expert order requantised to NVFP4 per row, with the
+// rule of quant_nvfp4_kernel (the NVFP4 chain's opt-in H1 requantisation).
+// One warp per row: the row maximum, then lane c takes the 64-element chunks
+// c, c + 32, ...: four E4M3 scales and 32 bytes of codes each.  The scales
+// go out as rows [S, I/16] or as one 16-byte chunk per 64 elements (its four
+// bytes first, the rest 0), the token-side layout of the NVFP4 tiles.
+__global__ void __launch_bounds__(128) requant_h1_nvfp4_kernel(const uint4* __restrict__ h, int I, long S,
+                                                               const int32_t* __restrict__ meta, uint4* __restrict__ q,
+                                                               uint8_t* __restrict__ s, float* __restrict__ gs,
+                                                               int chunked) {
+  griddep_wait();   // H1 is the predecessor's output
+  const long r = (long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= S || r >= __ldg(meta)) return;
+  const uint4* hr = h + (size_t)r * (I / 8);
+  float amax = 0.f;
+  for (int i = lane; i < I / 8; i += 32) {
+    const uint4 v = hr[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  float g = __fdiv_rn(amax, 2688.f);
+  if (!(g > 0.f)) g = 1.f;
+  if (lane == 0) gs[r] = g;
+  const float den6 = __fmul_rn(6.f, g);
+  for (int c = lane; c < I / 64; c += 32) {
+    uint32_t sw = 0;
+#pragma unroll
+    for (int b4 = 0; b4 < 4; ++b4) {   // the chunk's four 16-element blocks
+      float v[16];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint4 u = hr[8 * c + 2 * b4 + hh];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * hh + 2 * j] = bf16_lo(w[j]);
+          v[8 * hh + 2 * j + 1] = bf16_hi(w[j]);
+        }
+      }
+      float ab = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
+      const uint32_t s8 = f32x2_to_e4m3x2(__fdiv_rn(ab, den6), 0.f) & 0xFFu;
+      const float denom = __fmul_rn(e4m3_code_to_f32(s8), g);
+      uint2 out = make_uint2(0u, 0u);
+      if (denom > 0.f) {
+        float y[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] = __fdiv_rn(v[i], denom);
+        out = make_uint2(f32x8_to_e2m1x8(y), f32x8_to_e2m1x8(y + 8));
+      }
+      reinterpret_cast<uint2*>(q)[(size_t)r * (I / 16) + 4 * c + b4] = out;
+      sw |= s8 << (8 * b4);
+      if (!chunked) s[(size_t)r * (I / 16) + 4 * c + b4] = (uint8_t)s8;
+    }
+    if (chunked) reinterpret_cast<uint4*>(s)[(size_t)r * (I / 64) + c] = make_uint4(sw, 0u, 0u, 0u);
+  }
+}
+
+cudaError_t launch_requant_h1_nvfp4(const uint16_t* h, int I, long S, const int32_t* meta, uint8_t* q, uint8_t* s,
+                                    float* gs, int chunked, cudaStream_t st) {
+  if (S <= 0) return cudaSuccess;
+  if (I % 64 != 0) return cudaErrorInvalidValue;
+  return launch_pdl(requant_h1_nvfp4_kernel, dim3((unsigned)((S + 3) / 4)), dim3(128), 0, st, (const uint4*)h, I, S,
+                    meta, (uint4*)q, s, gs, chunked);
 }
 
 __global__ void __launch_bounds__(256) zero_f32_kernel(float4* __restrict__ a, long n4) {

@@ -271,6 +271,7 @@ struct FcwParams {
   uint16_t* h_bf16;              // [S, I]
   // FC2
   const float* alpha2;
+  const float* w2_gs;            // [E_loc] global scale (NVFP4 FC2 on the requantised H1)
   float* y_out;                  // fp32 [S, H]
   int* err;                      // device status word
 };
@@ -291,6 +292,23 @@ cudaError_t launch_fcw(const FcwParams& p, const uint8_t* w, const uint8_t* x, c
 cudaError_t launch_fcw_nv(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
                           int E_loc, int tile_rows, long max_tiles, cudaStream_t st);
 size_t packed_scale_bytes_nv(int E_loc, int H, int I);
+// NVFP4 FC2 on the same tiles, for an H1 requantised per row to NVFP4
+// (requant_h1_nvfp4): weights W2 on the MMA M side in 256-row tiles (two
+// M = 128 halves), H1 rows as the token side (packed E2M1 [S, K/2], scale
+// chunks [S, K/4], global scales p.xg [S]), K = I a multiple of 128 (a last
+// half stage of 128 elements is allowed); Y fp32 = alpha2 * w2_gs * xg * acc.
+// Weight scales packed by launch_pack_scales_nv2.
+cudaError_t launch_fcw_nv2(const FcwParams& p, const uint8_t* w, const uint8_t* x, const uint8_t* xs, long S,
+                           int E_loc, int tile_rows, long max_tiles, cudaStream_t st);
+size_t packed_scale_bytes_nv2(int E_loc, int H, int I);
+cudaError_t launch_pack_scales_nv2(const uint8_t* w2_scale, int E_loc, int H, int I, uint8_t* out, cudaStream_t st);
+// The bf16 H1 rows [S, I] (rows < meta[0]) quantised per row to NVFP4 with
+// the per-token rule of quant_nvfp4: packed E2M1 [S, I/2], global scales
+// [S], and the E4M3 scales either as rows [S, I/16] (chunked = 0) or as one
+// 16-byte chunk per 64 elements, its four bytes first, [S, I/4] (chunked =
+// 1, the token-side scale layout of the NVFP4 tiles).  I a multiple of 64.
+cudaError_t launch_requant_h1_nvfp4(const uint16_t* h, int I, long S, const int32_t* meta, uint8_t* q, uint8_t* s,
+                                    float* gs, int chunked, cudaStream_t st);
 // NVFP4 FC2 on the decode tiles: the weights expanded to exact bf16 (code x
 // E4M3 block scale) in shared memory by converter warps, times the bf16 H1
 // rows [S, K] on tcgen05.mma.kind::f16; 256 rows of H per weight tile, up to

@@ -25,7 +25,7 @@ bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
   size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
-  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, t2off, t2info, total;
+  size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, hq, hqs, hg, t2off, t2info, total;
 };
 
 // Decode-like routings (about six or fewer rows per expert) take the
@@ -100,15 +100,24 @@ size_t packed_fc1d_bytes(const situ_moe_args* a) {
 size_t packed_fc2d_bytes(const situ_moe_args* a) {
   return packed_scale_bytes(a->num_local_experts, a->H, a->I, false, fcw_n_rows(false));
 }
-// NVFP4: one packing, the FC1 decode tiles
+// NVFP4: two packings, the FC1 tiles and the FC2 tiles of the requantised
+// H1 (h1_nvfp4)
+size_t packed_nv1_bytes(const situ_moe_args* a) { return packed_scale_bytes_nv(a->num_local_experts, a->H, a->I); }
 size_t packed_total_bytes(const situ_moe_args* a) {
-  if (a->weight_dtype == SITU_W_NVFP4) return packed_scale_bytes_nv(a->num_local_experts, a->H, a->I);
+  if (a->weight_dtype == SITU_W_NVFP4)
+    return packed_nv1_bytes(a) + packed_scale_bytes_nv2(a->num_local_experts, a->H, a->I);
   return packed_fc1_bytes(a) + packed_fc2_bytes(a) + packed_fc1d_bytes(a) + packed_fc2d_bytes(a);
 }
-// the four packings into one buffer (layout above)
-cudaError_t pack_all_scales(const situ_moe_args* a, uint8_t* dst, cudaStream_t st) {
+// the packings into one buffer (layout above); fc2_nv: the NVFP4 FC2 one
+// too (always for the caller's buffer; inside a call only when H1 is
+// requantised)
+cudaError_t pack_all_scales(const situ_moe_args* a, uint8_t* dst, cudaStream_t st, bool fc2_nv = true) {
   const int E = a->num_local_experts;
-  if (a->weight_dtype == SITU_W_NVFP4) return launch_pack_scales_nv(a->w1_scale, E, a->H, a->I, dst, st);
+  if (a->weight_dtype == SITU_W_NVFP4) {
+    cudaError_t e = launch_pack_scales_nv(a->w1_scale, E, a->H, a->I, dst, st);
+    if (e == cudaSuccess && fc2_nv) e = launch_pack_scales_nv2(a->w2_scale, E, a->H, a->I, dst + packed_nv1_bytes(a), st);
+    return e;
+  }
   cudaError_t e = launch_pack_scales(a->w1_scale, E, a->H, a->I, true, dst, st);
   dst += packed_fc1_bytes(a);
   if (e == cudaSuccess) e = launch_pack_scales(a->w2_scale, E, a->H, a->I, false, dst, st);
@@ -160,6 +169,12 @@ Layout make_layout(const situ_moe_args* a) {
   L.wxs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->H) : wnv ? S * (size_t)(a->H / 4) : 0);
   L.whs = take(w ? 2 * S * (size_t)fcw_scale_stride(a->I) : 0);
   L.xg = take(wnv ? 4 * S : 0);
+  // H1 requantised to NVFP4: packed codes, scales (chunks of 16 bytes per 64
+  // elements, or rows of I/16 bytes), global scales
+  const bool h1nv = a->h1_nvfp4 != 0;
+  L.hq = take(h1nv ? S * (size_t)(a->I / 2) : 0);
+  L.hqs = take(h1nv ? S * (size_t)(a->I / 4) : 0);
+  L.hg = take(h1nv ? 4 * S : 0);
   // NVFP4 FC2 on 128-token tiles: its own tile table
   const bool wide2 = nv_wide_fc2(a);
   L.t2off = take(wide2 ? 4 * (E + 1) : 0);
@@ -188,6 +203,9 @@ situ_status validate(const situ_moe_args* a) {
   const bool nv = a->act_dtype == SITU_ACT_NVFP4 && a->weight_dtype == SITU_W_NVFP4;
   if (!(w4a16 || w4a8 || nv)) return SITU_ERR_UNSUPPORTED;
   if (a->activation != SITU_ACT_FN_SITU && a->activation != SITU_ACT_FN_SWIGLU_BIAS) return SITU_ERR_UNSUPPORTED;
+  // the requantised NVFP4 H1 is an option of the NVFP4 chain on the shapes of
+  // its tiles (H a multiple of 256, I of 128), whichever routing size
+  if (a->h1_nvfp4 != 0 && (a->h1_nvfp4 != 1 || !nv || !nv_tile_shapes(a))) return SITU_ERR_UNSUPPORTED;
   // one configuration per shape: -1 (auto) or 0 (the first valid one) select it
   for (int g = 0; g < 2; ++g)
     if (a->tactic[g] != -1 && a->tactic[g] != 0) return SITU_ERR_UNSUPPORTED;
@@ -336,7 +354,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
   cudaError_t err = launch_permute(a->topk_ids, a->T, a->top_k, a->num_local_experts,
                                    a->local_expert_offset, tile_n, counts, offsets, tile_offsets,
                                    tile_info, psrc, s2r, meta, (int32_t*)(ws + L.blk), st);
-  if (err == cudaSuccess && fcwnv && nv_wide_fc2(a))
+  const bool h1nv = a->h1_nvfp4 != 0;
+  if (err == cudaSuccess && fcwnv && nv_wide_fc2(a) && !h1nv)
     err = launch_tile_table(offsets, a->num_local_experts, kNvFc2WideTile, (int32_t*)(ws + L.t2off),
                             (int2*)(ws + L.t2info), st);
   if (err != cudaSuccess) return SITU_ERR_CUDA;
@@ -348,7 +367,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
                            const uint8_t*& wsp4) -> cudaError_t {
     wsp1 = (const uint8_t*)a->scales_packed;
     if (!wsp1) {
-      cudaError_t e2 = pack_all_scales(a, ws + L.wsp, st);
+      cudaError_t e2 = pack_all_scales(a, ws + L.wsp, st, h1nv);
       if (e2 != cudaSuccess) return e2;
       wsp1 = ws + L.wsp;
     }
@@ -467,6 +486,33 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if ((err = launch_fcw_nv(w, a->w1, g.x, g.xs, S, a->num_local_experts, tile_n, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(3);
+    if (h1nv) {
+      // H1 requantised per row to NVFP4 (scale chunks of the tiles' layout),
+      // then FC2 as NVFP4 x NVFP4 on the same token tiles (kind::mxf4nvf4)
+      uint8_t* hq = ws + L.hq;
+      uint8_t* hqs = ws + L.hqs;
+      float* hg = (float*)(ws + L.hg);
+      if ((err = launch_requant_h1_nvfp4(h1, a->I, S, meta, hq, hqs, hg, 1, st)) != cudaSuccess) return SITU_ERR_CUDA;
+      FcwParams w2;
+      std::memset(&w2, 0, sizeof(w2));
+      w2.offsets = offsets;
+      w2.tile_offsets = tile_offsets;
+      w2.tile_info = tile_info;
+      w2.E_loc = a->num_local_experts;
+      w2.I = a->I;
+      w2.err = meta + 2;
+      w2.wsp = wsp1 + packed_nv1_bytes(a);
+      w2.Mtot = a->H;
+      w2.K = a->I;
+      w2.n_ntiles = (a->H + fcw_n_rows(false) - 1) / fcw_n_rows(false);
+      w2.alpha2 = a->g2_alphas;
+      w2.w2_gs = a->w2_gscale;
+      w2.xg = hg;
+      w2.y_out = y;
+      if ((err = launch_fcw_nv2(w2, a->w2, hq, hqs, S, a->num_local_experts, tile_n, max_tiles, st)) != cudaSuccess)
+        return SITU_ERR_CUDA;
+      mark(4);
+    } else {
     FcvParams v;
     std::memset(&v, 0, sizeof(v));
     v.Mtot = a->H;
@@ -493,6 +539,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if ((err = launch_fcv(v, h1, S, a->num_local_experts, fc2_tile, fc2_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(4);
+    }
   } else if (decode_path) {
     // 8-token tiles: rows are converted once to f16 block rows, then FC1
     // (+SiTU, writing H1 as f16 block rows) and FC2
@@ -684,12 +731,23 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     if ((err = launch_fcp(f, g16.x16, S, pad128(a->H), a->w1, a->num_local_experts, true, nv, max_tiles, st)) !=
         cudaSuccess)
       return SITU_ERR_CUDA;
-    // H1 (bf16, expert order) to f16 rows with one scale per row
+    // H1 (bf16, expert order) to f16 rows with one scale per row; with the
+    // NVFP4 H1 option, requantised to NVFP4 first and converted exactly
+    // (code x block scale in f16, the row's global scale as the row scale)
     Gather16Params h16;
     std::memset(&h16, 0, sizeof(h16));
     h16.act = SITU_ACT_BF16;
     h16.row_scale = 1;
     h16.x_bf16 = h1;
+    if (h1nv) {
+      if ((err = launch_requant_h1_nvfp4(h1, a->I, S, meta, ws + L.hq, ws + L.hqs, (float*)(ws + L.hg), 0, st)) !=
+          cudaSuccess)
+        return SITU_ERR_CUDA;
+      h16.act = SITU_ACT_NVFP4;
+      h16.x_q = ws + L.hq;
+      h16.x_s = ws + L.hqs;
+      h16.x_gs = (const float*)(ws + L.hg);
+    }
     h16.permuted_src = nullptr;
     h16.meta = meta;
     h16.K = a->I;
@@ -767,11 +825,13 @@ int32_t situ_moe_forward_launches(const situ_moe_args* a) {
   const int perm = permute_launches(a->T, a->top_k, a->num_local_experts);
   const int pack = a->scales_packed ? 0 : 4;
   if (fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
-  if (fcw_nv_shapes(a)) return perm + (nv_wide_fc2(a) ? 1 : 0) + (a->scales_packed ? 0 : 1) + 4;
+  const int h1nv = a->h1_nvfp4 != 0 ? 1 : 0;   // + the requantisation (+ its scale packing)
+  if (fcw_nv_shapes(a))
+    return perm + (nv_wide_fc2(a) && !h1nv ? 1 : 0) + (a->scales_packed ? 0 : 1 + h1nv) + 4 + h1nv;
   if (takes_decode_path(a)) return perm + 4;
   if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2))
     return perm + pack + 4 + (a->fuse_combine ? 1 : 0);   // + zeroing the accumulator
-  return perm + 5;
+  return perm + 5 + h1nv;
 }
 
 situ_status situ_moe_device_status(const situ_moe_args* a, const void* workspace, void* stream,

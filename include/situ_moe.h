@@ -317,6 +317,15 @@ typedef struct situ_moe_args {
                                      epilogue, before H1 is rounded for FC2, and the
                                      un-permute sum is unweighted (the MegaMoE option of PR
                                      #17865); 0: the weight is applied in the sum */
+  int32_t h1_nvfp4;               /* NVFP4 only.  0 (default): H1 stays bf16 and FC2 multiplies
+                                     it with the NVFP4 weights.  1: H1, rounded to bf16, is
+                                     requantised per token to NVFP4 with the rule of
+                                     situ_moe_quant_nvfp4 (the per-token NVFP4 activation
+                                     scaling of the FlashInfer 0.6.18 MoE-LoRA AOT notes, as an
+                                     unfused quantisation step), and FC2 runs NVFP4 x NVFP4
+                                     (kind::mxf4nvf4 on the NVFP4 tiles).  Needs H a
+                                     multiple of 256 and I of 128; other shapes and format
+                                     pairs: SITU_ERR_UNSUPPORTED. */
   int32_t tactic[2];              /* kernel configuration of FC1 / FC2, as the TokenSpeed SiTU
                                      runtime API's `tactic` pair: -1 = auto, the first valid
                                      configuration.  This library has one configuration per
@@ -432,10 +441,11 @@ int32_t situ_moe_forward_launches(const situ_moe_args* args);
  * prefill tiles, and the decode tiles of bf16 and MXFP8 activations): per
  * (local expert, weight tile, 128 elements of K) the UE8M0 bytes of the
  * tile's rows; the buffer holds four such packings (the prefill and the
- * decode tiles of FC1 and of FC2).  NVFP4 (the decode tiles of NVFP4
- * activations, FC1 only): per (local expert, 128 gate + 128 up rows, 256
- * elements of K) eight blocks of the E4M3 bytes, one per K = 64 MMA and W1
- * half.  Packing depends only on w1_scale, w2_scale, num_local_experts, H
+ * decode tiles of FC1 and of FC2).  NVFP4 (the tiles of NVFP4
+ * activations): per (local expert, 128 gate + 128 up rows, 256 elements of
+ * K) eight blocks of the E4M3 bytes, one per K = 64 MMA and W1 half; then
+ * the same for W2 in tiles of 256 rows of H (two halves of 128) and stages
+ * of 256 elements of I (the FC2 of a requantised NVFP4 H1, h1_nvfp4).  Packing depends only on w1_scale, w2_scale, num_local_experts, H
  * and I, so it is done once per weight set; pass the result as
  * args->scales_packed.  Without it the forward packs into its workspace on
  * every call (same result, about 25% more HBM traffic for a decode step).

@@ -56,7 +56,7 @@ class _Args(ctypes.Structure):
         ("w2", ctypes.c_void_p), ("w2s", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p),
         ("beta", ctypes.c_void_p), ("beta_lin", ctypes.c_void_p),
         ("alpha_g", ctypes.c_void_p), ("alpha_u", ctypes.c_void_p), ("alpha2", ctypes.c_void_p),
-        ("activation", ctypes.c_int), ("topk_in_fc1", ctypes.c_int),
+        ("activation", ctypes.c_int), ("topk_in_fc1", ctypes.c_int), ("h1_nvfp4", ctypes.c_int),
     ]
 
 
@@ -218,13 +218,15 @@ def moe_forward(*, T, H, I, num_experts_total, num_local_experts, local_expert_o
                 gemm1_beta, hidden_states=None, hidden_states_q=None, hidden_states_scale=None,
                 hidden_states_gscale=None, w1_gscale=None, w2_gscale=None, g1_alphas=None,
                 g1_alphas_up=None, g2_alphas=None, tokens=None, activation=0,
-                apply_topk_in_fc1=0) -> np.ndarray:
+                apply_topk_in_fc1=0, h1_nvfp4=0) -> np.ndarray:
     """Reference layer output (fp64 [n_tok, H]) for ``tokens`` (all T if None).
 
     activation: ACT_FN_SITU (gemm1_alpha / gemm1_beta = beta / linear beta)
     or ACT_FN_SWIGLU_BIAS (alpha / beta); apply_topk_in_fc1: the routing
     weight scales H1 (before its rounding) and the un-permute sum is
-    unweighted.
+    unweighted; h1_nvfp4 (NVFP4 weights): H1, rounded to bf16, is requantised
+    per token to NVFP4 (the quant_nvfp4 rule) and FC2 takes its exact
+    dequantisation.
 
     hidden_states: uint16 bf16 bits [T,H] (act=ACT_BF16);
     hidden_states_q / hidden_states_scale: E4M3 [T,H] + UE8M0 [T,H/32]
@@ -259,6 +261,7 @@ def moe_forward(*, T, H, I, num_experts_total, num_local_experts, local_expert_o
     args.alpha2 = c(g2_alphas, np.float32)
     args.activation = int(activation)
     args.topk_in_fc1 = int(apply_topk_in_fc1)
+    args.h1_nvfp4 = int(h1_nvfp4)
     if tokens is None:
         n_tok, tok_ptr = T, None
     else:

@@ -238,18 +238,16 @@ typedef struct { const uint16_t* x; int H; uint8_t* q; uint8_t* s; float* gs; } 
  *   s      = E4M3(amax_block16 / (6 * gs))   (round to nearest even)
  *   denom  = value(s) * gs
  *   code_i = E2M1(x_i / denom), or 0 when denom is 0. */
-static void nvq_row(void* p, long t) {
-  nvq_ctx* c = (nvq_ctx*)p;
-  const uint16_t* xr = c->x + (size_t)t * c->H;
+static void nvq_one_row(const uint16_t* xr, int H, uint8_t* q, uint8_t* s, float* gs_out) {
   float amax = 0.0f;
-  for (int i = 0; i < c->H; ++i) {
+  for (int i = 0; i < H; ++i) {
     float a = fabsf((float)oracle_bf16_value(xr[i]));
     if (a > amax) amax = a;
   }
   float gs = amax / 2688.0f;
   if (!(gs > 0.0f)) gs = 1.0f;
-  c->gs[t] = gs;
-  for (int b = 0; b < c->H / 16; ++b) {
+  *gs_out = gs;
+  for (int b = 0; b < H / 16; ++b) {
     float ab = 0.0f;
     for (int i = 0; i < 16; ++i) {
       float a = fabsf((float)oracle_bf16_value(xr[b * 16 + i]));
@@ -259,7 +257,7 @@ static void nvq_row(void* p, long t) {
     float qv = ab / den6;
     unsigned s8 = oracle_e4m3_encode((double)qv);
     float denom = (float)oracle_e4m3_value(s8) * gs;
-    c->s[(size_t)t * (c->H / 16) + b] = (uint8_t)s8;
+    s[b] = (uint8_t)s8;
     for (int i = 0; i < 16; i += 2) {
       unsigned c0 = 0, c1 = 0;
       if (denom > 0.0f) {
@@ -268,9 +266,15 @@ static void nvq_row(void* p, long t) {
         c0 = oracle_e2m1_encode((double)y0);
         c1 = oracle_e2m1_encode((double)y1);
       }
-      c->q[(size_t)t * (c->H / 2) + (b * 16 + i) / 2] = (uint8_t)(c0 | (c1 << 4));
+      q[(b * 16 + i) / 2] = (uint8_t)(c0 | (c1 << 4));
     }
   }
+}
+
+static void nvq_row(void* p, long t) {
+  nvq_ctx* c = (nvq_ctx*)p;
+  nvq_one_row(c->x + (size_t)t * c->H, c->H, c->q + (size_t)t * (c->H / 2), c->s + (size_t)t * (c->H / 16),
+              c->gs + t);
 }
 
 /* x: bf16 [T,H]; q: packed E2M1 [T,H/2] (element 2i in the low nibble);
@@ -420,6 +424,7 @@ typedef struct {
   const float* alpha2;      /* g2_alphas    [E_loc] or NULL (1) */
   int activation;           /* ACT_FN_SITU (beta, beta_lin) or ACT_FN_SWIGLU_BIAS (alpha, beta) */
   int topk_in_fc1;          /* 1: the routing weight scales H1 instead of the FC2 output */
+  int h1_nvfp4;             /* 1 (NVFP4 weights): H1 requantised per token to NVFP4 before FC2 */
 } oracle_args;
 
 /* Dequantise one packed FP4 matrix row (n elements) with its block scales:
@@ -510,7 +515,22 @@ static void run_expert(void* p, long e) {
       hf[i] = (float)h_act;
     }
     /* The FC1 output as FC2 consumes it. */
-    if (a->act == ACT_MXFP8) {
+    if (nv && a->h1_nvfp4) {
+      /* the NVFP4 chain with H1 requantised: H1 rounded to bf16, then the
+       * per-token NVFP4 quantisation of that row (the rule of
+       * oracle_quant_nvfp4) and its exact dequantisation code * scale * gs */
+      uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+      uint8_t* q = (uint8_t*)malloc((size_t)I / 2);
+      uint8_t* sc = (uint8_t*)malloc((size_t)I / 16);
+      float gs = 1.0f;
+      for (int i = 0; i < I; ++i) hb[i] = oracle_f32_to_bf16(hf[i]);
+      nvq_one_row(hb, I, q, sc, &gs);
+      for (int i = 0; i < I; ++i) {
+        unsigned code = (i & 1) ? (q[i / 2] >> 4) : (q[i / 2] & 15u);
+        h[i] = oracle_e2m1_value(code) * oracle_e4m3_value(sc[i / 16]) * (double)gs;
+      }
+      free(hb); free(q); free(sc);
+    } else if (a->act == ACT_MXFP8) {
       uint8_t q[32];
       for (int b = 0; b < I / 32; ++b) {
         double sc = oracle_ue8m0_value(mxfp8_block(hf + b * 32, 32, q));

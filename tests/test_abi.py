@@ -102,10 +102,13 @@ def test_packed_scales_size_and_errors(lib):
     n = lib.situ_moe_packed_scales_size(ctypes.byref(ok))
     assert n > 0
     assert lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=256, I=96))) == 0   # I % 128
-    # NVFP4: one packing, for the FC1 decode tiles (H a multiple of 256, I of 128):
-    # E_loc x I/128 weight tiles x H/256 stages x 4 KB
+    # NVFP4: two packings (H a multiple of 256, I of 128): the FC1 tiles, E_loc x
+    # I/128 weight tiles x H/256 stages x 4 KB, then the FC2 tiles of a requantised
+    # H1, E_loc x H/256 weight tiles x ceil(I/256) stages x 4 KB
     nv = lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=512, I=256, act_dtype=2, weight_dtype=1)))
-    assert nv == 8 * 2 * 2 * 4096
+    assert nv == 8 * 2 * 2 * 4096 + 8 * 2 * 1 * 4096
+    nv3 = lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=512, I=384, act_dtype=2, weight_dtype=1)))
+    assert nv3 == 8 * 3 * 2 * 4096 + 8 * 2 * 2 * 4096   # a half last stage of I counts whole
     assert lib.situ_moe_packed_scales_size(ctypes.byref(_args(H=384, I=128, act_dtype=2, weight_dtype=1))) == 0
     assert lib.situ_moe_packed_scales_size(None) == 0
     buf = ctypes.c_void_p(256)
@@ -291,6 +294,42 @@ def test_forward_tactic_field(lib):
         a = _args()
         a.tactic[0], a.tactic[1] = t
         assert _fwd(lib, a) == 3
+
+
+def _nv_args(**over):
+    a = _args(**{**dict(H=256, I=128, act_dtype=2, weight_dtype=1), **over})
+    for f in ("hidden_states_q", "hidden_states_scale", "hidden_states_gscale", "w1_gscale", "w2_gscale"):
+        setattr(a, f, 0x1000)
+    return a
+
+
+def test_h1_nvfp4_option(lib):
+    """The requantised NVFP4 H1 belongs to the NVFP4 chain on its tile shapes:
+    one more launch (the requantisation), plus the FC2 scale packing when the
+    call packs its own scales; the 128-token FC2 tile table is not needed."""
+    n = lambda a: lib.situ_moe_forward_launches(ctypes.byref(a))
+    a = _nv_args()
+    a.h1_nvfp4 = 1
+    assert n(a) == 8                      # permute, 2 packings, gather, FC1, requant, FC2, combine
+    a.scales_packed = 0x4000
+    assert n(a) == 6
+    wide = _nv_args(T=300, num_experts_total=8, num_local_experts=8, top_k=2)
+    wide.scales_packed = 0x4000
+    assert n(wide) == 6                   # 64-token tiles, 75 rows per expert: the second table
+    wide.h1_nvfp4 = 1                     # (fcv's 128-token tiles) is left out
+    assert n(wide) == 6
+    f16 = _nv_args(T=2056, num_experts_total=8, num_local_experts=8, top_k=2)
+    f16.h1_nvfp4 = 1
+    assert n(f16) == 9                    # f16 prefill tiles: + the requantisation
+    for bad in (_args(), _args(H=256, I=128)):   # MXFP4 pairs
+        bad.h1_nvfp4 = 1
+        assert _fwd(lib, bad) == 3
+    odd = _nv_args(H=384)                 # H not a multiple of 256
+    odd.h1_nvfp4 = 1
+    assert _fwd(lib, odd) == 3
+    two = _nv_args()
+    two.h1_nvfp4 = 2
+    assert _fwd(lib, two) == 3
 
 
 def test_forward_rejects_unknown_activation(lib):

@@ -576,3 +576,53 @@ def test_route_topk_feeds_the_layer():
     kw = W.oracle_kwargs(wl)
     kw["topk_ids"], kw["topk_weights"] = rid, rw
     assert_parity(out, oracle.moe_forward(**kw), "routed from logits, decode")
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 chain with H1 requantised per token (opt-in, h1_nvfp4): FC2 as NVFP4 x
+# NVFP4 on kind::mxf4nvf4 on the NVFP4 tiles, or through the f16 prefill tiles
+# ---------------------------------------------------------------------------
+
+_H1NV_SHAPES = [
+    # 16-token tiles: a hot expert over six tiles, one FC2 weight tile (H = 256)
+    (dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4), 3),
+    # I = 384 (Kimi-K3): FC2 in one whole and one half stage of 256 elements
+    (dict(T=96, H=512, I=384, E_total=64, E_loc=64, off=0, K=4), None),
+    # 64-token tiles (25 rows per expert), a hot expert over four of them
+    (dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2), 5),
+    # a filtered shard on 64-token tiles, two FC2 weight tiles
+    (dict(T=300, H=512, I=256, E_total=16, E_loc=8, off=4, K=2), None),
+    # above 512 rows per expert: the f16 prefill tiles take the requantised rows
+    (dict(T=2100, H=256, I=128, E_total=4, E_loc=4, off=0, K=2), None),
+]
+
+
+@pytest.mark.parametrize("over,hot", _H1NV_SHAPES)
+def test_h1_nvfp4_chain(over, hot):
+    wl = W.make("tiny", device="cuda", act=W.ACT_NVFP4, wt=W.W_NVFP4, params="k3_random", **over)
+    if hot is not None:
+        wl.topk_ids[:, 0] = hot
+    for pack in (True, False):
+        layer = binding.Layer(wl, pack_scales=pack, h1_nvfp4=True)
+        out = layer()
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        toks = token_subset(wl.T, 256, seed=7)
+        got = out.float().cpu().numpy()
+        assert_parity(got if toks is None else got[toks], oracle_out(wl, toks, h1_nvfp4=1), f"h1 nvfp4 {over}")
+        if pack:
+            first = got
+        else:
+            assert np.array_equal(got, first)
+
+
+@pytest.mark.parametrize("T", [1, 256, 2048])
+def test_h1_nvfp4_on_the_nvfp4_workload(T):
+    wl = W.make("nvfp4", device="cuda", T=T)
+    layer = binding.Layer(wl, h1_nvfp4=True)
+    out = layer().float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    toks = token_subset(T, 128, seed=T)
+    ref = oracle_out(wl, toks, h1_nvfp4=1)
+    assert_parity(out if toks is None else out[toks], ref, f"NVFP4 T={T}, H1 requantised")

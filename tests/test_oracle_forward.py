@@ -143,7 +143,17 @@ def _swiglu_bias_np(g, u, alpha, beta):
     return g * sigmoid(g * alpha) * (u + beta)
 
 
-def brute_force(kw, alpha_power=1, activation=0, topk_in_fc1=0):
+def _nvfp4_round_trip(h_bf16_values):
+    """H1 (bf16 values, one row) requantised per token to NVFP4 with the
+    oracle's own quantiser (pinned in test_oracle_formats against an
+    independent torch formulation), dequantised exactly here."""
+    bits = torch.from_numpy(np.ascontiguousarray(h_bf16_values, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)[None, :]
+    q, s, g = oracle.quant_nvfp4(bits)
+    return _dq_fp4(q, s, True)[0] * float(g[0])
+
+
+def brute_force(kw, alpha_power=1, activation=0, topk_in_fc1=0, h1_nvfp4=0):
     T, H, I, K = kw["T"], kw["H"], kw["I"], kw["top_k"]
     off, E_loc = kw["local_expert_offset"], kw["num_local_experts"]
     act, nv = kw["act"], kw["wt"] == W.W_NVFP4
@@ -181,6 +191,8 @@ def brute_force(kw, alpha_power=1, activation=0, topk_in_fc1=0):
                 a = a * w                  # the routing weight scales H1 before its rounding
             a = a.astype(np.float32)
             h = _mxfp8_round_trip(a) if act == W.ACT_MXFP8 else _bf16(a)
+            if nv and h1_nvfp4:
+                h = _nvfp4_round_trip(h)
             y = a2[e] * g2 * (W2 @ h)
             out[t] += (1.0 if topk_in_fc1 else w) * y
     return out
@@ -355,3 +367,51 @@ def test_topk_in_fc1_differs_only_by_rounding_position():
     assert np.max(np.abs(a - b)) <= 2e-2 * rms
     assert np.sqrt(np.mean((a - b) ** 2)) <= 2.0 ** -8 * rms
     assert not np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 chain with H1 requantised per token (FlashInfer 0.6.18 MoE-LoRA AOT
+# release notes, "Summary": per-token NVFP4 activation scaling; the prior art
+# quantises the activation unfused)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_h1_nvfp4_matches_brute_force(seed):
+    wl = _small(W.ACT_NVFP4, W.W_NVFP4, seed, I=64)
+    kw = _kwargs(wl)
+    _close(oracle.moe_forward(**kw, h1_nvfp4=1), brute_force(kw, h1_nvfp4=1))
+
+
+def test_h1_nvfp4_is_the_bf16_chain_within_the_nvfp4_error():
+    """Requantising H1 moves each FC2 input by at most half an E2M1 step of
+    its block (the quantiser's rounding), so the output stays within the
+    bound that error implies, and it does move (the option is not a no-op)."""
+    wl = _small(W.ACT_NVFP4, W.W_NVFP4, 4, T=16, I=64, H=128)
+    kw = _kwargs(wl)
+    ref = oracle.moe_forward(**kw)
+    got = oracle.moe_forward(**kw, h1_nvfp4=1)
+    assert not np.array_equal(ref, got)
+    rel = np.sqrt(np.mean((got - ref) ** 2)) / np.sqrt(np.mean(ref ** 2))
+    # E2M1 has one mantissa bit: relative rounding error up to 1/3 per
+    # element at the block maximum's binade, smaller on average
+    assert 1e-3 < rel < 0.25, rel
+
+
+def test_h1_nvfp4_on_an_exactly_representable_h1_is_the_bf16_chain():
+    """When every H1 value is an E2M1 code times a power of two that the
+    quantiser reproduces, requantising changes nothing: with SwiGLU (both
+    caps off), unit alphas and a W1 whose up half is zero except one row,
+    H1 has one non-zero element per row, which NVFP4 holds exactly (it is
+    its block's and row's maximum: code 6 under the scale 448 * gs)."""
+    wl = _small(W.ACT_NVFP4, W.W_NVFP4, 5, T=6, I=32, H=64, K=1, E_total=4, E_loc=4, off=0)
+    kw = _kwargs(wl)
+    kw["gemm1_alpha"] = np.zeros_like(kw["gemm1_alpha"])
+    kw["gemm1_beta"] = np.zeros_like(kw["gemm1_beta"])
+    w1 = kw["w1"].copy()
+    w1[:, 32 + 1:, :] = 0            # up rows other than row 0 give u = 0
+    kw["w1"] = w1
+    ref = oracle.moe_forward(**kw)
+    got = oracle.moe_forward(**kw, h1_nvfp4=1)
+    # one non-zero h per row: its NVFP4 round trip is the bf16 value times
+    # (6 * E4M3(448) * gs) / (amax) = 1 up to the fp32 steps of the rule
+    _close(got, ref, rel=1e-6)

@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
                                                  ctypes.POINTER(ctypes.c_int32)]
             l.situ_moe_wait_selftest.restype = ctypes.c_int
             l.situ_moe_wait_selftest.argtypes = [vp, vp]
+            l.situ_moe_forward_wait_test.restype = ctypes.c_int
+            l.situ_moe_forward_wait_test.argtypes = [ctypes.POINTER(SituMoeArgs), vp, sz, vp, i32, i32]
             l.situ_tc_peak.restype = ctypes.c_int
             l.situ_tc_peak.argtypes = [i32, i32, vp, ctypes.POINTER(ctypes.c_double), vp]
             _lib = l
@@ -272,6 +274,16 @@ def situ_moe_wait_selftest(status: torch.Tensor, stream=None) -> None:
     wait limit the kernel records SITU_SELFTEST_WAIT_CODE in ``status`` (an
     int32 tensor on the device, zeroed by the caller) and returns."""
     _check("situ_moe_wait_selftest", lib().situ_moe_wait_selftest(_p(status), _stream(stream)))
+
+
+def situ_moe_forward_wait_test(args: SituMoeArgs, workspace: torch.Tensor, skip_stage: int, wait_us: int,
+                               stream=None) -> None:
+    """situ_moe_forward whose FC1 (block-scaled decode tiles) leaves K stage
+    ``skip_stage`` of CTA 0 unissued, with every wait limited to ``wait_us``:
+    the failure path on purpose (read the outcome with situ_moe_device_status)."""
+    _check("situ_moe_forward_wait_test", lib().situ_moe_forward_wait_test(
+        ctypes.byref(args), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
+        int(skip_stage), int(wait_us)))
 
 
 SITU_TC_MXF8F6F4, SITU_TC_MXF4NVF4, SITU_TC_BF16 = 0, 1, 2

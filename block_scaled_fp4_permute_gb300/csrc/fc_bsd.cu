@@ -171,10 +171,10 @@ __device__ __forceinline__ bool bar_red_and(int id, int n, bool v) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void drain_wait(uint32_t a, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint32_t a, uint32_t parity, unsigned long long limit = kWaitNs) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try(a, parity))
-    if (globaltimer() - t0 > kWaitNs) return;
+    if (globaltimer() - t0 > limit) return;
 }
 
 }  // namespace
@@ -209,6 +209,10 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   // K stages; the NVFP4 FC2 (K = I, a multiple of 128) may end in a half
   // stage, whose missing half TMA fills with zeros and whose MMAs are skipped
   const int nk = (p.K + C::kKS - 1) / C::kKS;
+  // every wait's limit (a test may shorten it), and the one stage a test may
+  // leave unissued in CTA 0 (-1: none) so that the waits for it run out
+  const unsigned long long lim = p.wait_ns ? p.wait_ns : kWaitNs;
+  const long skip = (blockIdx.x == 0 && p.skip_stage1 > 0) ? (long)p.skip_stage1 - 1 : -1;
 
   const uint32_t sbase = saddr(smem);
   const uint32_t bar0 = sbase + C::kOffBar;
@@ -271,11 +275,11 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       for (int kk = 0; kk < nk; ++kk, ++it) {
         const int s = (int)(it % kStages);
         const long r = it / kStages;
-        if (r > 0 && !mbar_wait_warp(empty(s), (uint32_t)((r - 1) & 1), p.err, 41)) {
+        if (r > 0 && !mbar_wait_warp(empty(s), (uint32_t)((r - 1) & 1), p.err, 41, lim)) {
           ok = false;
           break;
         }
-        if (leader) {
+        if (leader && it != skip) {
           mbar_expect_tx(full(s), C::kTx);
           const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
@@ -296,7 +300,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
     }
     if (leader)
       for (long j = it - 1; j >= 0 && j >= it - kStages; --j)
-        drain_wait(full((int)(j % kStages)), (uint32_t)((j / kStages) & 1));
+        drain_wait(full((int)(j % kStages)), (uint32_t)((j / kStages) & 1), lim);
     __syncwarp();
   } else if (warp == 5) {
     // ---------------- scale copies + MMA issuer ----------------
@@ -307,13 +311,13 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
     bool ok = true;
     for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
       const int buf = li & 1, use = li >> 1;
-      if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 42)) break;
+      if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 42, lim)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t d1 = tmem + (uint32_t)(buf * C::kAccStride);
       const uint32_t d2 = d1 + NB;
       for (int kk = 0; kk < nk; ++kk, ++it) {
         const int s = (int)(it % kStages);
-        if (!mbar_wait_warp(full(s), (uint32_t)((it / kStages) & 1), p.err, 43)) {
+        if (!mbar_wait_warp(full(s), (uint32_t)((it / kStages) & 1), p.err, 43, lim)) {
           ok = false;
           break;
         }
@@ -371,7 +375,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
     }
     if (leader) {
       mma_commit(drain);
-      drain_wait(drain, 0);
+      drain_wait(drain, 0, lim);
     }
     __syncwarp();
   } else {
@@ -388,7 +392,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int nrows = min(TT, __ldg(p.offsets + e + 1) - row0);
       // every epilogue thread takes the same decision (the waits are
       // bounded, so all 128 reach the reduction)
-      if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 46))) break;
+      if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 46, lim))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * C::kAccStride);
       float a1[kTok], a2[kTok];

@@ -274,6 +274,12 @@ struct FcwParams {
   const float* w2_gs;            // [E_loc] global scale (NVFP4 FC2 on the requantised H1)
   float* y_out;                  // fp32 [S, H]
   int* err;                      // device status word
+  // failure-path test (situ_moe_forward_wait_test): every wait's limit in ns
+  // (0: the default 200 ms), and 1 + the K stage (the producer's running
+  // count) that CTA 0 leaves unissued (0: none), so that a zeroed struct
+  // injects nothing
+  unsigned long long wait_ns;
+  int skip_stage1;
 };
 // one bounded mbarrier wait that nothing completes: records `code` in
 // *status after the wait limit and returns (the failure path's self-test)

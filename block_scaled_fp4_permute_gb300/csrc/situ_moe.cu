@@ -306,8 +306,15 @@ size_t situ_moe_workspace_size(const situ_moe_args* args) {
   return make_layout(args).total;
 }
 
+// The failure-path test's injection into the FC1 of the block-scaled decode
+// tiles (situ_moe_forward_wait_test); null for every other call.
+struct WaitTest {
+  unsigned long long wait_ns;
+  int skip_stage;
+};
+
 static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t workspace_bytes,
-                                void* stream, void* const* events) {
+                                void* stream, void* const* events, const WaitTest* wt = nullptr) {
   situ_status s = validate(a);
   if (s != SITU_OK) return s;
   if (a->T == 0) return SITU_OK;
@@ -425,8 +432,14 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     w.h = ws + L.h16;
     w.hs = ws + L.whs;
     w.hs_stride = fcw_scale_stride(a->I);
+    if (wt) {
+      w.wait_ns = wt->wait_ns;
+      w.skip_stage1 = wt->skip_stage + 1;
+    }
     if ((err = launch_fcw(w, a->w1, g.x, g.xs, S, a->num_local_experts, true, lo, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
+    w.wait_ns = 0;
+    w.skip_stage1 = 0;
     mark(3);
     w.wsp = wsp4;
     w.Mtot = a->H;
@@ -794,6 +807,17 @@ situ_status situ_moe_forward_profiled(const situ_moe_args* a, void* workspace,
                                       size_t workspace_bytes, void* stream, void* const* events) {
   if (!events) return SITU_ERR_NULL_ARG;
   return forward_impl(a, workspace, workspace_bytes, stream, events);
+}
+
+situ_status situ_moe_forward_wait_test(const situ_moe_args* a, void* workspace, size_t workspace_bytes, void* stream,
+                                       int32_t skip_stage, int32_t wait_us) {
+  if (!a) return SITU_ERR_NULL_ARG;
+  if (skip_stage < 0 || wait_us < 1 || wait_us > 1000000) return SITU_ERR_BAD_SHAPE;
+  if (validate(a) != SITU_OK) return validate(a);
+  // only the block-scaled decode tiles carry the injection
+  if (!(fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2))) return SITU_ERR_UNSUPPORTED;
+  const WaitTest wt = {1000ull * (unsigned long long)wait_us, skip_stage};
+  return forward_impl(a, workspace, workspace_bytes, stream, nullptr, &wt);
 }
 
 size_t situ_moe_packed_scales_size(const situ_moe_args* a) {

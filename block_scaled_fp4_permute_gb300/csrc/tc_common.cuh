@@ -39,15 +39,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity; false (and an error
-// code in *err) if it does not complete within kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int* err, int code) {
+// code in *err) if it does not complete within `limit` ns (kWaitNs unless a
+// kernel takes a shorter per-call limit).
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int* err, int code,
+                                          unsigned long long limit = kWaitNs) {
   if (mbar_try(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(a, parity)) return true;
     if ((i & 1023u) == 0) {
       // give up past the limit, or as soon as another CTA has given up
-      if (globaltimer() - t0 > kWaitNs) {
+      if (globaltimer() - t0 > limit) {
         atomicCAS(err, 0, code);
         return false;
       }
@@ -58,8 +60,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, int* err,
 
 // The same bounded wait taken by every lane of a warp; the outcome is the
 // AND over the lanes, so the warp leaves a loop together.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t a, uint32_t parity, int* err, int code) {
-  return __all_sync(0xffffffffu, mbar_wait(a, parity, err, code));
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t a, uint32_t parity, int* err, int code,
+                                               unsigned long long limit = kWaitNs) {
+  return __all_sync(0xffffffffu, mbar_wait(a, parity, err, code, limit));
 }
 
 // One lane of the converged warp, picked by elect.sync. The MMA issuers run
@@ -79,6 +82,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// The tile of a tensor map at (x, y) brought into L2 ahead of its load (no
+// shared memory, no barrier: a hint that deepens the copy pipeline).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle,

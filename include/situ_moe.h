@@ -398,6 +398,28 @@ situ_status situ_moe_device_status(const situ_moe_args* args, const void* worksp
 situ_status situ_moe_wait_selftest(int32_t* device_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * situ_moe_forward_wait_test -- situ_moe_forward with its failure path
+ * taken on purpose.
+ *
+ * A test of the GEMMs' own unwinding, without a fault: the forward runs as
+ * situ_moe_forward does, except that in its FC1 (the block-scaled decode
+ * tiles, which these arguments must select, else UNSUPPORTED) every bounded
+ * wait gives up after wait_us microseconds instead of 200 ms, and CTA 0's
+ * copy producer leaves its K stage number skip_stage (counted across its
+ * work items) unissued.  The MMA issuer's wait for that stage then runs out:
+ * the kernel records its code in the workspace's status word, waits (bounded)
+ * for the copies and MMAs it issued, releases its tensor memory and returns;
+ * the other CTAs and the kernels after it see the word and skip their work.
+ * The output is then undefined and situ_moe_device_status reports
+ * SITU_ERR_DEVICE_TIMEOUT; the next situ_moe_forward with the same
+ * workspace clears the word and runs normally.  Asynchronous on `stream`.
+ * The pages define no counterpart.  Errors: those of situ_moe_forward,
+ * BAD_SHAPE (skip_stage < 0, wait_us outside 1..1000000), UNSUPPORTED.
+ * --------------------------------------------------------------------- */
+situ_status situ_moe_forward_wait_test(const situ_moe_args* args, void* workspace, size_t workspace_bytes,
+                                       void* stream, int32_t skip_stage, int32_t wait_us);
+
+/* ------------------------------------------------------------------------
  * situ_tc_peak -- dense throughput of one tensor-core MMA kind on this GPU.
  *
  * Enqueues one kernel with one CTA per SM.  Each CTA fills a 128-row A tile

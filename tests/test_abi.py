@@ -187,6 +187,19 @@ def test_route_topk_argument_errors(lib):
     assert f(None, 0, 8, 2, 1, None, None, None) == 0   # T == 0: nothing
 
 
+def test_forward_wait_test_argument_errors(lib):
+    f = lib.situ_moe_forward_wait_test
+    a = _args(H=256, I=128)   # the block-scaled decode tiles
+    assert f(None, ctypes.c_void_p(0x2000), 1 << 40, None, 0, 100) == 1
+    assert f(ctypes.byref(a), ctypes.c_void_p(0x2000), 1 << 40, None, -1, 100) == 2
+    assert f(ctypes.byref(a), ctypes.c_void_p(0x2000), 1 << 40, None, 0, 0) == 2
+    assert f(ctypes.byref(a), ctypes.c_void_p(0x2000), 1 << 40, None, 0, 2000000) == 2
+    assert f(ctypes.byref(_args()), ctypes.c_void_p(0x2000), 1 << 40, None, 0, 100) == 3   # register tiles
+    bad = _args(H=256, I=128)
+    bad.gemm1_beta = None
+    assert f(ctypes.byref(bad), ctypes.c_void_p(0x2000), 1 << 40, None, 0, 100) == 1
+
+
 def test_tc_peak_argument_errors(lib):
     vp = ctypes.c_void_p
     d = ctypes.c_double(0.0)

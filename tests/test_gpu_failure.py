@@ -51,3 +51,38 @@ def test_context_stays_usable_after_the_wait_ran_out():
     a = np.abs(ref)
     half_ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 8), 0.0)
     assert float(np.max(np.abs(out - ref) - half_ulp)) <= 2e-2 * rms
+
+
+def _parity(out, ref):
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    a = np.abs(ref)
+    half_ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 8), 0.0)
+    assert float(np.max(np.abs(out - ref) - half_ulp)) <= 2e-2 * rms
+
+
+@pytest.mark.parametrize("skip_stage", [0, 1, 5, 12])
+def test_gemm_gives_up_a_stage_that_never_lands_and_unwinds(skip_stage):
+    """The FC1 GEMM's own failure path: CTA 0's producer leaves one K stage
+    unissued, so the MMA issuer's bounded wait for it runs out (20 ms here).
+    The call reports SITU_ERR_DEVICE_TIMEOUT through the status word with the
+    MMA issuer's code (43), and returns within a few limits; a normal forward
+    on the same workspace then matches the oracle, so the kernel drained its
+    copies and MMAs and released its tensor memory."""
+    # the block-scaled decode tiles with more work items than CTAs: 64 experts x
+    # 4 FC1 weight tiles, 8 K stages each, so CTA 0 runs two items (16 stages)
+    wl = W.make("tiny", device="cuda", T=96, H=1024, I=512, E_total=64, E_loc=64, off=0, K=4,
+                params="k3_random")
+    layer = binding.Layer(wl)
+    ref = oracle.moe_forward(**W.oracle_kwargs(wl))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    binding.situ_moe_forward_wait_test(layer.args, layer.workspace, skip_stage, 20000)
+    code = layer.device_status()
+    waited = time.perf_counter() - t0
+    assert code == 43, code
+    assert waited < 10.0
+    for _ in range(2):
+        out = layer().float().cpu().numpy()
+        torch.cuda.synchronize()
+        assert layer.device_status() == 0
+        _parity(out, ref)

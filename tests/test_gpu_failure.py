@@ -65,7 +65,9 @@ def test_gemm_gives_up_a_stage_that_never_lands_and_unwinds(skip_stage):
     """The FC1 GEMM's own failure path: CTA 0's producer leaves one K stage
     unissued, so the MMA issuer's bounded wait for it runs out (20 ms here).
     The call reports SITU_ERR_DEVICE_TIMEOUT through the status word with the
-    MMA issuer's code (43), and returns within a few limits; a normal forward
+    code of the first wait that ran out -- the epilogue's wait for the
+    accumulator (46), which starts first, or the MMA issuer's wait for the
+    stage (43) -- and returns within a few limits; a normal forward
     on the same workspace then matches the oracle, so the kernel drained its
     copies and MMAs and released its tensor memory."""
     # the block-scaled decode tiles with more work items than CTAs: 64 experts x
@@ -79,7 +81,7 @@ def test_gemm_gives_up_a_stage_that_never_lands_and_unwinds(skip_stage):
     binding.situ_moe_forward_wait_test(layer.args, layer.workspace, skip_stage, 20000)
     code = layer.device_status()
     waited = time.perf_counter() - t0
-    assert code == 43, code
+    assert code in (43, 46), code
     assert waited < 10.0
     for _ in range(2):
         out = layer().float().cpu().numpy()

@@ -195,31 +195,11 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const bool leader = elect_one();
     long it = 0;
     bool ok = true;
-    // L2 prefetch kPf stages ahead of the loads (into the next item when
-    // the current one ends sooner): the shared ring holds only kStages
-    // stages, less than a DRAM round trip of MMA work
-    constexpr int kPf = 8;
-    if (leader && kPf > 0 && (long)blockIdx.x < total) {
-      const int2 t0 = __ldg(p.tile_info + blockIdx.x / p.n_ntiles);
-      const int wr0 = t0.x * p.Mtot + (int)(blockIdx.x % p.n_ntiles) * C::NH;
-      for (int kk = 0; kk < kPf && kk < nk; ++kk) {
-        tma_prefetch_2d(&tmA, kk * kBK, t0.y);
-        tma_prefetch_2d(&tmB, kk * kBK, wr0);
-        if (FC1) tma_prefetch_2d(&tmB, kk * kBK, wr0 + p.I);
-      }
-    }
     for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
       const int tile = (int)(item / p.n_ntiles), ntile = (int)(item % p.n_ntiles);
       const int2 ti = __ldg(p.tile_info + tile);
       const int e = ti.x, row0 = ti.y;
       const int wrow = e * p.Mtot + ntile * C::NH;
-      const long nitem = item + gridDim.x;   // this CTA's next item, for the prefetch
-      int2 tn = make_int2(0, 0);
-      int wrow_n = 0;
-      if (nitem < total) {
-        tn = __ldg(p.tile_info + nitem / p.n_ntiles);
-        wrow_n = tn.x * p.Mtot + (int)(nitem % p.n_ntiles) * C::NH;
-      }
       const uint8_t* xsb = p.xsp + (size_t)tile * nk * kSfBlock;
       const uint8_t* xsb_lo = LO ? p.xsp_lo + (size_t)tile * nk * kSfBlock : nullptr;
       const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + ntile) * nk * (2 * kSfBlock);
@@ -241,19 +221,6 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           bulk_load(sf_smem, xsb + (size_t)kk * kSfBlock, kSfBlock, full(s));
           if (LO) bulk_load(sf_smem + kSfBlock, xsb_lo + (size_t)kk * kSfBlock, kSfBlock, full(s));
           bulk_load(sf_smem + C::kNA * kSfBlock, wsb + (size_t)kk * 2 * kSfBlock, 2 * kSfBlock, full(s));
-          // the stage kPf ahead
-          const int pk = kk + kPf;
-          if (pk < nk) {
-            tma_prefetch_2d(&tmA, pk * kBK, row0);
-            if (LO) tma_prefetch_2d(&tmAl, pk * kBK, row0);
-            tma_prefetch_2d(&tmB, pk * kBK, wrow);
-            if (FC1) tma_prefetch_2d(&tmB, pk * kBK, wrow + p.I);
-          } else if (nitem < total && pk - nk < nk) {
-            tma_prefetch_2d(&tmA, (pk - nk) * kBK, tn.y);
-            if (LO) tma_prefetch_2d(&tmAl, (pk - nk) * kBK, tn.y);
-            tma_prefetch_2d(&tmB, (pk - nk) * kBK, wrow_n);
-            if (FC1) tma_prefetch_2d(&tmB, (pk - nk) * kBK, wrow_n + p.I);
-          }
         }
         __syncwarp();
       }

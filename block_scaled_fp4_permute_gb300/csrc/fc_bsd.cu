@@ -245,65 +245,34 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tm_holder;
-  // the set-up above may overlap the predecessor's tail
+  // the set-up above may overlap the predecessor's tail; everything below
+  // reads its outputs
   griddep_launch_dependents();
-  // A stage's weights (codes and packed scales) are inputs and its tile comes
-  // from the permute's table, which was complete before this kernel's
-  // predecessor was launched; only the token-side rows are the predecessor's
-  // output.  So the producer issues the weights of its first kStages stages
-  // now -- while the predecessor (the gather, or FC1) still runs -- and their
-  // token rows after the wait.
-  const long total0 = (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
-  auto issue_weights = [&](long it, long item, int kk) {
-    const int s = (int)(it % kStages), nt = (int)(item % p.n_ntiles);
-    const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
-    const int wrow = ti.x * p.Mtot + nt * NH;
-    const uint8_t* wsb = p.wsp + ((size_t)ti.x * p.n_ntiles + nt) * nk * (C::kWSf * kSfBlock);
-    const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
-    mbar_expect_tx(full(s), C::kTx);
-    // x = kk * 128: codes of the MXFP4 map, bytes of the packed NVFP4 maps;
-    // either way one 128-byte row of the stage
-    tma_load_2d(a_smem, &tmW, kk * kRowB, wrow, full(s));
-    // FC1: the up half; NVFP4 FC2: rows 128..255 (its map's boxes are 128 rows)
-    if (FC1 || NV) tma_load_2d(a_smem + kNH1 * kRowB, &tmW, kk * kRowB, wrow + (FC1 ? p.I : kNH1), full(s));
-    bulk_load(sbase + C::kOffSF + s * C::kSfBytes, wsb + (size_t)kk * C::kWSf * kSfBlock, C::kWSf * kSfBlock, full(s));
-  };
-  long pre = 0;   // stages whose weights are in flight before the wait
-  if (warp == 4 && (long)blockIdx.x < total0) {
-    const bool leader = elect_one();
-    for (long it = 0; it < kStages; ++it) {
-      const long item = blockIdx.x + (it / nk) * (long)gridDim.x;
-      if (item >= total0) break;
-      if (leader && it != skip) issue_weights(it, item, (int)(it % nk));
-      pre = it + 1;
-    }
-    __syncwarp();
-  }
   griddep_wait();
   // an earlier CTA that timed out leaves no work (total = 0)
-  const long total = *reinterpret_cast<volatile int*>(p.err) != 0 ? 0 : total0;
+  const long total = *reinterpret_cast<volatile int*>(p.err) != 0
+                         ? 0
+                         : (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
 
-  if (warp == 4) {
+  if ((long)blockIdx.x >= total) {
+    // no item for this CTA
+  } else if (warp == 4) {
     // ---------------- TMA producer ----------------
-    // the whole warp walks the loop; one elected lane issues the copies.
-    // With no work left (an earlier timeout) it still completes the stages
-    // whose weights it issued, so that nothing is in flight at exit.
-    const long ptotal = total > 0 ? total : (pre > 0 ? total0 : 0);
+    // the whole warp walks the loop; one elected lane issues the copies
     const bool leader = elect_one();
     long it = 0;
     bool ok = true;
     // the tile of the next item is read one item ahead, so that its
     // latency hides behind this item's loads
-    int2 ti_next = (long)blockIdx.x < ptotal ? __ldg(p.tile_info + blockIdx.x / p.n_ntiles) : make_int2(0, 0);
-    for (long item = blockIdx.x; item < ptotal && ok; item += gridDim.x) {
+    int2 ti_next = __ldg(p.tile_info + blockIdx.x / p.n_ntiles);
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const int nt = (int)(item % p.n_ntiles);
       const int2 ti = ti_next;
-      if (item + gridDim.x < ptotal) ti_next = __ldg(p.tile_info + (item + gridDim.x) / p.n_ntiles);
-      const int row0 = ti.y;
+      if (item + gridDim.x < total) ti_next = __ldg(p.tile_info + (item + gridDim.x) / p.n_ntiles);
+      const int e = ti.x, row0 = ti.y;
+      const int wrow = e * p.Mtot + nt * NH;
+      const uint8_t* wsb = p.wsp + ((size_t)e * p.n_ntiles + nt) * nk * (C::kWSf * kSfBlock);
       for (int kk = 0; kk < nk; ++kk, ++it) {
-        if (total == 0 && it >= pre) {
-          ok = false;
-          break;
-        }
         const int s = (int)(it % kStages);
         const long r = it / kStages;
         if (r > 0 && !mbar_wait_warp(empty(s), (uint32_t)((r - 1) & 1), p.err, 41, lim)) {
@@ -311,9 +280,16 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
           break;
         }
         if (leader && it != skip) {
-          if (it >= pre) issue_weights(it, item, kk);
+          mbar_expect_tx(full(s), C::kTx);
+          const uint32_t a_smem = sbase + C::kOffA + s * C::kABytes;
           const uint32_t sf_smem = sbase + C::kOffSF + s * C::kSfBytes;
+          // x = kk * 128: codes of the MXFP4 map, bytes of the E4M3 / packed
+          // NVFP4 maps; either way one 128-byte row of the stage
+          tma_load_2d(a_smem, &tmW, kk * kRowB, wrow, full(s));
+          // FC1: the up half; NVFP4 FC2: rows 128..255 (its map's boxes are 128 rows)
+          if (FC1 || NV) tma_load_2d(a_smem + kNH1 * kRowB, &tmW, kk * kRowB, wrow + (FC1 ? p.I : kNH1), full(s));
           tma_load_2d(sbase + C::kOffB + s * C::kBBytes, &tmX, kk * kRowB, RM * row0, full(s));
+          bulk_load(sf_smem, wsb + (size_t)kk * C::kWSf * kSfBlock, C::kWSf * kSfBlock, full(s));
 #pragma unroll
           for (int b = 0; b < C::kTSf; ++b)
             tma_load_2d(sf_smem + C::kWSf * kSfBlock + b * C::kTSfBytes, &tmS, 16 * (C::kTSf * kk + b), RM * row0,
@@ -326,8 +302,6 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       for (long j = it - 1; j >= 0 && j >= it - kStages; --j)
         drain_wait(full((int)(j % kStages)), (uint32_t)((j / kStages) & 1), lim);
     __syncwarp();
-  } else if ((long)blockIdx.x >= total) {
-    // no item for this CTA
   } else if (warp == 5) {
     // ---------------- scale copies + MMA issuer ----------------
     // the whole warp walks the loop; one elected lane issues
@@ -1048,6 +1022,21 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int nt = (int)(item % p.n_ntiles);
       const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
       const int wrow = ti.x * p.Mtot + nt * kNH2;
+      // the next item's weight rows into L2 now: its packed codes and E4M3
+      // scales are two contiguous runs (kNH2 rows of K/2 and K/16 bytes), so
+      // two bulk prefetches stand in for a ring deeper than shared memory holds
+      const long inext = item + gridDim.x;
+      if (leader && inext < total) {
+        const int ntn = (int)(inext % p.n_ntiles);
+        const int en = __ldg(p.tile_info + inext / p.n_ntiles).x;
+        const int r0 = ntn * kNH2;
+        const int rows = min(kNH2, p.Mtot - r0);
+        const size_t row = (size_t)en * p.Mtot + r0;
+        const uint32_t cb = (uint32_t)rows * (uint32_t)(p.K / 2), sb = (uint32_t)rows * (uint32_t)(p.K / 16);
+        bulk_prefetch_l2(p.w + row * (size_t)(p.K / 2), cb & ~15u);
+        if ((reinterpret_cast<uintptr_t>(p.ws + row * (size_t)(p.K / 16)) & 15u) == 0)
+          bulk_prefetch_l2(p.ws + row * (size_t)(p.K / 16), sb & ~15u);
+      }
       for (int kk = 0; kk < nk; ++kk, ++it) {
         const int s = (int)(it % kVStages);
         const long r = it / kVStages;

@@ -84,12 +84,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// The tile of a tensor map at (x, y) brought into L2 ahead of its load (no
-// shared memory, no barrier: a hint that deepens the copy pipeline).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
+// Contiguous global bytes brought into L2 ahead of their use (bytes a
+// multiple of 16, address 16-byte aligned).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle,

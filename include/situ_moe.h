@@ -263,6 +263,15 @@ situ_status situ_moe_quant_nvfp4(const void* x_bf16, int32_t T, int32_t H, uint8
  * the local shard inside [0, num_experts_total).  MXFP4 weight scale bytes
  * must lie in [2, 252] so that every dequantised weight is a bf16 normal or
  * zero (the layer's synthetic and real checkpoints are far inside this).
+ * Representation: the block-scaled tensor-core paths scale every 32 (MXFP4)
+ * or 16 (NVFP4) elements on their own, bf16 rows entering as two MXFP8 rows
+ * (exact within 2^14 of their block's maximum, an absolute error below
+ * 2^-22 of it further down).  The f16 prefill tiles, which take H or I not
+ * multiples of 128 and NVFP4 routings above 512 rows per expert, hold an
+ * activation row in f16 under one scale for the row and a weight row
+ * relative to its largest block scale: activation elements more than 2^-24
+ * below their row's maximum, and weight blocks more than 2^-23 below their
+ * row's largest block scale, contribute nothing there.
  * --------------------------------------------------------------------- */
 /* FC1's gated activation (situ_moe_args.activation). */
 typedef enum { SITU_ACT_FN_SITU = 0, SITU_ACT_FN_SWIGLU_BIAS = 1 } situ_act_fn;

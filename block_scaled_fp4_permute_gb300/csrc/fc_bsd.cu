@@ -1060,30 +1060,23 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
     // ---------------- converters: thread = weight row n of the tile ----------------
     const int n = tid - 192;
     long it = 0;
-    // this thread's weight row of an item's tile (null past H)
-    auto row_of = [&](long item) -> const uint8_t* {
-      const int grow = (int)(item % p.n_ntiles) * kNH2 + n;
-      if (grow >= p.Mtot) return nullptr;
-      return p.ws + ((size_t)__ldg(p.tile_info + item / p.n_ntiles).x * p.Mtot + grow) * (size_t)nsb;
-    };
-    // the row's four scale bytes of a stage (its 16-element blocks)
-    auto load_sc = [&](const uint8_t* srow, int kk) -> uint32_t {
-      if (!srow) return 0u;
-      const uint8_t* q = srow + 4 * kk;
-      return (uint32_t)__ldg(q) | ((uint32_t)__ldg(q + 1) << 8) | ((uint32_t)__ldg(q + 2) << 16) |
-             ((uint32_t)__ldg(q + 3) << 24);
-    };
-    // each scale word is loaded a stage before its use, the first one of an
-    // item during the previous item's last stage, so that no item starts on
-    // a global-memory round trip
-    const uint8_t* srow = (long)blockIdx.x < total ? row_of(blockIdx.x) : nullptr;
-    uint32_t sc = load_sc(srow, 0);
     for (long item = blockIdx.x; item < total; item += gridDim.x) {
-      const long inext = item + gridDim.x;
-      const uint8_t* srow_next = inext < total ? row_of(inext) : nullptr;
+      const int nt = (int)(item % p.n_ntiles);
+      const int e = __ldg(p.tile_info + item / p.n_ntiles).x;
+      const int grow = nt * kNH2 + n;
+      const bool valid = grow < p.Mtot;
+      const uint8_t* srow = p.ws + ((size_t)e * p.Mtot + (valid ? grow : 0)) * (size_t)nsb;
+      // the row's four scale bytes of a stage (its 16-element blocks)
+      auto load_sc = [&](int kk) -> uint32_t {
+        if (!valid || kk >= nk) return 0u;
+        const uint8_t* q = srow + 4 * kk;
+        return (uint32_t)__ldg(q) | ((uint32_t)__ldg(q + 1) << 8) | ((uint32_t)__ldg(q + 2) << 16) |
+               ((uint32_t)__ldg(q + 3) << 24);
+      };
+      uint32_t sc = load_sc(0);
       bool ok = true;
       for (int kk = 0; kk < nk; ++kk, ++it) {
-        const uint32_t sc_next = kk + 1 < nk ? load_sc(srow, kk + 1) : load_sc(srow_next, 0);
+        const uint32_t sc_next = load_sc(kk + 1);
         const int s = (int)(it % kVStages);
         if (!mbar_wait(full(s), (uint32_t)((it / kVStages) & 1), p.err, 54)) {
           ok = false;
@@ -1110,7 +1103,6 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         sc = sc_next;
       }
       if (!ok) break;
-      srow = srow_next;
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------

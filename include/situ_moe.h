@@ -210,9 +210,9 @@ situ_status situ_moe_quant_mxfp8(const void* x_bf16, int32_t T, int32_t H, uint8
  * per-token scaling (the NVFP4 variant's hidden_states / hidden_states_scale
  * / hidden_states_gscale).
  *
- * FlashInfer 0.6.18 SM100a+SM103a MoE-LoRA AOT release notes: the NVFP4
- * path takes "per-token NVFP4 activation scaling" (they note that
- * TRT-LLM-Gen ships no fused SiTU GEMM1 for it).  The pages do not fix the
+ * FlashInfer 0.6.18 SM100a+SM103a MoE-LoRA AOT release notes, Summary: the
+ * NVFP4 path scales its activations per token (and TRT-LLM-Gen has no fused
+ * SiTU GEMM1 for that case).  The pages do not fix the
  * rule; this library uses, per token row, with every step one fp32
  * operation rounded to nearest even:
  *   gscale = amax_row / 2688 (= 6 * 448; 1 for an all-zero row),

@@ -11,8 +11,9 @@
  *   - the block-scaled number formats the layer consumes: E2M1 (FP4) values,
  *     UE8M0 power-of-two block scales and E4M3 ("fn") values;
  *   - the per-token NVFP4 activation quantisation of the NVFP4 variant
- *     (FlashInfer 0.6.18 MoE-LoRA AOT release notes, "per-token NVFP4
- *     activation scaling"; the rule itself is a reading, see below);
+ *     (FlashInfer 0.6.18 MoE-LoRA AOT release notes, Summary: the NVFP4
+ *     path scales its activations per token; the rule itself is a reading,
+ *     see below);
  *   - the per-token MXFP8 activation quantisation of the w4a8 chain
  *     (TokenSpeed SiTU, "Activation precision (w4a16 vs w4a8)" and
  *     "Supported contract": MXFP8 activations with a per-token

@@ -390,6 +390,26 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int2 ti = __ldg(p.tile_info + tile);
       const int e = ti.x, row0 = ti.y;
       const int nrows = min(TT, __ldg(p.offsets + e + 1) - row0);
+      // the item's constants while the MMAs run: the expert's scales (c0, c1:
+      // FC1 gate / up, FC2 output; bt, btl: the activation's caps) and, for
+      // NVFP4 tokens, lane j's token global scale (tokens j and j + 32)
+      float c0s, c1s = 1.f, bt = 0.f, btl = 0.f;
+      if (FC1) {
+        c0s = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
+        c1s = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
+        if (NV) {
+          c0s *= __ldg(p.w1_gs + 2 * e);
+          c1s *= __ldg(p.w1_gs + 2 * e + 1);
+        }
+        bt = __ldg(p.beta + e);
+        btl = __ldg(p.beta_lin + e);
+      } else {
+        c0s = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * (NV ? __ldg(p.w2_gs + e) : 1.f);
+      }
+      float gxl[TT > 32 ? 2 : 1];
+#pragma unroll
+      for (int h = 0; h < (TT > 32 ? 2 : 1); ++h)
+        gxl[h] = (NV && 32 * h + lane < nrows) ? __ldg(p.xg + row0 + 32 * h + lane) : 0.f;
       // every epilogue thread takes the same decision (the waits are
       // bounded, so all 128 reach the reduction)
       if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 46, lim))) break;
@@ -426,7 +446,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         // scale) products of W2 rows n1 = nt * 256 + l and n2 = n1 + 128; the
         // expert's global scale, alpha2 and the row's H1 global scale make them
         // Y.  Y rows leave as 128-byte segments (a warp's 32 consecutive n).
-        const float a2s = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * __ldg(p.w2_gs + e);
+        const float a2s = c0s;
         const int n1 = nt * kNH2 + l, n2 = n1 + 128;
         for (int c0 = 0; c0 < TT; c0 += 16) {
           tmem_ld16(t1 + c0, a1);
@@ -435,8 +455,9 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int t = c0 + j;
+            const float gx = __shfl_sync(0xffffffffu, (TT > 32 && (t & 32)) ? gxl[TT > 32 ? 1 : 0] : gxl[0], t & 31);
             if (t >= nrows) break;
-            const float sc = a2s * __ldg(p.xg + row0 + t);
+            const float sc = a2s * gx;
             float* yr = p.y_out + (size_t)(row0 + t) * p.Mtot;
             if (n1 < p.Mtot) yr[n1] = a1[j] * sc;
             if (n2 < p.Mtot) yr[n2] = a2[j] * sc;
@@ -451,20 +472,20 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         // H1 in bf16), which the FC2 of NVFP4 weights reads.
         // The tile's token columns 16 at a time.
         const int i0 = nt * kNH1 + warp * 32;
-        const float ag = (p.alpha_g ? __ldg(p.alpha_g + e) : 1.f) * __ldg(p.w1_gs + 2 * e);
-        const float au = (p.alpha_u ? __ldg(p.alpha_u + e) : 1.f) * __ldg(p.w1_gs + 2 * e + 1);
-        const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+        const float ag = c0s, au = c1s;
         for (int c0 = 0; c0 < TT; c0 += 16) {
           tmem_ld16(t1 + c0, a1);
           tmem_ld16(t1 + NB + c0, a2);
           if (c0 >= nrows || i0 >= p.I) continue;
+          uint32_t hmax = 0;   // largest |H1| of the chunk (bf16 bits; ordered as the magnitudes)
+          float gx[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)   // zero past nrows (the lanes' loads)
+            gx[j] = __shfl_sync(0xffffffffu, (TT > 32 && ((c0 + j) & 32)) ? gxl[TT > 32 ? 1 : 0] : gxl[0], (c0 + j) & 31);
           float hv[16];
           with_act(p.act_kind, bt, btl, [&](auto act) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float gx = c0 + j < nrows ? __ldg(p.xg + row0 + c0 + j) : 0.f;
-              hv[j] = act(a1[j] * (ag * gx), a2[j] * (au * gx));
-            }
+            for (int j = 0; j < 16; ++j) hv[j] = act(a1[j] * (ag * gx[j]), a2[j] * (au * gx[j]));
           });
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -472,7 +493,13 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
             if (t >= nrows) break;
             float h = hv[j];
             if (p.topk_fc1) h *= __ldg(p.topk_weights + __ldg(p.permuted_src + row0 + t));
-            p.h_bf16[(size_t)(row0 + t) * p.I + i0 + lane] = (uint16_t)(f32x2_to_bf16x2(h, 0.f) & 0xFFFFu);
+            const uint32_t hb = f32x2_to_bf16x2(h, 0.f) & 0xFFFFu;
+            p.h_bf16[(size_t)(row0 + t) * p.I + i0 + lane] = (uint16_t)hb;
+            hmax = max(hmax, hb & 0x7FFFu);
+          }
+          if (p.h1max) {
+            hmax = __reduce_max_sync(0xffffffffu, hmax);
+            if (lane == 0 && hmax != 0) atomicMax(p.h1max, hmax << 16);
           }
         }
         // every column is in registers or stored: hand the accumulator back
@@ -483,9 +510,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
         // accumulators; warp w holds the 32-element block i0 .. i0 + 31
         const int i0 = nt * kNH1 + warp * 32;
         if (i0 < p.I) {
-          const float ag = p.alpha_g ? __ldg(p.alpha_g + e) : 1.f;
-          const float au = p.alpha_u ? __ldg(p.alpha_u + e) : 1.f;
-          const float bt = __ldg(p.beta + e), btl = __ldg(p.beta_lin + e);
+          const float ag = c0s, au = c1s;
           const int sbyte = tok_scale_byte(i0 / 32);   // FC2's K block of this warp
           // the activation of all 16 token columns first (independent
           // chains; the columns past nrows hold other rows or zeros and are
@@ -523,7 +548,7 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       } else {
         // FC2: row n = nt * 256 + l (first accumulator) and nt * 256 + 128 + l
         // (second); Y rows leave as 128-byte segments
-        const float a2s = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
+        const float a2s = c0s;
         const int n1 = nt * kNH2 + l, n2 = nt * kNH2 + 128 + l;
 #pragma unroll
         for (int t = 0; t < kTok; ++t) {
@@ -1159,10 +1184,10 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
       const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
       const int e = ti.x, row0 = ti.y;
       const int nrows = min(NB, __ldg(p.offsets + e + 1) - row0);
+      const float sc = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * __ldg(p.gs + e);   // while the MMAs run
       if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 56))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * 2 * NB);
-      const float sc = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * __ldg(p.gs + e);
       const int n1 = nt * kNH2 + l, n2 = n1 + 128;
       // 16 token columns at a time from each accumulator
       for (int c0 = 0; c0 < NB; c0 += 16) {
@@ -1188,6 +1213,434 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
+}
+
+// ---------------------------------------------------------------------------
+// fct_kernel: the same FC2 (NVFP4 weights, bf16 H1) with the expanded weights
+// in TMEM, for token tiles of 16 and 64 rows.
+//
+// The converters write each stage's bf16 A operand (256 weight rows x 64
+// elements) straight into TMEM with tcgen05.st, and the MMAs read A from
+// there (tcgen05.mma.kind::f16 with A in tensor memory: lane = weight row,
+// two bf16 of K per column).  Shared memory then holds only the packed codes
+// and the token rows, in stages of K = 128: the codes as 64-byte rows (64-byte
+// swizzle), since a TMA box moves about one row per three cycles per SM
+// whatever its width (32-byte rows held fcv_kernel's weight stream near
+// 3 TB/s); each stage feeds two K = 64 A slots.  Each item's E4M3 scales
+// (256 rows x K/16 bytes, one contiguous run) arrive in one bulk copy into a
+// four-deep buffer instead of per-thread global loads.
+//
+// Both operands are f16 when the FC1 has recorded H1's largest magnitude m
+// (h1max): a code times its E4M3 scale is a normal f16 (2^-10 to 2688 in
+// magnitude, at most six significant bits), so one f16 multiply per pair
+// makes the A operand; the token rows come from an f16 copy of H1 scaled by
+// 2^-s (h1_to_f16_kernel, between the two GEMMs), s chosen so that m lands
+// in [2^14, 2^15), and the epilogue multiplies by 2^s.  Every H1 value within 2^31 of
+// m is then exact; smaller ones keep an absolute error below 2^-32 m.
+// Without h1max (or with a non-finite m) the operands are bf16.  Each item's
+// scales come in one bulk copy when the scale array is 16-byte aligned, else
+// the converters read their row's bytes from global memory.
+// TMEM: the two accumulator buffers (2 x 2 x NB columns), then A slots of
+// 64 columns (32 per M = 128 half of the tile).  A converter warp writes the
+// TMEM lanes of its quarter (warp % 4), so warp w converts weight rows
+// 128 * ((w - 6) / 4) + 32 * (w % 4) + lane.  Warp roles as fcv_kernel.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr int kTScBuf = 4;                      // item scale buffers
+constexpr int kTScBytes = 256 * 32;             // one item's scales, K <= 512
+constexpr int kTBK = 128;                       // K elements per TMA stage
+constexpr int kTRBytes = 256 * 64;              // packed codes of a stage: 256 rows x 64 bytes
+template <int NB>
+struct CfgT {
+  static_assert(NB == 16 || NB == 64, "TMEM tiles: 16 or 64 token rows");
+  static constexpr int kStages = NB == 16 ? 8 : 5;     // codes + token rows in shared memory
+  static constexpr int kAccCols = 4 * NB;              // two buffers of two NB-column accumulators
+  static constexpr int kASlots = (512 - kAccCols) / 64;
+  static constexpr int kXBytes = NB * 256;             // bf16 token rows: two boxes of 64 elements
+  static constexpr int kOffR = 0;
+  static constexpr int kOffX = kOffR + kStages * kTRBytes;
+  static constexpr int kOffSc = kOffX + kStages * kXBytes;
+  static constexpr int kOffBar = kOffSc + kTScBuf * kTScBytes;
+  // full, empty per stage; conv, aempty per A slot; scfull, scfree per scale
+  // buffer; acc_full[2], acc_empty[2]; drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 * kTScBuf + 5;
+  static constexpr int kOffTm = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffTm + 16 + 1024;
+  static constexpr uint32_t kTx = kXBytes + kTRBytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kXBytes % 2048 == 0 && kOffX % 1024 == 0, "swizzle atoms");
+  static_assert(kASlots >= 2, "TMEM budget");
+  static constexpr uint32_t kIdesc = CfgV<NB>::kIdesc;
+};
+
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 consecutive TMEM columns of the warp's 32 lanes, one row per thread
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+}  // namespace
+
+template <int NB>
+__global__ void __launch_bounds__(kVThreads, 1)
+fct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+           const __grid_constant__ CUtensorMap tmXh, const FcvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using C = CfgT<NB>;
+  constexpr int D1 = C::kStages, D2 = C::kASlots;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nk = p.K / kTBK;                    // TMA stages per item, two A slots each
+  const int nsb = p.K / 16;                     // E4M3 scales per weight row
+
+  const uint32_t sbase = saddr(smem);
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto full = [&](int s) { return bar0 + 8 * s; };
+  auto empty = [&](int s) { return bar0 + 8 * (D1 + s); };
+  auto conv = [&](int s) { return bar0 + 8 * (2 * D1 + s); };
+  auto aempty = [&](int s) { return bar0 + 8 * (2 * D1 + D2 + s); };
+  auto scfull = [&](int b) { return bar0 + 8 * (2 * D1 + 2 * D2 + b); };
+  auto scfree = [&](int b) { return bar0 + 8 * (2 * D1 + 2 * D2 + kTScBuf + b); };
+  auto acc_full = [&](int b) { return bar0 + 8 * (2 * D1 + 2 * D2 + 2 * kTScBuf + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8 * (2 * D1 + 2 * D2 + 2 * kTScBuf + 2 + b); };
+  const uint32_t drain = bar0 + 8 * (2 * D1 + 2 * D2 + 2 * kTScBuf + 4);
+  uint32_t* tm_holder = reinterpret_cast<uint32_t*>(smem + C::kOffTm);
+
+  if (tid == 0) {
+    for (int s = 0; s < D1; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int s = 0; s < D2; ++s) {
+      mbar_init(conv(s), 256);
+      mbar_init(aempty(s), 1);
+    }
+    for (int b = 0; b < kTScBuf; ++b) {
+      mbar_init(scfull(b), 1);
+      mbar_init(scfree(b), 256);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tm_holder)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tm_holder;
+  griddep_launch_dependents();
+  griddep_wait();
+  const long total = *reinterpret_cast<volatile int*>(p.err) != 0
+                         ? 0
+                         : (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
+  // f16 operands with H1 scaled by 2^-sig (the largest |H1|, recorded by the
+  // FC1 before, brought into [2^14, 2^15)); bf16 without the record
+  const uint32_t mbits = p.h1max ? *reinterpret_cast<const volatile unsigned*>(p.h1max) : 0x7F800000u;
+  const bool f16m = mbits < 0x7F800000u;
+  const int sig = mbits >= 0x00800000u ? min(113, max(-126, (int)(mbits >> 23) - 127 - 14)) : 0;
+  const bool sc_bulk = (reinterpret_cast<uintptr_t>(p.ws) & 15u) == 0;
+
+  if ((long)blockIdx.x >= total) {
+    // no item for this CTA
+  } else if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    const bool leader = elect_one();
+    const CUtensorMap* mx = f16m ? &tmXh : &tmX;
+    long it = 0;
+    int li = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+      const int nt = (int)(item % p.n_ntiles);
+      const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
+      const int wrow = ti.x * p.Mtot + nt * kNH2;
+      // the item's scales: rows wrow .. of K/16 bytes, one contiguous run
+      const int b = li % kTScBuf;
+      if (li >= kTScBuf && !mbar_wait_warp(scfree(b), (uint32_t)((li / kTScBuf - 1) & 1), p.err, 62)) break;
+      if (leader) {
+        if (sc_bulk) {
+          const uint32_t bytes = (uint32_t)min(kNH2, p.Mtot - nt * kNH2) * (uint32_t)nsb;
+          mbar_expect_tx(scfull(b), bytes);
+          bulk_load(sbase + C::kOffSc + b * kTScBytes, p.ws + (size_t)wrow * nsb, bytes, scfull(b));
+        } else {
+          mbar_arrive(scfull(b));   // the converters read the scales themselves
+        }
+      }
+      __syncwarp();
+      for (int kk = 0; kk < nk; ++kk, ++it) {
+        const int s = (int)(it % D1);
+        const long r = it / D1;
+        if (r > 0 && !mbar_wait_warp(empty(s), (uint32_t)((r - 1) & 1), p.err, 61)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          mbar_expect_tx(full(s), C::kTx);
+          const uint32_t xs = sbase + C::kOffX + s * C::kXBytes;
+          tma_load_2d(sbase + C::kOffR + s * kTRBytes, &tmW, kk * (kTBK / 2), wrow, full(s));
+          tma_load_2d(xs, mx, kk * kTBK, ti.y, full(s));
+          tma_load_2d(xs + NB * 128, mx, kk * kTBK + 64, ti.y, full(s));
+        }
+        __syncwarp();
+      }
+    }
+    // unwind: the copies of the last stages and scale buffers may still be landing
+    if (leader) {
+      for (long j = it - 1; j >= 0 && j >= it - D1; --j) drain_wait(full((int)(j % D1)), (uint32_t)((j / D1) & 1));
+      for (int j = li - 1; j >= 0 && j >= li - kTScBuf; --j)
+        drain_wait(scfull(j % kTScBuf), (uint32_t)((j / kTScBuf) & 1));
+    }
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ---------------- converters: thread = weight row n of the tile ----------------
+    const int q = warp & 3, mt = (warp - 6) >> 2;
+    const int n = mt * 128 + q * 32 + lane;
+    const uint32_t tlane = (uint32_t)(q * 32) << 16;
+    const int sw = (n >> 1) & 3;   // 64-byte swizzle: 16-byte chunk j of row n sits at chunk j ^ sw
+    long it = 0, ia = 0;           // TMA stages, A slots
+    int li = 0;
+    bool ok = true;
+    // The store of a half into TMEM is waited for, and the half handed to the
+    // MMA, only after the next half has been converted, so the store's
+    // latency overlaps that work (two register sets, one per half of a stage).
+    int pend = -1;                 // A slot of the stored, not yet handed over half
+    auto hand_over = [&]() {
+      if (pend < 0) return;
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(conv(pend));
+      pend = -1;
+    };
+    // the K = 64 half u of stage s1 (row n) as 32 bf16 pairs
+    auto convert = [&](int s1, int u, uint32_t sc, uint32_t* a) {
+      const uint8_t* raw = smem + C::kOffR + s1 * kTRBytes + n * 64;
+      const uint4 q0 = *reinterpret_cast<const uint4*>(raw + (((2 * u) ^ sw) << 4));
+      const uint4 q1 = *reinterpret_cast<const uint4*>(raw + (((2 * u + 1) ^ sw) << 4));
+      const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      uint32_t f[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] = e4m3_pair_f16((sc >> (8 * j)) & 0xFFu);
+      if (f16m) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {   // word j = elements 8j .. 8j + 7 (block j / 2)
+          uint32_t d[4];
+          e2m1x8_f16(w[j], d);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a[4 * j + i] = mul_f16x2(d[i], f[j >> 1]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t d[4];
+          e2m1x8_f16(w[j], d);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a[4 * j + i] = scaled_bf16x2(d[i], f[j >> 1]);
+        }
+      }
+    };
+    uint32_t a0[32], a1[32];
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+      const int nt = (int)(item % p.n_ntiles);
+      const bool valid = nt * kNH2 + n < p.Mtot;
+      const int b = li % kTScBuf;
+      if (!mbar_wait(scfull(b), (uint32_t)((li / kTScBuf) & 1), p.err, 65)) break;
+      const uint8_t* srow = smem + C::kOffSc + b * kTScBytes + n * nsb;
+      // unaligned scale array: the row's bytes straight from global memory
+      const uint16_t* grow =
+          sc_bulk ? nullptr
+                  : reinterpret_cast<const uint16_t*>(
+                        p.ws + ((size_t)__ldg(p.tile_info + item / p.n_ntiles).x * p.Mtot + nt * kNH2 + (valid ? n : 0)) *
+                                   nsb);
+      for (int kk = 0; kk < nk && ok; ++kk, ++it) {
+        const int s1 = (int)(it % D1);
+        if (!mbar_wait(full(s1), (uint32_t)((it / D1) & 1), p.err, 63)) {
+          ok = false;
+          break;
+        }
+        // the row's scale bytes of the stage: four per half (its 16-element blocks)
+        uint2 sc = make_uint2(0u, 0u);
+        if (valid && sc_bulk) {
+          sc = *reinterpret_cast<const uint2*>(srow + 8 * kk);
+        } else if (valid) {
+          sc.x = (uint32_t)__ldg(grow + 4 * kk) | ((uint32_t)__ldg(grow + 4 * kk + 1) << 16);
+          sc.y = (uint32_t)__ldg(grow + 4 * kk + 2) | ((uint32_t)__ldg(grow + 4 * kk + 3) << 16);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u, ++ia) {
+          const int s2 = (int)(ia % D2);
+          if (ia >= D2 && !mbar_wait(aempty(s2), (uint32_t)((ia / D2 - 1) & 1), p.err, 64)) {
+            ok = false;
+            break;
+          }
+          uint32_t* a = u ? a1 : a0;
+          convert(s1, u, u ? sc.y : sc.x, a);
+          hand_over();   // the previous half, stored while this one converted
+          // TMEM column c of the slot holds elements 2c, 2c + 1 of the row
+          tmem_st32(tmem + tlane + (uint32_t)(C::kAccCols + s2 * 64 + mt * 32), a);
+          pend = s2;
+        }
+      }
+      if (ok) mbar_arrive(scfree(b));
+    }
+    if (ok) {
+      hand_over();
+    } else if (pend >= 0) {
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    const bool leader = elect_one();
+    // kind::f16 operand types: bf16 (1) or f16 (0) for A (bits 7..9) and B (10..12)
+    const uint32_t idesc = f16m ? (C::kIdesc & ~((7u << 7) | (7u << 10))) : C::kIdesc;
+    long it = 0, ia = 0;
+    int li = 0;
+    bool ok = true;
+    for (long item = blockIdx.x; item < total && ok; item += gridDim.x, ++li) {
+      const int buf = li & 1, use = li >> 1;
+      if (use > 0 && !mbar_wait_warp(acc_empty(buf), (uint32_t)((use - 1) & 1), p.err, 66)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t d1 = tmem + (uint32_t)(buf * 2 * NB);
+      const uint32_t d2 = d1 + NB;
+      for (int kk = 0; kk < nk && ok; ++kk, ++it) {
+        const int s1 = (int)(it % D1);
+        if (!mbar_wait_warp(full(s1), (uint32_t)((it / D1) & 1), p.err, 67)) {
+          ok = false;
+          break;
+        }
+        for (int u = 0; u < 2; ++u, ++ia) {
+          const int s2 = (int)(ia % D2);
+          if (!mbar_wait_warp(conv(s2), (uint32_t)((ia / D2) & 1), p.err, 68)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          if (leader) {
+            const uint32_t a1 = tmem + (uint32_t)(C::kAccCols + s2 * 64);
+            // the half's token rows: the stage's u-th box of 64 elements
+            const uint64_t bd = sdesc(sbase + C::kOffX + s1 * C::kXBytes + u * NB * 128);
+#pragma unroll
+            for (uint32_t k4 = 0; k4 < 4; ++k4) {   // K = 16 per MMA: 8 TMEM columns, 32 bytes of each token row
+              const uint32_t acc = (kk | u | (int)k4) != 0;
+              mma_bf16_ta(d1, a1 + 8 * k4, bd + 2 * k4, idesc, acc);
+              mma_bf16_ta(d2, a1 + 32 + 8 * k4, bd + 2 * k4, idesc, acc);
+            }
+            mma_commit(aempty(s2));
+            if (u == 1) mma_commit(empty(s1));
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      if (leader) mma_commit(acc_full(buf));
+      __syncwarp();
+    }
+    if (leader) {
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: thread = weight row (TMEM lane) ----------------
+    const int l = warp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    for (int li = 0;; ++li) {
+      const long item = blockIdx.x + (long)li * gridDim.x;
+      if (item >= total) break;
+      const int buf = li & 1;
+      const int nt = (int)(item % p.n_ntiles);
+      const int2 ti = __ldg(p.tile_info + item / p.n_ntiles);
+      const int e = ti.x, row0 = ti.y;
+      const int nrows = min(NB, __ldg(p.offsets + e + 1) - row0);
+      // while the MMAs run; f16 mode undoes H1's 2^-sig
+      const float sc = (p.alpha2 ? __ldg(p.alpha2 + e) : 1.f) * __ldg(p.gs + e) * (f16m ? exp2i(sig) : 1.f);
+      if (!bar_red_and(2, 128, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 69))) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t t1 = tmem + lane_off + (uint32_t)(buf * 2 * NB);
+      const int n1 = nt * kNH2 + l, n2 = n1 + 128;
+      for (int c0 = 0; c0 < NB; c0 += 16) {
+        float a1[16], a2[16];
+        tmem_ld16(t1 + c0, a1);
+        tmem_ld16(t1 + NB + c0, a2);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          if (c0 + t >= nrows) break;
+          float* yr = p.y_out + (size_t)(row0 + c0 + t) * p.Mtot;
+          if (n1 < p.Mtot) yr[n1] = a1[t] * sc;
+          if (n2 < p.Mtot) yr[n2] = a2[t] * sc;
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(acc_empty(buf));
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
+template <int NB>
+cudaError_t launch_fct_t(const FcvParams& p, const uint16_t* h_bf16, const uint16_t* h_f16, long S, int E_loc,
+                         long max_tiles, cudaStream_t st) {
+  using C = CfgT<NB>;
+  CUtensorMap m[3];
+  // packed codes in boxes of 64 bytes (128 codes) x 256 rows, 64-byte
+  // swizzle; H1 bf16 in boxes of 64 elements x NB rows, 128-byte swizzle
+  if (!make_map(&m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.w, (uint64_t)(p.K / 2), (uint64_t)E_loc * p.Mtot,
+                (uint64_t)(p.K / 2), kTBK / 2, kNH2, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&m[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h_bf16, (uint64_t)p.K, (uint64_t)S, (uint64_t)p.K * 2,
+                kVBK, NB, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h_f16 ? h_f16 : h_bf16, (uint64_t)p.K, (uint64_t)S,
+                (uint64_t)p.K * 2, kVBK, NB, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  FcvParams q = p;
+  if (!h_f16) q.h1max = nullptr;   // no f16 copy: bf16 operands
+  static int set_for[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(attr_mutex());
+    if (dev >= 64 || set_for[dev] == 0) {
+      cudaError_t err = cudaFuncSetAttribute(fct_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) set_for[dev] = 1;
+    }
+  }
+  const long items = max_tiles * p.n_ntiles;
+  const long grid = items < sm_count_w() ? items : sm_count_w();
+  if (grid <= 0) return cudaSuccess;
+  return launch_pdl(fct_kernel<NB>, dim3((unsigned)grid), dim3(kVThreads), (size_t)C::kSmem, st, m[0], m[1], m[2], q);
 }
 
 template <int NB>
@@ -1220,12 +1673,52 @@ cudaError_t launch_fcv_t(const FcvParams& p, const uint16_t* h_bf16, long S, int
   return launch_pdl(fcv_kernel<NB>, dim3((unsigned)grid), dim3(kVThreads), (size_t)C::kSmem, st, m[0], m[1], p);
 }
 
-cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, int tile_rows, long max_tiles,
-                       cudaStream_t st) {
+// the TMEM-operand kernel takes the 16- and 64-row tiles (an item's scales,
+// 256 rows of K/16 bytes, fit its 8 KB buffers)
+bool fct_applies(int K, int tile_rows) { return (tile_rows == kTok || tile_rows == 64) && K <= 512 && K % kTBK == 0; }
+
+// H1 (bf16 [S, I], the first meta[0] rows in use) as f16 times 2^-sig, sig
+// from the largest magnitude the FC1 recorded (as fct_kernel derives it);
+// 8 elements per thread.
+__global__ void __launch_bounds__(256) h1_to_f16_kernel(const uint4* __restrict__ h, const int32_t* meta,
+                                                        const unsigned* h1max, int I, uint4* __restrict__ hf) {
+  griddep_wait();   // H1 and its maximum are the predecessor's output
+  griddep_launch_dependents();
+  const uint32_t mbits = *reinterpret_cast<const volatile unsigned*>(h1max);
+  if (mbits >= 0x7F800000u) return;   // not finite: the FC2 takes bf16 operands
+  const int sig = mbits >= 0x00800000u ? min(113, max(-126, (int)(mbits >> 23) - 127 - 14)) : 0;
+  const float sc = exp2i(-sig);
+  const long n8 = (long)__ldg(meta) * (I / 8);
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n8; i += (long)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(h + i);
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = pack_f16x2(bf16_lo(in[j]) * sc, bf16_hi(in[j]) * sc);
+    hf[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_h1_to_f16(const uint16_t* h_bf16, long S, int I, const int32_t* meta, const unsigned* h1max,
+                             uint16_t* h_f16, cudaStream_t st) {
+  const long n8 = S * (I / 8);
+  const long grid = std::min<long>((n8 + 255) / 256, 4L * sm_count_w());
+  if (grid <= 0) return cudaSuccess;
+  return launch_pdl(h1_to_f16_kernel, dim3((unsigned)grid), dim3(256), 0, st, (const uint4*)h_bf16, meta, h1max, I,
+                    (uint4*)h_f16);
+}
+
+cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, const uint16_t* h_f16, long S, int E_loc,
+                       int tile_rows, long max_tiles, cudaStream_t st) {
   if (S <= 0) return cudaSuccess;
   if (tile_rows == 128) return launch_fcv_t<128>(p, h_bf16, S, E_loc, max_tiles, st);
-  if (tile_rows == 64) return launch_fcv_t<64>(p, h_bf16, S, E_loc, max_tiles, st);
-  if (tile_rows == kTok) return launch_fcv_t<kTok>(p, h_bf16, S, E_loc, max_tiles, st);
+  const bool ta = fct_applies(p.K, tile_rows);
+  if (tile_rows == 64)
+    return ta ? launch_fct_t<64>(p, h_bf16, h_f16, S, E_loc, max_tiles, st)
+              : launch_fcv_t<64>(p, h_bf16, S, E_loc, max_tiles, st);
+  if (tile_rows == kTok)
+    return ta ? launch_fct_t<kTok>(p, h_bf16, h_f16, S, E_loc, max_tiles, st)
+              : launch_fcv_t<kTok>(p, h_bf16, S, E_loc, max_tiles, st);
   return cudaErrorInvalidValue;
 }
 

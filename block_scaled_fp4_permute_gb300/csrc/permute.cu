@@ -124,7 +124,7 @@ permute_scan_kernel(int32_t* __restrict__ blk_counts, int nblk, int E_loc, long 
   if (threadIdx.x == 0) {
     offsets[E_loc] = R;
     if (tile_offsets) tile_offsets[E_loc] = tiles;
-    if (meta) { meta[0] = R; meta[1] = tiles; meta[2] = 0; }
+    if (meta) { meta[0] = R; meta[1] = tiles; meta[2] = 0; meta[3] = 0; }
   }
   // 3. rows >= R of permuted_src hold -1
   for (long r = R + threadIdx.x; r < S; r += blockDim.x) permuted_src[r] = -1;
@@ -245,7 +245,7 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
   if (threadIdx.x == 0) {
     offsets[E_loc] = R;
     if (tile_offsets) tile_offsets[E_loc] = tiles;
-    if (meta) { meta[0] = R; meta[1] = tiles; meta[2] = 0; }
+    if (meta) { meta[0] = R; meta[1] = tiles; meta[2] = 0; meta[3] = 0; }
   }
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;

@@ -269,6 +269,7 @@ struct FcwParams {
   const float* w1_gs;            // [E_loc, 2] gate / up global scale
   const float* xg;               // [S] the row's per-token global scale
   uint16_t* h_bf16;              // [S, I]
+  unsigned* h1max;               // non-null: raised to the largest |H1| (fp32 bits; cleared before)
   // FC2
   const float* alpha2;
   const float* w2_gs;            // [E_loc] global scale (NVFP4 FC2 on the requantised H1)
@@ -331,10 +332,20 @@ struct FcvParams {
   int E_loc, n_ntiles;
   float* y_out;
   int* err;
+  const unsigned* h1max;         // the largest |H1| (fp32 bits), or null: the 16- and
+                                 // 64-row tiles then multiply bf16 operands, not f16 ones
 };
-// tile_rows: the token tile of p's tile table, 16, 64 or 128
-cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, long S, int E_loc, int tile_rows, long max_tiles,
-                       cudaStream_t st);
+// tile_rows: the token tile of p's tile table, 16, 64 or 128; h_f16 (may be
+// null): H1 as f16 times 2^-s (launch_h1_to_f16), which the 16- and 64-row
+// tiles multiply on f16 operands when p.h1max holds a finite maximum
+cudaError_t launch_fcv(const FcvParams& p, const uint16_t* h_bf16, const uint16_t* h_f16, long S, int E_loc,
+                       int tile_rows, long max_tiles, cudaStream_t st);
+// H1 bf16 [S, I] (meta[0] rows in use) to f16 times 2^-s, s from the largest
+// magnitude *h1max that the FC1 recorded; nothing when it is not finite
+cudaError_t launch_h1_to_f16(const uint16_t* h_bf16, long S, int I, const int32_t* meta, const unsigned* h1max,
+                             uint16_t* h_f16, cudaStream_t st);
+// whether launch_fcv takes these tiles on the kernel that can use f16 operands
+bool fct_applies(int K, int tile_rows);
 cudaError_t launch_pack_scales_nv(const uint8_t* w1_scale, int E_loc, int H, int I, uint8_t* out, cudaStream_t st);
 size_t fcd_smem_bytes(int K, bool nvfp4);
 cudaError_t launch_fcd(const FcdParams& p, bool fc1, bool nvfp4, long max_tiles, cudaStream_t st);

@@ -24,7 +24,7 @@ bool aligned_to(const void* p, uintptr_t a) { return p == nullptr || (reinterpre
 bool aligned16(const void* p) { return aligned_to(p, 16); }
 
 struct Layout {
-  size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, y;
+  size_t counts, offsets, tile_offsets, tile_info, meta, psrc, s2r, blk, h1, h1f, y;
   size_t x16, x16s, h16, h16s, xsp, hsp, wsp, wxs, whs, ys, xg, hq, hqs, hg, t2off, t2info, total;
 };
 
@@ -146,6 +146,8 @@ Layout make_layout(const situ_moe_args* a) {
   L.s2r = take(4 * S);
   L.blk = take(permute_scratch_bytes(a->T, a->top_k, a->num_local_experts));
   L.h1 = take(2 * S * (size_t)a->I);
+  // NVFP4 tiles with bf16 H1: its scaled f16 copy for the FC2's f16 operands
+  L.h1f = take(fcw_nv_shapes(a) && a->h1_nvfp4 == 0 ? 2 * S * (size_t)a->I : 0);
   L.y = take(4 * S * (size_t)a->H);
   // decode path: f16 block rows of the input and of H1
   L.x16 = take(2 * S * (size_t)pad128(a->H));
@@ -496,6 +498,10 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     w.w1_gs = a->w1_gscale;
     w.xg = g.xg;
     w.h_bf16 = h1;
+    // H1's largest magnitude, for an FC2 that multiplies on f16 operands
+    const int fc2_rows = nv_wide_fc2(a) ? kNvFc2WideTile : tile_n;
+    unsigned* h1max = !h1nv && fct_applies(a->I, fc2_rows) ? (unsigned*)(meta + 3) : nullptr;
+    w.h1max = h1max;
     if ((err = launch_fcw_nv(w, a->w1, g.x, g.xs, S, a->num_local_experts, tile_n, max_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(3);
@@ -541,6 +547,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     v.n_ntiles = (a->H + fcw_n_rows(false) - 1) / fcw_n_rows(false);
     v.y_out = y;
     v.err = meta + 2;
+    v.h1max = h1max;
     int fc2_tile = tile_n;
     long fc2_tiles = max_tiles;
     if (nv_wide_fc2(a)) {
@@ -549,7 +556,9 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
       v.tile_offsets = (const int32_t*)(ws + L.t2off);
       v.tile_info = (const int2*)(ws + L.t2info);
     }
-    if ((err = launch_fcv(v, h1, S, a->num_local_experts, fc2_tile, fc2_tiles, st)) != cudaSuccess)
+    uint16_t* h1f = h1max ? (uint16_t*)(ws + L.h1f) : nullptr;
+    if (h1f && (err = launch_h1_to_f16(h1, S, a->I, meta, h1max, h1f, st)) != cudaSuccess) return SITU_ERR_CUDA;
+    if ((err = launch_fcv(v, h1, h1f, S, a->num_local_experts, fc2_tile, fc2_tiles, st)) != cudaSuccess)
       return SITU_ERR_CUDA;
     mark(4);
     }
@@ -850,8 +859,12 @@ int32_t situ_moe_forward_launches(const situ_moe_args* a) {
   const int pack = a->scales_packed ? 0 : 4;
   if (fcw_shapes(a) && fcq_supported(a->H, a->I, a->w1, a->w2)) return perm + pack + 4;
   const int h1nv = a->h1_nvfp4 != 0 ? 1 : 0;   // + the requantisation (+ its scale packing)
-  if (fcw_nv_shapes(a))
-    return perm + (nv_wide_fc2(a) && !h1nv ? 1 : 0) + (a->scales_packed ? 0 : 1 + h1nv) + 4 + h1nv;
+  if (fcw_nv_shapes(a)) {
+    // + H1 to f16 for an FC2 on f16 operands
+    const int fc2_rows = nv_wide_fc2(a) ? kNvFc2WideTile : nv_wide(a) ? kNvWideTile : fcw_token_tile();
+    const int f16 = !h1nv && fct_applies(a->I, fc2_rows) ? 1 : 0;
+    return perm + (nv_wide_fc2(a) && !h1nv ? 1 : 0) + (a->scales_packed ? 0 : 1 + h1nv) + 4 + h1nv + f16;
+  }
   if (takes_decode_path(a)) return perm + 4;
   if (takes_block_scaled_path(a) && fcq_supported(a->H, a->I, a->w1, a->w2))
     return perm + pack + 4 + (a->fuse_combine ? 1 : 0);   // + zeroing the accumulator

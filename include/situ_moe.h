@@ -271,7 +271,13 @@ situ_status situ_moe_quant_nvfp4(const void* x_bf16, int32_t T, int32_t H, uint8
  * activation row in f16 under one scale for the row and a weight row
  * relative to its largest block scale: activation elements more than 2^-24
  * below their row's maximum, and weight blocks more than 2^-23 below their
- * row's largest block scale, contribute nothing there.
+ * row's largest block scale, contribute nothing there.  The NVFP4 FC2 on
+ * tiles of up to 64 tokens takes the bf16 H1 as f16 under one power of two
+ * for the whole call (its largest magnitude brought into [2^14, 2^15)): exact
+ * within 2^31 of that maximum, an absolute error below 2^-32 of it further
+ * down.  SiTU's capped factors carry an absolute error of a few fp32 ulps
+ * of the cap near 0, so a layer whose pre-activations all lie below about
+ * 1e-5 of the caps misses the relative parity bar.
  * --------------------------------------------------------------------- */
 /* FC1's gated activation (situ_moe_args.activation). */
 typedef enum { SITU_ACT_FN_SITU = 0, SITU_ACT_FN_SWIGLU_BIAS = 1 } situ_act_fn;

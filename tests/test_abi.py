@@ -235,15 +235,14 @@ def test_forward_launch_count(lib):
     assert n(pre) == 5
     pre.fuse_combine = 1
     assert n(pre) == 6
-    # NVFP4 tiles: permute, gather, FC1 (mxf4nvf4), FC2 (fcv_kernel, bf16-expanded weights on
-    # kind::f16), combine,
-    # plus one scale packing
+    # NVFP4 tiles: permute, gather, FC1 (mxf4nvf4), H1 to f16, FC2 (weights expanded to f16 in
+    # TMEM, kind::f16), combine, plus one scale packing
     nv = _args(H=256, I=128, act_dtype=2, weight_dtype=1)
     for f in ("hidden_states_q", "hidden_states_scale", "hidden_states_gscale", "w1_gscale", "w2_gscale"):
         setattr(nv, f, 0x1000)
-    assert n(nv) == 6
+    assert n(nv) == 7
     nv.scales_packed = 0x4000
-    assert n(nv) == 5
+    assert n(nv) == 6
     assert n(_args(T=0)) == 0
     bad = _args()
     bad.gemm1_alpha = None
@@ -252,8 +251,8 @@ def test_forward_launch_count(lib):
 
 
 @pytest.mark.parametrize("T,launches", [
-    (50, 6),     # 12.5 rows per expert: 16-token tiles, one tile table
-    (100, 6),    # 25: both GEMMs on 64-token tiles, still one tile table
+    (50, 7),     # 12.5 rows per expert: 16-token tiles, one tile table, H1 to f16 for the FC2
+    (100, 7),    # 25: both GEMMs on 64-token tiles, still one tile table
     (300, 7),    # 75: FC2 on 128-token tiles of a second tile table
     (2048, 7),   # 512: the widest routing still on the NVFP4 tiles (4,096 slots, one permute launch)
     (2056, 8),   # 514: the f16 prefill tiles, and three permute launches from 4,097 slots on

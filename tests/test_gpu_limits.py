@@ -11,7 +11,10 @@ container against the oracle:
   * the f16 prefill tiles hold the weights as E2M1 x 2^(s_b - s_max) in f16,
     relative to the row's largest block scale, and the activations as f16
     rows with one scale per row;
-  * the register decode tiles hold both as f16 blocks.
+  * the register decode tiles hold both as f16 blocks;
+  * the NVFP4 FC2 on 16- and 64-token tiles multiplies f16 operands: the
+    weights as E2M1 x E4M3 products (exact in f16) and H1 scaled by one
+    power of two that brings its largest magnitude into [2^14, 2^15).
 
 So the inputs here have 32-element activation blocks spanning up to 2^31,
 H1 blocks spanning about 2^20 (some up rows of W1 get block scales 2^-20
@@ -44,9 +47,12 @@ PATHS = {
     # f16 prefill tiles on NVFP4 beyond 512 rows per expert
     "f16_prefill_nvfp4": dict(T=2048, H=256, I=128, E_total=4, E_loc=4, off=0, K=2, act=W.ACT_NVFP4,
                               wt=W.W_NVFP4, params="k3_random"),
-    # NVFP4 tiles (kind::mxf4nvf4 FC1, bf16-expanded kind::f16 FC2)
+    # NVFP4 tiles (kind::mxf4nvf4 FC1, FC2 on f16 operands in kind::f16)
     "nvfp4_tiles": dict(T=96, H=256, I=128, E_total=64, E_loc=64, off=0, K=4, act=W.ACT_NVFP4,
                         wt=W.W_NVFP4, params="k3_random"),
+    # ... 64 tokens wide
+    "nvfp4_tiles64": dict(T=200, H=256, I=128, E_total=16, E_loc=16, off=0, K=2, act=W.ACT_NVFP4,
+                          wt=W.W_NVFP4, params="k3_random"),
     # register decode tiles (fcd): odd shapes at decode size
     "register_decode": dict(T=16, H=160, I=96, E_total=8, E_loc=8, off=0, K=2, params="k3_random"),
 }
@@ -157,3 +163,37 @@ def test_mxfp4_scale_bytes_at_the_documented_bounds(path):
     assert np.all(np.isfinite(out))
     rel, cos = assert_parity(out, oracle_out(wl), f"{path}: scale bytes 2 / 252 (H={H})")
     print(f"{path}: bound scale bytes worst excess {rel:.3e} of rms, cosine {cos:.7f}")
+
+
+NV_TILE_PATHS = ["nvfp4_tiles", "nvfp4_tiles64"]
+
+
+@pytest.mark.parametrize("path", NV_TILE_PATHS)
+@pytest.mark.parametrize("case", ["beyond_f16", "below_f16", "one_outlier_token"])
+def test_h1_range_of_the_f16_fc2(path, case):
+    """The NVFP4 FC2 scales H1 by one power of two into f16 range:
+    H1 far beyond f16 (inputs x 2048: |H1| ~ 1e5 and more), far below it
+    (inputs x 2^-20: |H1| ~ 1e-14), and one token 2^12 above the rest,
+    whose H1 sets the scale for every other token; those are checked
+    against the oracle on their own as well.  The caps are off (H1 =
+    g sigmoid(g) u), so that H1's magnitude follows the inputs: with caps,
+    SiTU's tanh factors near 0 carry the epilogue's absolute error, a limit
+    of the activation and not of the FC2's operands."""
+    over = dict(PATHS[path])
+    wl = W.make("tiny", device="cuda", beta=0.0, beta_lin=0.0, **over)
+    x = wl.x_bf16.float()
+    if case == "beyond_f16":
+        x *= 2048.0
+    elif case == "below_f16":
+        x *= 2.0 ** -20
+    else:
+        x[3] *= 4096.0
+    wl.x_bf16 = x.to(torch.bfloat16)
+    layer, out = run_layer(wl)
+    assert layer.device_status() == 0
+    ref = oracle_out(wl)
+    rel, cos = assert_parity(out, ref, f"{path}: {case}")
+    print(f"{path}: {case} worst excess {rel:.3e} of rms, cosine {cos:.7f}, |out| max {np.abs(ref).max():.3e}")
+    if case == "one_outlier_token":
+        rest = np.arange(wl.T) != 3
+        assert_parity(out[rest], ref[rest], f"{path}: the tokens other than the outlier")

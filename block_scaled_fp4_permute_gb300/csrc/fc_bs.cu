@@ -152,9 +152,6 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const long total = (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
-  if ((long)blockIdx.x >= total) return;
-  if (*reinterpret_cast<volatile int*>(p.err) != 0) return;   // an earlier CTA timed out
   const int nk = p.K / kBK;
 
   const uint32_t sbase = saddr(smem);
@@ -188,8 +185,19 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tm_holder;
+  // the set-up above overlaps the predecessor's tail (programmatic launch).
+  // The successor is not released early: launched at the start of this
+  // persistent kernel, FC2's grid or the combine's 57 k CTAs slowed the w4a8
+  // prefill step from 1.11 to 1.24 ms.
+  griddep_wait();
+  // no items when an earlier kernel's wait ran out
+  const long total = *reinterpret_cast<volatile int*>(p.err) != 0
+                         ? 0
+                         : (long)__ldg(p.tile_offsets + p.E_loc) * p.n_ntiles;
 
-  if (warp == 0) {
+  if ((long)blockIdx.x >= total) {
+    // no item for this CTA
+  } else if (warp == 0) {
     // ---------------- TMA producer ----------------
     // the whole warp walks the loop; one elected lane issues the copies
     const bool leader = elect_one();
@@ -455,6 +463,7 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(256) gather8_kernel(const Gather8Params p) {
+  griddep_wait();   // the tile table and the activations (FC1 is released at the end)
   const int tile = blockIdx.x;
   if (tile >= __ldg(p.tile_offsets + p.E_loc)) return;
   const int2 ti = __ldg(p.tile_info + tile);
@@ -616,8 +625,7 @@ cudaError_t launch_fcq_t(const FcqParams& p, const CUtensorMap& a, const CUtenso
   const long items = max_tiles * p.n_ntiles;   // upper bound; the kernel reads the true count
   const long grid = items < sm_count() ? items : sm_count();
   if (grid <= 0) return cudaSuccess;
-  fcq_kernel<FC1, LO><<<(unsigned)grid, kThreads, C::kSmem, st>>>(a, al, b, p);
-  return cudaGetLastError();
+  return launch_pdl(fcq_kernel<FC1, LO>, dim3((unsigned)grid), dim3(kThreads), (size_t)C::kSmem, st, a, al, b, p);
 }
 
 }  // namespace
@@ -662,8 +670,7 @@ cudaError_t launch_pack_scales(const uint8_t* ws, int E_loc, int H, int I, bool 
 
 cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
-  gather8_kernel<<<(unsigned)max_tiles, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gather8_kernel, dim3((unsigned)max_tiles), dim3(256), 0, st, p);
 }
 
 cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, const uint8_t* xq_lo, long S, const uint8_t* w,

@@ -247,7 +247,6 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   const uint32_t tmem = *tm_holder;
   // the set-up above may overlap the predecessor's tail; everything below
   // reads its outputs
-  griddep_launch_dependents();
   griddep_wait();
   // an earlier CTA that timed out leaves no work (total = 0)
   const long total = *reinterpret_cast<volatile int*>(p.err) != 0
@@ -579,7 +578,6 @@ fcw_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) {
-  griddep_launch_dependents();
   griddep_wait();   // the permute's outputs
   const long r = blockIdx.x;
   if (r >= __ldg(p.meta)) return;
@@ -645,7 +643,6 @@ __global__ void __launch_bounds__(128) gather_hl_kernel(const GatherHLParams p) 
 // once instead of once per kept slot.
 constexpr int kGatherTokThreads = 32;
 __global__ void __launch_bounds__(kGatherTokThreads) gather_hl_tok_kernel(const GatherHLParams p) {
-  griddep_launch_dependents();
   griddep_wait();   // the permute's outputs
   const long t = blockIdx.x;
   const int lane = threadIdx.x;
@@ -1030,7 +1027,6 @@ fcv_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tm_holder;
-  griddep_launch_dependents();
   griddep_wait();
   const long total = *reinterpret_cast<volatile int*>(p.err) != 0
                          ? 0
@@ -1357,7 +1353,6 @@ fct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUte
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tm_holder;
-  griddep_launch_dependents();
   griddep_wait();
   const long total = *reinterpret_cast<volatile int*>(p.err) != 0
                          ? 0

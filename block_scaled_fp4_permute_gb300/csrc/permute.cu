@@ -8,7 +8,8 @@
 //
 // Up to kPermChunk slots (decode) one CTA does everything in one launch
 // (permute_small_kernel).  Beyond that, three launches over chunks of
-// kPermChunk slots:
+// kPermChunk slots (the second and third with programmatic dependent launch,
+// waiting for their predecessor before they read its output):
 //   count   -- per-chunk histogram in shared memory (block-local atomics);
 //   scan    -- one block: per-expert prefix over chunks, then an exclusive
 //              scan over experts of the counts and of the GEMM token tiles
@@ -24,9 +25,12 @@
 
 namespace situ {
 
-constexpr int kPermThreads = 256;
-constexpr int kPermWarps = kPermThreads / kWarp;
-constexpr int kPermSlotsPerWarp = kPermChunk / kPermWarps;   // 512
+// count and scatter take 1024 threads per chunk (4 slots each; 128 per warp
+// in the scatter), or 256 when 32 warps' counts of E_loc experts would not
+// fit in shared memory
+constexpr int kPermThreads = 1024;
+constexpr int kPermThreadsFew = 256;
+constexpr size_t kPermMaxSmem = 160 * 1024;
 
 __device__ __forceinline__ int local_expert(int id, int off, int E_loc) {
   int e = id - off;
@@ -37,6 +41,7 @@ __global__ void __launch_bounds__(kPermThreads)
 permute_count_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int off,
                      int32_t* __restrict__ blk_counts) {
   extern __shared__ int32_t hist[];
+  griddep_launch_dependents();   // the scan may start launching
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   long base = (long)blockIdx.x * kPermChunk;
@@ -86,6 +91,8 @@ permute_scan_kernel(int32_t* __restrict__ blk_counts, int nblk, int E_loc, long 
                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                     int32_t* __restrict__ tile_offsets, int2* __restrict__ tile_info,
                     int32_t* __restrict__ permuted_src, int32_t* __restrict__ meta) {
+  griddep_wait();   // the chunk counts
+  griddep_launch_dependents();
   // 1. per expert: prefix over chunks (becomes each chunk's base), total count
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
     int run = 0;
@@ -134,12 +141,15 @@ __global__ void __launch_bounds__(kPermThreads)
 permute_scatter_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int off,
                        const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
                        int32_t* __restrict__ permuted_src, int32_t* __restrict__ slot_to_row) {
-  extern __shared__ int32_t wcnt[];   // [kPermWarps][E_loc]
+  extern __shared__ int32_t wcnt[];   // [warps][E_loc]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kPermWarps * E_loc; i += blockDim.x) wcnt[i] = 0;
+  const int nwarps = blockDim.x >> 5, per_warp = kPermChunk / nwarps;
+  for (int i = threadIdx.x; i < nwarps * E_loc; i += blockDim.x) wcnt[i] = 0;
+  griddep_wait();   // the chunk bases and the offsets
+  griddep_launch_dependents();
   __syncthreads();
-  const long wbase = (long)blockIdx.x * kPermChunk + (long)warp * kPermSlotsPerWarp;
-  for (int r = 0; r < kPermSlotsPerWarp; r += kWarp) {
+  const long wbase = (long)blockIdx.x * kPermChunk + (long)warp * per_warp;
+  for (int r = 0; r < per_warp; r += kWarp) {
     long s = wbase + r + lane;
     if (s < S) {
       int e = local_expert(__ldg(ids + s), off, E_loc);
@@ -149,7 +159,7 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int o
   __syncthreads();
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
     int run = offsets[e] + blk_base[(size_t)blockIdx.x * E_loc + e];
-    for (int w = 0; w < kPermWarps; ++w) {
+    for (int w = 0; w < nwarps; ++w) {
       int v = wcnt[w * E_loc + e];
       wcnt[w * E_loc + e] = run;
       run += v;
@@ -158,7 +168,7 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int o
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
   int32_t* my = wcnt + warp * E_loc;
-  for (int r = 0; r < kPermSlotsPerWarp; r += kWarp) {
+  for (int r = 0; r < per_warp; r += kWarp) {
     long s = wbase + r + lane;
     int e = -1;
     if (s < S) e = local_expert(__ldg(ids + s), off, E_loc);
@@ -308,7 +318,9 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
   long S = (long)T * K;
   int nblk = (int)((S + kPermChunk - 1) / kPermChunk);
   size_t hist_smem = sizeof(int32_t) * (size_t)E_loc;
-  size_t wcnt_smem = sizeof(int32_t) * (size_t)kPermWarps * E_loc;
+  const int sthreads = sizeof(int32_t) * (size_t)(kPermThreads / kWarp) * E_loc <= kPermMaxSmem ? kPermThreads
+                                                                                                : kPermThreadsFew;
+  size_t wcnt_smem = sizeof(int32_t) * (size_t)(sthreads / kWarp) * E_loc;
   int dev = 0;
   cudaGetDevice(&dev);
   if (nblk == 1 && E_loc <= kSmallMaxExperts) {
@@ -341,11 +353,14 @@ cudaError_t launch_permute(const int32_t* ids, int T, int K, int E_loc, int off,
     }
   }
   permute_count_kernel<<<nblk, kPermThreads, hist_smem, st>>>(ids, S, E_loc, off, blk_counts);
-  permute_scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, E_loc, S, tile_n, counts, offsets,
-                                          tile_offsets, tile_info, permuted_src, meta);
-  permute_scatter_kernel<<<nblk, kPermThreads, wcnt_smem, st>>>(ids, S, E_loc, off, blk_counts,
-                                                                offsets, permuted_src, slot_to_row);
-  return cudaGetLastError();
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess)
+    err = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, st, blk_counts, nblk, E_loc, S, tile_n, counts,
+                     offsets, tile_offsets, tile_info, permuted_src, meta);
+  if (err == cudaSuccess)
+    err = launch_pdl(permute_scatter_kernel, dim3(nblk), dim3(sthreads), wcnt_smem, st, (const int32_t*)ids, S, E_loc,
+                     off, (const int32_t*)blk_counts, (const int32_t*)offsets, permuted_src, slot_to_row);
+  return err;
 }
 
 int permute_launches(int T, int K, int E_loc) {

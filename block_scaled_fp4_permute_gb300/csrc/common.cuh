@@ -178,25 +178,33 @@ __device__ __forceinline__ uint32_t split_hl32(const float* v, uint32_t* hi, uin
 // factor's limit (g*sigmoid(g), u).  With E(y) = exp(-y):
 //   sigmoid(g) = 1 / (1 + E(g)),  tanh(y) = (1 - E(2y)) / (1 + E(2y)),
 // so the whole product is one fraction and takes three fast exponentials and
-// one division.  The exponent arguments are clamped to [-25, 25], where
-// tanh is +-1 and sigmoid 0 or 1 to within 1.4e-11 absolute, which keeps
-// the product of the three denominators below 4e32.  The error is a few
-// fp32 ulps of the factors' magnitudes (absolute, not relative, near 0).
-// k0 = 2/b and k1 = 2/bl are the expert's constants, 0 for a cap that is
-// off; the body has no branches, so that the element loops of the
-// epilogues interleave many independent chains.
-__device__ __forceinline__ float exp_neg_clamped(float y) { return __expf(-fminf(fmaxf(y, -25.f), 25.f)); }
+// one division.  Each E is 2^z with z = -y * log2(e), log2(e) folded into
+// the constants, and z clamped at 25 log2(e) (y >= -25), where tanh is -1
+// and sigmoid 0 to within 1.4e-11 absolute; larger y only drives E to 0, so
+// the product of the three denominators stays below 4e32.  The error is a
+// few fp32 ulps of the factors' magnitudes (absolute, not relative, near 0).
+// k0 = -2 log2(e)/b and k1 = -2 log2(e)/bl are the expert's constants, 0
+// for a cap that is off; the body has no branches, so that the element loops
+// of the epilogues interleave many independent chains.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float exp2_approx(float z) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(z));
+  return r;
+}
+// 2^min(z, 25 log2 e)
+__device__ __forceinline__ float exp2_clamped(float z) { return exp2_approx(fminf(z, 25.f * kLog2e)); }
 __device__ __forceinline__ float situ_k(float g, float u, float b, float k0, float bl, float k1) {
-  const float e0 = exp_neg_clamped(g);
-  const float e1 = exp_neg_clamped(k0 * g);
-  const float e2 = exp_neg_clamped(k1 * u);
-  const float ng = k0 > 0.f ? b * (1.f - e1) : g;
-  const float dg = k0 > 0.f ? 1.f + e1 : 1.f;
-  const float nu = k1 > 0.f ? bl * (1.f - e2) : u;
-  const float du = k1 > 0.f ? 1.f + e2 : 1.f;
+  const float e0 = exp2_clamped(-kLog2e * g);
+  const float e1 = exp2_clamped(k0 * g);
+  const float e2 = exp2_clamped(k1 * u);
+  const float ng = k0 < 0.f ? b * (1.f - e1) : g;
+  const float dg = k0 < 0.f ? 1.f + e1 : 1.f;
+  const float nu = k1 < 0.f ? bl * (1.f - e2) : u;
+  const float du = k1 < 0.f ? 1.f + e2 : 1.f;
   return __fdividef(ng * nu, ((1.f + e0) * dg) * du);
 }
-__device__ __forceinline__ float situ_cap_k(float b) { return b > 0.f ? 2.f / b : 0.f; }
+__device__ __forceinline__ float situ_cap_k(float b) { return b > 0.f ? -2.f * kLog2e / b : 0.f; }
 
 // SwigluBias g * sigmoid(alpha * g) * (u + beta), the exponent argument
 // clamped to [-80, 80], where sigmoid is 0 or 1 to fp32 precision.

@@ -53,6 +53,7 @@
 // is bounded; on expiry the CTA records an error code, drains what it issued,
 // releases TMEM and returns.
 #include "situ_internal.h"
+#include "../../include/situ_moe.h"
 #include "tc_common.cuh"
 #include <cuda_fp16.h>
 
@@ -684,6 +685,39 @@ __global__ void __launch_bounds__(kGatherTokThreads) gather_hl_tok_kernel(const 
   }
 }
 
+// NVFP4 token rows by token: token t's packed codes and its scale chunks
+// (the E4M3 scales of each 64-element K step as a 16-byte chunk, its four
+// bytes first) are read once and written to the rows of all its kept slots,
+// with the token's global scale; one CTA per token instead of one per row.
+constexpr int kGatherNvThreads = 128;
+__global__ void __launch_bounds__(kGatherNvThreads) gather_nv_tok_kernel(const GatherHLParams p) {
+  griddep_wait();   // the permute's outputs
+  const long t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int K = p.K, top_k = p.top_k;
+  __shared__ int rows[SITU_MAX_TOP_K];
+  if (tid < top_k) rows[tid] = __ldg(p.slot_to_row + t * top_k + tid);
+  __syncthreads();
+  const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * (K / 2));
+  for (int i = tid; i < K / 32; i += kGatherNvThreads) {
+    const uint4 v = __ldg(src + i);
+    for (int j = 0; j < top_k; ++j) {
+      const int r = rows[j];
+      if (r >= 0) reinterpret_cast<uint4*>(p.x + (size_t)r * (K / 2))[i] = v;
+    }
+  }
+  const uint8_t* ss = p.x_s + (size_t)t * (K / 16);
+  for (int c = tid; c < K / 64; c += kGatherNvThreads) {
+    const uint32_t v = (uint32_t)__ldg(ss + 4 * c) | ((uint32_t)__ldg(ss + 4 * c + 1) << 8) |
+                       ((uint32_t)__ldg(ss + 4 * c + 2) << 16) | ((uint32_t)__ldg(ss + 4 * c + 3) << 24);
+    for (int j = 0; j < top_k; ++j) {
+      const int r = rows[j];
+      if (r >= 0) reinterpret_cast<uint4*>(p.xs + (size_t)r * (K / 4))[c] = make_uint4(v, 0u, 0u, 0u);
+    }
+  }
+  if (tid < top_k && rows[tid] >= 0) p.xg[rows[tid]] = __ldg(p.x_gs + t);
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -735,6 +769,10 @@ cudaError_t launch_gather_hl(const GatherHLParams& p, cudaStream_t st) {
     const int nb = p.K / 32;
     const dim3 grid((unsigned)p.T, (unsigned)((nb + kGatherTokThreads - 1) / kGatherTokThreads));
     return launch_pdl(gather_hl_tok_kernel, grid, dim3(kGatherTokThreads), 0, st, p);
+  }
+  if (p.act == 2 && p.slot_to_row) {
+    if (p.T <= 0) return cudaSuccess;
+    return launch_pdl(gather_nv_tok_kernel, dim3((unsigned)p.T), dim3(kGatherNvThreads), 0, st, p);
   }
   return launch_pdl(gather_hl_kernel, dim3((unsigned)p.S), dim3(128), 0, st, p);
 }

@@ -453,10 +453,10 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
       return SITU_ERR_CUDA;
     mark(4);
   } else if (fcwnv) {
-    // NVFP4 at decode: FC1 (+SiTU) on 16-token block-scaled tiles with both
-    // operands E2M1 (kind::mxf4nvf4), writing H1 as bf16 rows; FC2 on the
-    // same tiles with the weights expanded to bf16 in shared memory
-    // (kind::f16)
+    // NVFP4 at decode: FC1 (+SiTU) on 16- or 64-token block-scaled tiles
+    // with both operands E2M1 (kind::mxf4nvf4), writing H1 as bf16 rows; FC2
+    // on the same tiles with the weights expanded to f16 in TMEM, or on
+    // 128-token tiles expanded to bf16 in shared memory (kind::f16)
     const uint8_t *wsp1, *wsp2, *wsp3, *wsp4;
     if ((err = packed_scales(wsp1, wsp2, wsp3, wsp4)) != cudaSuccess) return SITU_ERR_CUDA;
     GatherHLParams g;
@@ -467,6 +467,8 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     g.x_gs = a->hidden_states_gscale;
     g.xg = (float*)(ws + L.xg);
     g.permuted_src = psrc;
+    g.slot_to_row = s2r;   // by token: each row read once for all its slots
+    g.T = a->T;
     g.meta = meta;
     g.top_k = a->top_k;
     g.K = a->H;

@@ -41,6 +41,7 @@
 // word, waits (bounded) for its copies and MMAs in flight, releases TMEM
 // and returns.
 #include "situ_internal.h"
+#include "../../include/situ_moe.h"
 #include "tc_common.cuh"
 
 namespace situ {
@@ -568,6 +569,72 @@ __global__ void __launch_bounds__(256) gather8_kernel(const Gather8Params p) {
   }
 }
 
+// MXFP8 rows by token, a warp per token: token t's E4M3 row is read once
+// and written to the rows of all its kept slots (lane j < top_k holds slot
+// j's row, which the others take by shuffle).  The scale blocks are then
+// written per tile, each as whole 512-byte blocks: lane i of the tile's warp
+// holds rows i, i + 32, i + 64 and i + 96, whose words for one stage are the
+// 16 bytes at 16 i of the stage's block.  Their words come from the
+// token-major scale rows; the padding rows of partly filled tiles get finite
+// (2^-127) scales.
+constexpr int kGather8TokWarps = 4;
+constexpr int kGather8TokUnroll = 8;   // 16-byte pieces per lane per pass
+__global__ void __launch_bounds__(32 * kGather8TokWarps) gather8_tok_kernel(const Gather8Params p) {
+  griddep_wait();   // the permute's outputs and the activations
+  const int lane = threadIdx.x & 31;
+  const long gw = (long)blockIdx.x * kGather8TokWarps + (threadIdx.x >> 5);
+  const long nw = (long)gridDim.x * kGather8TokWarps;
+  const int K = p.K, nk = K / kBK, n16 = K / 16, top_k = p.top_k;
+  const int n_tiles = __ldg(p.tile_offsets + p.E_loc);
+  for (long tile = gw; tile < n_tiles; tile += nw) {
+    const int2 ti = __ldg(p.tile_info + tile);
+    const int nrows = min(kBM, __ldg(p.offsets + ti.x + 1) - ti.y);
+    const uint8_t* srow[4];
+    bool has[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int m = lane + 32 * q;
+      has[q] = m < nrows;
+      srow[q] = p.x_s + (size_t)(has[q] ? __ldg(p.permuted_src + ti.y + m) / top_k : 0) * (K / 32);
+    }
+    uint4* blocks = reinterpret_cast<uint4*>(p.xsp + (size_t)tile * nk * kSfBlock) + lane;
+    for (int kk = 0; kk < nk; ++kk) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint8_t* ss = srow[q] + 4 * kk;
+        w[q] = !has[q] ? 0u
+               : p.s_vec ? __ldg(reinterpret_cast<const uint32_t*>(ss))
+                         : (uint32_t)__ldg(ss) | ((uint32_t)__ldg(ss + 1) << 8) | ((uint32_t)__ldg(ss + 2) << 16) |
+                               ((uint32_t)__ldg(ss + 3) << 24);
+      }
+      blocks[(size_t)kk * (kSfBlock / 16)] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  for (long t = gw; t < p.T; t += nw) {
+    const int my_r = lane < top_k ? __ldg(p.slot_to_row + t * top_k + lane) : -1;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * K);
+    for (int i0 = 0; i0 < n16; i0 += 32 * kGather8TokUnroll) {
+      uint4 v[kGather8TokUnroll];
+#pragma unroll
+      for (int u = 0; u < kGather8TokUnroll; ++u) {
+        const int i = i0 + 32 * u + lane;
+        if (i < n16) v[u] = __ldg(src + i);
+      }
+      for (int j = 0; j < top_k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_r, j);
+        if (r < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
+#pragma unroll
+        for (int u = 0; u < kGather8TokUnroll; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < n16) dst[i] = v[u];
+        }
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // pack_scales: a weight's UE8M0 scales [E_loc, Mtot, K/32] rearranged into
 // the scale blocks of the GEMM's N tiles: per (expert, N tile, stage) two
@@ -687,6 +754,13 @@ cudaError_t launch_pack_scales(const uint8_t* ws, int E_loc, int H, int I, bool 
 
 cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
+  if (!p.x_bf16 && p.slot_to_row) {
+    // MXFP8: a warp per tile's scale blocks, then per token's row, at most
+    // one wave of 16 CTAs per SM
+    const long units = std::max<long>(p.T, max_tiles);
+    const long grid = std::min<long>((units + kGather8TokWarps - 1) / kGather8TokWarps, 16L * sm_count());
+    return launch_pdl(gather8_tok_kernel, dim3((unsigned)grid), dim3(32 * kGather8TokWarps), 0, st, p);
+  }
   // bf16 rows: one full wave of 8 CTAs per SM (or fewer units); MXFP8: a CTA per tile
   const long grid = p.x_bf16 ? std::min<long>(max_tiles * (kBM / kGatherRowsHL), 8L * sm_count()) : max_tiles;
   return p.x_bf16 ? launch_pdl(gather8_kernel<true>, dim3((unsigned)grid), dim3(256), 0, st, p)

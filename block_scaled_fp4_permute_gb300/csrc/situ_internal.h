@@ -222,6 +222,10 @@ struct Gather8Params {
   uint8_t* xsp;
   uint8_t* x8_lo;
   uint8_t* xsp_lo;
+  // MXFP8 rows by token (non-null slot_to_row): each token's row read once
+  // for all its kept slots, the scale blocks written per tile
+  const int32_t* slot_to_row;
+  int T;
 };
 cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st);
 // Decode tiles on the block-scaled tensor cores (fc_bsd.cu): weights on

@@ -654,6 +654,10 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     g8.xsp = ws + L.xsp;
     g8.x8_lo = lo ? g8.x8 + (size_t)S * a->H : nullptr;
     g8.xsp_lo = lo ? g8.xsp + fcq_act_scale_bytes(max_tiles, a->H) : nullptr;
+    // MXFP8 rows by token (each row read once for its kept slots); bf16 rows
+    // are split per row
+    g8.slot_to_row = lo ? nullptr : s2r;
+    g8.T = a->T;
     if ((err = launch_gather8(g8, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(2);
     FcqParams q;

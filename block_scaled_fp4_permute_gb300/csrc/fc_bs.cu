@@ -204,9 +204,13 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
     const bool leader = elect_one();
     long it = 0;
     bool ok = true;
+    // the tile of the next item is read one item ahead, so that its latency
+    // hides behind this item's copies (FC2's items are three stages long)
+    int2 ti_next = __ldg(p.tile_info + blockIdx.x / p.n_ntiles);
     for (long item = blockIdx.x; item < total && ok; item += gridDim.x) {
       const int tile = (int)(item / p.n_ntiles), ntile = (int)(item % p.n_ntiles);
-      const int2 ti = __ldg(p.tile_info + tile);
+      const int2 ti = ti_next;
+      if (item + gridDim.x < total) ti_next = __ldg(p.tile_info + (item + gridDim.x) / p.n_ntiles);
       const int e = ti.x, row0 = ti.y;
       const int wrow = e * p.Mtot + ntile * C::NH;
       const uint8_t* xsb = p.xsp + (size_t)tile * nk * kSfBlock;
@@ -304,6 +308,8 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       const int e = ti.x, row0 = ti.y;
       const int nrows = min(kBM, __ldg(p.offsets + e + 1) - row0);
       const int nbase = ntile * C::NH;
+      // FC2's output scale, loaded while the MMAs run
+      const float a2 = (!FC1 && p.alpha2) ? __ldg(p.alpha2 + e) : 1.f;
       // warp-uniform outcome: the tcgen05.ld below are .sync.aligned
       if (!__all_sync(0xffffffffu, mbar_wait(acc_full(buf), (uint32_t)((li >> 1) & 1), p.err, 26))) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -361,7 +367,6 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
           dst[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
         }
       } else if (p.y_scale == nullptr) {
-        const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
         // this warp's staging block; the warp owns tile rows 32 quarter .. + 31
         uint8_t* yst = smem + C::kOffY + (warp - 4) * 32 * C::kYRow;
         const int wrow0 = quarter * 32;
@@ -403,7 +408,6 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       } else {
         // Y as f16 rows with a power-of-two scale per 32 columns: half the
         // bytes of the fp32 rows that the combine reads back
-        const float a2 = p.alpha2 ? __ldg(p.alpha2 + e) : 1.f;
         uint8_t* yst = smem + C::kOffY + (warp - 4) * 32 * C::kYRow;
         const int wrow0 = quarter * 32;
         uint16_t* y16 = reinterpret_cast<uint16_t*>(p.y_out);

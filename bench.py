@@ -172,7 +172,8 @@ def algorithmic_bytes(wl, R, touched, h1_nvfp4=False):
     y_bytes = 2 + 1 / 32 if blk_prefill else 4
     return {
         "permute": T * K * 4 + 2 * T * K * 4 + 2 * wl.E_loc * 4,
-        "gather": 2 * R * x_row,
+        # the input read once, the expert-ordered rows written once
+        "gather": act_in + R * x_row,
         "fc1": w1 + R * x_row + R * h_row,
         "fc2": w2 + R * h_in + R * H * y_bytes,
         "combine": R * H * y_bytes + route + out,

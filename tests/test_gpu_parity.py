@@ -295,6 +295,29 @@ def test_weight_scales_two_byte_aligned(over):
         assert np.array_equal(out.float().cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("over", [
+    # block-scaled prefill tiles (the token gather), a filtered shard, decode tiles
+    dict(T=300, H=256, I=128, E_total=4, E_loc=4, off=0, K=2, act=W.ACT_MXFP8, params="k3_random"),
+    dict(T=257, H=640, I=256, E_total=6, E_loc=3, off=2, K=3, act=W.ACT_MXFP8, params="k3_random"),
+    dict(T=24, H=512, I=256, E_total=32, E_loc=8, off=8, K=4, act=W.ACT_MXFP8, params="k3_random"),
+])
+def test_activation_scales_two_byte_aligned(over):
+    """MXFP8 activation scales at an address 2 mod 4 (the forward asks
+    block-scale arrays for 2-byte alignment only) give the same bytes as
+    aligned ones.  The quantiser writes 16-byte aligned arrays, so its scales
+    are copied to the odd address and the forward runs alone."""
+    wl = W.make("tiny", device="cuda", **over)
+    _, ref = run_layer(wl)
+    x_q, x_s = binding.situ_moe_quant_mxfp8(wl.x_bf16)
+    x_scale = _at_byte_offset(x_s, 2)
+    assert x_scale.data_ptr() % 4 == 2
+    layer = binding.Layer(wl, x_q=x_q, x_scale=x_scale)
+    binding.situ_moe_forward(layer.args, layer.workspace)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert np.array_equal(layer.out.float().cpu().numpy(), ref)
+
+
 def test_prefill_w4a8_subset():
     wl = wl_("prefill_w4a8")
     layer, out = run_layer(wl)

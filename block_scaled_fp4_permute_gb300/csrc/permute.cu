@@ -209,15 +209,20 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
   int32_t* wcnt = sm;                  // [nw][E_loc]
   int32_t* cnt = sm + nw * E_loc;      // [E_loc]
   int32_t* offs = cnt + E_loc;         // [E_loc]
+  // the lane's slots' local experts, loaded once (all four loads in flight
+  // while the counts are cleared) for both the histogram and the scatter
+  constexpr int kPerLane = kPerWarp / kWarp;   // 4
+  int le[kPerLane];
+#pragma unroll
+  for (int u = 0; u < kPerLane; ++u) {
+    const int s = warp * kPerWarp + u * kWarp + lane;
+    le[u] = s < S ? local_expert(__ldg(ids + s), off, E_loc) : -1;
+  }
   for (int i = threadIdx.x; i < nw * E_loc; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  for (int r = 0; r < kPerWarp; r += kWarp) {
-    const int s = warp * kPerWarp + r + lane;
-    if (s < S) {
-      const int e = local_expert(__ldg(ids + s), off, E_loc);
-      if (e >= 0) atomicAdd(&wcnt[warp * E_loc + e], 1);
-    }
-  }
+#pragma unroll
+  for (int u = 0; u < kPerLane; ++u)
+    if (le[u] >= 0) atomicAdd(&wcnt[warp * E_loc + le[u]], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
     int run = 0;
@@ -237,9 +242,12 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
     sc += cnt[e];
     st += (cnt[e] + tile_n - 1) / tile_n;
   }
-  int R, tiles;
-  int pc = block_exclusive_scan(sc, &R);
-  int pt = block_exclusive_scan(st, &tiles);
+  // one scan of both prefixes: slots in the low 16 bits, tiles in the high
+  // (at most kPermChunk slots and kPermChunk + kSmallMaxExperts tiles)
+  int both;
+  const int pb = block_exclusive_scan(sc | (st << 16), &both);
+  const int R = both & 0xFFFF, tiles = both >> 16;
+  int pc = pb & 0xFFFF, pt = pb >> 16;
   for (int e = e0; e < e1; ++e) {
     offs[e] = pc;
     offsets[e] = pc;
@@ -260,10 +268,10 @@ permute_small_kernel(const int32_t* __restrict__ ids, int S, int E_loc, int off,
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
   int32_t* my = wcnt + warp * E_loc;
-  for (int r = 0; r < kPerWarp; r += kWarp) {
-    const int s = warp * kPerWarp + r + lane;
-    int e = -1;
-    if (s < S) e = local_expert(__ldg(ids + s), off, E_loc);
+#pragma unroll
+  for (int u = 0; u < kPerLane; ++u) {
+    const int s = warp * kPerWarp + u * kWarp + lane;
+    const int e = le[u];
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
       const int row = offs[e] + my[e] + __popc(peers & lt);

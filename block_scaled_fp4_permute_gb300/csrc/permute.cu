@@ -93,13 +93,22 @@ permute_scan_kernel(int32_t* __restrict__ blk_counts, int nblk, int E_loc, long 
                     int32_t* __restrict__ permuted_src, int32_t* __restrict__ meta) {
   griddep_wait();   // the chunk counts
   griddep_launch_dependents();
-  // 1. per expert: prefix over chunks (becomes each chunk's base), total count
+  // 1. per expert: prefix over chunks (becomes each chunk's base), total
+  // count; the chunk counts are loaded 16 at a time, so that each batch costs
+  // one memory round trip instead of one per chunk
+  constexpr int kScanBatch = 16;
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
     int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-      int v = blk_counts[(size_t)b * E_loc + e];
-      blk_counts[(size_t)b * E_loc + e] = run;
-      run += v;
+    for (int b0 = 0; b0 < nblk; b0 += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j)
+        v[j] = b0 + j < nblk ? blk_counts[(size_t)(b0 + j) * E_loc + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) {
+        if (b0 + j < nblk) blk_counts[(size_t)(b0 + j) * E_loc + e] = run;
+        run += v[j];
+      }
     }
     counts[e] = run;
   }
@@ -145,17 +154,25 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int o
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5, per_warp = kPermChunk / nwarps;
   for (int i = threadIdx.x; i < nwarps * E_loc; i += blockDim.x) wcnt[i] = 0;
+  const long wbase = (long)blockIdx.x * kPermChunk + (long)warp * per_warp;
+  // the lane's slots' local experts, loaded once for the counts and the
+  // scatter (4 per lane on 1,024 threads, 16 on 256) while the scan runs:
+  // the routing is the caller's input, which the count kernel (launched
+  // after everything before this call) has already read
+  constexpr int kMaxPerLane = kPermChunk / kPermThreadsFew;
+  const int n_lane = per_warp / kWarp;
+  int le[kMaxPerLane];
+#pragma unroll
+  for (int u = 0; u < kMaxPerLane; ++u) {
+    const long s = wbase + u * kWarp + lane;
+    le[u] = (u < n_lane && s < S) ? local_expert(__ldg(ids + s), off, E_loc) : -1;
+  }
   griddep_wait();   // the chunk bases and the offsets
   griddep_launch_dependents();
   __syncthreads();
-  const long wbase = (long)blockIdx.x * kPermChunk + (long)warp * per_warp;
-  for (int r = 0; r < per_warp; r += kWarp) {
-    long s = wbase + r + lane;
-    if (s < S) {
-      int e = local_expert(__ldg(ids + s), off, E_loc);
-      if (e >= 0) atomicAdd(&wcnt[warp * E_loc + e], 1);
-    }
-  }
+#pragma unroll
+  for (int u = 0; u < kMaxPerLane; ++u)
+    if (le[u] >= 0) atomicAdd(&wcnt[warp * E_loc + le[u]], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) {
     int run = offsets[e] + blk_base[(size_t)blockIdx.x * E_loc + e];
@@ -168,10 +185,11 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, long S, int E_loc, int o
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
   int32_t* my = wcnt + warp * E_loc;
-  for (int r = 0; r < per_warp; r += kWarp) {
-    long s = wbase + r + lane;
-    int e = -1;
-    if (s < S) e = local_expert(__ldg(ids + s), off, E_loc);
+#pragma unroll
+  for (int u = 0; u < kMaxPerLane; ++u) {
+    if (u >= n_lane) break;   // warp-uniform
+    const long s = wbase + u * kWarp + lane;
+    const int e = le[u];
     unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
       int row = my[e] + __popc(peers & lt);

@@ -462,115 +462,69 @@ fcq_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
 }
 
 // ---------------------------------------------------------------------------
-// gather8: per token tile, the MXFP8 activation rows copied into expert
-// order (16-byte copies, one warp per row), or bf16 rows split into hi / lo
-// MXFP8 rows, and their UE8M0 scales written as the tile's scale blocks.
+// gather8: the token rows of the block-scaled prefill tiles in expert order.
+// bf16 rows are split into hi / lo MXFP8 rows per row, their UE8M0 scales
+// written into the tile's scale blocks; MXFP8 rows are copied per token
+// (gather8_tok_kernel below).
 // ---------------------------------------------------------------------------
 
-// One unit of work: n rows of a tile.  bf16 rows, split into hi + lo, go in
-// units of 16 rows that the CTAs walk grid-stride, so that the last wave is
-// not left to a few CTAs (the EP shard's gather 0.048 -> 0.033 ms); MXFP8
-// rows, which are only copied, one tile per CTA (grid-stride units of any
-// size from 32 to 128 rows were slower there: 0.131-0.134 against 0.125 ms).
+// One unit of work: 16 rows of a tile, which the CTAs walk grid-stride, so
+// that the last wave is not left to a few CTAs (the EP shard's gather 0.048
+// -> 0.033 ms against a CTA per 128-row tile).
 constexpr int kGatherRowsHL = 16;
-constexpr int kGatherRowsQ = kBM;
-template <int n>
-__device__ __forceinline__ void gather8_rows(const Gather8Params& p, int tile, int m0) {
+__device__ __forceinline__ void gather8_hl_rows(const Gather8Params& p, int tile, int m0) {
   const int2 ti = __ldg(p.tile_info + tile);
   const int row0 = ti.y;
   const int nrows = min(kBM, __ldg(p.offsets + ti.x + 1) - row0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = p.K, n16 = K / 16, nsb = K / 32, nk = K / kBK;
+  const int K = p.K, nsb = K / 32, nk = K / kBK;
   uint8_t* blocks = p.xsp + (size_t)tile * nk * kSfBlock;
-  if (p.x_bf16) {
-    // bf16 rows: hi / lo E4M3 rows (split_hl32), one lane per 32-element block
-    uint8_t* blocks_lo = p.xsp_lo + (size_t)tile * nk * kSfBlock;
-    for (int m = m0 + warp; m < m0 + n; m += 8) {
-      if (m < nrows) {
-        const long r = row0 + m;
-        const long t = __ldg(p.permuted_src + r) / p.top_k;
-        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.x_bf16) + (size_t)t * K * 2);
-        uint4* dh = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
-        uint4* dl = reinterpret_cast<uint4*>(p.x8_lo + (size_t)r * K);
-        for (int b = lane; b < nsb; b += 32) {
-          float v[32];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 w = __ldg(src + 4 * b + q);
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              v[8 * q + 2 * j] = bf16_lo(u[j]);
-              v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
-            }
-          }
-          uint32_t hi[8], lo[8];
-          const uint32_t sb = split_hl32(v, hi, lo);
-          dh[2 * b] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          dh[2 * b + 1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-          dl[2 * b] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          dl[2 * b + 1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-          const size_t o = (size_t)(b / 4) * kSfBlock + sf_offset(m, b & 3);
-          blocks[o] = (uint8_t)(sb & 0xFFu);
-          blocks_lo[o] = (uint8_t)(sb >> 8);
-        }
-      } else {
-        for (int kk = lane; kk < nk; kk += 32) {
-          *reinterpret_cast<uint32_t*>(blocks + (size_t)kk * kSfBlock + sf_offset(m, 0)) = 0u;
-          *reinterpret_cast<uint32_t*>(blocks_lo + (size_t)kk * kSfBlock + sf_offset(m, 0)) = 0u;
-        }
-      }
-    }
-    return;
-  }
-  for (int m = m0 + warp; m < m0 + n; m += 8) {
+  // bf16 rows: hi / lo E4M3 rows (split_hl32), one lane per 32-element block
+  uint8_t* blocks_lo = p.xsp_lo + (size_t)tile * nk * kSfBlock;
+  for (int m = m0 + warp; m < m0 + kGatherRowsHL; m += 8) {
     if (m < nrows) {
       const long r = row0 + m;
       const long t = __ldg(p.permuted_src + r) / p.top_k;
-      const uint4* src = reinterpret_cast<const uint4*>(p.x_q + (size_t)t * K);
-      uint4* dst = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
-      // all of the lane's loads first, then the stores: one L2 round trip
-      // per row instead of one per 16-byte piece
-      constexpr int kU = 8;
-      for (int i0 = 0; i0 < n16; i0 += 32 * kU) {
-        uint4 v[kU];
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.x_bf16) + (size_t)t * K * 2);
+      uint4* dh = reinterpret_cast<uint4*>(p.x8 + (size_t)r * K);
+      uint4* dl = reinterpret_cast<uint4*>(p.x8_lo + (size_t)r * K);
+      for (int b = lane; b < nsb; b += 32) {
+        float v[32];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int i = i0 + 32 * u + lane;
-          if (i < n16) v[u] = __ldg(src + i);
-        }
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = __ldg(src + 4 * b + q);
+          const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int i = i0 + 32 * u + lane;
-          if (i < n16) dst[i] = v[u];
+          for (int j = 0; j < 4; ++j) {
+            v[8 * q + 2 * j] = bf16_lo(u[j]);
+            v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
+          }
         }
-      }
-      const uint8_t* ss = p.x_s + (size_t)t * nsb;
-      for (int kk = lane; kk < nk; kk += 32) {
-        const uint32_t w = p.s_vec ? __ldg(reinterpret_cast<const uint32_t*>(ss) + kk)
-                                   : (uint32_t)__ldg(ss + 4 * kk) | ((uint32_t)__ldg(ss + 4 * kk + 1) << 8) |
-                                         ((uint32_t)__ldg(ss + 4 * kk + 2) << 16) |
-                                         ((uint32_t)__ldg(ss + 4 * kk + 3) << 24);
-        *reinterpret_cast<uint32_t*>(blocks + (size_t)kk * kSfBlock + sf_offset(m, 0)) = w;
+        uint32_t hi[8], lo[8];
+        const uint32_t sb = split_hl32(v, hi, lo);
+        dh[2 * b] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        dh[2 * b + 1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        dl[2 * b] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        dl[2 * b + 1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        const size_t o = (size_t)(b / 4) * kSfBlock + sf_offset(m, b & 3);
+        blocks[o] = (uint8_t)(sb & 0xFFu);
+        blocks_lo[o] = (uint8_t)(sb >> 8);
       }
     } else {
       // rows past the expert's end: finite (2^-127) scales
-      for (int kk = lane; kk < nk; kk += 32)
+      for (int kk = lane; kk < nk; kk += 32) {
         *reinterpret_cast<uint32_t*>(blocks + (size_t)kk * kSfBlock + sf_offset(m, 0)) = 0u;
+        *reinterpret_cast<uint32_t*>(blocks_lo + (size_t)kk * kSfBlock + sf_offset(m, 0)) = 0u;
+      }
     }
   }
 }
 
-template <bool HL>
 __global__ void __launch_bounds__(256) gather8_kernel(const Gather8Params p) {
-  griddep_wait();   // the tile table and the activations (FC1 is released at the end)
-  if (HL) {
-    constexpr int per = kBM / kGatherRowsHL;
-    const int units = __ldg(p.tile_offsets + p.E_loc) * per;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) gather8_rows<kGatherRowsHL>(p, u / per, (u % per) * kGatherRowsHL);
-  } else if ((int)blockIdx.x < __ldg(p.tile_offsets + p.E_loc)) {
-    gather8_rows<kGatherRowsQ>(p, blockIdx.x, 0);
-  }
+  griddep_wait();   // the tile table and the activations
+  constexpr int per = kBM / kGatherRowsHL;
+  const int units = __ldg(p.tile_offsets + p.E_loc) * per;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) gather8_hl_rows(p, u / per, (u % per) * kGatherRowsHL);
 }
 
 // MXFP8 rows by token, a warp per token: token t's E4M3 row is read once
@@ -758,17 +712,17 @@ cudaError_t launch_pack_scales(const uint8_t* ws, int E_loc, int H, int I, bool 
 
 cudaError_t launch_gather8(const Gather8Params& p, long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
-  if (!p.x_bf16 && p.slot_to_row) {
+  if (!p.x_bf16) {
     // MXFP8: a warp per tile's scale blocks, then per token's row, at most
     // one wave of 16 CTAs per SM
+    if (!p.slot_to_row) return cudaErrorInvalidValue;
     const long units = std::max<long>(p.T, max_tiles);
     const long grid = std::min<long>((units + kGather8TokWarps - 1) / kGather8TokWarps, 16L * sm_count());
     return launch_pdl(gather8_tok_kernel, dim3((unsigned)grid), dim3(32 * kGather8TokWarps), 0, st, p);
   }
-  // bf16 rows: one full wave of 8 CTAs per SM (or fewer units); MXFP8: a CTA per tile
-  const long grid = p.x_bf16 ? std::min<long>(max_tiles * (kBM / kGatherRowsHL), 8L * sm_count()) : max_tiles;
-  return p.x_bf16 ? launch_pdl(gather8_kernel<true>, dim3((unsigned)grid), dim3(256), 0, st, p)
-                  : launch_pdl(gather8_kernel<false>, dim3((unsigned)grid), dim3(256), 0, st, p);
+  // bf16 rows: one full wave of 8 CTAs per SM (or fewer units)
+  const long grid = std::min<long>(max_tiles * (kBM / kGatherRowsHL), 8L * sm_count());
+  return launch_pdl(gather8_kernel, dim3((unsigned)grid), dim3(256), 0, st, p);
 }
 
 cudaError_t launch_fcq(const FcqParams& p, const uint8_t* xq, const uint8_t* xq_lo, long S, const uint8_t* w,

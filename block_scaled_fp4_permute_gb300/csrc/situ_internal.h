@@ -222,8 +222,8 @@ struct Gather8Params {
   uint8_t* xsp;
   uint8_t* x8_lo;
   uint8_t* xsp_lo;
-  // MXFP8 rows by token (non-null slot_to_row): each token's row read once
-  // for all its kept slots, the scale blocks written per tile
+  // MXFP8 rows by token: each token's row read once for all its kept slots
+  // (slot_to_row, required for MXFP8), the scale blocks written per tile
   const int32_t* slot_to_row;
   int T;
 };

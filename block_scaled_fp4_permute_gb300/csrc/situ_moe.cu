@@ -656,7 +656,7 @@ static situ_status forward_impl(const situ_moe_args* a, void* workspace, size_t 
     g8.xsp_lo = lo ? g8.xsp + fcq_act_scale_bytes(max_tiles, a->H) : nullptr;
     // MXFP8 rows by token (each row read once for its kept slots); bf16 rows
     // are split per row
-    g8.slot_to_row = lo ? nullptr : s2r;
+    g8.slot_to_row = s2r;
     g8.T = a->T;
     if ((err = launch_gather8(g8, max_tiles, st)) != cudaSuccess) return SITU_ERR_CUDA;
     mark(2);

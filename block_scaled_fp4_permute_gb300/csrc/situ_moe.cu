@@ -2,7 +2,8 @@
 // workspace layout and the launch sequence of the layer.
 //
 // situ_moe_forward enqueues, on the caller's stream:
-//   permute (3 launches) -> gather -> FC1 (+SiTU) -> FC2 -> combine.
+//   permute (1 launch up to 4,096 slots, else 3) -> gather -> FC1 (+SiTU)
+//   -> FC2 -> combine.
 // No host synchronisation: the number of kept rows and the GEMM token tiles
 // live on the device (written by the permute) and every later kernel reads
 // them there; grids are sized for the worst case and surplus CTAs exit.
